@@ -1,0 +1,212 @@
+"""Seeded synthetic inputs for the FP8 rowwise-scaled grouped GEMM.
+
+This module holds no part of the GEMM's arithmetic.  It only makes inputs, and it is
+the one module that both the CUDA path's tests/benchmark and the CPU oracle's tests
+draw inputs from.
+
+Group metadata (m_sizes, zero_start_index_M) comes from splitmix64 (Steele, Lea and
+Flood, "Fast splittable pseudorandom number generators", OOPSLA 2014), so it is the
+same on every machine.  Each 64-bit output x gives the uniform u = (x >> 11) * 2^-53.
+
+Bulk data is standard normal fp32 from torch.randn under a seeded torch.Generator on
+the chosen device.  It is quantised per row to OCP FP8 E4M3 with scale = amax / 448:
+one scale per row of A and one per (group, n) row of B, both kept in fp32.  A row whose
+amax is 0 gets scale 1 and all-zero codes.  CPU and GPU generators give different
+streams; every consumer reads back the bytes it was actually given.
+
+The workloads are the five shape families the method was swept on (MSLK #471 "Back the
+FP8 rowwise grouped GEMM ops with FlyDSL on ROCm": DS-V3, llama3-70b and llama3-405b
+shape sweeps, plus the padded layout's test of empty, partial and full groups).
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import torch
+
+MASK64 = (1 << 64) - 1
+E4M3_MAX = 448.0
+
+
+def splitmix64(state: int):
+    """Generator of splitmix64 outputs from a 64-bit seed."""
+    x = state & MASK64
+    while True:
+        x = (x + 0x9E3779B97F4A7C15) & MASK64
+        z = x
+        z = ((z ^ (z >> 30)) * 0xBF58476D1CE4E5B9) & MASK64
+        z = ((z ^ (z >> 27)) * 0x94D049BB133111EB) & MASK64
+        yield z ^ (z >> 31)
+
+
+def uniforms(seed: int, count: int) -> list[float]:
+    g = splitmix64(seed)
+    return [(next(g) >> 11) * 2.0 ** -53 for _ in range(count)]
+
+
+def zipf_probs(G: int, s: float) -> list[float]:
+    w = [(j + 1) ** (-s) for j in range(G)]
+    tot = sum(w)
+    return [x / tot for x in w]
+
+
+def multinomial_counts(seed: int, total: int, probs: list[float]) -> list[int]:
+    """``total`` independent categorical draws by inverse CDF over fp64 cumulative
+    probabilities; returns the count per category."""
+    cdf = []
+    acc = 0.0
+    for p in probs:
+        acc += p
+        cdf.append(acc)
+    counts = [0] * len(probs)
+    for u in uniforms(seed, total):
+        j = 0
+        while j < len(cdf) - 1 and u >= cdf[j]:
+            j += 1
+        counts[j] += 1
+    return counts
+
+
+@dataclass(frozen=True)
+class Workload:
+    """One problem: layout, sizes and group metadata (m_sizes or zero_start_index_M)."""
+    name: str
+    layout: str            # "stacked" or "dynamic"
+    G: int
+    N: int
+    K: int
+    rows: int              # total_M (stacked) or G * expected_m (dynamic)
+    meta: tuple            # m_sizes (stacked) or zero_start_index_M (dynamic)
+    seed: int
+    expected_m: int = 0    # dynamic only
+    note: str = ""
+    tags: tuple = field(default_factory=tuple)
+
+    @property
+    def total_M(self) -> int:
+        return self.rows
+
+    def valid_rows(self) -> int:
+        if self.layout == "stacked":
+            return sum(self.meta)
+        return sum(max(0, min(v, self.expected_m)) for v in self.meta)
+
+    def nonempty_groups(self) -> int:
+        if self.layout == "stacked":
+            return sum(1 for m in self.meta if m > 0)
+        return sum(1 for v in self.meta if min(v, self.expected_m) > 0)
+
+    def flops(self) -> int:
+        """Algorithmic flops: 2 * (valid rows) * N * K."""
+        return 2 * self.valid_rows() * self.N * self.K
+
+    def bytes(self) -> int:
+        """Algorithmic HBM bytes of one call: every valid row of A and its scale, the
+        weights and scales of non-empty groups only, the metadata, and the output
+        (owned rows for stacked; the whole slab for dynamic, whose padding is
+        written with zeros)."""
+        v = self.valid_rows()
+        nz = self.nonempty_groups()
+        b = v * self.K + 4 * v + nz * self.N * self.K + 4 * nz * self.N + 8 * self.G
+        if self.layout == "stacked":
+            b += 2 * v * self.N
+        else:
+            b += 2 * self.G * self.expected_m * self.N
+        return b
+
+
+def _stacked(name, cfg, sub, G, N, K, m_sizes, note="", tags=()):
+    return Workload(name=name, layout="stacked", G=G, N=N, K=K, rows=sum(m_sizes),
+                    meta=tuple(int(m) for m in m_sizes), seed=1000 * cfg + sub, note=note,
+                    tags=tuple(tags))
+
+
+def workloads() -> dict[str, Workload]:
+    """The five configurations, by name.  Seeds are 1000 * config + sub-case."""
+    w: dict[str, Workload] = {}
+    # 0: small stacked case with an empty group
+    w["c0_stacked_small"] = _stacked("c0_stacked_small", 0, 0, 4, 256, 512, [0, 3, 17, 44],
+                                     "G=4, m_sizes=[0,3,17,44], N=256, K=512", ("parity",))
+    # 1: dynamic (padded) layout with an empty and a full group, K and N tails
+    G, E = 8, 128
+    u = uniforms(1000 * 1 + 0, G)
+    zsi = [1 + int(127 * x) for x in u]
+    zsi[0] = 0
+    zsi[7] = 128
+    w["c1_dynamic_tails"] = Workload(
+        name="c1_dynamic_tails", layout="dynamic", G=G, N=1000, K=1000, rows=G * E,
+        meta=tuple(zsi), seed=1000, expected_m=E,
+        note="G=8, expected_m=128, N=K=1000, zero_start_index_M uniform [1,127], "
+             "group 0 empty, group 7 full", tags=("parity",))
+    # 2: DS-V3-shaped MoE, 32 local experts, Zipf(1.1) routing of 8192 token-rows
+    m2 = multinomial_counts(1000 * 2 + 0, 8192, zipf_probs(32, 1.1))
+    w["c2a_dsv3_gate_up"] = _stacked("c2a_dsv3_gate_up", 2, 1, 32, 4096, 7168, m2,
+                                     "DS-V3 gate_up: G=32, total_M=8192 Zipf(1.1), "
+                                     "N=4096, K=7168", ("perf",))
+    w["c2b_dsv3_down"] = _stacked("c2b_dsv3_down", 2, 2, 32, 7168, 2048, m2,
+                                  "DS-V3 down: G=32, total_M=8192 Zipf(1.1), N=7168, K=2048",
+                                  ("perf",))
+    # 3: llama3-70b-shaped sweep, uniform routing over 16 groups
+    for i, tm in enumerate([1, 16, 128, 1024, 8192]):
+        m3 = multinomial_counts(1000 * 3 + i, tm, [1.0 / 16] * 16)
+        nm = f"c3_llama70b_m{tm}"
+        w[nm] = _stacked(nm, 3, i, 16, 8192, 8192, m3,
+                         f"llama3-70b: G=16, N=K=8192, total_M={tm} uniform", ("perf",))
+    # 4: llama3-405b-shaped
+    m4 = multinomial_counts(1000 * 4 + 0, 16384, [1.0 / 16] * 16)
+    w["c4_llama405b"] = _stacked("c4_llama405b", 4, 0, 16, 16384, 16384, m4,
+                                 "llama3-405b: G=16, N=K=total_M=16384 uniform", ("perf",))
+    return w
+
+
+# -------------------------------------------------------------------------------------
+# bulk data
+# -------------------------------------------------------------------------------------
+def quantize_rows(x: torch.Tensor):
+    """Per-row E4M3 quantisation of fp32 x [R, K]: returns (codes as uint8, scale fp32).
+
+    scale = amax / 448 (fp32); codes = e4m3(clamp(x / scale, -448, 448)), using
+    torch's round-to-nearest-even cast.  amax == 0 gives scale 1 and zero codes."""
+    x = x.float()
+    if x.shape[-1] == 0:
+        return (torch.zeros(x.shape, dtype=torch.uint8, device=x.device),
+                torch.ones(x.shape[:-1], dtype=torch.float32, device=x.device))
+    amax = x.abs().amax(dim=-1)
+    scale = torch.where(amax > 0, amax / E4M3_MAX, torch.ones_like(amax))
+    q = (x / scale.unsqueeze(-1)).clamp(-E4M3_MAX, E4M3_MAX).to(torch.float8_e4m3fn)
+    return q.view(torch.uint8), scale.float()
+
+
+def make_inputs(wl: Workload, device="cpu", chunk_rows: int = 8192):
+    """Materialise a workload: A [rows, K] u8, B [G, N, K] u8, scale_a [rows] f32,
+    scale_b [G, N] f32, meta [G] int64 (m_sizes or zero_start_index_M), all on
+    ``device``.  Data comes from torch.randn under Generator(seed); A first, then B
+    group by group, in chunks of ``chunk_rows`` rows to bound the fp32 temporaries."""
+    device = torch.device(device)
+    gen = torch.Generator(device=device)
+    gen.manual_seed(wl.seed)
+    G, N, K, R = wl.G, wl.N, wl.K, wl.rows
+    A = torch.empty((R, K), dtype=torch.uint8, device=device)
+    sa = torch.empty((R,), dtype=torch.float32, device=device)
+    for r0 in range(0, R, chunk_rows):
+        r1 = min(R, r0 + chunk_rows)
+        x = torch.randn((r1 - r0, K), generator=gen, device=device, dtype=torch.float32)
+        A[r0:r1], sa[r0:r1] = quantize_rows(x)
+    B = torch.empty((G, N, K), dtype=torch.uint8, device=device)
+    sb = torch.empty((G, N), dtype=torch.float32, device=device)
+    for g in range(G):
+        for n0 in range(0, N, chunk_rows):
+            n1 = min(N, n0 + chunk_rows)
+            x = torch.randn((n1 - n0, K), generator=gen, device=device, dtype=torch.float32)
+            B[g, n0:n1], sb[g, n0:n1] = quantize_rows(x)
+    meta = torch.tensor(list(wl.meta), dtype=torch.int64, device=device)
+    return {"A": A, "B": B, "scale_a": sa, "scale_b": sb, "meta": meta}
+
+
+def random_codes(shape, gen: torch.Generator, device="cpu", allow_nan: bool = False):
+    """Uniformly random E4M3 byte codes (every code, NaN codes optional)."""
+    c = torch.randint(0, 256, shape, generator=gen, device=device, dtype=torch.int32)
+    if not allow_nan:
+        nan = (c & 0x7F) == 0x7F
+        c = torch.where(nan, c ^ 0x01, c)  # 0x7F -> 0x7E (448), 0xFF -> 0xFE (-448)
+    return c.to(torch.uint8)
