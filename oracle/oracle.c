@@ -194,10 +194,13 @@ static double dot_lut(const uint8_t *arow, const uint8_t *brow, int64_t K, const
     return s;
 }
 
-/* One output element: exact fp64 dot product, scales applied once, one rounding. */
+/* One output element: exact fp64 dot product, scales applied once, one rounding.
+ * An empty reduction (K = 0) is +0.0 whatever the scales: the op zeroes its output
+ * for a contraction of length zero (MSLK #471, commit zeroing an empty reduction). */
 static uint16_t oracle_element(const uint8_t *arow, const uint8_t *brow, int64_t K,
                                float sa, float sb, const double *lut)
 {
+    if (K == 0) return 0x0000u;
     double s = dot_lut(arow, brow, K, lut);
 #if ORACLE_MUTANT == 10
     double ab = (double)sa; (void)sb; /* mutant: scale_b forgotten */
@@ -237,6 +240,7 @@ static uint16_t element_gn(const uint8_t *arow, const uint8_t *B, const float *s
                            int64_t g, int64_t n, int64_t N, int64_t K, float sa, const double *lut)
 {
 #if ORACLE_MUTANT == 2
+    if (K == 0) return 0x0000u;
     double s = 0.0;
     const uint8_t *bg = B + (size_t)g * (size_t)N * (size_t)K;
     for (int64_t k = 0; k < K; ++k) {

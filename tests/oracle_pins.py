@@ -390,6 +390,10 @@ def pin_k_zero(orc):
     dy = orc.dynamic(np.zeros((6, 0), np.uint8), B, np.ones(6, np.float32),
                      np.ones((G, N), np.float32), [2, 3], 3)
     assert np.all(dy == 0)
+    # +0.0 even with negative or NaN scales: the empty reduction is zeroed, not scaled
+    out, _ = orc.stacked(A, B, np.array([-1, np.nan, 2, -3, 1], np.float32),
+                         -np.ones((G, N), np.float32), [2, 2], total_M=5, out=poison)
+    assert np.all(out[:4] == 0) and np.all(out[4] == 0x1234)
 
 
 def pin_sampled_rows(orc, seed=41):
