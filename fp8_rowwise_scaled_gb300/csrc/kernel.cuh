@@ -1,0 +1,634 @@
+// kernel.cuh -- persistent, warp-specialised FP8 rowwise-scaled grouped GEMM for sm_103a.
+//
+// Operation (MSLK #471 "Back the FP8 rowwise grouped GEMM ops with FlyDSL on ROCm",
+// commit introducing the rowwise scaling scheme): for every row r of group g,
+//   out[r, n] = bf16_rne((acc[r, n] * scale_a[r]) * scale_b[g, n]),
+//   acc[r, n] = sum_k A[r, k] * B[g, n, k]   (e4m3 x e4m3, fp32 accumulator in TMEM)
+// The K loop accumulates unscaled; the two scales are applied once, in the epilogue,
+// on the fp32 accumulator (never rounded before that).
+//
+// CTA organisation (one CTA per SM, persistent over output tiles):
+//   loader warp(s)   TMA (one elected thread) or cp.async (4 warps) fill an S-stage
+//                    ring of 128-byte-swizzled shared-memory tiles (full/empty mbarriers)
+//   MMA warp         allocates TMEM; one thread issues tcgen05.mma (K = 32 per
+//                    instruction, 4 per 128-byte stage) into one of two TMEM
+//                    accumulators, and tcgen05.commit releases stages / accumulators
+//   4 epilogue warps tcgen05.ld the accumulator, scale, convert to bf16, store with
+//                    row / column predicates; padding rows get +0.0
+//
+// Group/tile scheduler (MSLK #471, commits on the packed and padded layouts and on the
+// group resolution step): each CTA reads the [G] metadata once, prefix-sums it in shared
+// memory, and enumerates output tiles over groups that have rows, so an empty group
+// generates no tile.  Within a group tiles run n-major (all m-tiles of one weight
+// n-tile are consecutive), so concurrently running CTAs share a weight tile in L2.
+//
+// Two tile shapes:
+//   normal  (kSwap = false): MMA M = 128 activation rows, MMA N = kTileN weight rows.
+//   swap-AB (kSwap = true) : MMA M = 128 weight rows, MMA N = kTileN activation rows;
+//                            for few rows per group the weights fill the 128-row side.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include "ptx.cuh"
+
+namespace mslkb {
+
+constexpr int kMaxGroups = 1024;
+constexpr int kBK = 128;  // bytes (= e4m3 elements) of K per pipeline stage
+constexpr uint32_t kStatusTimeout = 1u;
+constexpr uint32_t kStatusClamped = 2u;
+
+struct GemmParams {
+  const uint8_t* A;        // [rows, K] e4m3
+  const uint8_t* B;        // [G, N, K] e4m3
+  const float* scale_a;    // [rows]
+  const float* scale_b;    // [G, N]
+  const int64_t* meta;     // [G] m_sizes (stacked) or zero_start_index_M (dynamic)
+  uint16_t* out;           // [rows, N] bf16 bits
+  uint32_t* status;        // device status word
+  int32_t rows;            // total_M (stacked) or G * E (dynamic)
+  int32_t G;
+  int32_t N;
+  int32_t K;
+  int32_t E;               // expected_m (dynamic only)
+  int32_t num_kb;          // ceil(K / 128)
+  int32_t copy_width;      // cp.async loader: bytes per copy (16, 8, 4) or 1 (byte loads)
+  uint64_t timeout_ns;     // give-up time of one pipeline wait
+};
+
+template <int kTileN_, int kStages_, bool kSwap_, bool kTma_, bool kDynamic_>
+struct KernelCfg {
+  static constexpr int kTileN = kTileN_;     // MMA N
+  static constexpr int kStages = kStages_;
+  static constexpr bool kSwap = kSwap_;
+  static constexpr bool kTma = kTma_;
+  static constexpr bool kDynamic = kDynamic_;
+  static constexpr int kMmaM = 128;
+  static constexpr int kActRows = kSwap ? kTileN : kMmaM;  // activation rows per tile
+  static constexpr int kWRows = kSwap ? kMmaM : kTileN;    // weight rows per tile
+  static constexpr int kActBytes = kActRows * kBK;
+  static constexpr int kWBytes = kWRows * kBK;
+  static constexpr int kStageBytes = kActBytes + kWBytes;
+  static constexpr int kLoaderWarps = kTma ? 1 : 4;
+  static constexpr int kLoaderThreads = 32 * kLoaderWarps;
+  static constexpr int kMmaWarp = kLoaderWarps;
+  static constexpr int kEpiWarp0 = kLoaderWarps + 1;
+  static constexpr int kThreads = 32 * (kLoaderWarps + 1 + 4);
+  static constexpr int kAccCols = kTileN;  // fp32 TMEM columns of one accumulator
+  static constexpr int kTmemCols = (2 * kAccCols <= 32)    ? 32
+                                   : (2 * kAccCols <= 64)  ? 64
+                                   : (2 * kAccCols <= 128) ? 128
+                                   : (2 * kAccCols <= 256) ? 256
+                                                           : 512;
+  static constexpr int kCpLag = kStages - 2;  // cp.async groups kept in flight per thread
+  static constexpr uint32_t kIdesc = ptx::idesc_e4m3_f32(kMmaM, kTileN);
+
+  // shared memory layout, from a 1024-byte aligned base
+  static constexpr int kOffAct = 0;
+  static constexpr int kOffW = kStages * kActBytes;
+  static constexpr int kOffBar = kOffW + kStages * kWBytes;
+  static constexpr int kNumBars = 2 * kStages + 4;
+  static constexpr int kOffMisc = kOffBar + 8 * kNumBars;  // tmem address, abort flag
+  static constexpr int kOffSched = kOffMisc + 16;
+  static constexpr int kSchedBytes = 2 * 4 * (kMaxGroups + 1);
+  static constexpr int kSmemBytes = kOffSched + kSchedBytes + 1024;  // + alignment slack
+
+  static_assert(kTileN % 16 == 0 && kTileN >= 16 && kTileN <= 256, "MMA N for M = 128");
+  static_assert(kActBytes % 1024 == 0 && kWBytes % 1024 == 0, "swizzle atoms");
+  static_assert(kStages >= 3, "pipeline depth");
+  static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+  static_assert(2 * kAccCols <= 512, "two accumulators must fit TMEM");
+};
+
+struct TileCoord {
+  int32_t g;          // group
+  int32_t m0;         // first activation row (global row index)
+  int32_t n0;         // first weight row / output column
+  int32_t valid_end;  // rows < valid_end get the product
+  int32_t zero_end;   // rows in [valid_end, zero_end) get +0.0 (padding)
+};
+
+// Shared-memory scheduler tables.
+//   rowinfo[g]: stacked -> first row of group g (G + 1 entries, clamped prefix);
+//               dynamic -> valid rows v_g of slab g.
+//   tile_pre[g]: exclusive prefix of output tiles over groups (G + 1 entries).
+struct Sched {
+  const int32_t* rowinfo;
+  const int32_t* tile_pre;
+  int32_t G;
+  int32_t E;
+  int32_t n_tiles_n;
+  int32_t total;
+};
+
+template <class Cfg>
+__device__ __forceinline__ int32_t group_rows(const Sched& s, int32_t g) {
+  if constexpr (Cfg::kDynamic) return s.rowinfo[g];
+  else return s.rowinfo[g + 1] - s.rowinfo[g];
+}
+
+template <class Cfg>
+__device__ __forceinline__ TileCoord decode_tile(const Sched& s, int32_t t) {
+  // largest g with tile_pre[g] <= t  (tile_pre[0] = 0 <= t < tile_pre[G] = total)
+  int32_t lo = 0, hi = s.G;
+  while (hi - lo > 1) {
+    int32_t mid = (lo + hi) >> 1;
+    if (s.tile_pre[mid] <= t) lo = mid;
+    else hi = mid;
+  }
+  const int32_t g = lo;
+  const int32_t cnt = group_rows<Cfg>(s, g);
+  const int32_t mt = (cnt + Cfg::kActRows - 1) / Cfg::kActRows;
+  const int32_t local = t - s.tile_pre[g];
+  const int32_t n_idx = local / mt;
+  const int32_t m_idx = local - n_idx * mt;
+  TileCoord c;
+  c.g = g;
+  const int32_t base = Cfg::kDynamic ? g * s.E : s.rowinfo[g];
+  c.m0 = base + m_idx * Cfg::kActRows;
+  c.n0 = n_idx * Cfg::kWRows;
+  c.valid_end = base + cnt;
+  c.zero_end = Cfg::kDynamic ? base + s.E : base + cnt;
+  return c;
+}
+
+// Bounded mbarrier wait: false if the CTA is aborting or the wait gave up, in which
+// case the abort flag and the device status word are set.
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile uint32_t* abort,
+                                         uint32_t* status, uint64_t timeout_ns) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = ptx::globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if ((it & 255u) == 0) {
+      if (*abort) return false;
+      if (ptx::globaltimer_ns() - t0 > timeout_ns) {
+        *abort = 1u;
+        atomicOr(status, kStatusTimeout);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const uint32_t l = __bfloat16_as_ushort(__float2bfloat16_rn(lo));
+  const uint32_t h = __bfloat16_as_ushort(__float2bfloat16_rn(hi));
+  return l | (h << 16);
+}
+
+// Inclusive warp scan of 64-bit values.
+__device__ __forceinline__ int64_t warp_incl_scan(int64_t v, uint32_t lane) {
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int64_t o = __shfl_up_sync(0xffffffffu, v, d);
+    if (lane >= static_cast<uint32_t>(d)) v += o;
+  }
+  return v;
+}
+
+// One warp builds the scheduler tables from the [G] metadata (lane l takes a
+// contiguous chunk of groups; chunks are combined with warp scans).
+template <class Cfg>
+__device__ void build_sched(const GemmParams& p, int32_t* rowinfo, int32_t* tile_pre,
+                            uint32_t lane) {
+  const int32_t G = p.G;
+  const int32_t per = (G + 31) / 32;
+  const int32_t g0 = min(G, static_cast<int32_t>(lane) * per);
+  const int32_t g1 = min(G, g0 + per);
+  const int64_t ntn = (p.N + Cfg::kWRows - 1) / Cfg::kWRows;
+  bool clamped = false;
+  if constexpr (Cfg::kDynamic) {
+    for (int32_t g = g0; g < g1; ++g) {
+      int64_t v = p.meta[g];
+      v = v < 0 ? 0 : (v > p.E ? p.E : v);
+      rowinfo[g] = static_cast<int32_t>(v);
+    }
+  } else {
+    // clamped exclusive prefix: off_g = min(sum_{h<g} max(m_h, 0), total_M)
+    int64_t my_sum = 0;
+    for (int32_t g = g0; g < g1; ++g) {
+      const int64_t m = p.meta[g];
+      if (m < 0) clamped = true;
+      my_sum += m < 0 ? 0 : m;
+    }
+    const int64_t total = p.rows;
+    int64_t run = warp_incl_scan(my_sum, lane) - my_sum;
+    for (int32_t g = g0; g < g1; ++g) {
+      const int64_t m = p.meta[g];
+      rowinfo[g] = static_cast<int32_t>(run < total ? run : total);
+      run += m < 0 ? 0 : m;
+    }
+    if (lane == 31) {  // the last chunk ends at G, so run is the sum over all groups
+      if (run > total) clamped = true;
+      rowinfo[G] = static_cast<int32_t>(run < total ? run : total);
+    }
+  }
+  __syncwarp();
+  int64_t my_tiles = 0;
+  for (int32_t g = g0; g < g1; ++g) {
+    int64_t cnt;
+    if constexpr (Cfg::kDynamic) cnt = rowinfo[g];
+    else cnt = static_cast<int64_t>(rowinfo[g + 1]) - rowinfo[g];
+    my_tiles += ((cnt + Cfg::kActRows - 1) / Cfg::kActRows) * ntn;
+  }
+  const int64_t incl = warp_incl_scan(my_tiles, lane);
+  int64_t tp = incl - my_tiles;
+  for (int32_t g = g0; g < g1; ++g) {
+    tile_pre[g] = static_cast<int32_t>(tp);
+    int64_t cnt;
+    if constexpr (Cfg::kDynamic) cnt = rowinfo[g];
+    else cnt = static_cast<int64_t>(rowinfo[g + 1]) - rowinfo[g];
+    tp += ((cnt + Cfg::kActRows - 1) / Cfg::kActRows) * ntn;
+  }
+  if (lane == 31) tile_pre[G] = static_cast<int32_t>(incl);
+  const bool any_clamped = __any_sync(0xffffffffu, clamped);
+  if (any_clamped && lane == 0 && blockIdx.x == 0) atomicOr(p.status, kStatusClamped);
+}
+
+// cp.async loader: one 16-byte chunk of a swizzled tile row.
+__device__ __forceinline__ void load_chunk(uint32_t dst, const uint8_t* row_ptr, bool row_ok,
+                                           int32_t k, int32_t K, int32_t width,
+                                           const uint8_t* any_valid) {
+  if (width == 16) {
+    const bool ok = row_ok && k < K;  // K % 16 == 0 on this path
+    ptx::cp_async<16>(dst, ok ? row_ptr + k : any_valid, ok ? 16u : 0u);
+  } else if (width == 8) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int32_t kk = k + 8 * h;
+      const bool ok = row_ok && kk < K;  // K % 8 == 0 on this path
+      ptx::cp_async<8>(dst + 8 * h, ok ? row_ptr + kk : any_valid, ok ? 8u : 0u);
+    }
+  } else if (width == 4) {
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      const int32_t kk = k + 4 * h;
+      const bool ok = row_ok && kk < K;  // K % 4 == 0 on this path
+      ptx::cp_async<4>(dst + 4 * h, ok ? row_ptr + kk : any_valid, ok ? 4u : 0u);
+    }
+  } else {
+    uint32_t w[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int32_t kk = k + i;
+      const uint32_t b = (row_ok && kk < K) ? static_cast<uint32_t>(__ldg(row_ptr + kk)) : 0u;
+      w[i >> 2] |= b << (8 * (i & 3));
+    }
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(w[0]), "r"(w[1]),
+                 "r"(w[2]), "r"(w[3])
+                 : "memory");
+  }
+}
+
+template <class Cfg>
+__global__ void __launch_bounds__(Cfg::kThreads, 1)
+    grouped_gemm_kernel(const __grid_constant__ GemmParams p,
+                        const __grid_constant__ CUtensorMap tmA,
+                        const __grid_constant__ CUtensorMap tmB) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t s_act = ptx::smem_addr(smem + Cfg::kOffAct);
+  const uint32_t s_w = ptx::smem_addr(smem + Cfg::kOffW);
+  const uint32_t s_bar = ptx::smem_addr(smem + Cfg::kOffBar);
+  auto full_bar = [&](int s) { return s_bar + 8u * s; };
+  auto empty_bar = [&](int s) { return s_bar + 8u * (Cfg::kStages + s); };
+  auto tfull_bar = [&](int b) { return s_bar + 8u * (2 * Cfg::kStages + b); };
+  auto tempty_bar = [&](int b) { return s_bar + 8u * (2 * Cfg::kStages + 2 + b); };
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + Cfg::kOffMisc);
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + Cfg::kOffMisc + 4);
+  int32_t* rowinfo = reinterpret_cast<int32_t*>(smem + Cfg::kOffSched);
+  int32_t* tile_pre = rowinfo + (kMaxGroups + 1);
+
+  const uint32_t warp = threadIdx.x >> 5;
+  const uint32_t lane = threadIdx.x & 31u;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < Cfg::kStages; ++s) {
+      ptx::mbar_init(full_bar(s), Cfg::kTma ? 1u : static_cast<uint32_t>(Cfg::kLoaderThreads));
+      ptx::mbar_init(empty_bar(s), 1u);
+    }
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(tfull_bar(b), 1u);
+      ptx::mbar_init(tempty_bar(b), 4u);
+    }
+    *abort_flag = 0u;
+    ptx::fence_mbar_init();
+    ptx::fence_proxy_async_smem();
+  }
+  if constexpr (Cfg::kTma) {
+    if (warp == 0 && lane == 0 && p.num_kb > 0) {
+      ptx::prefetch_tensormap(&tmA);
+      ptx::prefetch_tensormap(&tmB);
+    }
+  }
+  if (warp == Cfg::kMmaWarp) {
+    ptx::tmem_alloc(ptx::smem_addr(tmem_holder), Cfg::kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  if (warp == Cfg::kEpiWarp0) build_sched<Cfg>(p, rowinfo, tile_pre, lane);
+  ptx::tc_fence_before_sync();
+  __syncthreads();
+  ptx::tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_holder;
+
+  Sched sched;
+  sched.rowinfo = rowinfo;
+  sched.tile_pre = tile_pre;
+  sched.G = p.G;
+  sched.E = p.E;
+  sched.n_tiles_n = (p.N + Cfg::kWRows - 1) / Cfg::kWRows;
+  sched.total = tile_pre[p.G];
+  const bool has_k = p.num_kb > 0;
+
+  if (warp < static_cast<uint32_t>(Cfg::kLoaderWarps)) {
+    // ------------------------------------------------------------------ loader
+    if constexpr (Cfg::kTma) {
+      if (lane == 0 && has_k) {
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        for (int32_t t = blockIdx.x; ok && t < sched.total; t += gridDim.x) {
+          const TileCoord c = decode_tile<Cfg>(sched, t);
+          for (int32_t kb = 0; kb < p.num_kb; ++kb) {
+            if (!wait_bar(empty_bar(stage), phase ^ 1u, abort_flag, p.status, p.timeout_ns)) {
+              ok = false;
+              break;
+            }
+            ptx::mbar_arrive_expect_tx(full_bar(stage), Cfg::kStageBytes);
+            ptx::tma_load_2d(s_act + stage * Cfg::kActBytes, &tmA, full_bar(stage), kb * kBK,
+                             c.m0);
+            ptx::tma_load_3d(s_w + stage * Cfg::kWBytes, &tmB, full_bar(stage), kb * kBK, c.n0,
+                             c.g);
+            if (++stage == Cfg::kStages) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+        }
+        // tail: wait until the MMA has released every stage it was given
+        for (int i = 0; ok && i < Cfg::kStages; ++i) {
+          ok = wait_bar(empty_bar(stage), phase ^ 1u, abort_flag, p.status, p.timeout_ns);
+          if (++stage == Cfg::kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+    } else {
+      if (has_k) {
+        const uint32_t tid = threadIdx.x;  // 0 .. kLoaderThreads - 1
+        int stage = 0;
+        uint32_t phase = 0;
+        int64_t fills = 0;  // stages issued by this thread
+        bool ok = true;
+        for (int32_t t = blockIdx.x; ok && t < sched.total; t += gridDim.x) {
+          const TileCoord c = decode_tile<Cfg>(sched, t);
+          const uint8_t* b_group = p.B + static_cast<size_t>(c.g) * p.N * p.K;
+          for (int32_t kb = 0; kb < p.num_kb; ++kb) {
+            if (!wait_bar(empty_bar(stage), phase ^ 1u, abort_flag, p.status, p.timeout_ns)) {
+              ok = false;
+              break;
+            }
+            const int32_t k0 = kb * kBK;
+            constexpr int kChunks = (Cfg::kActRows + Cfg::kWRows) * 8;
+            for (int i = tid; i < kChunks; i += Cfg::kLoaderThreads) {
+              const int r_all = i >> 3;
+              const int ch = i & 7;
+              const bool is_act = r_all < Cfg::kActRows;
+              const int r = is_act ? r_all : r_all - Cfg::kActRows;
+              const uint32_t dst = (is_act ? s_act + stage * Cfg::kActBytes
+                                           : s_w + stage * Cfg::kWBytes) +
+                                   r * 128 + (static_cast<uint32_t>(ch ^ (r & 7)) << 4);
+              const uint8_t* row_ptr;
+              bool row_ok;
+              if (is_act) {
+                const int32_t R = c.m0 + r;
+                row_ok = R < p.rows;
+                row_ptr = p.A + static_cast<size_t>(row_ok ? R : 0) * p.K;
+              } else {
+                const int32_t n = c.n0 + r;
+                row_ok = n < p.N;
+                row_ptr = b_group + static_cast<size_t>(row_ok ? n : 0) * p.K;
+              }
+              load_chunk(dst, row_ptr, row_ok, k0 + ch * 16, p.K, p.copy_width, p.A);
+            }
+            ptx::cp_async_commit();
+            if (fills >= Cfg::kCpLag) {
+              ptx::cp_async_wait<Cfg::kCpLag>();
+              ptx::fence_proxy_async_smem();
+              ptx::mbar_arrive(full_bar(static_cast<int>((fills - Cfg::kCpLag) % Cfg::kStages)));
+            }
+            ++fills;
+            if (++stage == Cfg::kStages) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+        }
+        ptx::cp_async_wait<0>();
+        ptx::fence_proxy_async_smem();
+        if (ok) {
+          for (int64_t f = (fills > Cfg::kCpLag ? fills - Cfg::kCpLag : 0); f < fills; ++f)
+            ptx::mbar_arrive(full_bar(static_cast<int>(f % Cfg::kStages)));
+          if (tid == 0) {
+            for (int i = 0; ok && i < Cfg::kStages; ++i) {
+              ok = wait_bar(empty_bar(stage), phase ^ 1u, abort_flag, p.status, p.timeout_ns);
+              if (++stage == Cfg::kStages) {
+                stage = 0;
+                phase ^= 1u;
+              }
+            }
+          }
+        }
+      }
+    }
+  } else if (warp == static_cast<uint32_t>(Cfg::kMmaWarp)) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0 && has_k) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      for (int32_t t = blockIdx.x; ok && t < sched.total; t += gridDim.x) {
+        if (!wait_bar(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p.status, p.timeout_ns)) break;
+        ptx::tc_fence_after_sync();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * Cfg::kAccCols);
+        for (int32_t kb = 0; kb < p.num_kb; ++kb) {
+          if (!wait_bar(full_bar(stage), phase, abort_flag, p.status, p.timeout_ns)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after_sync();
+          const uint64_t act_desc = ptx::sw128_kmajor_desc(s_act + stage * Cfg::kActBytes);
+          const uint64_t w_desc = ptx::sw128_kmajor_desc(s_w + stage * Cfg::kWBytes);
+          const uint64_t a_desc = Cfg::kSwap ? w_desc : act_desc;
+          const uint64_t b_desc = Cfg::kSwap ? act_desc : w_desc;
+#pragma unroll
+          for (int k = 0; k < kBK / 32; ++k) {
+            // advance 32 bytes of K inside the 128-byte swizzled row: +2 in 16-byte units
+            ptx::mma_f8f6f4(d_tmem, a_desc + 2u * k, b_desc + 2u * k, Cfg::kIdesc,
+                            (kb > 0 || k > 0) ? 1u : 0u);
+          }
+          ptx::mma_commit(empty_bar(stage));
+          if (++stage == Cfg::kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        ptx::mma_commit(tfull_bar(acc));
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------------ epilogue
+    const uint32_t q = warp & 3u;           // TMEM lane quadrant this warp may access
+    const uint32_t ew = warp - Cfg::kEpiWarp0;
+    if constexpr (Cfg::kDynamic) {
+      // rows of each slab past its last computed tile: pure padding, written +0.0
+      const int32_t gw = blockIdx.x * 4 + ew;
+      const int32_t nw = gridDim.x * 4;
+      for (int32_t g = 0; g < p.G; ++g) {
+        const int32_t v = rowinfo[g];
+        const int32_t covered = ((v + Cfg::kActRows - 1) / Cfg::kActRows) * Cfg::kActRows;
+        const int32_t z0 = g * p.E + (covered < p.E ? covered : p.E);
+        const int32_t z1 = (g + 1) * p.E;
+        for (int32_t r = z0 + gw; r < z1; r += nw) {
+          uint16_t* orow = p.out + static_cast<size_t>(r) * p.N;
+          for (int32_t col = lane * 8; col < p.N; col += 256)
+            *reinterpret_cast<uint4*>(orow + col) = make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+    }
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int32_t t = blockIdx.x; t < sched.total; t += gridDim.x) {
+      TileCoord c = decode_tile<Cfg>(sched, t);
+      // an empty reduction (K = 0) writes +0.0 to every owned row, whatever the scales
+      if (!has_k) c.valid_end = c.m0;
+      if (has_k) {
+        if (!wait_bar(tfull_bar(acc), acc_phase, abort_flag, p.status, p.timeout_ns)) break;
+        ptx::tc_fence_after_sync();
+      }
+      const uint32_t t_acc =
+          tmem_base + ((32u * q) << 16) + static_cast<uint32_t>(acc * Cfg::kAccCols);
+      if constexpr (!Cfg::kSwap) {
+        // thread = one activation row; 32 output columns per TMEM load
+        const int32_t R = c.m0 + static_cast<int32_t>(32u * q + lane);
+        const bool row_val = R < c.valid_end;
+        const bool row_zero = !row_val && R < c.zero_end;
+        const bool warp_any =
+            __any_sync(0xffffffffu, row_val || row_zero);
+        const float sa = row_val ? __ldg(p.scale_a + R) : 0.0f;
+        const float* sb_g = p.scale_b + static_cast<size_t>(c.g) * p.N;
+        uint16_t* orow = p.out + static_cast<size_t>(row_val || row_zero ? R : 0) * p.N;
+        if (warp_any) {
+#pragma unroll 1
+          for (int cc = 0; cc < Cfg::kTileN / 32; ++cc) {
+            const int32_t col0 = c.n0 + cc * 32;
+            // lane j holds scale_b of column col0 + j; broadcast by shuffle below
+            const float sb_l = (col0 + static_cast<int32_t>(lane) < p.N)
+                                   ? __ldg(sb_g + col0 + lane) : 0.0f;
+            uint32_t v[32];
+            if (has_k) {
+              ptx::tmem_ld_x32(t_acc + static_cast<uint32_t>(cc * 32), v);
+              ptx::tmem_ld_wait();
+            } else {
+#pragma unroll
+              for (int j = 0; j < 32; ++j) v[j] = 0u;
+            }
+#pragma unroll
+            for (int j8 = 0; j8 < 4; ++j8) {
+              float y[8];
+#pragma unroll
+              for (int j = 0; j < 8; ++j) {
+                const float sb = __shfl_sync(0xffffffffu, sb_l, j8 * 8 + j);
+                y[j] = (__uint_as_float(v[j8 * 8 + j]) * sa) * sb;
+              }
+              const int32_t col = col0 + j8 * 8;
+              if (col + 7 < p.N) {
+                if (row_val) {
+                  *reinterpret_cast<uint4*>(orow + col) =
+                      make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]),
+                                 pack_bf16x2(y[4], y[5]), pack_bf16x2(y[6], y[7]));
+                } else if (row_zero) {
+                  *reinterpret_cast<uint4*>(orow + col) = make_uint4(0u, 0u, 0u, 0u);
+                }
+              }
+            }
+          }
+        }
+      } else {
+        // thread = one weight row (output column n); TMEM columns are activation rows
+        const int32_t n = c.n0 + static_cast<int32_t>(32u * q + lane);
+        const bool col_ok = n < p.N;
+        const float sb = col_ok ? __ldg(p.scale_b + static_cast<size_t>(c.g) * p.N + n) : 0.0f;
+#pragma unroll 1
+        for (int cc = 0; cc < (Cfg::kTileN + 31) / 32; ++cc) {
+          constexpr int kCols = Cfg::kTileN < 32 ? Cfg::kTileN : 32;
+          const int32_t m_first = c.m0 + cc * 32;
+          if (m_first >= c.zero_end) break;
+          // lane j holds scale_a of row m_first + j
+          const int32_t Rl = m_first + static_cast<int32_t>(lane);
+          const float sa_l = (lane < static_cast<uint32_t>(kCols) && Rl < c.valid_end)
+                                 ? __ldg(p.scale_a + Rl) : 0.0f;
+          uint32_t v[kCols];
+          if (has_k) {
+            if constexpr (kCols == 16) {
+              ptx::tmem_ld_x16(t_acc, v);
+            } else {
+              ptx::tmem_ld_x32(t_acc + static_cast<uint32_t>(cc * 32), v);
+            }
+            ptx::tmem_ld_wait();
+          } else {
+#pragma unroll
+            for (int j = 0; j < kCols; ++j) v[j] = 0u;
+          }
+#pragma unroll
+          for (int j = 0; j < kCols; ++j) {
+            const float sa = __shfl_sync(0xffffffffu, sa_l, j);
+            const int32_t R = m_first + j;
+            if (R < c.valid_end) {
+              const float y = (__uint_as_float(v[j]) * sa) * sb;
+              if (col_ok)
+                p.out[static_cast<size_t>(R) * p.N + n] =
+                    __bfloat16_as_ushort(__float2bfloat16_rn(y));
+            } else if (R < c.zero_end) {
+              if (col_ok) p.out[static_cast<size_t>(R) * p.N + n] = 0;
+            }
+          }
+        }
+      }
+      if (has_k) {
+        ptx::tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(tempty_bar(acc));
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+    }
+  }
+
+  // ------------------------------------------------------------------ teardown
+  ptx::tc_fence_before_sync();
+  __syncthreads();
+  if (*abort_flag) {
+    // let any copy or MMA still in flight land before the memory is released
+    const uint64_t t0 = ptx::globaltimer_ns();
+    while (ptx::globaltimer_ns() - t0 < 2000000ull) ptx::nanosleep(1000);
+  }
+  if (warp == static_cast<uint32_t>(Cfg::kMmaWarp)) {
+    ptx::tc_fence_after_sync();
+    ptx::tmem_dealloc(tmem_base, Cfg::kTmemCols);
+  }
+}
+
+}  // namespace mslkb

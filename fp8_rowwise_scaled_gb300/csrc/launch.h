@@ -1,0 +1,70 @@
+// launch.h -- internal: the table of compiled kernel variants and how to launch one.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "kernel.cuh"
+
+namespace mslkb {
+
+struct LaunchArgs {
+  GemmParams params;
+  CUtensorMap tmA;   // activation tiles [rows, K], box (128 B, act_rows)
+  CUtensorMap tmB;   // weight tiles [G, N, K], box (128 B, w_rows, 1)
+  dim3 grid;
+  cudaStream_t stream;
+};
+
+using LaunchFn = cudaError_t (*)(const LaunchArgs&);
+using AttrFn = cudaError_t (*)();
+
+struct VariantInfo {
+  const char* name;
+  int tile_n;     // MMA N
+  int stages;
+  bool swap;
+  bool tma;
+  bool dynamic;
+  int threads;
+  int smem;
+  int act_rows;   // activation rows per tile
+  int w_rows;     // weight rows per tile
+  LaunchFn launch;
+  AttrFn set_attr;
+};
+
+template <class Cfg>
+cudaError_t launch_variant(const LaunchArgs& a) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = a.grid;
+  cfg.blockDim = dim3(Cfg::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = Cfg::kSmemBytes;
+  cfg.stream = a.stream;
+  cfg.attrs = nullptr;
+  cfg.numAttrs = 0;
+  return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<Cfg>, a.params, a.tmA, a.tmB);
+}
+
+template <class Cfg>
+cudaError_t set_attr_variant() {
+  return cudaFuncSetAttribute(grouped_gemm_kernel<Cfg>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
+}
+
+template <class Cfg>
+constexpr VariantInfo make_variant(const char* name) {
+  return VariantInfo{name,         Cfg::kTileN,   Cfg::kStages,     Cfg::kSwap,
+                     Cfg::kTma,    Cfg::kDynamic, Cfg::kThreads,    Cfg::kSmemBytes,
+                     Cfg::kActRows, Cfg::kWRows,  &launch_variant<Cfg>, &set_attr_variant<Cfg>};
+}
+
+// Defined in the variants_*.cu translation units.
+extern const VariantInfo kVariantsStackedTma[];
+extern const int kNumVariantsStackedTma;
+extern const VariantInfo kVariantsDynamicTma[];
+extern const int kNumVariantsDynamicTma;
+extern const VariantInfo kVariantsCpAsync[];
+extern const int kNumVariantsCpAsync;
+
+}  // namespace mslkb

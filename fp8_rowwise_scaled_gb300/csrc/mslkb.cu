@@ -1,0 +1,406 @@
+// mslkb.cu -- the C ABI of libmslkb.so (declared in include/mslkb.h): argument checks,
+// variant selection, TMA descriptor encoding and the launch of one persistent kernel.
+//
+// Host-side counterpart of the op modules and dispatcher of MSLK #471 "Back the FP8
+// rowwise grouped GEMM ops with FlyDSL on ROCm" (commits moving operand marshalling,
+// grid extent and tile selection into one dispatcher; the K-tail variant selected on the
+// host): every decision here uses host-known values only (sizes, alignments, SM count);
+// the group metadata stays on the device and is read by the kernel's scheduler.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "launch.h"
+#include "mslkb.h"
+
+namespace {
+
+using mslkb::GemmParams;
+using mslkb::LaunchArgs;
+using mslkb::VariantInfo;
+
+constexpr int kVersion = 10000;  // 1.0.0
+constexpr int kMaxDevices = 64;
+constexpr uint64_t kWaitTimeoutNs = 1000000000ull;  // one pipeline wait gives up after ~1 s
+
+__device__ uint32_t g_device_status;  // MSLKB_DEV_* bits, per device
+
+thread_local int t_last_cuda_error = 0;
+std::atomic<int> g_forced_variant{-1};
+
+// ---------------------------------------------------------------------------------
+// variant table: stacked TMA, dynamic TMA, cp.async (both layouts)
+// ---------------------------------------------------------------------------------
+int num_variants() {
+  return mslkb::kNumVariantsStackedTma + mslkb::kNumVariantsDynamicTma +
+         mslkb::kNumVariantsCpAsync;
+}
+
+const VariantInfo* variant(int i) {
+  if (i < 0) return nullptr;
+  if (i < mslkb::kNumVariantsStackedTma) return &mslkb::kVariantsStackedTma[i];
+  i -= mslkb::kNumVariantsStackedTma;
+  if (i < mslkb::kNumVariantsDynamicTma) return &mslkb::kVariantsDynamicTma[i];
+  i -= mslkb::kNumVariantsDynamicTma;
+  if (i < mslkb::kNumVariantsCpAsync) return &mslkb::kVariantsCpAsync[i];
+  return nullptr;
+}
+
+int find_variant(bool dynamic, bool tma, bool swap, int tile_n) {
+  for (int i = 0; i < num_variants(); ++i) {
+    const VariantInfo* v = variant(i);
+    if (v->dynamic == dynamic && v->tma == tma && v->swap == swap && v->tile_n == tile_n) return i;
+  }
+  return -1;
+}
+
+// ---------------------------------------------------------------------------------
+// per-device state
+// ---------------------------------------------------------------------------------
+struct DeviceState {
+  bool ready = false;
+  bool supported = false;
+  int sm_count = 0;
+  uint32_t* status_ptr = nullptr;
+  uint64_t attr_done[2] = {0, 0};  // one bit per variant
+};
+
+std::mutex g_mutex;
+DeviceState g_devices[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+bool g_encode_tried = false;
+
+mslkb_status cuda_fail(cudaError_t e) {
+  t_last_cuda_error = static_cast<int>(e);
+  return MSLKB_ERR_CUDA;
+}
+
+// Device query, status-word address and driver entry point, once per device.
+mslkb_status device_state(DeviceState** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev < 0 || dev >= kMaxDevices) return MSLKB_ERR_DEVICE;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceState& st = g_devices[dev];
+  if (!st.ready) {
+    int major = 0, minor = 0, sms = 0;
+    if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess)
+      return cuda_fail(e);
+    if ((e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess)
+      return cuda_fail(e);
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return cuda_fail(e);
+    st.supported = (major == 10 && minor == 3);
+    st.sm_count = sms;
+    if (st.supported) {
+      void* p = nullptr;
+      if ((e = cudaGetSymbolAddress(&p, g_device_status)) != cudaSuccess) return cuda_fail(e);
+      st.status_ptr = static_cast<uint32_t*>(p);
+    }
+    if (!g_encode_tried) {
+      g_encode_tried = true;
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+      e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                           cudaEnableDefault, &q);
+      if (e == cudaSuccess && q == cudaDriverEntryPointSuccess)
+        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    st.ready = true;
+  }
+  if (!st.supported) return MSLKB_ERR_DEVICE;
+  *out = &st;
+  return MSLKB_OK;
+}
+
+mslkb_status ensure_attr(DeviceState* st, int vi) {
+  const uint64_t bit = 1ull << (vi & 63);
+  {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (st->attr_done[vi >> 6] & bit) return MSLKB_OK;
+  }
+  cudaError_t e = variant(vi)->set_attr();
+  if (e != cudaSuccess) return cuda_fail(e);
+  std::lock_guard<std::mutex> lock(g_mutex);
+  st->attr_done[vi >> 6] |= bit;
+  return MSLKB_OK;
+}
+
+// ---------------------------------------------------------------------------------
+// planning (pure host)
+// ---------------------------------------------------------------------------------
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+int copy_width_for(int64_t K, int64_t a_align, int64_t b_align) {
+  const int64_t al = a_align < b_align ? a_align : b_align;
+  for (int w : {16, 8, 4})
+    if (K % w == 0 && al % w == 0) return w;
+  return 1;
+}
+
+// Upper bound on output tiles for a variant (the kernel's own count never exceeds it).
+int64_t tiles_bound(const VariantInfo* v, int layout, int64_t rows, int64_t G, int64_t N) {
+  const int64_t ntn = ceil_div(N, v->w_rows);
+  if (layout == 0) {
+    const int64_t nz = G < rows ? G : rows;  // non-empty groups
+    const int64_t mt = (rows + nz * (v->act_rows - 1)) / v->act_rows;
+    return mt * ntn;
+  }
+  return G * ceil_div(rows, v->act_rows) * ntn;  // rows = expected_m here
+}
+
+mslkb_status plan(int layout, int64_t rows, int64_t G, int64_t N, int64_t K, int num_sms,
+                  int64_t a_align, int64_t b_align, mslkb_plan_info* info) {
+  if (layout != 0 && layout != 1) return MSLKB_ERR_SHAPE;
+  if (num_sms <= 0 || rows < 0 || G < 0 || N < 0 || K < 0) return MSLKB_ERR_SHAPE;
+  const bool dynamic = layout == 1;
+  const bool tma = (K % 16 == 0) && (a_align % 16 == 0) && (b_align % 16 == 0);
+  // rows of one group: the slab height (dynamic) or the mean over the groups that can
+  // be non-empty (stacked; the counts themselves stay on the device)
+  int64_t per_group = rows;
+  if (!dynamic && G > 0 && rows > 0) per_group = rows / (G < rows ? G : rows);
+  bool swap;
+  int tile_n;
+  if (per_group <= 16) {
+    swap = true;
+    tile_n = 16;
+  } else if (per_group <= 32 && tma) {
+    swap = true;
+    tile_n = 32;
+  } else if (per_group <= 64 && tma) {
+    swap = true;
+    tile_n = 64;
+  } else {
+    swap = false;
+    tile_n = 128;
+    if (tma) {
+      const int wide = find_variant(dynamic, true, false, 256);
+      if (wide >= 0 && tiles_bound(variant(wide), layout, rows, G, N) >= num_sms) tile_n = 256;
+    }
+  }
+  int vi = g_forced_variant.load();
+  if (vi < 0) {
+    vi = find_variant(dynamic, tma, swap, tile_n);
+    if (vi < 0 && !tma) vi = find_variant(dynamic, false, false, 128);
+  }
+  const VariantInfo* v = variant(vi);
+  if (v == nullptr || v->dynamic != dynamic || (v->tma && !tma)) return MSLKB_ERR_SHAPE;
+  const int64_t bound = tiles_bound(v, layout, rows, G, N);
+  if (bound > INT32_MAX) return MSLKB_ERR_SHAPE;
+  int64_t grid = bound < num_sms ? bound : num_sms;
+  if (dynamic) {  // padding rows are zeroed by every CTA's epilogue warps
+    const int64_t zero_ctas = ceil_div(G * rows, 32);
+    if (grid < zero_ctas) grid = zero_ctas < num_sms ? zero_ctas : num_sms;
+  }
+  if (grid < 1) grid = 1;
+  std::memset(info, 0, sizeof(*info));
+  info->variant = vi;
+  info->swap_ab = v->swap;
+  info->tile_m = v->act_rows;
+  info->tile_n = v->w_rows;
+  info->stages = v->stages;
+  info->tma = v->tma;
+  info->copy_width = v->tma ? 16 : copy_width_for(K, a_align, b_align);
+  info->grid = static_cast<int32_t>(grid);
+  info->threads = v->threads;
+  info->smem_bytes = v->smem;
+  info->tiles_bound = bound;
+  return MSLKB_OK;
+}
+
+int64_t addr_align(const void* p) {
+  const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+  if (a == 0) return 256;
+  return static_cast<int64_t>(a & (~a + 1));  // lowest set bit
+}
+
+// ---------------------------------------------------------------------------------
+// tensor maps
+// ---------------------------------------------------------------------------------
+mslkb_status encode_maps(LaunchArgs* la, const VariantInfo* v, const void* A, const void* B,
+                         int64_t rows, int64_t G, int64_t N, int64_t K) {
+  std::memset(&la->tmA, 0, sizeof(la->tmA));
+  std::memset(&la->tmB, 0, sizeof(la->tmB));
+  if (!v->tma || K == 0) return MSLKB_OK;
+  if (g_encode == nullptr) return cuda_fail(cudaErrorNotSupported);
+  const cuuint32_t elem_strides[3] = {1, 1, 1};
+  {
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K)};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(mslkb::kBK),
+                               static_cast<cuuint32_t>(v->act_rows)};
+    CUresult r = g_encode(&la->tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(A), dims,
+                          strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+      t_last_cuda_error = static_cast<int>(r);
+      return MSLKB_ERR_CUDA;
+    }
+  }
+  {
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(N),
+                                static_cast<cuuint64_t>(G)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(N * K)};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(mslkb::kBK),
+                               static_cast<cuuint32_t>(v->w_rows), 1};
+    CUresult r = g_encode(&la->tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(B), dims,
+                          strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+      t_last_cuda_error = static_cast<int>(r);
+      return MSLKB_ERR_CUDA;
+    }
+  }
+  return MSLKB_OK;
+}
+
+// ---------------------------------------------------------------------------------
+// the two entry points share everything but the layout
+// ---------------------------------------------------------------------------------
+mslkb_status check_sizes(int64_t rows, int64_t G, int64_t N, int64_t K) {
+  if (rows < 0 || G < 0 || N < 0 || K < 0) return MSLKB_ERR_SHAPE;
+  if (G > MSLKB_MAX_GROUPS) return MSLKB_ERR_SHAPE;
+  if (N % 8 != 0) return MSLKB_ERR_SHAPE;
+  if (rows > MSLKB_MAX_DIM || N > MSLKB_MAX_DIM || K > MSLKB_MAX_DIM) return MSLKB_ERR_SHAPE;
+  return MSLKB_OK;
+}
+
+mslkb_status run(int layout, const void* A, const void* B, const float* scale_a,
+                 const float* scale_b, const int64_t* meta, void* out, int64_t rows, int64_t G,
+                 int64_t E, int64_t N, int64_t K, void* stream) {
+  // rows: total_M (stacked) or G * E (dynamic)
+  if (rows == 0 || N == 0 || G == 0) return MSLKB_OK;  // nothing is owned or written
+  if (out == nullptr || meta == nullptr || scale_a == nullptr || scale_b == nullptr)
+    return MSLKB_ERR_NULL;
+  if (K > 0 && (A == nullptr || B == nullptr)) return MSLKB_ERR_NULL;
+  if (reinterpret_cast<uintptr_t>(out) % 16 != 0) return MSLKB_ERR_ALIGN;
+  if (G * N > MSLKB_MAX_DIM || N * K >= (1ll << 40)) return MSLKB_ERR_SHAPE;
+
+  DeviceState* st = nullptr;
+  mslkb_status s = device_state(&st);
+  if (s != MSLKB_OK) return s;
+
+  mslkb_plan_info info;
+  s = plan(layout, layout == 0 ? rows : E, G, N, K, st->sm_count, addr_align(A), addr_align(B),
+           &info);
+  if (s != MSLKB_OK) return s;
+  const VariantInfo* v = variant(info.variant);
+  if ((s = ensure_attr(st, info.variant)) != MSLKB_OK) return s;
+
+  LaunchArgs la;
+  std::memset(&la, 0, sizeof(la));
+  GemmParams& p = la.params;
+  p.A = static_cast<const uint8_t*>(A);
+  p.B = static_cast<const uint8_t*>(B);
+  p.scale_a = scale_a;
+  p.scale_b = scale_b;
+  p.meta = meta;
+  p.out = static_cast<uint16_t*>(out);
+  p.status = st->status_ptr;
+  p.rows = static_cast<int32_t>(rows);
+  p.G = static_cast<int32_t>(G);
+  p.N = static_cast<int32_t>(N);
+  p.K = static_cast<int32_t>(K);
+  p.E = static_cast<int32_t>(E);
+  p.num_kb = static_cast<int32_t>(ceil_div(K, mslkb::kBK));
+  p.copy_width = info.copy_width;
+  p.timeout_ns = kWaitTimeoutNs;
+  if ((s = encode_maps(&la, v, A, B, rows, G, N, K)) != MSLKB_OK) return s;
+  la.grid = dim3(static_cast<unsigned>(info.grid), 1, 1);
+  la.stream = static_cast<cudaStream_t>(stream);
+  cudaError_t e = v->launch(la);
+  if (e != cudaSuccess) return cuda_fail(e);
+  return MSLKB_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+mslkb_status mslkb_f8f8bf16_rowwise_grouped_stacked(const void* A, const void* B,
+                                                    const float* scale_a, const float* scale_b,
+                                                    const int64_t* m_sizes, void* out,
+                                                    int64_t total_M, int64_t G, int64_t N,
+                                                    int64_t K, void* stream) {
+  mslkb_status s = check_sizes(total_M, G, N, K);
+  if (s != MSLKB_OK) return s;
+  return run(0, A, B, scale_a, scale_b, m_sizes, out, total_M, G, 0, N, K, stream);
+}
+
+mslkb_status mslkb_f8f8bf16_rowwise_grouped_dynamic(const void* A, const void* B,
+                                                    const float* scale_a, const float* scale_b,
+                                                    const int64_t* zero_start_index_M, void* out,
+                                                    int64_t G, int64_t expected_m, int64_t N,
+                                                    int64_t K, void* stream) {
+  if (expected_m < 0) return MSLKB_ERR_SHAPE;
+  mslkb_status s = check_sizes(0, G, N, K);
+  if (s != MSLKB_OK) return s;
+  if (expected_m > 0 && G > MSLKB_MAX_DIM / expected_m) return MSLKB_ERR_SHAPE;
+  return run(1, A, B, scale_a, scale_b, zero_start_index_M, out, G * expected_m, G, expected_m, N,
+             K, stream);
+}
+
+const char* mslkb_status_string(mslkb_status status) {
+  switch (status) {
+    case MSLKB_OK: return "ok";
+    case MSLKB_ERR_NULL: return "a required pointer is NULL";
+    case MSLKB_ERR_SHAPE: return "unsupported or negative size (N must be a multiple of 8)";
+    case MSLKB_ERR_ALIGN: return "out must be 16-byte aligned";
+    case MSLKB_ERR_DEVICE: return "the current device is not sm_103 (GB300)";
+    case MSLKB_ERR_CUDA: return "a CUDA call failed (see mslkb_last_cuda_error)";
+  }
+  return "unknown status";
+}
+
+int mslkb_last_cuda_error(void) { return t_last_cuda_error; }
+
+mslkb_status mslkb_get_device_status(void* stream, uint32_t* flags) {
+  if (flags == nullptr) return MSLKB_ERR_NULL;
+  DeviceState* st = nullptr;
+  mslkb_status s = device_state(&st);
+  if (s != MSLKB_OK) return s;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  uint32_t value = 0;
+  cudaError_t e = cudaMemcpyAsync(&value, st->status_ptr, sizeof(uint32_t),
+                                  cudaMemcpyDeviceToHost, cs);
+  if (e == cudaSuccess) e = cudaMemsetAsync(st->status_ptr, 0, sizeof(uint32_t), cs);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(cs);
+  if (e != cudaSuccess) return cuda_fail(e);
+  *flags = value;
+  return MSLKB_OK;
+}
+
+mslkb_status mslkb_plan(int32_t layout, int64_t rows, int64_t G, int64_t N, int64_t K,
+                        int32_t num_sms, int64_t a_align, int64_t b_align,
+                        mslkb_plan_info* info) {
+  if (info == nullptr) return MSLKB_ERR_NULL;
+  mslkb_status s = check_sizes(layout == 0 ? rows : 0, G, N, K);
+  if (s != MSLKB_OK) return s;
+  if (a_align <= 0 || b_align <= 0) return MSLKB_ERR_SHAPE;
+  return plan(layout, rows, G, N, K, num_sms, a_align, b_align, info);
+}
+
+int32_t mslkb_num_variants(void) { return num_variants(); }
+
+const char* mslkb_variant_name(int32_t i) {
+  const VariantInfo* v = variant(i);
+  return v ? v->name : nullptr;
+}
+
+mslkb_status mslkb_force_variant(int32_t i) {
+  if (i < -1 || i >= num_variants()) return MSLKB_ERR_SHAPE;
+  g_forced_variant.store(i);
+  return MSLKB_OK;
+}
+
+int32_t mslkb_version(void) { return kVersion; }
+
+}  // extern "C"

@@ -1,0 +1,176 @@
+/*
+ * mslkb.h -- C ABI of libmslkb.so: the FP8 rowwise-scaled grouped GEMM
+ * f8f8bf16_rowwise_grouped for NVIDIA GB300 (sm_103a), stacked and dynamic layouts.
+ *
+ * The operation (MSLK #471 "Back the FP8 rowwise grouped GEMM ops with FlyDSL on ROCm":
+ * commit introducing the rowwise scaling scheme; PR Summary table) is, for each group g
+ * and every row r that group owns,
+ *
+ *     out[r, n] = bf16_rne( scale_a[r] * scale_b[g, n] * sum_k A[r, k] * B[g, n, k] )
+ *
+ * with A and B in OCP FP8 E4M3 ("e4m3fn"), scale_a and scale_b in fp32, the sum held in
+ * fp32 and never rounded before the scales are applied (once, after the K loop), and
+ * the result rounded to bf16 with round-to-nearest-even.
+ *
+ * Conventions shared by every entry point
+ * ----------------------------------------
+ * - Pointers named as device pointers must point to memory the current CUDA device
+ *   can access (device or managed memory).  They are owned by the caller, are only
+ *   read/written by work enqueued on `stream`, and are not retained after the call
+ *   returns.  Every buffer is dense and row-major with the sizes given; strided views
+ *   are not supported (the kernel addresses the output as one flat row-major buffer:
+ *   MSLK #471, commit rejecting a strided output).
+ * - `stream` is a cudaStream_t passed as void*; NULL means the legacy default stream.
+ *   Calls are asynchronous: they enqueue work and return without synchronising.
+ *   No call allocates device memory, so calls may be captured in a CUDA graph once
+ *   the library has been used on that device (the first call on a device performs
+ *   one-time set-up: device query, kernel attributes, driver entry point).
+ * - Sizes are int64_t.  Errors are reported by the return value; nothing is enqueued
+ *   when a call returns anything but MSLKB_OK.  Argument checks happen before any CUDA
+ *   call, so a bad argument is reported even where no GPU is present.
+ * - The library is compiled for sm_103a only; any other device gives MSLKB_ERR_DEVICE.
+ * - Errors found on the device (a wait that timed out, m_sizes that overran total_M)
+ *   cannot be returned by an asynchronous call; they are OR-ed into a per-device status
+ *   word read by mslkb_get_device_status().
+ */
+#ifndef MSLKB_H_
+#define MSLKB_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MSLKB_API __attribute__((visibility("default")))
+#else
+#define MSLKB_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum mslkb_status {
+  MSLKB_OK = 0,
+  MSLKB_ERR_NULL = 1,   /* a pointer needed for the given sizes is NULL */
+  MSLKB_ERR_SHAPE = 2,  /* a size is negative, too large, or N is not a multiple of 8 */
+  MSLKB_ERR_ALIGN = 3,  /* out is not 16-byte aligned */
+  MSLKB_ERR_DEVICE = 4, /* the current device is not sm_103 (GB300 / B300) */
+  MSLKB_ERR_CUDA = 5    /* a CUDA runtime or driver call failed; see mslkb_last_cuda_error */
+} mslkb_status;
+
+/* Bits of the device status word (mslkb_get_device_status). */
+#define MSLKB_DEV_TIMEOUT 0x1u        /* a pipeline wait in the kernel gave up (~1 s)  */
+#define MSLKB_DEV_MSIZES_CLAMPED 0x2u /* m_sizes had a negative entry or summed past total_M */
+
+/* Limits. */
+#define MSLKB_MAX_GROUPS 1024         /* G (kernel keeps per-group tables in shared memory) */
+#define MSLKB_MAX_DIM 2147483647LL    /* every size, and total_M * K, N * K, rows * N ... */
+
+/*
+ * Stacked layout (op f8f8bf16_rowwise_grouped_stacked; MSLK #471, PR Summary table:
+ * "[G] int64 row counts", and the commits on the packed "sizes" layout and its tile
+ * retire guard).
+ *
+ *   A        device, e4m3 codes [total_M, K]      rows of all groups packed along M
+ *   B        device, e4m3 codes [G, N, K]         one [N, K] weight matrix per group
+ *   scale_a  device, fp32 [total_M]               one scale per row of A
+ *   scale_b  device, fp32 [G, N]                  one scale per (group, column)
+ *   m_sizes  device, int64 [G]                    rows per group, in group order
+ *   out      device, bf16 [total_M, N]            16-byte aligned
+ *
+ * Group g owns rows [off_g, off_g + m_g) with off_0 = 0, off_{g+1} = off_g + m_g.
+ * Empty groups own no rows and cost no work.  Each m_g is clamped into
+ * [0, total_M - off_g]; if any entry needed clamping, MSLKB_DEV_MSIZES_CLAMPED is set in
+ * the device status word.  Rows of out past the last group are left untouched.
+ * K = 0 writes +0.0 to every owned row (MSLK #471, commit zeroing an empty reduction).
+ * Any K >= 0 is accepted: when K is a multiple of 16 and A and B are 16-byte aligned
+ * the tiles are fetched by TMA; otherwise a narrower asynchronous copy path is used,
+ * with zero fill past K (MSLK #471, commit on the K tail).
+ * N must be a multiple of 8, the width of one 16-byte bf16 store (MSLK #471, commits on
+ * the N tail and on predicating a store on its last column).
+ */
+MSLKB_API mslkb_status mslkb_f8f8bf16_rowwise_grouped_stacked(
+    const void *A, const void *B, const float *scale_a, const float *scale_b,
+    const int64_t *m_sizes, void *out, int64_t total_M, int64_t G, int64_t N, int64_t K,
+    void *stream);
+
+/*
+ * Dynamic (padded) layout (op f8f8bf16_rowwise_grouped_dynamic; MSLK #471, PR Summary
+ * table: "[G, M, K] slabs, runtime valid-row count", commit adding the padded layout and
+ * commit adding its test: padding rows asserted zero).
+ *
+ *   A                   device, e4m3 codes [G * expected_m, K]   one slab per group
+ *   B                   device, e4m3 codes [G, N, K]
+ *   scale_a             device, fp32 [G * expected_m]
+ *   scale_b             device, fp32 [G, N]
+ *   zero_start_index_M  device, int64 [G]      valid rows at the top of each slab
+ *   out                 device, bf16 [G * expected_m, N], 16-byte aligned
+ *
+ * Group g owns slab rows [g*E, (g+1)*E) with E = expected_m; the first
+ * v_g = min(max(zero_start_index_M[g], 0), E) rows are computed and every other row of
+ * the slab is written +0.0, whatever A and scale_a hold there (the zeroed-output
+ * contract, folded into the kernel so that every output byte is written once).
+ * K and N rules as for the stacked layout.
+ */
+MSLKB_API mslkb_status mslkb_f8f8bf16_rowwise_grouped_dynamic(
+    const void *A, const void *B, const float *scale_a, const float *scale_b,
+    const int64_t *zero_start_index_M, void *out, int64_t G, int64_t expected_m,
+    int64_t N, int64_t K, void *stream);
+
+/* Static description of a status code.  Never NULL. */
+MSLKB_API const char *mslkb_status_string(mslkb_status status);
+
+/* The cudaError_t (as int) behind the last MSLKB_ERR_CUDA returned on this thread. */
+MSLKB_API int mslkb_last_cuda_error(void);
+
+/*
+ * Reads the device status word of the current device and clears it.  Enqueued on
+ * `stream` and then waits for that stream, so it orders after earlier calls on it.
+ * flags: host pointer receiving the MSLKB_DEV_* bits.
+ */
+MSLKB_API mslkb_status mslkb_get_device_status(void *stream, uint32_t *flags);
+
+/*
+ * Kernel variants and the plan the host would choose.  Pure host code: no CUDA call.
+ * layout: 0 = stacked (rows = total_M), 1 = dynamic (rows = expected_m per group).
+ * num_sms: streaming multiprocessors of the target device.
+ * a_align / b_align: the byte alignment of the A and B base addresses (e.g. 256).
+ */
+typedef struct mslkb_plan_info {
+  int32_t variant;      /* index into the variant table, see mslkb_variant_name */
+  int32_t swap_ab;      /* 1: weights take the MMA M side and tokens the N side */
+  int32_t tile_m;       /* activation rows per tile */
+  int32_t tile_n;       /* weight rows (output columns) per tile */
+  int32_t stages;       /* shared-memory pipeline depth */
+  int32_t tma;          /* 1: TMA loads; 0: cp.async loader */
+  int32_t copy_width;   /* bytes per asynchronous copy of the cp.async loader */
+  int32_t grid;         /* persistent CTAs launched */
+  int32_t threads;      /* threads per CTA */
+  int32_t smem_bytes;   /* dynamic shared memory per CTA */
+  int64_t tiles_bound;  /* host upper bound on output tiles */
+} mslkb_plan_info;
+
+MSLKB_API mslkb_status mslkb_plan(int32_t layout, int64_t rows, int64_t G, int64_t N, int64_t K,
+                        int32_t num_sms, int64_t a_align, int64_t b_align,
+                        mslkb_plan_info *info);
+
+/* Number of kernel variants and the name of one (NULL past the end). */
+MSLKB_API int32_t mslkb_num_variants(void);
+MSLKB_API const char *mslkb_variant_name(int32_t variant);
+
+/*
+ * Test hook: force every following call on any thread to use one variant (index from
+ * mslkb_variant_name; -1 restores the heuristic).  A variant that cannot serve a call
+ * (a TMA variant with K % 16 != 0, say) makes that call return MSLKB_ERR_SHAPE.
+ * Used to check that different variants give bit-identical results.
+ */
+MSLKB_API mslkb_status mslkb_force_variant(int32_t variant);
+
+/* Library version, as major * 10000 + minor * 100 + patch. */
+MSLKB_API int32_t mslkb_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MSLKB_H_ */

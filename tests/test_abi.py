@@ -1,0 +1,176 @@
+"""C-ABI checks that need no GPU: the library builds, loads and exports every symbol
+include/mslkb.h declares; argument errors are reported before any CUDA call; the host
+planner picks the intended kernel variant for each workload shape."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import fp8_rowwise_scaled_gb300 as fx
+from fp8_rowwise_scaled_gb300 import build as fxbuild
+from fp8_rowwise_scaled_gb300.synthetic import workloads
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mslkb.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    fxbuild.build()
+    return fx.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"MSLKB_API\s+[\w\s\*]*?\b(mslkb_\w+)\s*\(", text)))
+
+
+def test_header_declares_entry_points():
+    names = declared_functions()
+    assert "mslkb_f8f8bf16_rowwise_grouped_stacked" in names
+    assert "mslkb_f8f8bf16_rowwise_grouped_dynamic" in names
+    assert len(names) >= 10
+
+
+def test_exports_every_declared_symbol(L):
+    for name in declared_functions():
+        assert hasattr(L, name), f"{name} not exported"
+
+
+def test_exports_nothing_else(L):
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", fx.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {ln.split()[-1] for ln in out.splitlines() if " T " in ln}
+    assert exported == set(declared_functions())
+
+
+def test_status_strings(L):
+    for s in range(6):
+        assert fx.mslkb_status_string(s)
+    assert fx.mslkb_status_string(99) == "unknown status"
+    assert fx.mslkb_version() == 10000
+
+
+def _stacked(**kw):
+    a = dict(A=16, B=16, scale_a=16, scale_b=16, m_sizes=16, out=256, total_M=4, G=2, N=8, K=16)
+    a.update(kw)
+    return fx.mslkb_f8f8bf16_rowwise_grouped_stacked(a["A"], a["B"], a["scale_a"], a["scale_b"],
+                                                     a["m_sizes"], a["out"], a["total_M"],
+                                                     a["G"], a["N"], a["K"], 0)
+
+
+def _dynamic(**kw):
+    a = dict(A=16, B=16, scale_a=16, scale_b=16, zsi=16, out=256, G=2, E=4, N=8, K=16)
+    a.update(kw)
+    return fx.mslkb_f8f8bf16_rowwise_grouped_dynamic(a["A"], a["B"], a["scale_a"], a["scale_b"],
+                                                     a["zsi"], a["out"], a["G"], a["E"], a["N"],
+                                                     a["K"], 0)
+
+
+@pytest.mark.parametrize("call", [_stacked, _dynamic], ids=["stacked", "dynamic"])
+def test_argument_errors_before_cuda(L, call):
+    # These return before any CUDA call, so they behave the same with or without a GPU.
+    assert call(N=12) == fx.MSLKB_ERR_SHAPE          # N not a multiple of 8
+    assert call(K=-1) == fx.MSLKB_ERR_SHAPE
+    assert call(G=-1) == fx.MSLKB_ERR_SHAPE
+    assert call(G=fx.MAX_GROUPS + 1) == fx.MSLKB_ERR_SHAPE
+    assert call(N=1 << 33) == fx.MSLKB_ERR_SHAPE     # beyond 32-bit sizes
+    assert call(out=0) == fx.MSLKB_ERR_NULL
+    assert call(scale_a=0) == fx.MSLKB_ERR_NULL
+    assert call(scale_b=0) == fx.MSLKB_ERR_NULL
+    assert call(A=0) == fx.MSLKB_ERR_NULL
+    assert call(B=0) == fx.MSLKB_ERR_NULL
+    assert call(out=264) == fx.MSLKB_ERR_ALIGN       # 8-byte aligned only
+    # nothing owned or written: OK without touching the device
+    assert call(G=0) == fx.MSLKB_OK
+    assert call(N=0) == fx.MSLKB_OK
+    assert call(A=0, B=0, K=0, G=0) == fx.MSLKB_OK
+
+
+def test_argument_errors_layout_specific(L):
+    assert _stacked(total_M=-1) == fx.MSLKB_ERR_SHAPE
+    assert _stacked(total_M=0) == fx.MSLKB_OK
+    assert _stacked(m_sizes=0) == fx.MSLKB_ERR_NULL
+    assert _dynamic(E=-1) == fx.MSLKB_ERR_SHAPE
+    assert _dynamic(E=0) == fx.MSLKB_OK
+    assert _dynamic(zsi=0) == fx.MSLKB_ERR_NULL
+    assert _dynamic(G=1024, E=1 << 22) == fx.MSLKB_ERR_SHAPE  # G * E beyond 32 bits
+    # K = 0 needs no A or B
+    assert _stacked(A=0, B=0, K=0, G=0) == fx.MSLKB_OK
+
+
+def test_variant_table(L):
+    n = fx.mslkb_num_variants()
+    names = [fx.variant_name(i) for i in range(n)]
+    assert all(names) and len(set(names)) == n
+    assert fx.variant_name(n) is None and fx.variant_name(-1) is None
+    for layout in ("stacked", "dynamic"):
+        for v in ("tile128x256_tma", "tile128x128_tma", "swap_w128xa16_tma", "tile128x128_cpasync"):
+            assert f"{layout}_{v}" in names
+    with pytest.raises(fx.MslkbError):
+        fx.mslkb_force_variant(n)
+    fx.mslkb_force_variant(-1)
+
+
+GB300_SMS = 152
+
+
+@pytest.mark.parametrize("name,expect", [
+    ("c0_stacked_small", "stacked_swap_w128xa16_tma"),
+    ("c1_dynamic_tails", "dynamic_tile128x128_cpasync"),
+    ("c2a_dsv3_gate_up", "stacked_tile128x256_tma"),
+    ("c2b_dsv3_down", "stacked_tile128x256_tma"),
+    ("c3_llama70b_m1", "stacked_swap_w128xa16_tma"),
+    ("c3_llama70b_m16", "stacked_swap_w128xa16_tma"),
+    ("c3_llama70b_m128", "stacked_swap_w128xa16_tma"),
+    ("c3_llama70b_m1024", "stacked_swap_w128xa64_tma"),
+    ("c3_llama70b_m8192", "stacked_tile128x256_tma"),
+    ("c4_llama405b", "stacked_tile128x256_tma"),
+])
+def test_plan_per_workload(L, name, expect):
+    wl = workloads()[name]
+    layout = 0 if wl.layout == "stacked" else 1
+    rows = wl.rows if layout == 0 else wl.expected_m
+    info = fx.mslkb_plan(layout, rows, wl.G, wl.N, wl.K, GB300_SMS)
+    assert fx.variant_name(info.variant) == expect
+    assert 1 <= info.grid <= GB300_SMS
+    assert info.smem_bytes <= 232448
+    assert info.threads in (192, 288)
+
+
+def test_plan_copy_width(L):
+    # TMA needs K % 16 == 0 and 16-byte aligned bases; otherwise the copy width follows
+    # the largest of 16 / 8 / 4 / 1 that K and both alignments allow
+    assert fx.mslkb_plan(0, 512, 4, 256, 512, 152).tma == 1
+    i = fx.mslkb_plan(0, 512, 4, 256, 1000, 152)
+    assert (i.tma, i.copy_width) == (0, 8)
+    i = fx.mslkb_plan(0, 512, 4, 256, 512, 152, a_align=8)
+    assert (i.tma, i.copy_width) == (0, 8)
+    assert fx.mslkb_plan(0, 512, 4, 256, 1004, 152).copy_width == 4
+    assert fx.mslkb_plan(0, 512, 4, 256, 1001, 152).copy_width == 1
+    assert fx.mslkb_plan(0, 512, 4, 256, 0, 152).tma == 1
+
+
+def test_plan_forced_variant(L):
+    try:
+        fx.mslkb_force_variant(fx.variant_index("dynamic_tile128x128_tma"))
+        with pytest.raises(fx.MslkbError):   # wrong layout
+            fx.mslkb_plan(0, 512, 4, 256, 512, 152)
+        assert fx.mslkb_plan(1, 128, 4, 256, 512, 152).variant == \
+            fx.variant_index("dynamic_tile128x128_tma")
+        with pytest.raises(fx.MslkbError):   # TMA variant, K not a multiple of 16
+            fx.mslkb_plan(1, 128, 4, 256, 1000, 152)
+    finally:
+        fx.mslkb_force_variant(-1)
+
+
+def test_plan_grid_bounds(L):
+    # tiles bound for stacked: (total_M + nz * (tile_m - 1)) / tile_m * ceil(N / tile_n)
+    i = fx.mslkb_plan(0, 1, 16, 8192, 8192, 152)
+    assert i.tiles_bound == 64 and i.grid == 64
+    i = fx.mslkb_plan(0, 16384, 16, 16384, 16384, 152)
+    assert i.grid == 152 and i.tiles_bound == (16384 + 16 * 127) // 128 * 64
+    i = fx.mslkb_plan(1, 128, 8, 1000, 1000, 152)
+    assert i.tiles_bound == 8 * 1 * 8 and i.grid == 64
