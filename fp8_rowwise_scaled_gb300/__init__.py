@@ -89,6 +89,10 @@ def lib() -> ctypes.CDLL:
             L.mslkb_variant_name.restype = ctypes.c_char_p
             L.mslkb_force_variant.argtypes = [ctypes.c_int32]
             L.mslkb_force_variant.restype = ctypes.c_int
+            L.mslkb_set_accumulation_chunk.argtypes = [ctypes.c_int32]
+            L.mslkb_set_accumulation_chunk.restype = ctypes.c_int
+            L.mslkb_accumulation_chunk.argtypes = []
+            L.mslkb_accumulation_chunk.restype = ctypes.c_int32
             L.mslkb_version.argtypes = []
             L.mslkb_version.restype = ctypes.c_int32
             _lib = L
@@ -152,6 +156,16 @@ def mslkb_force_variant(i: int) -> None:
     s = lib().mslkb_force_variant(i)
     if s != MSLKB_OK:
         raise MslkbError(s, "mslkb_force_variant")
+
+
+def mslkb_set_accumulation_chunk(kblocks: int) -> None:
+    s = lib().mslkb_set_accumulation_chunk(kblocks)
+    if s != MSLKB_OK:
+        raise MslkbError(s, "mslkb_set_accumulation_chunk")
+
+
+def mslkb_accumulation_chunk() -> int:
+    return lib().mslkb_accumulation_chunk()
 
 
 def mslkb_version() -> int:

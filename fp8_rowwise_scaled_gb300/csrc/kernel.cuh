@@ -56,10 +56,11 @@ struct GemmParams {
   int32_t E;               // expected_m (dynamic only)
   int32_t num_kb;          // ceil(K / 128)
   int32_t copy_width;      // cp.async loader: bytes per copy (16, 8, 4) or 1 (byte loads)
+  int32_t kb_per_chunk;    // K blocks the tensor core sums before the epilogue takes over
   uint64_t timeout_ns;     // give-up time of one pipeline wait
 };
 
-template <int kTileN_, int kStages_, bool kSwap_, bool kTma_, bool kDynamic_>
+template <int kTileN_, int kStages_, bool kSwap_, bool kTma_, bool kDynamic_, int kEpiWarps_ = 4>
 struct KernelCfg {
   static constexpr int kTileN = kTileN_;     // MMA N
   static constexpr int kStages = kStages_;
@@ -76,7 +77,10 @@ struct KernelCfg {
   static constexpr int kLoaderThreads = 32 * kLoaderWarps;
   static constexpr int kMmaWarp = kLoaderWarps;
   static constexpr int kEpiWarp0 = kLoaderWarps + 1;
-  static constexpr int kThreads = 32 * (kLoaderWarps + 1 + 4);
+  static constexpr int kEpiWarps = kEpiWarps_;            // 4, or 8 (two per TMEM quadrant)
+  static constexpr int kThreads = 32 * (kLoaderWarps + 1 + kEpiWarps);
+  // accumulator columns one epilogue thread owns (and keeps in fp32 registers)
+  static constexpr int kThreadCols = kSwap ? kTileN : kTileN / (kEpiWarps / 4);
   static constexpr int kAccCols = kTileN;  // fp32 TMEM columns of one accumulator
   static constexpr int kTmemCols = (2 * kAccCols <= 32)    ? 32
                                    : (2 * kAccCols <= 64)  ? 64
@@ -101,6 +105,8 @@ struct KernelCfg {
   static_assert(kStages >= 3, "pipeline depth");
   static_assert(kSmemBytes <= 232448, "shared memory per CTA");
   static_assert(2 * kAccCols <= 512, "two accumulators must fit TMEM");
+  static_assert(kEpiWarps == 4 || (kEpiWarps == 8 && !kSwap), "epilogue warp split");
+  static_assert(kThreadCols % 16 == 0, "TMEM load granularity");
 };
 
 struct TileCoord {
@@ -314,7 +320,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(tfull_bar(b), 1u);
-      ptx::mbar_init(tempty_bar(b), 4u);
+      ptx::mbar_init(tempty_bar(b), static_cast<uint32_t>(Cfg::kEpiWarps));
     }
     *abort_flag = 0u;
     ptx::fence_mbar_init();
@@ -449,53 +455,64 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     }
   } else if (warp == static_cast<uint32_t>(Cfg::kMmaWarp)) {
     // ------------------------------------------------------------------ MMA issuer
+    // The tensor core sums at most kb_per_chunk K blocks into one TMEM chunk buffer
+    // (two buffers, alternating); the epilogue adds every chunk into fp32 registers with
+    // round-to-nearest, so the tensor core's own accumulation only ever spans a chunk.
     if (lane == 0 && has_k) {
       int stage = 0;
       uint32_t phase = 0;
-      int acc = 0;
-      uint32_t acc_phase = 0;
+      uint32_t chunk = 0;  // chunks issued by this CTA: buffer = chunk & 1
       bool ok = true;
+      const int32_t kpc = p.kb_per_chunk;
       for (int32_t t = blockIdx.x; ok && t < sched.total; t += gridDim.x) {
-        if (!wait_bar(tempty_bar(acc), acc_phase ^ 1u, abort_flag, p.status, p.timeout_ns)) break;
-        ptx::tc_fence_after_sync();
-        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * Cfg::kAccCols);
-        for (int32_t kb = 0; kb < p.num_kb; ++kb) {
-          if (!wait_bar(full_bar(stage), phase, abort_flag, p.status, p.timeout_ns)) {
+        for (int32_t kb0 = 0; ok && kb0 < p.num_kb; kb0 += kpc) {
+          const int buf = static_cast<int>(chunk & 1u);
+          const uint32_t use = chunk >> 1;  // how often this buffer was used before
+          if (!wait_bar(tempty_bar(buf), (use & 1u) ^ 1u, abort_flag, p.status, p.timeout_ns)) {
             ok = false;
             break;
           }
           ptx::tc_fence_after_sync();
-          const uint64_t act_desc = ptx::sw128_kmajor_desc(s_act + stage * Cfg::kActBytes);
-          const uint64_t w_desc = ptx::sw128_kmajor_desc(s_w + stage * Cfg::kWBytes);
-          const uint64_t a_desc = Cfg::kSwap ? w_desc : act_desc;
-          const uint64_t b_desc = Cfg::kSwap ? act_desc : w_desc;
+          const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * Cfg::kAccCols);
+          const int32_t kb1 = min(p.num_kb, kb0 + kpc);
+          for (int32_t kb = kb0; kb < kb1; ++kb) {
+            if (!wait_bar(full_bar(stage), phase, abort_flag, p.status, p.timeout_ns)) {
+              ok = false;
+              break;
+            }
+            ptx::tc_fence_after_sync();
+            const uint64_t act_desc = ptx::sw128_kmajor_desc(s_act + stage * Cfg::kActBytes);
+            const uint64_t w_desc = ptx::sw128_kmajor_desc(s_w + stage * Cfg::kWBytes);
+            const uint64_t a_desc = Cfg::kSwap ? w_desc : act_desc;
+            const uint64_t b_desc = Cfg::kSwap ? act_desc : w_desc;
 #pragma unroll
-          for (int k = 0; k < kBK / 32; ++k) {
-            // advance 32 bytes of K inside the 128-byte swizzled row: +2 in 16-byte units
-            ptx::mma_f8f6f4(d_tmem, a_desc + 2u * k, b_desc + 2u * k, Cfg::kIdesc,
-                            (kb > 0 || k > 0) ? 1u : 0u);
+            for (int k = 0; k < kBK / 32; ++k) {
+              // advance 32 bytes of K inside the 128-byte swizzled row: +2 in 16-byte units
+              ptx::mma_f8f6f4(d_tmem, a_desc + 2u * k, b_desc + 2u * k, Cfg::kIdesc,
+                              (kb > kb0 || k > 0) ? 1u : 0u);
+            }
+            ptx::mma_commit(empty_bar(stage));
+            if (++stage == Cfg::kStages) {
+              stage = 0;
+              phase ^= 1u;
+            }
           }
-          ptx::mma_commit(empty_bar(stage));
-          if (++stage == Cfg::kStages) {
-            stage = 0;
-            phase ^= 1u;
-          }
+          if (!ok) break;
+          ptx::mma_commit(tfull_bar(buf));
+          ++chunk;
         }
-        if (!ok) break;
-        ptx::mma_commit(tfull_bar(acc));
-        acc ^= 1;
-        if (acc == 0) acc_phase ^= 1u;
       }
     }
     __syncwarp();
   } else {
     // ------------------------------------------------------------------ epilogue
-    const uint32_t q = warp & 3u;           // TMEM lane quadrant this warp may access
+    const uint32_t q = warp & 3u;  // TMEM lane quadrant this warp may access
     const uint32_t ew = warp - Cfg::kEpiWarp0;
+    const int32_t col_base = static_cast<int32_t>(ew >> 2) * Cfg::kThreadCols;  // column slice
     if constexpr (Cfg::kDynamic) {
       // rows of each slab past its last computed tile: pure padding, written +0.0
-      const int32_t gw = blockIdx.x * 4 + ew;
-      const int32_t nw = gridDim.x * 4;
+      const int32_t gw = blockIdx.x * Cfg::kEpiWarps + ew;
+      const int32_t nw = gridDim.x * Cfg::kEpiWarps;
       for (int32_t g = 0; g < p.G; ++g) {
         const int32_t v = rowinfo[g];
         const int32_t covered = ((v + Cfg::kActRows - 1) / Cfg::kActRows) * Cfg::kActRows;
@@ -508,50 +525,85 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         }
       }
     }
-    int acc = 0;
-    uint32_t acc_phase = 0;
-    for (int32_t t = blockIdx.x; t < sched.total; t += gridDim.x) {
+    uint32_t chunk = 0;
+    bool ok = true;
+    const int32_t kpc = p.kb_per_chunk;
+    for (int32_t t = blockIdx.x; ok && t < sched.total; t += gridDim.x) {
       TileCoord c = decode_tile<Cfg>(sched, t);
       // an empty reduction (K = 0) writes +0.0 to every owned row, whatever the scales
       if (!has_k) c.valid_end = c.m0;
-      if (has_k) {
-        if (!wait_bar(tfull_bar(acc), acc_phase, abort_flag, p.status, p.timeout_ns)) break;
-        ptx::tc_fence_after_sync();
-      }
-      const uint32_t t_acc =
-          tmem_base + ((32u * q) << 16) + static_cast<uint32_t>(acc * Cfg::kAccCols);
+      // fp32 accumulator of this thread (round-to-nearest adds of the TMEM chunks)
+      float acc[Cfg::kThreadCols];
+#pragma unroll
+      for (int j = 0; j < Cfg::kThreadCols; ++j) acc[j] = 0.0f;
+      // TMEM data is needed only when this warp's lanes hold rows with computed values
+      bool warp_any;
       if constexpr (!Cfg::kSwap) {
-        // thread = one activation row; 32 output columns per TMEM load
+        warp_any = c.m0 + static_cast<int32_t>(32u * q) < c.valid_end;  // lane 0's row
+      } else {
+        warp_any = c.n0 + static_cast<int32_t>(32u * q) < p.N && c.m0 < c.valid_end;
+      }
+      if (has_k) {
+        for (int32_t kb0 = 0; kb0 < p.num_kb; kb0 += kpc) {
+          const int buf = static_cast<int>(chunk & 1u);
+          const uint32_t use = chunk >> 1;
+          if (!wait_bar(tfull_bar(buf), use & 1u, abort_flag, p.status, p.timeout_ns)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after_sync();
+          if (warp_any) {
+            const uint32_t t_buf = tmem_base + ((32u * q) << 16) +
+                                   static_cast<uint32_t>(buf * Cfg::kAccCols + col_base);
+            if constexpr (Cfg::kThreadCols % 32 == 0) {
+#pragma unroll
+              for (int pc = 0; pc < Cfg::kThreadCols / 32; ++pc) {
+                uint32_t v[32];
+                ptx::tmem_ld_x32(t_buf + static_cast<uint32_t>(pc * 32), v);
+                ptx::tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) acc[pc * 32 + j] += __uint_as_float(v[j]);
+              }
+            } else {
+#pragma unroll
+              for (int pc = 0; pc < Cfg::kThreadCols / 16; ++pc) {
+                uint32_t v[16];
+                ptx::tmem_ld_x16(t_buf + static_cast<uint32_t>(pc * 16), v);
+                ptx::tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 16; ++j) acc[pc * 16 + j] += __uint_as_float(v[j]);
+              }
+            }
+          }
+          ptx::tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(tempty_bar(buf));
+          ++chunk;
+        }
+        if (!ok) break;
+      }
+      if constexpr (!Cfg::kSwap) {
+        // thread = one activation row; 8 output columns per 16-byte store
         const int32_t R = c.m0 + static_cast<int32_t>(32u * q + lane);
         const bool row_val = R < c.valid_end;
         const bool row_zero = !row_val && R < c.zero_end;
-        const bool warp_any =
-            __any_sync(0xffffffffu, row_val || row_zero);
-        const float sa = row_val ? __ldg(p.scale_a + R) : 0.0f;
-        const float* sb_g = p.scale_b + static_cast<size_t>(c.g) * p.N;
-        uint16_t* orow = p.out + static_cast<size_t>(row_val || row_zero ? R : 0) * p.N;
-        if (warp_any) {
-#pragma unroll 1
-          for (int cc = 0; cc < Cfg::kTileN / 32; ++cc) {
-            const int32_t col0 = c.n0 + cc * 32;
+        if (__any_sync(0xffffffffu, row_val || row_zero)) {
+          const float sa = row_val ? __ldg(p.scale_a + R) : 0.0f;
+          const float* sb_g = p.scale_b + static_cast<size_t>(c.g) * p.N;
+          uint16_t* orow = p.out + static_cast<size_t>(row_val || row_zero ? R : 0) * p.N;
+#pragma unroll
+          for (int pc = 0; pc < Cfg::kThreadCols / 32; ++pc) {
+            const int32_t col0 = c.n0 + col_base + pc * 32;
             // lane j holds scale_b of column col0 + j; broadcast by shuffle below
             const float sb_l = (col0 + static_cast<int32_t>(lane) < p.N)
                                    ? __ldg(sb_g + col0 + lane) : 0.0f;
-            uint32_t v[32];
-            if (has_k) {
-              ptx::tmem_ld_x32(t_acc + static_cast<uint32_t>(cc * 32), v);
-              ptx::tmem_ld_wait();
-            } else {
-#pragma unroll
-              for (int j = 0; j < 32; ++j) v[j] = 0u;
-            }
 #pragma unroll
             for (int j8 = 0; j8 < 4; ++j8) {
               float y[8];
 #pragma unroll
               for (int j = 0; j < 8; ++j) {
                 const float sb = __shfl_sync(0xffffffffu, sb_l, j8 * 8 + j);
-                y[j] = (__uint_as_float(v[j8 * 8 + j]) * sa) * sb;
+                y[j] = (acc[pc * 32 + j8 * 8 + j] * sa) * sb;
               }
               const int32_t col = col0 + j8 * 8;
               if (col + 7 < p.N) {
@@ -567,37 +619,25 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
           }
         }
       } else {
-        // thread = one weight row (output column n); TMEM columns are activation rows
+        // thread = one weight row (output column n); accumulator columns are activation rows
         const int32_t n = c.n0 + static_cast<int32_t>(32u * q + lane);
         const bool col_ok = n < p.N;
         const float sb = col_ok ? __ldg(p.scale_b + static_cast<size_t>(c.g) * p.N + n) : 0.0f;
-#pragma unroll 1
-        for (int cc = 0; cc < (Cfg::kTileN + 31) / 32; ++cc) {
+#pragma unroll
+        for (int pc = 0; pc < (Cfg::kTileN + 31) / 32; ++pc) {
           constexpr int kCols = Cfg::kTileN < 32 ? Cfg::kTileN : 32;
-          const int32_t m_first = c.m0 + cc * 32;
+          const int32_t m_first = c.m0 + pc * 32;
           if (m_first >= c.zero_end) break;
           // lane j holds scale_a of row m_first + j
           const int32_t Rl = m_first + static_cast<int32_t>(lane);
           const float sa_l = (lane < static_cast<uint32_t>(kCols) && Rl < c.valid_end)
                                  ? __ldg(p.scale_a + Rl) : 0.0f;
-          uint32_t v[kCols];
-          if (has_k) {
-            if constexpr (kCols == 16) {
-              ptx::tmem_ld_x16(t_acc, v);
-            } else {
-              ptx::tmem_ld_x32(t_acc + static_cast<uint32_t>(cc * 32), v);
-            }
-            ptx::tmem_ld_wait();
-          } else {
-#pragma unroll
-            for (int j = 0; j < kCols; ++j) v[j] = 0u;
-          }
 #pragma unroll
           for (int j = 0; j < kCols; ++j) {
             const float sa = __shfl_sync(0xffffffffu, sa_l, j);
             const int32_t R = m_first + j;
             if (R < c.valid_end) {
-              const float y = (__uint_as_float(v[j]) * sa) * sb;
+              const float y = (acc[pc * 32 + j] * sa) * sb;
               if (col_ok)
                 p.out[static_cast<size_t>(R) * p.N + n] =
                     __bfloat16_as_ushort(__float2bfloat16_rn(y));
@@ -606,13 +646,6 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
             }
           }
         }
-      }
-      if (has_k) {
-        ptx::tc_fence_before_sync();
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(tempty_bar(acc));
-        acc ^= 1;
-        if (acc == 0) acc_phase ^= 1u;
       }
     }
   }

@@ -32,6 +32,10 @@ __device__ uint32_t g_device_status;  // MSLKB_DEV_* bits, per device
 
 thread_local int t_last_cuda_error = 0;
 std::atomic<int> g_forced_variant{-1};
+// K blocks (of 128) the tensor core accumulates before the epilogue adds the partial sum
+// into round-to-nearest fp32 registers; 0 = the whole K in the tensor core.
+constexpr int kDefaultKbPerChunk = 4;
+std::atomic<int> g_kb_per_chunk{kDefaultKbPerChunk};
 
 // ---------------------------------------------------------------------------------
 // variant table: stacked TMA, dynamic TMA, cp.async (both layouts)
@@ -312,6 +316,10 @@ mslkb_status run(int layout, const void* A, const void* B, const float* scale_a,
   p.E = static_cast<int32_t>(E);
   p.num_kb = static_cast<int32_t>(ceil_div(K, mslkb::kBK));
   p.copy_width = info.copy_width;
+  {
+    const int kpc = g_kb_per_chunk.load();
+    p.kb_per_chunk = (kpc <= 0 || kpc > p.num_kb) ? (p.num_kb > 0 ? p.num_kb : 1) : kpc;
+  }
   p.timeout_ns = kWaitTimeoutNs;
   if ((s = encode_maps(&la, v, A, B, rows, G, N, K)) != MSLKB_OK) return s;
   la.grid = dim3(static_cast<unsigned>(info.grid), 1, 1);
@@ -400,6 +408,14 @@ mslkb_status mslkb_force_variant(int32_t i) {
   g_forced_variant.store(i);
   return MSLKB_OK;
 }
+
+mslkb_status mslkb_set_accumulation_chunk(int32_t kblocks) {
+  if (kblocks < 0) return MSLKB_ERR_SHAPE;
+  g_kb_per_chunk.store(kblocks);
+  return MSLKB_OK;
+}
+
+int32_t mslkb_accumulation_chunk(void) { return g_kb_per_chunk.load(); }
 
 int32_t mslkb_version(void) { return kVersion; }
 

@@ -120,7 +120,8 @@ MSLKB_API mslkb_status mslkb_f8f8bf16_rowwise_grouped_dynamic(
 /* Static description of a status code.  Never NULL. */
 MSLKB_API const char *mslkb_status_string(mslkb_status status);
 
-/* The cudaError_t (as int) behind the last MSLKB_ERR_CUDA returned on this thread. */
+/* The cudaError_t (or, for a failed tensor-map encode, the CUresult) behind the last
+ * MSLKB_ERR_CUDA returned on this thread. */
 MSLKB_API int mslkb_last_cuda_error(void);
 
 /*
@@ -165,6 +166,19 @@ MSLKB_API const char *mslkb_variant_name(int32_t variant);
  * Used to check that different variants give bit-identical results.
  */
 MSLKB_API mslkb_status mslkb_force_variant(int32_t variant);
+
+/*
+ * Accumulation chunk.  The tensor core's own fp32 accumulation adds with round-toward-
+ * zero; over a long K with cancelling partial sums that bias exceeds the tolerance of
+ * 1e-6 * sum|terms|.  So the kernel lets the tensor core sum at most `kblocks` blocks of
+ * 128 K elements into one TMEM buffer, and its epilogue adds each such partial sum into
+ * fp32 registers with round-to-nearest (the accumulator is still fp32 and is never
+ * rounded to a narrower type before the scales are applied).  Default 4 (512 K elements);
+ * 0 lets the tensor core accumulate the whole K.  Applies to every following call from
+ * any thread; a tuning and test hook.  Negative values give MSLKB_ERR_SHAPE.
+ */
+MSLKB_API mslkb_status mslkb_set_accumulation_chunk(int32_t kblocks);
+MSLKB_API int32_t mslkb_accumulation_chunk(void);
 
 /* Library version, as major * 10000 + minor * 100 + patch. */
 MSLKB_API int32_t mslkb_version(void);

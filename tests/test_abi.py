@@ -101,6 +101,18 @@ def test_argument_errors_layout_specific(L):
     assert _stacked(A=0, B=0, K=0, G=0) == fx.MSLKB_OK
 
 
+def test_accumulation_chunk_setting(L):
+    old = fx.mslkb_accumulation_chunk()
+    assert old == 4
+    try:
+        fx.mslkb_set_accumulation_chunk(0)
+        assert fx.mslkb_accumulation_chunk() == 0
+        with pytest.raises(fx.MslkbError):
+            fx.mslkb_set_accumulation_chunk(-1)
+    finally:
+        fx.mslkb_set_accumulation_chunk(old)
+
+
 def test_variant_table(L):
     n = fx.mslkb_num_variants()
     names = [fx.variant_name(i) for i in range(n)]
@@ -137,7 +149,7 @@ def test_plan_per_workload(L, name, expect):
     assert fx.variant_name(info.variant) == expect
     assert 1 <= info.grid <= GB300_SMS
     assert info.smem_bytes <= 232448
-    assert info.threads in (192, 288)
+    assert info.threads in (192, 288, 320)
 
 
 def test_plan_copy_width(L):

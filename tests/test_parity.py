@@ -294,6 +294,20 @@ def test_accumulator_cancellation(orc):
         _check_full(prob, orc, variant=v, what=f"cancellation {v}")
 
 
+@pytest.mark.parametrize("kpc", [0, 1, 3, 4, 32])
+def test_accumulation_chunk_lengths(orc, kpc):
+    """Every chunk length (0 = the whole K in the tensor core) stays within tolerance on
+    random data, including a K whose last chunk is partial."""
+    prob = _rand_problem("stacked", 3, 264, 128 * 13 + 64, [150, 0, 77], seed=21)
+    old = fx.mslkb_accumulation_chunk()
+    try:
+        fx.mslkb_set_accumulation_chunk(kpc)
+        for v in ("stacked_tile128x256_tma", "stacked_swap_w128xa32_tma"):
+            _check_full(prob, orc, variant=v, what=f"chunk {kpc} {v}")
+    finally:
+        fx.mslkb_set_accumulation_chunk(old)
+
+
 def test_cuda_graph_replay(orc):
     prob = _rand_problem("stacked", 4, 256, 512, [64, 0, 100, 3], seed=19)
     eager = bits_of(prob.run_gpu())
