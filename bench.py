@@ -1,0 +1,502 @@
+"""Benchmark of the FP8 rowwise-scaled grouped GEMM on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gemm|reference]
+                    [--workload NAME] [--no-sweep] [--no-cpu]
+
+One step = one call of the whole hot path (host checks and planning, the device group
+scheduler, the TMA/tcgen05 pipeline and the fused epilogue) on one batch of seeded
+synthetic input resident in HBM.  Prints ONE JSON line (rank 0).
+
+Headline workload: the largest single-GPU configuration, llama3-405b-shaped stacked
+G=16, N=K=total_M=16384 (inputs 5.1 GB, larger than L2, so no flush is needed).  The
+metric is FP8 grouped GEMM TFLOPS (2 * sum_g m_g * N * K per call); the line also carries
+us/call, the roofline fraction, the end-to-end figure through host buffers, the CPU
+oracle baseline, the SM clocks seen, and a per-shape sweep of the other shapes
+(DS-V3 gate_up/down, llama3-70b total_M in {1, 16, 128, 1024, 8192}) timed by CUDA-graph
+replay with rotating input sets sized past twice the L2.
+
+--impl reference times the CPU oracle (the plain fp64 C reference) on the same workload,
+one bounded row sample per step, on the host cores.
+
+Multi-GPU (torchrun, one rank per GPU): every rank runs the same workload on its own GPU
+(independent replicas, no collective on the data path); the time is the max over ranks
+and the value is the work of all ranks divided by it ("weak" scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "FP8 grouped GEMM TFLOPS, µs/call, % of roofline (FP8 peak or HBM) per shape"
+UNIT = "TFLOPS"
+HEADLINE = "c4_llama405b"
+SWEEP = ["c2a_dsv3_gate_up", "c2b_dsv3_down", "c3_llama70b_m1", "c3_llama70b_m16",
+         "c3_llama70b_m128", "c3_llama70b_m1024", "c3_llama70b_m8192"]
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+FP8_OVER_BF16 = 2.0  # nominal dense ratio (4.5 / 2.25 PFLOP/s)
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return json.load(f), "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "fp8_rowwise_scaled_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def dram_traffic(workload: str):
+    """Per-launch DRAM bytes from a committed ncu capture, if it was taken on the current
+    kernel source; else None."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(workload)
+    if not e or e.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while the timed region runs."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.file = None
+
+    def __enter__(self):
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        self.file.flush()
+
+    def summary(self):
+        try:
+            with open(self.file.name) as f:
+                rows = [ln.strip().split(", ") for ln in f if ln.strip()]
+            os.unlink(self.file.name)
+        except OSError:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"]}
+        sm, mx, pw, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+                pw.append(float(r[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"]}
+        loaded = [s for s, p in zip(sm, pw) if p > 0.3 * max(pw)] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm), "power_w_max": max(pw)}
+
+
+# ---------------------------------------------------------------------------------------
+# distributed plumbing (replicas; the barrier and max-over-ranks timing only)
+# ---------------------------------------------------------------------------------------
+def dist_setup(backend):
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group(backend)
+    return rank, local, ws
+
+
+def dist_max(value: float, ws: int, device):
+    if ws == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def dist_barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------------------
+# CPU oracle timing (the reference arm and the cpu_baseline field)
+# ---------------------------------------------------------------------------------------
+def oracle_sample_inputs(wl, rows: int, seed: int):
+    """A bounded sample of the workload on the host: `rows` activation rows against one
+    group's full [N, K] weights (the work of `rows` output rows of the workload)."""
+    import numpy as np
+    import torch
+    from fp8_rowwise_scaled_gb300.synthetic import quantize_rows
+    g = torch.Generator().manual_seed(seed)
+    A, sa = quantize_rows(torch.randn((rows, wl.K), generator=g))
+    B = torch.empty((1, wl.N, wl.K), dtype=torch.uint8)
+    sb = torch.empty((1, wl.N), dtype=torch.float32)
+    step = 4096
+    for n0 in range(0, wl.N, step):
+        q, s = quantize_rows(torch.randn((min(step, wl.N - n0), wl.K), generator=g))
+        B[0, n0:n0 + q.shape[0]] = q
+        sb[0, n0:n0 + q.shape[0]] = s
+    return (A.numpy(), B.numpy(), sa.numpy(), sb.numpy(), np.array([rows], np.int64))
+
+
+def time_oracle(wl, rows: int, reps: int = 1, warm: int = 0, seed: int = 7):
+    import oracle
+    orc = oracle.load(0)
+    A, B, sa, sb, meta = oracle_sample_inputs(wl, rows, seed)
+    threads = len(os.sched_getaffinity(0))
+    for _ in range(warm):
+        orc.stacked(A, B, sa, sb, meta, threads=threads)
+    times = []
+    for _ in range(reps):
+        t0 = time.perf_counter()
+        orc.stacked(A, B, sa, sb, meta, threads=threads)
+        times.append(time.perf_counter() - t0)
+    flops = 2.0 * rows * wl.N * wl.K
+    return flops, times, threads
+
+
+# ---------------------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------------------
+def run_call(fx, inp, out, wl, stream_ptr):
+    if wl.layout == "stacked":
+        s = fx.mslkb_f8f8bf16_rowwise_grouped_stacked(
+            inp["A"].data_ptr(), inp["B"].data_ptr(), inp["scale_a"].data_ptr(),
+            inp["scale_b"].data_ptr(), inp["meta"].data_ptr(), out.data_ptr(), wl.rows, wl.G,
+            wl.N, wl.K, stream_ptr)
+    else:
+        s = fx.mslkb_f8f8bf16_rowwise_grouped_dynamic(
+            inp["A"].data_ptr(), inp["B"].data_ptr(), inp["scale_a"].data_ptr(),
+            inp["scale_b"].data_ptr(), inp["meta"].data_ptr(), out.data_ptr(), wl.G,
+            wl.expected_m, wl.N, wl.K, stream_ptr)
+    if s != 0:
+        raise fx.MslkbError(s, wl.name)
+
+
+def roofline_times(wl, pk):
+    """(t_fp8, t_hbm) in seconds for one call at the measured (burst) peaks."""
+    fp8 = pk["bf16_tflops"] * FP8_OVER_BF16 * 1e12
+    return wl.flops() / fp8, wl.bytes() / (pk["hbm_gbs"] * 1e9)
+
+
+def plan_for(fx, wl, sms):
+    return fx.mslkb_plan(0 if wl.layout == "stacked" else 1,
+                         wl.rows if wl.layout == "stacked" else wl.expected_m, wl.G, wl.N,
+                         wl.K, sms)
+
+
+def sweep_shape(fx, wl, pk, device):
+    """us/call of one shape by CUDA-graph replay (median of 7), rotating input sets so
+    the data touched by one replay cycle exceeds twice the L2."""
+    import torch
+    from fp8_rowwise_scaled_gb300.synthetic import make_inputs
+    ws_bytes = max(1, wl.bytes())
+    n_sets = max(1, min(16, math.ceil(2 * L2_BYTES / ws_bytes)))
+    base = make_inputs(wl, device)
+    sets = [base] + [{k: v.clone() for k, v in base.items()} for _ in range(n_sets - 1)]
+    outs = [torch.empty((wl.rows, wl.N), dtype=torch.bfloat16, device=device) for _ in sets]
+    stream = torch.cuda.Stream(device=device)
+    sp = stream.cuda_stream
+    with torch.cuda.stream(stream):
+        t_end = time.perf_counter() + 0.5  # clock ramp
+        while time.perf_counter() < t_end:
+            for i in range(n_sets):
+                run_call(fx, sets[i], outs[i], wl, sp)
+            stream.synchronize()
+    # calls per replay: enough for ~2 ms of work, a multiple of the set count
+    t_est = max(roofline_times(wl, pk)) * 1.5 + 3e-6
+    reps = max(1, min(200, int(2e-3 / t_est) // n_sets)) * n_sets
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for r in range(reps):
+            i = r % n_sets
+            run_call(fx, sets[i], outs[i], wl, sp)
+    times = []
+    for _ in range(8):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        graph.replay()
+        e1.record(stream)
+        e1.synchronize()
+        times.append(e0.elapsed_time(e1) * 1e3 / reps)  # us per call
+    us = statistics.median(times[1:])
+    t_fp8, t_hbm = roofline_times(wl, pk)
+    t_roof = max(t_fp8, t_hbm)
+    plan = plan_for(fx, wl, torch.cuda.get_device_properties(device).multi_processor_count)
+    res = {
+        "workload": wl.name, "us_per_call": round(us, 3),
+        "tflops": round(wl.flops() / (us * 1e-6) / 1e12, 2),
+        "gbs": round(wl.bytes() / (us * 1e-6) / 1e9, 1),
+        "bound": "tensor" if t_fp8 >= t_hbm else "hbm",
+        "roofline_frac": round(t_roof / (us * 1e-6), 4),
+        "frac_of_fp8_peak": round(t_fp8 / (us * 1e-6), 4),
+        "frac_of_hbm": round(t_hbm / (us * 1e-6), 4),
+        "variant": fx.variant_name(plan.variant), "grid": plan.grid,
+        "input_sets": n_sets, "calls_per_replay": reps,
+        "nonempty_groups": wl.nonempty_groups(),
+    }
+    del graph, sets, outs, base
+    torch.cuda.empty_cache()
+    return res
+
+
+def gpu_arm(args):
+    import torch
+    rank, local, ws = dist_setup("nccl")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    import fp8_rowwise_scaled_gb300 as fx
+    from fp8_rowwise_scaled_gb300 import build as fxbuild
+    from fp8_rowwise_scaled_gb300.synthetic import make_inputs, workloads
+    fxbuild.build()
+    fx.lib()
+    if args.chunk is not None:
+        fx.mslkb_set_accumulation_chunk(args.chunk)
+    pk, pk_kind = peaks()
+    wl = workloads()[args.workload]
+    inp = make_inputs(wl, device)
+    out = torch.empty((wl.rows, wl.N), dtype=torch.bfloat16, device=device)
+    stream = torch.cuda.Stream(device=device)
+    sp = stream.cuda_stream
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    plan = plan_for(fx, wl, sms)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        # clock ramp (0.5 s), then the untimed warm-up steps
+        t_end = time.perf_counter() + 0.5
+        while time.perf_counter() < t_end:
+            run_call(fx, inp, out, wl, sp)
+            stream.synchronize()
+        e0.record(stream)
+        for _ in range(args.warmup):
+            run_call(fx, inp, out, wl, sp)
+        e1.record(stream)
+        e1.synchronize()
+        t_call = e0.elapsed_time(e1) / 1e3 / max(1, args.warmup)
+        steps = args.steps if args.steps is not None else max(20, math.ceil(1.5 / max(t_call, 1e-6)))
+        stream.synchronize()
+        dist_barrier(ws)
+        torch.cuda.synchronize()
+        with ClockSampler(local) as clk:
+            e0.record(stream)
+            for _ in range(steps):
+                run_call(fx, inp, out, wl, sp)
+            e1.record(stream)
+            e1.synchronize()
+        torch.cuda.synchronize()
+        dist_barrier(ws)
+    t_total = e0.elapsed_time(e1) / 1e3
+    t_max = dist_max(t_total, ws, device)
+    ms_per_step = t_max / steps * 1e3
+    value = ws * wl.flops() * steps / t_max / 1e12
+    status = fx.device_status(stream)
+
+    # roofline of the one kernel launched per step (per-launch time = per-step time)
+    t_launch = t_total / steps
+    t_fp8, t_hbm = roofline_times(wl, pk)
+    if t_fp8 >= t_hbm:
+        peak = pk["bf16_tflops"] * FP8_OVER_BF16
+        roof = {"bound": "tensor", "achieved": round(wl.flops() / t_launch / 1e12, 2),
+                "peak": round(peak, 1), "unit": "TFLOP/s",
+                "peak_source": f"{pk_kind} bf16 burst {pk['bf16_tflops']} TFLOP/s x "
+                               f"{FP8_OVER_BF16:g} (nominal fp8/bf16 dense ratio)"}
+    else:
+        roof = {"bound": "hbm", "achieved": round(wl.bytes() / t_launch / 1e9, 1),
+                "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "peak_source": f"{pk_kind} copy bandwidth"}
+    roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
+    roof["traffic"] = dram_traffic(wl.name)
+    roof["algorithmic"] = {"flops": wl.flops(), "bytes": wl.bytes()}
+    roof["kernel"] = fx.variant_name(plan.variant)
+
+    # end to end through the C ABI with host buffers: H2D inputs, call, D2H result
+    host = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in inp.items()}
+    for k in inp:
+        host[k].copy_(inp[k])
+    host_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    dev = {k: torch.empty_like(v) for k, v in inp.items()}
+    e2e_steps = max(3, min(steps, 10))
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = host_out.numel() * host_out.element_size()
+    with torch.cuda.stream(stream):
+        for k in dev:  # one untimed round
+            dev[k].copy_(host[k], non_blocking=True)
+        run_call(fx, dev, out, wl, sp)
+        host_out.copy_(out, non_blocking=True)
+        stream.synchronize()
+        dist_barrier(ws)
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            for k in dev:
+                dev[k].copy_(host[k], non_blocking=True)
+            run_call(fx, dev, out, wl, sp)
+            host_out.copy_(out, non_blocking=True)
+        e1.record(stream)
+        e1.synchronize()
+        dist_barrier(ws)
+    t_e2e = dist_max(e0.elapsed_time(e1) / 1e3, ws, device)
+    e2e = {"value": round(ws * wl.flops() * e2e_steps / t_e2e / 1e12, 3), "unit": UNIT,
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+           "ms_per_step": round(t_e2e / e2e_steps * 1e3, 3), "steps": e2e_steps}
+    del host, dev, host_out
+
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": ws,
+        "steps": steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3 x e4m3 -> fp32 accumulate -> bf16", "data": "synthetic",
+        "config": {"workload": wl.name, "layout": wl.layout, "G": wl.G, "N": wl.N, "K": wl.K,
+                   "total_M": wl.rows, "m_sizes": list(wl.meta), "seed": wl.seed,
+                   "us_per_call": round(ms_per_step * 1e3, 2),
+                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
+                   "l2": f"inputs larger than L2 ({wl.bytes() / 1e9:.2f} GB per call), no flush",
+                   "variant": fx.variant_name(plan.variant), "grid": plan.grid,
+                   "accumulation_chunk_kblocks": fx.mslkb_accumulation_chunk()},
+        "roofline": roof,
+        "e2e": e2e,
+        "gpu_launches": steps,
+        "clocks": clk.summary(),
+        "device_status": status,
+    }
+    if args.sweep and rank == 0:
+        shapes = []
+        for name in SWEEP:
+            try:
+                shapes.append(sweep_shape(fx, workloads()[name], pk, device))
+            except Exception as e:  # noqa: BLE001 - report and continue
+                shapes.append({"workload": name, "error": repr(e)})
+        shapes.append({"workload": wl.name, "us_per_call": round(ms_per_step * 1e3, 2),
+                       "tflops": round(value / ws, 2), "roofline_frac": roof["frac"],
+                       "bound": roof["bound"], "variant": fx.variant_name(plan.variant)})
+        result["per_shape"] = shapes
+    if args.cpu and rank == 0 and ws == 1:
+        rows = args.cpu_rows
+        flops, times, threads = time_oracle(wl, rows)
+        result["cpu_baseline"] = {
+            "value": round(flops / times[0] / 1e12, 6), "unit": UNIT, "cores": threads,
+            "kind": "oracle", "seconds": round(times[0], 2),
+            "sample": f"{rows} output rows x N={wl.N} x K={wl.K} of {wl.name} (one group's "
+                      f"weights), plain fp64 C oracle, OpenMP over rows"}
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def reference_arm(args):
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from fp8_rowwise_scaled_gb300.synthetic import workloads
+    wl = workloads()[args.workload]
+    import oracle
+    oracle.build()
+    steps = args.steps if args.steps is not None else 5
+    cores = len(os.sched_getaffinity(0))
+    # size each step's row sample so the whole run stays near two minutes: probe one
+    # row per core, then scale (at least one row per core, at most --cpu-rows)
+    _, probe, _ = time_oracle(wl, cores)
+    budget = 120.0 / (steps + args.warmup)
+    rows = cores * max(1, int(budget / max(probe[0], 1e-3)))
+    rows = max(1, min(rows, args.cpu_rows))
+    flops, times, threads = time_oracle(wl, rows, reps=steps, warm=args.warmup)
+    total = sum(times)
+    value = flops * steps / total / 1e12
+    result = {
+        "metric": METRIC, "value": round(value, 6), "unit": UNIT, "n_gpus": ws, "steps": steps,
+        "warmup": args.warmup, "ms_per_step": round(total / steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64 (exact e4m3 products, correctly rounded bf16)", "data": "synthetic",
+        "impl": "reference",
+        "config": {"workload": wl.name, "layout": wl.layout, "G": wl.G, "N": wl.N, "K": wl.K,
+                   "total_M": wl.rows},
+        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": threads,
+                         "kind": "oracle",
+                         "sample": f"per step {rows} output rows x N={wl.N} x K={wl.K} of "
+                                   f"{wl.name} (one group's weights)"},
+        "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(result), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default: enough for >= 1.5 s of kernel time)")
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["gemm", "reference"], default="gemm")
+    ap.add_argument("--workload", default=HEADLINE)
+    ap.add_argument("--chunk", type=int, default=None,
+                    help="tensor-core accumulation chunk in K blocks (default: library's)")
+    ap.add_argument("--no-sweep", dest="sweep", action="store_false")
+    ap.add_argument("--no-cpu", dest="cpu", action="store_false")
+    ap.add_argument("--cpu-rows", type=int, default=256,
+                    help="output rows of the CPU oracle sample")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        reference_arm(args)
+    else:
+        gpu_arm(args)
+
+
+if __name__ == "__main__":
+    main()
