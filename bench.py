@@ -263,14 +263,15 @@ def sweep_shape(fx, wl, pk, device):
             i = r % n_sets
             run_call(fx, sets[i], outs[i], wl, sp)
     times = []
-    for _ in range(8):
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        graph.replay()
-        e1.record(stream)
-        e1.synchronize()
-        times.append(e0.elapsed_time(e1) * 1e3 / reps)  # us per call
+    with torch.cuda.stream(stream):  # replay() launches on the current stream
+        for _ in range(8):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            graph.replay()
+            e1.record(stream)
+            e1.synchronize()
+            times.append(e0.elapsed_time(e1) * 1e3 / reps)  # us per call
     us = statistics.median(times[1:])
     t_fp8, t_hbm = roofline_times(wl, pk)
     t_roof = max(t_fp8, t_hbm)
