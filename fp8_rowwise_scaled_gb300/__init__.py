@@ -89,6 +89,9 @@ def lib() -> ctypes.CDLL:
             L.mslkb_variant_name.restype = ctypes.c_char_p
             L.mslkb_force_variant.argtypes = [ctypes.c_int32]
             L.mslkb_force_variant.restype = ctypes.c_int
+            L.mslkb_variant_resources.argtypes = [ctypes.c_int32, ctypes.POINTER(ctypes.c_int32),
+                                                  ctypes.POINTER(ctypes.c_int32)]
+            L.mslkb_variant_resources.restype = ctypes.c_int
             L.mslkb_set_accumulation_chunk.argtypes = [ctypes.c_int32]
             L.mslkb_set_accumulation_chunk.restype = ctypes.c_int
             L.mslkb_accumulation_chunk.argtypes = []
@@ -156,6 +159,15 @@ def mslkb_force_variant(i: int) -> None:
     s = lib().mslkb_force_variant(i)
     if s != MSLKB_OK:
         raise MslkbError(s, "mslkb_force_variant")
+
+
+def mslkb_variant_resources(i: int):
+    """(CTAs per SM, registers per thread) of kernel variant i on the current device."""
+    b, r = ctypes.c_int32(0), ctypes.c_int32(0)
+    s = lib().mslkb_variant_resources(i, ctypes.byref(b), ctypes.byref(r))
+    if s != MSLKB_OK:
+        raise MslkbError(s, "mslkb_variant_resources")
+    return int(b.value), int(r.value)
 
 
 def mslkb_set_accumulation_chunk(kblocks: int) -> None:

@@ -90,10 +90,16 @@ struct KernelCfg {
   static constexpr int kCpLag = kStages - 2;  // cp.async groups kept in flight per thread
   static constexpr uint32_t kIdesc = ptx::idesc_e4m3_f32(kMmaM, kTileN);
 
+  // 128-row tiles write the output through shared memory and TMA stores: each epilogue
+  // warp stages 32 rows x 32 columns of bf16 (2 KB, 64-byte swizzle) at a time
+  static constexpr bool kTmaStore = !kSwap;
+  static constexpr int kStageOutBytes = 32 * 32 * 2;
+
   // shared memory layout, from a 1024-byte aligned base
   static constexpr int kOffAct = 0;
   static constexpr int kOffW = kStages * kActBytes;
-  static constexpr int kOffBar = kOffW + kStages * kWBytes;
+  static constexpr int kOffOut = kOffW + kStages * kWBytes;
+  static constexpr int kOffBar = kOffOut + (kTmaStore ? kEpiWarps * kStageOutBytes : 0);
   static constexpr int kNumBars = 2 * kStages + 4;
   static constexpr int kOffMisc = kOffBar + 8 * kNumBars;  // tmem address, abort flag
   static constexpr int kOffSched = kOffMisc + 16;
@@ -294,13 +300,15 @@ template <class Cfg>
 __global__ void __launch_bounds__(Cfg::kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ GemmParams p,
                         const __grid_constant__ CUtensorMap tmA,
-                        const __grid_constant__ CUtensorMap tmB) {
+                        const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmC) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const uint32_t s_act = ptx::smem_addr(smem + Cfg::kOffAct);
   const uint32_t s_w = ptx::smem_addr(smem + Cfg::kOffW);
   const uint32_t s_bar = ptx::smem_addr(smem + Cfg::kOffBar);
+  const uint32_t s_out = ptx::smem_addr(smem + Cfg::kOffOut);
   auto full_bar = [&](int s) { return s_bar + 8u * s; };
   auto empty_bar = [&](int s) { return s_bar + 8u * (Cfg::kStages + s); };
   auto tfull_bar = [&](int b) { return s_bar + 8u * (2 * Cfg::kStages + b); };
@@ -532,6 +540,21 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
       TileCoord c = decode_tile<Cfg>(sched, t);
       // an empty reduction (K = 0) writes +0.0 to every owned row, whatever the scales
       if (!has_k) c.valid_end = c.m0;
+      // scales this thread needs, loaded before the chunk waits so their latency hides
+      // behind the MMA: scale_a of its row, and scale_b of column (col0 + lane) for each
+      // 32-column piece, broadcast by shuffle when the piece is stored
+      float sa_pre = 0.0f;
+      float sb_pre[Cfg::kSwap ? 1 : Cfg::kThreadCols / 32];
+      if constexpr (!Cfg::kSwap) {
+        const int32_t R = c.m0 + static_cast<int32_t>(32u * q + lane);
+        if (R < c.valid_end) sa_pre = __ldg(p.scale_a + R);
+        const float* sb_g = p.scale_b + static_cast<size_t>(c.g) * p.N;
+#pragma unroll
+        for (int pc = 0; pc < Cfg::kThreadCols / 32; ++pc) {
+          const int32_t col = c.n0 + col_base + pc * 32 + static_cast<int32_t>(lane);
+          sb_pre[pc] = col < p.N ? __ldg(sb_g + col) : 0.0f;
+        }
+      }
       // fp32 accumulator of this thread (round-to-nearest adds of the TMEM chunks)
       float acc[Cfg::kThreadCols];
 #pragma unroll
@@ -555,7 +578,9 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
           if (warp_any) {
             const uint32_t t_buf = tmem_base + ((32u * q) << 16) +
                                    static_cast<uint32_t>(buf * Cfg::kAccCols + col_base);
-            if constexpr (Cfg::kThreadCols % 32 == 0) {
+            // 128 accumulators per thread leave no room for 32 more load registers at the
+            // 168-register limit of 10+ warps per CTA: drain those 16 columns at a time
+            if constexpr (Cfg::kThreadCols % 32 == 0 && Cfg::kThreadCols < 128) {
 #pragma unroll
               for (int pc = 0; pc < Cfg::kThreadCols / 32; ++pc) {
                 uint32_t v[32];
@@ -583,20 +608,52 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         if (!ok) break;
       }
       if constexpr (!Cfg::kSwap) {
-        // thread = one activation row; 8 output columns per 16-byte store
+        // thread = one activation row
         const int32_t R = c.m0 + static_cast<int32_t>(32u * q + lane);
         const bool row_val = R < c.valid_end;
         const bool row_zero = !row_val && R < c.zero_end;
-        if (__any_sync(0xffffffffu, row_val || row_zero)) {
-          const float sa = row_val ? __ldg(p.scale_a + R) : 0.0f;
-          const float* sb_g = p.scale_b + static_cast<size_t>(c.g) * p.N;
+        const int32_t R_first = c.m0 + static_cast<int32_t>(32u * q);
+        if (Cfg::kTmaStore && R_first + 31 < c.zero_end) {
+          // all 32 rows of this warp are owned: stage 32 x 32 bf16 blocks in shared memory
+          // (64-byte swizzle: 16-byte chunk j of row r sits at chunk j ^ ((r >> 1) & 3))
+          // and let one lane store each block with TMA (whole lines, clipped at N)
+          const uint32_t stg = s_out + ew * Cfg::kStageOutBytes;
+#pragma unroll
+          for (int pc = 0; pc < Cfg::kThreadCols / 32; ++pc) {
+            const int32_t col0 = c.n0 + col_base + pc * 32;
+            const float sb_l = sb_pre[pc];
+            if (lane == 0) ptx::bulk_wait_read_all();  // staging buffer free again
+            __syncwarp();
+#pragma unroll
+            for (int ch = 0; ch < 4; ++ch) {  // 8 columns = one 16-byte chunk at a time
+              uint32_t w[4];
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const int cc = ch * 8 + 2 * j;
+                const float sb0 = __shfl_sync(0xffffffffu, sb_l, cc);
+                const float sb1 = __shfl_sync(0xffffffffu, sb_l, cc + 1);
+                w[j] = row_val ? pack_bf16x2((acc[pc * 32 + cc] * sa_pre) * sb0,
+                                             (acc[pc * 32 + cc + 1] * sa_pre) * sb1)
+                               : 0u;
+              }
+              const uint32_t a = stg + lane * 64u + ((static_cast<uint32_t>(ch) ^ ((lane >> 1) & 3u)) << 4);
+              ptx::st_shared_v4(a, w[0], w[1], w[2], w[3]);
+            }
+            ptx::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              ptx::tma_store_2d(&tmC, stg, col0, R_first);
+              ptx::bulk_commit();
+            }
+          }
+        } else if (__any_sync(0xffffffffu, row_val || row_zero)) {
+          // 8 output columns per 16-byte store, predicated per row and on the last column
+          const float sa = sa_pre;
           uint16_t* orow = p.out + static_cast<size_t>(row_val || row_zero ? R : 0) * p.N;
 #pragma unroll
           for (int pc = 0; pc < Cfg::kThreadCols / 32; ++pc) {
             const int32_t col0 = c.n0 + col_base + pc * 32;
-            // lane j holds scale_b of column col0 + j; broadcast by shuffle below
-            const float sb_l = (col0 + static_cast<int32_t>(lane) < p.N)
-                                   ? __ldg(sb_g + col0 + lane) : 0.0f;
+            const float sb_l = sb_pre[pc];
 #pragma unroll
             for (int j8 = 0; j8 < 4; ++j8) {
               float y[8];
@@ -648,6 +705,10 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         }
       }
     }
+  }
+
+  if constexpr (Cfg::kTmaStore) {
+    if (warp >= static_cast<uint32_t>(Cfg::kEpiWarp0) && lane == 0) ptx::bulk_wait_all();
   }
 
   // ------------------------------------------------------------------ teardown

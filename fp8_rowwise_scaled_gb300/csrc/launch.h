@@ -12,12 +12,14 @@ struct LaunchArgs {
   GemmParams params;
   CUtensorMap tmA;   // activation tiles [rows, K], box (128 B, act_rows)
   CUtensorMap tmB;   // weight tiles [G, N, K], box (128 B, w_rows, 1)
+  CUtensorMap tmC;   // output [rows, N] bf16, box (32, 32), 64-byte swizzle (128-row tiles)
   dim3 grid;
   cudaStream_t stream;
 };
 
 using LaunchFn = cudaError_t (*)(const LaunchArgs&);
 using AttrFn = cudaError_t (*)();
+using OccupancyFn = cudaError_t (*)(int* blocks_per_sm, int* regs_per_thread);
 
 struct VariantInfo {
   const char* name;
@@ -32,6 +34,7 @@ struct VariantInfo {
   int w_rows;     // weight rows per tile
   LaunchFn launch;
   AttrFn set_attr;
+  OccupancyFn occupancy;
 };
 
 template <class Cfg>
@@ -43,7 +46,7 @@ cudaError_t launch_variant(const LaunchArgs& a) {
   cfg.stream = a.stream;
   cfg.attrs = nullptr;
   cfg.numAttrs = 0;
-  return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<Cfg>, a.params, a.tmA, a.tmB);
+  return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<Cfg>, a.params, a.tmA, a.tmB, a.tmC);
 }
 
 template <class Cfg>
@@ -52,11 +55,23 @@ cudaError_t set_attr_variant() {
                               cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
 }
 
+// CTAs of this variant that fit on one SM (needs the shared-memory attribute set first)
+template <class Cfg>
+cudaError_t occupancy_variant(int* blocks_per_sm, int* regs_per_thread) {
+  cudaFuncAttributes fa;
+  cudaError_t e = cudaFuncGetAttributes(&fa, grouped_gemm_kernel<Cfg>);
+  if (e != cudaSuccess) return e;
+  *regs_per_thread = fa.numRegs;
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, grouped_gemm_kernel<Cfg>,
+                                                       Cfg::kThreads, Cfg::kSmemBytes);
+}
+
 template <class Cfg>
 constexpr VariantInfo make_variant(const char* name) {
-  return VariantInfo{name,         Cfg::kTileN,   Cfg::kStages,     Cfg::kSwap,
-                     Cfg::kTma,    Cfg::kDynamic, Cfg::kThreads,    Cfg::kSmemBytes,
-                     Cfg::kActRows, Cfg::kWRows,  &launch_variant<Cfg>, &set_attr_variant<Cfg>};
+  return VariantInfo{name,          Cfg::kTileN,   Cfg::kStages,        Cfg::kSwap,
+                     Cfg::kTma,     Cfg::kDynamic, Cfg::kThreads,       Cfg::kSmemBytes,
+                     Cfg::kActRows, Cfg::kWRows,   &launch_variant<Cfg>, &set_attr_variant<Cfg>,
+                     &occupancy_variant<Cfg>};
 }
 
 // Defined in the variants_*.cu translation units.

@@ -131,6 +131,11 @@ mslkb_status ensure_attr(DeviceState* st, int vi) {
   }
   cudaError_t e = variant(vi)->set_attr();
   if (e != cudaSuccess) return cuda_fail(e);
+  // a variant that cannot place one CTA on an SM is reported here, not at launch
+  int blocks = 0, regs = 0;
+  e = variant(vi)->occupancy(&blocks, &regs);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (blocks < 1) return cuda_fail(cudaErrorLaunchOutOfResources);
   std::lock_guard<std::mutex> lock(g_mutex);
   st->attr_done[vi >> 6] |= bit;
   return MSLKB_OK;
@@ -227,6 +232,25 @@ int64_t addr_align(const void* p) {
 // ---------------------------------------------------------------------------------
 // tensor maps
 // ---------------------------------------------------------------------------------
+mslkb_status encode_out_map(LaunchArgs* la, const VariantInfo* v, void* out, int64_t rows,
+                            int64_t N) {
+  std::memset(&la->tmC, 0, sizeof(la->tmC));
+  if (v->swap) return MSLKB_OK;  // swap-AB tiles store directly
+  if (g_encode == nullptr) return cuda_fail(cudaErrorNotSupported);
+  const cuuint32_t elem_strides[2] = {1, 1};
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(N) * 2};
+  const cuuint32_t box[2] = {32, 32};  // 32 bf16 (64 bytes) x 32 rows per warp block
+  CUresult r = g_encode(&la->tmC, CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, out, dims, strides, box,
+                        elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                        CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    t_last_cuda_error = static_cast<int>(r);
+    return MSLKB_ERR_CUDA;
+  }
+  return MSLKB_OK;
+}
+
 mslkb_status encode_maps(LaunchArgs* la, const VariantInfo* v, const void* A, const void* B,
                          int64_t rows, int64_t G, int64_t N, int64_t K) {
   std::memset(&la->tmA, 0, sizeof(la->tmA));
@@ -322,6 +346,7 @@ mslkb_status run(int layout, const void* A, const void* B, const float* scale_a,
   }
   p.timeout_ns = kWaitTimeoutNs;
   if ((s = encode_maps(&la, v, A, B, rows, G, N, K)) != MSLKB_OK) return s;
+  if ((s = encode_out_map(&la, v, out, rows, N)) != MSLKB_OK) return s;
   la.grid = dim3(static_cast<unsigned>(info.grid), 1, 1);
   la.stream = static_cast<cudaStream_t>(stream);
   cudaError_t e = v->launch(la);
@@ -406,6 +431,23 @@ const char* mslkb_variant_name(int32_t i) {
 mslkb_status mslkb_force_variant(int32_t i) {
   if (i < -1 || i >= num_variants()) return MSLKB_ERR_SHAPE;
   g_forced_variant.store(i);
+  return MSLKB_OK;
+}
+
+mslkb_status mslkb_variant_resources(int32_t i, int32_t* blocks_per_sm, int32_t* regs_per_thread) {
+  if (blocks_per_sm == nullptr || regs_per_thread == nullptr) return MSLKB_ERR_NULL;
+  const VariantInfo* v = variant(i);
+  if (v == nullptr) return MSLKB_ERR_SHAPE;
+  DeviceState* st = nullptr;
+  mslkb_status s = device_state(&st);
+  if (s != MSLKB_OK) return s;
+  cudaError_t e = v->set_attr();
+  if (e != cudaSuccess) return cuda_fail(e);
+  int blocks = 0, regs = 0;
+  e = v->occupancy(&blocks, &regs);
+  if (e != cudaSuccess) return cuda_fail(e);
+  *blocks_per_sm = blocks;
+  *regs_per_thread = regs;
   return MSLKB_OK;
 }
 

@@ -5,8 +5,8 @@
 namespace mslkb {
 
 const VariantInfo kVariantsCpAsync[] = {
-    make_variant<KernelCfg<128, 6, false, false, false>>("stacked_tile128x128_cpasync"),
-    make_variant<KernelCfg<128, 6, false, false, true>>("dynamic_tile128x128_cpasync"),
+    make_variant<KernelCfg<128, 6, false, false, false, 8>>("stacked_tile128x128_cpasync"),
+    make_variant<KernelCfg<128, 6, false, false, true, 8>>("dynamic_tile128x128_cpasync"),
     make_variant<KernelCfg<16, 11, true, false, false>>("stacked_swap_w128xa16_cpasync"),
     make_variant<KernelCfg<16, 11, true, false, true>>("dynamic_swap_w128xa16_cpasync"),
 };

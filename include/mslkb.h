@@ -160,6 +160,14 @@ MSLKB_API int32_t mslkb_num_variants(void);
 MSLKB_API const char *mslkb_variant_name(int32_t variant);
 
 /*
+ * Resources of one kernel variant on the current device: CTAs that fit on one SM (the
+ * library needs 1) and registers per thread.  Makes CUDA calls (device query, kernel
+ * attributes); the library runs the same check before a variant's first launch.
+ */
+MSLKB_API mslkb_status mslkb_variant_resources(int32_t variant, int32_t *blocks_per_sm,
+                                               int32_t *regs_per_thread);
+
+/*
  * Test hook: force every following call on any thread to use one variant (index from
  * mslkb_variant_name; -1 restores the heuristic).  A variant that cannot serve a call
  * (a TMA variant with K % 16 != 0, say) makes that call return MSLKB_ERR_SHAPE.

@@ -108,6 +108,12 @@ def _variants(prefix):
         return []
 
 
+def test_every_variant_fits_one_sm():
+    for i in range(fx.mslkb_num_variants()):
+        blocks, regs = fx.mslkb_variant_resources(i)
+        assert blocks >= 1, f"{fx.variant_name(i)}: {blocks} CTAs per SM, {regs} registers"
+
+
 @pytest.mark.parametrize("variant", _variants("stacked"))
 def test_stacked_variant_ragged(orc, variant):
     meta = [130, 0, 1, 257, 64, 0, 17]
