@@ -182,9 +182,6 @@ mslkb_status plan(int layout, int64_t rows, int64_t G, int64_t N, int64_t K, int
   } else if (per_group <= 32 && tma) {
     swap = true;
     tile_n = 32;
-  } else if (per_group <= 64 && tma) {
-    swap = true;
-    tile_n = 64;
   } else {
     swap = false;
     tile_n = 128;

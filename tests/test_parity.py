@@ -300,6 +300,24 @@ def test_accumulator_cancellation(orc):
         _check_full(prob, orc, variant=v, what=f"cancellation {v}")
 
 
+def test_accumulator_cancellation_inside_chunks(orc):
+    """The same stress at the scale of one accumulation chunk: every 512 K elements (the
+    default chunk) the second 256 products mirror the first 256 with the opposite sign,
+    so each chunk's own partial sums climb and cancel, and the chunk totals are ~0."""
+    K, N, M, half = 16384, 128, 24, 256
+    g = torch.Generator().manual_seed(23)
+    a = random_codes((M, K), g).numpy() & 0x7F
+    b = random_codes((1, N, K), g).numpy() & 0x7F
+    for k0 in range(0, K, 2 * half):
+        a[:, k0 + half:k0 + 2 * half] = a[:, k0:k0 + half] | 0x80
+        b[:, :, k0 + half:k0 + 2 * half] = b[:, :, k0:k0 + half]
+    a[:, K - 1] &= 0x7F
+    prob = Problem.from_numpy("stacked", a, b, np.ones(M, np.float32),
+                              np.ones((1, N), np.float32), [M])
+    for v in ("stacked_tile128x256_tma", "stacked_swap_w128xa32_tma"):
+        _check_full(prob, orc, variant=v, what=f"chunk-scale cancellation {v}")
+
+
 @pytest.mark.parametrize("kpc", [0, 1, 3, 4, 32])
 def test_accumulation_chunk_lengths(orc, kpc):
     """Every chunk length (0 = the whole K in the tensor core) stays within tolerance on
