@@ -48,7 +48,8 @@ class PlanInfo(ctypes.Structure):
                 ("stages", ctypes.c_int32), ("tma", ctypes.c_int32),
                 ("copy_width", ctypes.c_int32), ("grid", ctypes.c_int32),
                 ("threads", ctypes.c_int32), ("smem_bytes", ctypes.c_int32),
-                ("tiles_bound", ctypes.c_int64)]
+                ("tiles_bound", ctypes.c_int64), ("split_k", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
 
     def as_dict(self) -> dict:
         d = {f: getattr(self, f) for f, _ in self._fields_}
@@ -92,6 +93,8 @@ def lib() -> ctypes.CDLL:
             L.mslkb_variant_resources.argtypes = [ctypes.c_int32, ctypes.POINTER(ctypes.c_int32),
                                                   ctypes.POINTER(ctypes.c_int32)]
             L.mslkb_variant_resources.restype = ctypes.c_int
+            L.mslkb_set_split_k.argtypes = [ctypes.c_int32]
+            L.mslkb_set_split_k.restype = ctypes.c_int
             L.mslkb_set_accumulation_chunk.argtypes = [ctypes.c_int32]
             L.mslkb_set_accumulation_chunk.restype = ctypes.c_int
             L.mslkb_accumulation_chunk.argtypes = []
@@ -168,6 +171,12 @@ def mslkb_variant_resources(i: int):
     if s != MSLKB_OK:
         raise MslkbError(s, "mslkb_variant_resources")
     return int(b.value), int(r.value)
+
+
+def mslkb_set_split_k(enable: int) -> None:
+    s = lib().mslkb_set_split_k(enable)
+    if s != MSLKB_OK:
+        raise MslkbError(s, "mslkb_set_split_k")
 
 
 def mslkb_set_accumulation_chunk(kblocks: int) -> None:

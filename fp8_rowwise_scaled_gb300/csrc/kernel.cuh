@@ -57,6 +57,9 @@ struct GemmParams {
   int32_t num_kb;          // ceil(K / 128)
   int32_t copy_width;      // cp.async loader: bytes per copy (16, 8, 4) or 1 (byte loads)
   int32_t kb_per_chunk;    // K blocks the tensor core sums before the epilogue takes over
+  int32_t split_k;         // 1: split the last waves' tiles along K over all CTAs
+  float* sk_ws;            // split tiles: fp32 partial sums, 2 slots per CTA
+  uint32_t* sk_cnt;        // split tiles: arrival counters, one per (tile, epilogue warp)
   uint64_t timeout_ns;     // give-up time of one pipeline wait
 };
 
@@ -102,7 +105,8 @@ struct KernelCfg {
   static constexpr int kOffBar = kOffOut + (kTmaStore ? kEpiWarps * kStageOutBytes : 0);
   static constexpr int kNumBars = 2 * kStages + 4;
   static constexpr int kOffMisc = kOffBar + 8 * kNumBars;  // tmem address, abort flag
-  static constexpr int kOffSched = kOffMisc + 16;
+  static constexpr int kOffWork = kOffMisc + 16;           // the CTA's Work (below)
+  static constexpr int kOffSched = kOffWork + 64;
   static constexpr int kSchedBytes = 2 * 4 * (kMaxGroups + 1);
   static constexpr int kSmemBytes = kOffSched + kSchedBytes + 1024;  // + alignment slack
 
@@ -165,6 +169,77 @@ __device__ __forceinline__ TileCoord decode_tile(const Sched& s, int32_t t) {
   c.valid_end = base + cnt;
   c.zero_end = Cfg::kDynamic ? base + s.E : base + cnt;
   return c;
+}
+
+// Work of one CTA (all CTAs derive the same split).  With T tiles and P CTAs, the tiles
+// of all full waves but the last, [0, dp), run whole: tile t on CTA t % P.  The remaining
+// P + T % P tiles (all T when T < 2P) are cut into (tile, K-block) units, and each CTA
+// takes one contiguous range of those units, so every CTA gets the same amount of K work
+// (stream-K).  A tile whose units fall to several CTAs is finished by whichever of them
+// arrives last, from the fp32 partial sums the others published.
+struct Work {
+  int32_t dp_tiles;  // tiles run whole
+  int32_t n_dp;      // whole tiles of this CTA
+  int32_t nkb;       // K blocks per tile
+  int32_t sk_ctas;   // CTAs sharing the split region: min(P, units), each range non-empty
+  int64_t units;     // K-block units of the split region
+  int64_t sk_begin;  // this CTA's unit range
+  int64_t sk_end;
+  int32_t n_items;   // work items of this CTA
+};
+
+static_assert(sizeof(Work) <= 64, "Work must fit its shared-memory slot");
+
+struct Item {
+  int32_t tile;
+  int32_t kb0;       // K blocks [kb0, kb1) of the tile
+  int32_t kb1;
+  int32_t sk_tile;   // index of a tile shared with other CTAs, else -1
+};
+
+__device__ __forceinline__ Work make_work(int32_t T, int32_t nkb, bool split) {
+  const int32_t P = gridDim.x;
+  const int32_t c = blockIdx.x;
+  Work w;
+  w.nkb = nkb;
+  int32_t dp = T;
+  if (split && nkb > 0 && T % P != 0) dp = T >= 2 * P ? (T / P - 1) * P : 0;
+  w.dp_tiles = dp;
+  w.n_dp = c < dp ? (dp - 1 - c) / P + 1 : 0;
+  w.units = static_cast<int64_t>(T - dp) * nkb;
+  w.sk_ctas = static_cast<int32_t>(w.units < P ? w.units : P);
+  w.sk_begin = c < w.sk_ctas ? w.units * c / w.sk_ctas : w.units;
+  w.sk_end = c < w.sk_ctas ? w.units * (c + 1) / w.sk_ctas : w.units;
+  const int32_t n_sk = w.sk_end > w.sk_begin
+                           ? static_cast<int32_t>((w.sk_end - 1) / nkb - w.sk_begin / nkb + 1)
+                           : 0;
+  w.n_items = w.n_dp + n_sk;
+  return w;
+}
+
+__device__ __forceinline__ Item work_item(const Work& w, int32_t i) {
+  Item it;
+  if (i < w.n_dp) {
+    it.tile = blockIdx.x + i * gridDim.x;
+    it.kb0 = 0;
+    it.kb1 = w.nkb;
+    it.sk_tile = -1;
+    return it;
+  }
+  const int64_t t = w.sk_begin / w.nkb + (i - w.n_dp);
+  const int64_t u0 = w.sk_begin > t * w.nkb ? w.sk_begin : t * w.nkb;
+  const int64_t u1 = w.sk_end < (t + 1) * w.nkb ? w.sk_end : (t + 1) * w.nkb;
+  it.tile = w.dp_tiles + static_cast<int32_t>(t);
+  it.kb0 = static_cast<int32_t>(u0 - t * w.nkb);
+  it.kb1 = static_cast<int32_t>(u1 - t * w.nkb);
+  it.sk_tile = (it.kb0 == 0 && it.kb1 == w.nkb) ? -1 : static_cast<int32_t>(t);
+  return it;
+}
+
+// CTA whose unit range holds split-region unit u: the largest c with
+// floor(units * c / sk_ctas) <= u
+__device__ __forceinline__ int32_t unit_owner(const Work& w, int64_t u) {
+  return static_cast<int32_t>(((u + 1) * w.sk_ctas - 1) / w.units);
 }
 
 // Bounded mbarrier wait: false if the CTA is aborting or the wait gave up, in which
@@ -358,6 +433,11 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
   sched.n_tiles_n = (p.N + Cfg::kWRows - 1) / Cfg::kWRows;
   sched.total = tile_pre[p.G];
   const bool has_k = p.num_kb > 0;
+  // the work split lives in shared memory: every role reads it, none keeps it in registers
+  Work* work_smem = reinterpret_cast<Work*>(smem + Cfg::kOffWork);
+  if (threadIdx.x == 0) *work_smem = make_work(sched.total, p.num_kb, p.split_k != 0);
+  __syncthreads();
+  const Work& work = *work_smem;
 
   if (warp < static_cast<uint32_t>(Cfg::kLoaderWarps)) {
     // ------------------------------------------------------------------ loader
@@ -366,9 +446,10 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         int stage = 0;
         uint32_t phase = 0;
         bool ok = true;
-        for (int32_t t = blockIdx.x; ok && t < sched.total; t += gridDim.x) {
-          const TileCoord c = decode_tile<Cfg>(sched, t);
-          for (int32_t kb = 0; kb < p.num_kb; ++kb) {
+        for (int32_t i = 0; ok && i < work.n_items; ++i) {
+          const Item it = work_item(work, i);
+          const TileCoord c = decode_tile<Cfg>(sched, it.tile);
+          for (int32_t kb = it.kb0; kb < it.kb1; ++kb) {
             if (!wait_bar(empty_bar(stage), phase ^ 1u, abort_flag, p.status, p.timeout_ns)) {
               ok = false;
               break;
@@ -400,10 +481,11 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         uint32_t phase = 0;
         int64_t fills = 0;  // stages issued by this thread
         bool ok = true;
-        for (int32_t t = blockIdx.x; ok && t < sched.total; t += gridDim.x) {
-          const TileCoord c = decode_tile<Cfg>(sched, t);
+        for (int32_t i = 0; ok && i < work.n_items; ++i) {
+          const Item it = work_item(work, i);
+          const TileCoord c = decode_tile<Cfg>(sched, it.tile);
           const uint8_t* b_group = p.B + static_cast<size_t>(c.g) * p.N * p.K;
-          for (int32_t kb = 0; kb < p.num_kb; ++kb) {
+          for (int32_t kb = it.kb0; kb < it.kb1; ++kb) {
             if (!wait_bar(empty_bar(stage), phase ^ 1u, abort_flag, p.status, p.timeout_ns)) {
               ok = false;
               break;
@@ -472,8 +554,9 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
       uint32_t chunk = 0;  // chunks issued by this CTA: buffer = chunk & 1
       bool ok = true;
       const int32_t kpc = p.kb_per_chunk;
-      for (int32_t t = blockIdx.x; ok && t < sched.total; t += gridDim.x) {
-        for (int32_t kb0 = 0; ok && kb0 < p.num_kb; kb0 += kpc) {
+      for (int32_t i = 0; ok && i < work.n_items; ++i) {
+        const Item it = work_item(work, i);
+        for (int32_t kb0 = it.kb0; ok && kb0 < it.kb1; kb0 += kpc) {
           const int buf = static_cast<int>(chunk & 1u);
           const uint32_t use = chunk >> 1;  // how often this buffer was used before
           if (!wait_bar(tempty_bar(buf), (use & 1u) ^ 1u, abort_flag, p.status, p.timeout_ns)) {
@@ -482,7 +565,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
           }
           ptx::tc_fence_after_sync();
           const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * Cfg::kAccCols);
-          const int32_t kb1 = min(p.num_kb, kb0 + kpc);
+          const int32_t kb1 = min(it.kb1, kb0 + kpc);
           for (int32_t kb = kb0; kb < kb1; ++kb) {
             if (!wait_bar(full_bar(stage), phase, abort_flag, p.status, p.timeout_ns)) {
               ok = false;
@@ -536,8 +619,9 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     uint32_t chunk = 0;
     bool ok = true;
     const int32_t kpc = p.kb_per_chunk;
-    for (int32_t t = blockIdx.x; ok && t < sched.total; t += gridDim.x) {
-      TileCoord c = decode_tile<Cfg>(sched, t);
+    for (int32_t i = 0; ok && i < work.n_items; ++i) {
+      const Item it = work_item(work, i);
+      TileCoord c = decode_tile<Cfg>(sched, it.tile);
       // an empty reduction (K = 0) writes +0.0 to every owned row, whatever the scales
       if (!has_k) c.valid_end = c.m0;
       // scales this thread needs, loaded before the chunk waits so their latency hides
@@ -567,7 +651,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         warp_any = c.n0 + static_cast<int32_t>(32u * q) < p.N && c.m0 < c.valid_end;
       }
       if (has_k) {
-        for (int32_t kb0 = 0; kb0 < p.num_kb; kb0 += kpc) {
+        for (int32_t kb0 = it.kb0; kb0 < it.kb1; kb0 += kpc) {
           const int buf = static_cast<int>(chunk & 1u);
           const uint32_t use = chunk >> 1;
           if (!wait_bar(tfull_bar(buf), use & 1u, abort_flag, p.status, p.timeout_ns)) {
@@ -606,6 +690,49 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
           ++chunk;
         }
         if (!ok) break;
+      }
+      if (it.sk_tile >= 0) {
+        // One piece of a split tile.  Each epilogue warp publishes its partial sums and
+        // counts itself in; the warp that arrives last (same warp index, any CTA) adds the
+        // pieces in CTA order -- the same order whoever is last -- and stores the tile.
+        const int64_t u_first = static_cast<int64_t>(it.sk_tile) * work.nkb;
+        const int32_t c_first = unit_owner(work, u_first);
+        const int32_t c_last = unit_owner(work, u_first + work.nkb - 1);
+        constexpr size_t kPerWarp = 32 * Cfg::kThreadCols;
+        auto piece = [&](int32_t cta) -> float* {
+          // slot 0: the first tile of that CTA's range; slot 1: its last tile
+          const int64_t first_tile = (work.units * cta / work.sk_ctas) / work.nkb;
+          const int slot = (first_tile == it.sk_tile) ? 0 : 1;
+          return p.sk_ws + (static_cast<size_t>(cta * 2 + slot) * Cfg::kEpiWarps + ew) * kPerWarp;
+        };
+        float* mine = piece(blockIdx.x) + lane;
+#pragma unroll
+        for (int j = 0; j < Cfg::kThreadCols; ++j) __stcg(mine + j * 32, acc[j]);
+        __threadfence();
+        __syncwarp();
+        uint32_t* cnt = p.sk_cnt + static_cast<size_t>(it.sk_tile) * Cfg::kEpiWarps + ew;
+        uint32_t prev = 0;
+        if (lane == 0) {
+          prev = atomicAdd(cnt, 1u);
+          __threadfence();
+        }
+        prev = __shfl_sync(0xffffffffu, prev, 0);
+        __syncwarp();
+        if (prev != static_cast<uint32_t>(c_last - c_first)) continue;  // not the last piece
+        __threadfence();
+        // every piece, this CTA's own included, is read back from the workspace so that
+        // the sum runs in CTA order: ((p_first + p_next) + ...) + p_last
+        {
+          const float* src = piece(c_first) + lane;
+#pragma unroll
+          for (int j = 0; j < Cfg::kThreadCols; ++j) acc[j] = __ldcg(src + j * 32);
+        }
+        for (int32_t cta = c_first + 1; cta <= c_last; ++cta) {
+          const float* src = piece(cta) + lane;
+#pragma unroll
+          for (int j = 0; j < Cfg::kThreadCols; ++j) acc[j] += __ldcg(src + j * 32);
+        }
+        if (lane == 0) *cnt = 0u;  // ready for the next call
       }
       if constexpr (!Cfg::kSwap) {
         // thread = one activation row

@@ -32,6 +32,7 @@ struct VariantInfo {
   int smem;
   int act_rows;   // activation rows per tile
   int w_rows;     // weight rows per tile
+  int partial_bytes;  // fp32 partial sums of one tile (a split tile's piece)
   LaunchFn launch;
   AttrFn set_attr;
   OccupancyFn occupancy;
@@ -68,10 +69,10 @@ cudaError_t occupancy_variant(int* blocks_per_sm, int* regs_per_thread) {
 
 template <class Cfg>
 constexpr VariantInfo make_variant(const char* name) {
-  return VariantInfo{name,          Cfg::kTileN,   Cfg::kStages,        Cfg::kSwap,
-                     Cfg::kTma,     Cfg::kDynamic, Cfg::kThreads,       Cfg::kSmemBytes,
-                     Cfg::kActRows, Cfg::kWRows,   &launch_variant<Cfg>, &set_attr_variant<Cfg>,
-                     &occupancy_variant<Cfg>};
+  return VariantInfo{name,          Cfg::kTileN,   Cfg::kStages,  Cfg::kSwap,
+                     Cfg::kTma,     Cfg::kDynamic, Cfg::kThreads, Cfg::kSmemBytes,
+                     Cfg::kActRows, Cfg::kWRows,   Cfg::kEpiWarps * 32 * Cfg::kThreadCols * 4,
+                     &launch_variant<Cfg>, &set_attr_variant<Cfg>, &occupancy_variant<Cfg>};
 }
 
 // Defined in the variants_*.cu translation units.

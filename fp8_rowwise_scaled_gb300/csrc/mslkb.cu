@@ -13,7 +13,9 @@
 #include <atomic>
 #include <cstdint>
 #include <cstring>
+#include <map>
 #include <mutex>
+#include <utility>
 
 #include "launch.h"
 #include "mslkb.h"
@@ -36,6 +38,8 @@ std::atomic<int> g_forced_variant{-1};
 // into round-to-nearest fp32 registers; 0 = the whole K in the tensor core.
 constexpr int kDefaultKbPerChunk = 4;
 std::atomic<int> g_kb_per_chunk{kDefaultKbPerChunk};
+// 1: split the last waves' tiles along K over all CTAs (stream-K); 0: whole tiles only
+std::atomic<int> g_split_k{1};
 
 // ---------------------------------------------------------------------------------
 // variant table: stacked TMA, dynamic TMA, cp.async (both layouts)
@@ -123,6 +127,69 @@ mslkb_status device_state(DeviceState** out) {
   return MSLKB_OK;
 }
 
+// ---------------------------------------------------------------------------------
+// split-tile workspace, one per (device, stream): 2 partial-sum slots per CTA and one
+// arrival counter per (split tile, epilogue warp).  Calls on one stream run in order,
+// so they can share it; calls on different streams get different workspaces.
+// ---------------------------------------------------------------------------------
+struct Workspace {
+  float* partials = nullptr;
+  uint32_t* counters = nullptr;
+};
+std::map<std::pair<int, uintptr_t>, Workspace> g_workspaces;
+
+size_t max_partial_bytes() {
+  size_t m = 0;
+  for (int i = 0; i < num_variants(); ++i)
+    if (static_cast<size_t>(variant(i)->partial_bytes) > m) m = variant(i)->partial_bytes;
+  return m;
+}
+
+// Finds or creates the workspace of `stream`; leaves *ws empty (no splitting) when the
+// stream is being captured and has none yet, since allocating is not allowed there.
+mslkb_status stream_workspace(const DeviceState* st, cudaStream_t stream, Workspace* ws) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  const auto key = std::make_pair(dev, reinterpret_cast<uintptr_t>(stream));
+  {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    auto it = g_workspaces.find(key);
+    if (it != g_workspaces.end()) {
+      *ws = it->second;
+      return MSLKB_OK;
+    }
+  }
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if ((e = cudaStreamIsCapturing(stream, &cap)) != cudaSuccess) return cuda_fail(e);
+  if (cap != cudaStreamCaptureStatusNone) {
+    *ws = Workspace{};
+    return MSLKB_OK;
+  }
+  Workspace w;
+  const size_t slots = 2 * static_cast<size_t>(st->sm_count);
+  if ((e = cudaMalloc(&w.partials, slots * max_partial_bytes())) != cudaSuccess)
+    return cuda_fail(e);
+  const size_t ncnt = slots * 8;  // split tiles < 2 x CTAs, 8 epilogue warps at most
+  if ((e = cudaMalloc(&w.counters, ncnt * sizeof(uint32_t))) != cudaSuccess) {
+    cudaFree(w.partials);
+    return cuda_fail(e);
+  }
+  if ((e = cudaMemsetAsync(w.counters, 0, ncnt * sizeof(uint32_t), stream)) != cudaSuccess) {
+    cudaFree(w.partials);
+    cudaFree(w.counters);
+    return cuda_fail(e);
+  }
+  std::lock_guard<std::mutex> lock(g_mutex);
+  auto ins = g_workspaces.emplace(key, w);
+  if (!ins.second) {  // another thread created it first
+    cudaFree(w.partials);
+    cudaFree(w.counters);
+  }
+  *ws = ins.first->second;
+  return MSLKB_OK;
+}
+
 mslkb_status ensure_attr(DeviceState* st, int vi) {
   const uint64_t bit = 1ull << (vi & 63);
   {
@@ -199,7 +266,11 @@ mslkb_status plan(int layout, int64_t rows, int64_t G, int64_t N, int64_t K, int
   if (v == nullptr || v->dynamic != dynamic || (v->tma && !tma)) return MSLKB_ERR_SHAPE;
   const int64_t bound = tiles_bound(v, layout, rows, G, N);
   if (bound > INT32_MAX) return MSLKB_ERR_SHAPE;
-  int64_t grid = bound < num_sms ? bound : num_sms;
+  const int64_t nkb = ceil_div(K, mslkb::kBK);
+  const bool split = g_split_k.load() != 0 && nkb > 0;
+  // with splitting every CTA gets K work as long as there are units to share
+  const int64_t work = split ? bound * nkb : bound;
+  int64_t grid = work < num_sms ? work : num_sms;
   if (dynamic) {  // padding rows are zeroed by every CTA's epilogue warps
     const int64_t zero_ctas = ceil_div(G * rows, 32);
     if (grid < zero_ctas) grid = zero_ctas < num_sms ? zero_ctas : num_sms;
@@ -217,6 +288,7 @@ mslkb_status plan(int layout, int64_t rows, int64_t G, int64_t N, int64_t K, int
   info->threads = v->threads;
   info->smem_bytes = v->smem;
   info->tiles_bound = bound;
+  info->split_k = split ? 1 : 0;
   return MSLKB_OK;
 }
 
@@ -342,6 +414,16 @@ mslkb_status run(int layout, const void* A, const void* B, const float* scale_a,
     p.kb_per_chunk = (kpc <= 0 || kpc > p.num_kb) ? (p.num_kb > 0 ? p.num_kb : 1) : kpc;
   }
   p.timeout_ns = kWaitTimeoutNs;
+  p.split_k = 0;
+  if (info.split_k) {
+    Workspace ws;
+    if ((s = stream_workspace(st, static_cast<cudaStream_t>(stream), &ws)) != MSLKB_OK) return s;
+    if (ws.partials != nullptr) {
+      p.split_k = 1;
+      p.sk_ws = ws.partials;
+      p.sk_cnt = ws.counters;
+    }
+  }
   if ((s = encode_maps(&la, v, A, B, rows, G, N, K)) != MSLKB_OK) return s;
   if ((s = encode_out_map(&la, v, out, rows, N)) != MSLKB_OK) return s;
   la.grid = dim3(static_cast<unsigned>(info.grid), 1, 1);
@@ -445,6 +527,12 @@ mslkb_status mslkb_variant_resources(int32_t i, int32_t* blocks_per_sm, int32_t*
   if (e != cudaSuccess) return cuda_fail(e);
   *blocks_per_sm = blocks;
   *regs_per_thread = regs;
+  return MSLKB_OK;
+}
+
+mslkb_status mslkb_set_split_k(int32_t enable) {
+  if (enable != 0 && enable != 1) return MSLKB_ERR_SHAPE;
+  g_split_k.store(enable);
   return MSLKB_OK;
 }
 

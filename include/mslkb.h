@@ -22,9 +22,15 @@
  *   MSLK #471, commit rejecting a strided output).
  * - `stream` is a cudaStream_t passed as void*; NULL means the legacy default stream.
  *   Calls are asynchronous: they enqueue work and return without synchronising.
- *   No call allocates device memory, so calls may be captured in a CUDA graph once
- *   the library has been used on that device (the first call on a device performs
- *   one-time set-up: device query, kernel attributes, driver entry point).
+ *   The first call on a device performs one-time set-up (device query, kernel attributes,
+ *   driver entry point).  The first call on each stream (outside stream capture) also
+ *   allocates that stream's split-tile workspace (2 x #SMs x 128 KB of fp32 partial sums
+ *   plus counters, about 40 MB on GB300); later calls allocate nothing and may be
+ *   captured in a CUDA graph.  A call captured on a stream that has no workspace yet
+ *   runs without splitting tiles (same results within tolerance, possibly slower).
+ *   Calls on one stream share its workspace in stream order; a captured graph keeps the
+ *   workspace of the stream it was captured on, so two launches of such graphs, or one
+ *   and a call on that stream, must not run at the same time.
  * - Sizes are int64_t.  Errors are reported by the return value; nothing is enqueued
  *   when a call returns anything but MSLKB_OK.  Argument checks happen before any CUDA
  *   call, so a bad argument is reported even where no GPU is present.
@@ -149,6 +155,8 @@ typedef struct mslkb_plan_info {
   int32_t threads;      /* threads per CTA */
   int32_t smem_bytes;   /* dynamic shared memory per CTA */
   int64_t tiles_bound;  /* host upper bound on output tiles */
+  int32_t split_k;      /* 1: the last waves' tiles are split along K over all CTAs */
+  int32_t reserved;
 } mslkb_plan_info;
 
 MSLKB_API mslkb_status mslkb_plan(int32_t layout, int64_t rows, int64_t G, int64_t N, int64_t K,
@@ -174,6 +182,17 @@ MSLKB_API mslkb_status mslkb_variant_resources(int32_t variant, int32_t *blocks_
  * Used to check that different variants give bit-identical results.
  */
 MSLKB_API mslkb_status mslkb_force_variant(int32_t variant);
+
+/*
+ * Split policy (stream-K).  With T output tiles and P CTAs, tiles of all full waves but
+ * the last run whole; the remaining tiles are cut into K blocks and every CTA takes an
+ * equal contiguous share, so no SM idles in the last wave.  A split tile is finished by
+ * the CTA that completes its last piece, which adds the fp32 partial sums of all pieces
+ * in a fixed order (results do not depend on timing).  1 (default) enables it, 0 runs
+ * whole tiles only.  Applies to every following call from any thread; a tuning and test
+ * hook.  Other values give MSLKB_ERR_SHAPE.
+ */
+MSLKB_API mslkb_status mslkb_set_split_k(int32_t enable);
 
 /*
  * Accumulation chunk.  The tensor core's own fp32 accumulation adds with round-toward-

@@ -180,9 +180,20 @@ def test_plan_forced_variant(L):
 
 def test_plan_grid_bounds(L):
     # tiles bound for stacked: (total_M + nz * (tile_m - 1)) / tile_m * ceil(N / tile_n)
-    i = fx.mslkb_plan(0, 1, 16, 8192, 8192, 152)
-    assert i.tiles_bound == 64 and i.grid == 64
-    i = fx.mslkb_plan(0, 16384, 16, 16384, 16384, 152)
-    assert i.grid == 152 and i.tiles_bound == (16384 + 16 * 127) // 128 * 64
-    i = fx.mslkb_plan(1, 128, 8, 1000, 1000, 152)
-    assert i.tiles_bound == 8 * 1 * 8 and i.grid == 64
+    try:
+        fx.mslkb_set_split_k(0)  # whole tiles: one CTA per tile at most
+        i = fx.mslkb_plan(0, 1, 16, 8192, 8192, 152)
+        assert i.tiles_bound == 64 and i.grid == 64 and i.split_k == 0
+        i = fx.mslkb_plan(1, 128, 8, 1000, 1000, 152)
+        assert i.tiles_bound == 8 * 1 * 8 and i.grid == 64
+        fx.mslkb_set_split_k(1)  # split: every SM gets K work when there are units
+        i = fx.mslkb_plan(0, 1, 16, 8192, 8192, 152)
+        assert i.tiles_bound == 64 and i.grid == 152 and i.split_k == 1
+        i = fx.mslkb_plan(0, 16384, 16, 16384, 16384, 152)
+        assert i.grid == 152 and i.tiles_bound == (16384 + 16 * 127) // 128 * 64
+        i = fx.mslkb_plan(0, 64, 4, 256, 0, 152)  # K = 0: nothing to split
+        assert i.split_k == 0
+        with pytest.raises(fx.MslkbError):
+            fx.mslkb_set_split_k(2)
+    finally:
+        fx.mslkb_set_split_k(1)

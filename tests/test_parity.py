@@ -252,6 +252,15 @@ def test_layout_agreement_bitwise(orc):
         sad[gi * E:gi * E + m] = h["sa"][off:off + m]
         off += m
     pd = Problem.from_numpy("dynamic", Ad, h["B"], sad, h["sb"], meta, expected_m=E)
+    # the two layouts plan different grids, so split tiles would be cut differently
+    fx.mslkb_set_split_k(0)
+    try:
+        _layout_agreement(ps, pd, meta, E, N)
+    finally:
+        fx.mslkb_set_split_k(1)
+
+
+def _layout_agreement(ps, pd, meta, E, N):
     for tile in ("tile128x128_tma", "tile128x256_tma", "swap_w128xa16_tma"):
         a = bits_of(ps.run_gpu(variant=f"stacked_{tile}")).reshape(-1, N)
         b = bits_of(pd.run_gpu(variant=f"dynamic_{tile}")).reshape(-1, N)
@@ -334,20 +343,69 @@ def test_accumulation_chunk_lengths(orc, kpc):
 
 def test_cuda_graph_replay(orc):
     prob = _rand_problem("stacked", 4, 256, 512, [64, 0, 100, 3], seed=19)
-    eager = bits_of(prob.run_gpu())
     out = torch.empty((prob.rows, prob.N), dtype=torch.bfloat16, device="cuda")
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(s):
-        prob.run_gpu(out=out)  # warm: first call does one-time set-up outside capture
-    torch.cuda.current_stream().wait_stream(s)
+        prob.run_gpu(out=out)  # first call on s: one-time set-up outside capture
+    s.synchronize()
+    eager = bits_of(out)
     graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph):
+    with torch.cuda.graph(graph, stream=s):
         prob.run_gpu(out=out)
     out.zero_()
-    graph.replay()
-    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        graph.replay()
+    s.synchronize()
     assert np.array_equal(bits_of(out), eager)
+
+
+def test_cuda_graph_on_fresh_stream(orc):
+    """Captured on a stream never used before: no workspace can be allocated during
+    capture, so the call runs with whole tiles; still within tolerance."""
+    prob = _rand_problem("stacked", 4, 256, 1024, [64, 0, 100, 3], seed=20)
+    out = torch.zeros((prob.rows, prob.N), dtype=torch.bfloat16, device="cuda")
+    fresh = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=fresh):
+        prob.run_gpu(out=out)
+    with torch.cuda.stream(fresh):
+        graph.replay()
+    fresh.synchronize()
+    ref, ab = prob.oracle_full(orc)
+    compare(bits_of(out).ravel(), ref.ravel(), ab.ravel(), "graph on a fresh stream")
+
+
+@pytest.mark.parametrize("shape", ["few_tiles", "one_wave_plus", "many_waves"])
+def test_split_tiles(orc, shape):
+    """Stream-K: the last waves' tiles are cut along K over all CTAs and finished by the
+    last piece.  Split and whole-tile runs both match the oracle; split runs repeat bit
+    for bit."""
+    if shape == "few_tiles":      # T < #SMs: every tile split into several pieces
+        prob = _rand_problem("stacked", 2, 512, 4096, [1, 3], seed=31)
+    elif shape == "one_wave_plus":  # #SMs <= T < 2 #SMs
+        prob = _rand_problem("stacked", 3, 2048, 1024, [300, 129, 61], seed=32)
+    else:                          # T >= 2 #SMs: whole waves, then a split remainder
+        prob = _rand_problem("stacked", 4, 4096, 640, [400, 257, 0, 390], seed=33)
+    outs = {}
+    for split in (1, 0):
+        fx.mslkb_set_split_k(split)
+        try:
+            for v in ("stacked_tile128x256_tma", "stacked_swap_w128xa16_tma"):
+                gb, _ = _check_full(prob, orc, variant=v, what=f"{shape} split={split} {v}")
+                outs[(split, v)] = gb
+                if split:
+                    again = bits_of(prob.run_gpu(variant=v)).reshape(gb.shape)
+                    assert np.array_equal(gb, again), f"{shape} {v}: split run not repeatable"
+        finally:
+            fx.mslkb_set_split_k(1)
+    assert fx.device_status() == 0
+
+
+def test_dynamic_split_tiles(orc):
+    prob = _rand_problem("dynamic", 3, 1024, 2048, [5, 0, 77], E=96, seed=34)
+    for v in ("dynamic_tile128x256_tma", "dynamic_swap_w128xa16_tma", "dynamic_tile128x128_cpasync"):
+        _check_full(prob, orc, variant=v, what=f"dynamic split {v}")
 
 
 def test_empty_problems_are_noops():
