@@ -38,7 +38,8 @@ std::atomic<int> g_forced_variant{-1};
 // into round-to-nearest fp32 registers; 0 = the whole K in the tensor core.
 constexpr int kDefaultKbPerChunk = 4;
 std::atomic<int> g_kb_per_chunk{kDefaultKbPerChunk};
-// 1: split the last waves' tiles along K over all CTAs (stream-K); 0: whole tiles only
+// Split policy: 0 whole tiles only; 1 split the last waves' tiles along K over all CTAs
+// (stream-K) for swap-AB plans, where a piece's partial sums are small; 2 split every plan
 std::atomic<int> g_split_k{1};
 
 // ---------------------------------------------------------------------------------
@@ -267,7 +268,10 @@ mslkb_status plan(int layout, int64_t rows, int64_t G, int64_t N, int64_t K, int
   const int64_t bound = tiles_bound(v, layout, rows, G, N);
   if (bound > INT32_MAX) return MSLKB_ERR_SHAPE;
   const int64_t nkb = ceil_div(K, mslkb::kBK);
-  const bool split = g_split_k.load() != 0 && nkb > 0;
+  // Measured on GB300: splitting speeds up the swap-AB plans at small M (more SMs stream
+  // weights) but slows the 128-row-tile plans by 4-9% (128 KB of partial sums per piece).
+  const int policy = g_split_k.load();
+  const bool split = nkb > 0 && (policy == 2 || (policy == 1 && v->swap));
   // with splitting every CTA gets K work as long as there are units to share
   const int64_t work = split ? bound * nkb : bound;
   int64_t grid = work < num_sms ? work : num_sms;
@@ -531,7 +535,7 @@ mslkb_status mslkb_variant_resources(int32_t i, int32_t* blocks_per_sm, int32_t*
 }
 
 mslkb_status mslkb_set_split_k(int32_t enable) {
-  if (enable != 0 && enable != 1) return MSLKB_ERR_SHAPE;
+  if (enable < 0 || enable > 2) return MSLKB_ERR_SHAPE;
   g_split_k.store(enable);
   return MSLKB_OK;
 }

@@ -188,9 +188,11 @@ MSLKB_API mslkb_status mslkb_force_variant(int32_t variant);
  * the last run whole; the remaining tiles are cut into K blocks and every CTA takes an
  * equal contiguous share, so no SM idles in the last wave.  A split tile is finished by
  * the CTA that completes its last piece, which adds the fp32 partial sums of all pieces
- * in a fixed order (results do not depend on timing).  1 (default) enables it, 0 runs
- * whole tiles only.  Applies to every following call from any thread; a tuning and test
- * hook.  Other values give MSLKB_ERR_SHAPE.
+ * in a fixed order (results do not depend on timing).  0 runs whole tiles only; 1 (the
+ * default) splits plans with swap-AB tiles (few rows per group: each piece's partial sums
+ * are small, and more SMs stream the weights); 2 splits every plan.  Applies to every
+ * following call from any thread; a tuning and test hook.  Other values give
+ * MSLKB_ERR_SHAPE.
  */
 MSLKB_API mslkb_status mslkb_set_split_k(int32_t enable);
 

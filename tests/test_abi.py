@@ -48,7 +48,7 @@ def test_exports_nothing_else(L):
 
 def test_status_strings(L):
     for s in range(6):
-        assert fx.mslkb_status_string(s)
+        assert fx.mslkb_status_string(s) != "unknown status"
     assert fx.mslkb_status_string(99) == "unknown status"
     assert fx.mslkb_version() == 10000
 
@@ -186,14 +186,18 @@ def test_plan_grid_bounds(L):
         assert i.tiles_bound == 64 and i.grid == 64 and i.split_k == 0
         i = fx.mslkb_plan(1, 128, 8, 1000, 1000, 152)
         assert i.tiles_bound == 8 * 1 * 8 and i.grid == 64
-        fx.mslkb_set_split_k(1)  # split: every SM gets K work when there are units
+        fx.mslkb_set_split_k(1)  # auto: swap-AB plans split, every SM gets K work
         i = fx.mslkb_plan(0, 1, 16, 8192, 8192, 152)
         assert i.tiles_bound == 64 and i.grid == 152 and i.split_k == 1
-        i = fx.mslkb_plan(0, 16384, 16, 16384, 16384, 152)
+        i = fx.mslkb_plan(0, 16384, 16, 16384, 16384, 152)  # 128-row tiles: whole
         assert i.grid == 152 and i.tiles_bound == (16384 + 16 * 127) // 128 * 64
+        assert i.split_k == 0
         i = fx.mslkb_plan(0, 64, 4, 256, 0, 152)  # K = 0: nothing to split
         assert i.split_k == 0
+        fx.mslkb_set_split_k(2)  # every plan
+        assert fx.mslkb_plan(0, 16384, 16, 16384, 16384, 152).split_k == 1
+        assert fx.mslkb_plan(0, 512, 2, 4096, 64, 152).grid == 152
         with pytest.raises(fx.MslkbError):
-            fx.mslkb_set_split_k(2)
+            fx.mslkb_set_split_k(3)
     finally:
         fx.mslkb_set_split_k(1)

@@ -388,7 +388,7 @@ def test_split_tiles(orc, shape):
     else:                          # T >= 2 #SMs: whole waves, then a split remainder
         prob = _rand_problem("stacked", 4, 4096, 640, [400, 257, 0, 390], seed=33)
     outs = {}
-    for split in (1, 0):
+    for split in (2, 0):  # 2: every plan splits, so both tile shapes take the split path
         fx.mslkb_set_split_k(split)
         try:
             for v in ("stacked_tile128x256_tma", "stacked_swap_w128xa16_tma"):
@@ -404,8 +404,13 @@ def test_split_tiles(orc, shape):
 
 def test_dynamic_split_tiles(orc):
     prob = _rand_problem("dynamic", 3, 1024, 2048, [5, 0, 77], E=96, seed=34)
-    for v in ("dynamic_tile128x256_tma", "dynamic_swap_w128xa16_tma", "dynamic_tile128x128_cpasync"):
-        _check_full(prob, orc, variant=v, what=f"dynamic split {v}")
+    fx.mslkb_set_split_k(2)
+    try:
+        for v in ("dynamic_tile128x256_tma", "dynamic_swap_w128xa16_tma",
+                  "dynamic_tile128x128_cpasync"):
+            _check_full(prob, orc, variant=v, what=f"dynamic split {v}")
+    finally:
+        fx.mslkb_set_split_k(1)
 
 
 def test_empty_problems_are_noops():
