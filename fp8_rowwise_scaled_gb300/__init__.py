@@ -25,6 +25,8 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libmslkb.so")
 
 MSLKB_OK, MSLKB_ERR_NULL, MSLKB_ERR_SHAPE, MSLKB_ERR_ALIGN, MSLKB_ERR_DEVICE, MSLKB_ERR_CUDA = range(6)
+MSLKB_ERR_TOO_LARGE = 6
+NOALLOC_SCRATCH_BYTES = 8 << 20
 MSLKB_DEV_TIMEOUT = 0x1
 MSLKB_DEV_MSIZES_CLAMPED = 0x2
 MAX_GROUPS = 1024
@@ -71,7 +73,8 @@ def lib() -> ctypes.CDLL:
             L = ctypes.CDLL(LIB_PATH)
             p, i64 = ctypes.c_void_p, ctypes.c_int64
             for name in ("mslkb_f8f8bf16_rowwise_grouped_stacked",
-                         "mslkb_f8f8bf16_rowwise_grouped_dynamic"):
+                         "mslkb_f8f8bf16_rowwise_grouped_dynamic",
+                         "mslkb_f8f8bf16_rowwise_grouped_stacked_noalloc"):
                 fn = getattr(L, name)
                 fn.argtypes = [p, p, p, p, p, p, i64, i64, i64, i64, p]
                 fn.restype = ctypes.c_int
@@ -119,6 +122,14 @@ def mslkb_f8f8bf16_rowwise_grouped_dynamic(A, B, scale_a, scale_b, zero_start_in
     return lib().mslkb_f8f8bf16_rowwise_grouped_dynamic(A, B, scale_a, scale_b,
                                                         zero_start_index_M, out, G, expected_m,
                                                         N, K, stream)
+
+
+def mslkb_f8f8bf16_rowwise_grouped_stacked_noalloc(A, B, scale_a, scale_b, m_sizes, out,
+                                                   total_M, G, N, K, stream=0) -> int:
+    """The stacked call with its split-tile scratch in a static device array: allocates
+    nothing (for callers recording CUDA graphs or whose framework owns all memory)."""
+    return lib().mslkb_f8f8bf16_rowwise_grouped_stacked_noalloc(
+        A, B, scale_a, scale_b, m_sizes, out, total_M, G, N, K, stream)
 
 
 def mslkb_status_string(status: int) -> str:

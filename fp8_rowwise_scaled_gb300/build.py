@@ -23,8 +23,8 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmslkb.so")
-SOURCES = ["mslkb.cu", "variants_stacked_tma.cu", "variants_dynamic_tma.cu",
-           "variants_cpasync.cu"]
+SOURCES = ["mslkb.cu", "mslkb_noalloc.cu", "variants_stacked_tma.cu",
+           "variants_dynamic_tma.cu", "variants_cpasync.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 
 #include "kernel.cuh"
+#include "mslkb.h"
 
 namespace mslkb {
 
@@ -74,6 +75,18 @@ constexpr VariantInfo make_variant(const char* name) {
                      Cfg::kActRows, Cfg::kWRows,   Cfg::kEpiWarps * 32 * Cfg::kThreadCols * 4,
                      &launch_variant<Cfg>, &set_attr_variant<Cfg>, &occupancy_variant<Cfg>};
 }
+
+// Defined in mslkb.cu, for the allocation-free entry point in mslkb_noalloc.cu.
+mslkb_status stacked_precheck(const void* A, const void* B, const float* scale_a,
+                              const float* scale_b, const int64_t* m_sizes, void* out,
+                              int64_t total_M, int64_t G, int64_t N, int64_t K,
+                              bool* nothing_to_do);
+mslkb_status run_stacked_with_scratch(const void* A, const void* B, const float* scale_a,
+                                      const float* scale_b, const int64_t* m_sizes, void* out,
+                                      int64_t total_M, int64_t G, int64_t N, int64_t K,
+                                      void* stream, float* partials, size_t partial_bytes,
+                                      uint32_t* counters, size_t counter_count);
+void record_cuda_error(cudaError_t e);
 
 // Defined in the variants_*.cu translation units.
 extern const VariantInfo kVariantsStackedTma[];

@@ -439,6 +439,95 @@ mslkb_status run(int layout, const void* A, const void* B, const float* scale_a,
 
 }  // namespace
 
+namespace mslkb {
+
+// The checks the stacked entry point makes before any CUDA call (0 = go ahead, else the
+// status to return; *nothing_to_do set when the call owns no rows).  Used by the
+// allocation-free entry point in mslkb_noalloc.cu.
+mslkb_status stacked_precheck(const void* A, const void* B, const float* scale_a,
+                              const float* scale_b, const int64_t* m_sizes, void* out,
+                              int64_t total_M, int64_t G, int64_t N, int64_t K,
+                              bool* nothing_to_do) {
+  *nothing_to_do = false;
+  mslkb_status s = check_sizes(total_M, G, N, K);
+  if (s != MSLKB_OK) return s;
+  if (total_M == 0 || N == 0 || G == 0) {
+    *nothing_to_do = true;
+    return MSLKB_OK;
+  }
+  if (out == nullptr || m_sizes == nullptr || scale_a == nullptr || scale_b == nullptr)
+    return MSLKB_ERR_NULL;
+  if (K > 0 && (A == nullptr || B == nullptr)) return MSLKB_ERR_NULL;
+  if (reinterpret_cast<uintptr_t>(out) % 16 != 0) return MSLKB_ERR_ALIGN;
+  if (G * N > MSLKB_MAX_DIM || N * K >= (1ll << 40)) return MSLKB_ERR_SHAPE;
+  return MSLKB_OK;
+}
+
+// The stacked call with split-tile scratch supplied by the caller (partial sums and
+// arrival counters) instead of the per-stream workspace; allocates nothing.  Returns
+// MSLKB_ERR_TOO_LARGE when the plan's split tiles need more scratch than supplied.
+// The counters the launch uses are cleared on `stream` before the kernel.
+mslkb_status run_stacked_with_scratch(const void* A, const void* B, const float* scale_a,
+                                      const float* scale_b, const int64_t* m_sizes, void* out,
+                                      int64_t total_M, int64_t G, int64_t N, int64_t K,
+                                      void* stream, float* partials, size_t partial_bytes,
+                                      uint32_t* counters, size_t counter_count) {
+  DeviceState* st = nullptr;
+  mslkb_status s = device_state(&st);
+  if (s != MSLKB_OK) return s;
+  mslkb_plan_info info;
+  s = plan(0, total_M, G, N, K, st->sm_count, addr_align(A), addr_align(B), &info);
+  if (s != MSLKB_OK) return s;
+  const VariantInfo* v = variant(info.variant);
+  const size_t need_partials = 2 * static_cast<size_t>(info.grid) * v->partial_bytes;
+  const size_t need_counters = 2 * static_cast<size_t>(info.grid) * 8;
+  if (info.split_k && (need_partials > partial_bytes || need_counters > counter_count))
+    return MSLKB_ERR_TOO_LARGE;
+  if ((s = ensure_attr(st, info.variant)) != MSLKB_OK) return s;
+
+  LaunchArgs la;
+  std::memset(&la, 0, sizeof(la));
+  GemmParams& p = la.params;
+  p.A = static_cast<const uint8_t*>(A);
+  p.B = static_cast<const uint8_t*>(B);
+  p.scale_a = scale_a;
+  p.scale_b = scale_b;
+  p.meta = m_sizes;
+  p.out = static_cast<uint16_t*>(out);
+  p.status = st->status_ptr;
+  p.rows = static_cast<int32_t>(total_M);
+  p.G = static_cast<int32_t>(G);
+  p.N = static_cast<int32_t>(N);
+  p.K = static_cast<int32_t>(K);
+  p.E = 0;
+  p.num_kb = static_cast<int32_t>(ceil_div(K, mslkb::kBK));
+  p.copy_width = info.copy_width;
+  {
+    const int kpc = g_kb_per_chunk.load();
+    p.kb_per_chunk = (kpc <= 0 || kpc > p.num_kb) ? (p.num_kb > 0 ? p.num_kb : 1) : kpc;
+  }
+  p.timeout_ns = kWaitTimeoutNs;
+  p.split_k = info.split_k;
+  p.sk_ws = partials;
+  p.sk_cnt = counters;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  if (info.split_k) {
+    cudaError_t e = cudaMemsetAsync(counters, 0, need_counters * sizeof(uint32_t), cs);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
+  if ((s = encode_maps(&la, v, A, B, total_M, G, N, K)) != MSLKB_OK) return s;
+  if ((s = encode_out_map(&la, v, out, total_M, N)) != MSLKB_OK) return s;
+  la.grid = dim3(static_cast<unsigned>(info.grid), 1, 1);
+  la.stream = cs;
+  cudaError_t e = v->launch(la);
+  if (e != cudaSuccess) return cuda_fail(e);
+  return MSLKB_OK;
+}
+
+void record_cuda_error(cudaError_t e) { t_last_cuda_error = static_cast<int>(e); }
+
+}  // namespace mslkb
+
 extern "C" {
 
 mslkb_status mslkb_f8f8bf16_rowwise_grouped_stacked(const void* A, const void* B,
@@ -472,6 +561,9 @@ const char* mslkb_status_string(mslkb_status status) {
     case MSLKB_ERR_ALIGN: return "out must be 16-byte aligned";
     case MSLKB_ERR_DEVICE: return "the current device is not sm_103 (GB300)";
     case MSLKB_ERR_CUDA: return "a CUDA call failed (see mslkb_last_cuda_error)";
+    case MSLKB_ERR_TOO_LARGE:
+      return "the problem needs more split-tile scratch than the allocation-free entry "
+             "point holds (MSLKB_NOALLOC_SCRATCH_BYTES)";
   }
   return "unknown status";
 }

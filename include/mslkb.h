@@ -61,7 +61,8 @@ typedef enum mslkb_status {
   MSLKB_ERR_SHAPE = 2,  /* a size is negative, too large, or N is not a multiple of 8 */
   MSLKB_ERR_ALIGN = 3,  /* out is not 16-byte aligned */
   MSLKB_ERR_DEVICE = 4, /* the current device is not sm_103 (GB300 / B300) */
-  MSLKB_ERR_CUDA = 5    /* a CUDA runtime or driver call failed; see mslkb_last_cuda_error */
+  MSLKB_ERR_CUDA = 5,   /* a CUDA runtime or driver call failed; see mslkb_last_cuda_error */
+  MSLKB_ERR_TOO_LARGE = 6 /* needs more scratch than the allocation-free entry point holds */
 } mslkb_status;
 
 /* Bits of the device status word (mslkb_get_device_status). */
@@ -122,6 +123,33 @@ MSLKB_API mslkb_status mslkb_f8f8bf16_rowwise_grouped_dynamic(
     const void *A, const void *B, const float *scale_a, const float *scale_b,
     const int64_t *zero_start_index_M, void *out, int64_t G, int64_t expected_m,
     int64_t N, int64_t K, void *stream);
+
+/*
+ * Allocation-free stacked call (no counterpart on the pages: an addition of this library).
+ *
+ * For callers that must not allocate device memory: code recording a CUDA graph (memory
+ * allocation is not allowed during stream capture), plug-ins whose host framework owns
+ * every device allocation, and serving loops that cannot afford the device-wide
+ * synchronisation a cudaMalloc can cause.  Same arguments, layout, results and errors as
+ * mslkb_f8f8bf16_rowwise_grouped_stacked; the caller still provides inputs and output.
+ *
+ * Its split-tile scratch (fp32 partial sums and arrival counters) is a static device
+ * array of MSLKB_NOALLOC_SCRATCH_BYTES (8 MiB) that every GPU loading the library holds
+ * until the process exits.  The plans that split tiles by default (swap-AB tiles, up to
+ * 32 rows per group on average, e.g. MoE decode) need at most 2 x #SMs x 16 KB of it; a
+ * plan that needs more -- 128-row activation tiles split under mslkb_set_split_k(2), or a
+ * device with very many SMs -- returns MSLKB_ERR_TOO_LARGE and launches nothing.
+ * The first call on a device looks up the array's device address (a CUDA call);
+ * make that first call before any stream capture.  Each call clears the counters it
+ * uses on `stream` (cudaMemsetAsync) before its kernel.  All calls share the one array:
+ * calls that overlap on the GPU (different streams, or graphs replayed concurrently) race
+ * and must be serialised by the caller.
+ */
+#define MSLKB_NOALLOC_SCRATCH_BYTES (8u << 20)
+MSLKB_API mslkb_status mslkb_f8f8bf16_rowwise_grouped_stacked_noalloc(
+    const void *A, const void *B, const float *scale_a, const float *scale_b,
+    const int64_t *m_sizes, void *out, int64_t total_M, int64_t G, int64_t N, int64_t K,
+    void *stream);
 
 /* Static description of a status code.  Never NULL. */
 MSLKB_API const char *mslkb_status_string(mslkb_status status);

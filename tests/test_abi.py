@@ -47,7 +47,7 @@ def test_exports_nothing_else(L):
 
 
 def test_status_strings(L):
-    for s in range(6):
+    for s in range(7):
         assert fx.mslkb_status_string(s) != "unknown status"
     assert fx.mslkb_status_string(99) == "unknown status"
     assert fx.mslkb_version() == 10000
