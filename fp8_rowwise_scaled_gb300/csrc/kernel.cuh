@@ -79,9 +79,20 @@ struct KernelCfg {
   static constexpr int kLoaderWarps = kTma ? 1 : 4;
   static constexpr int kLoaderThreads = 32 * kLoaderWarps;
   static constexpr int kMmaWarp = kLoaderWarps;
-  static constexpr int kEpiWarp0 = kLoaderWarps + 1;
   static constexpr int kEpiWarps = kEpiWarps_;            // 4, or 8 (two per TMEM quadrant)
-  static constexpr int kThreads = 32 * (kLoaderWarps + 1 + kEpiWarps);
+  // Register split (128 x 256 tiles fed by TMA, 128 accumulator columns per thread):
+  // warpgroup 0 = TMA warp, MMA warp and two idle warps, dropping to kRegsLow; the 8
+  // epilogue warps (warpgroups 1-2) rise to kRegsHigh, enough for 128 fp32 accumulators
+  // plus 64 columns of TMEM loads in flight.
+  // Budget: launched with 384 x 168 registers = 128 x 40 + 256 x 232; per SM sub-partition
+  // one warpgroup-0 warp and two epilogue warps: (40 + 232 + 232) x 32 <= 16384.
+  static constexpr bool kRegSplit = kTma && !kSwap && kEpiWarps == 8 && kTileN == 256;
+  static constexpr int kIdleWarps = kRegSplit ? 2 : 0;
+  static constexpr int kEpiWarp0 = kLoaderWarps + 1 + kIdleWarps;
+  static constexpr int kThreads = 32 * (kLoaderWarps + 1 + kIdleWarps + kEpiWarps);
+  static constexpr int kLaunchRegs = kRegSplit ? 168 : 0;  // required at launch (0: any)
+  static constexpr int kRegsLow = 40;
+  static constexpr int kRegsHigh = 232;
   // accumulator columns one epilogue thread owns (and keeps in fp32 registers)
   static constexpr int kThreadCols = kSwap ? kTileN : kTileN / (kEpiWarps / 4);
   static constexpr int kAccCols = kTileN;  // fp32 TMEM columns of one accumulator
@@ -117,6 +128,9 @@ struct KernelCfg {
   static_assert(2 * kAccCols <= 512, "two accumulators must fit TMEM");
   static_assert(kEpiWarps == 4 || (kEpiWarps == 8 && !kSwap), "epilogue warp split");
   static_assert(kThreadCols % 16 == 0, "TMEM load granularity");
+  static_assert(!kRegSplit || (kThreads == 384 && kEpiWarp0 == 4 &&
+                               128 * kRegsLow + 256 * kRegsHigh == kThreads * kLaunchRegs),
+                "register split budget");
 };
 
 struct TileCoord {
@@ -439,6 +453,9 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
   __syncthreads();
   const Work& work = *work_smem;
 
+  if (warp < static_cast<uint32_t>(Cfg::kEpiWarp0)) {
+  // producer side: loader warp(s), MMA warp and (register split) two idle warps
+  if constexpr (Cfg::kRegSplit) ptx::setmaxnreg_dec<Cfg::kRegsLow>();
   if (warp < static_cast<uint32_t>(Cfg::kLoaderWarps)) {
     // ------------------------------------------------------------------ loader
     if constexpr (Cfg::kTma) {
@@ -595,7 +612,9 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
       }
     }
     __syncwarp();
+  }
   } else {
+    if constexpr (Cfg::kRegSplit) ptx::setmaxnreg_inc<Cfg::kRegsHigh>();
     // ------------------------------------------------------------------ epilogue
     const uint32_t q = warp & 3u;  // TMEM lane quadrant this warp may access
     const uint32_t ew = warp - Cfg::kEpiWarp0;
@@ -662,9 +681,23 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
           if (warp_any) {
             const uint32_t t_buf = tmem_base + ((32u * q) << 16) +
                                    static_cast<uint32_t>(buf * Cfg::kAccCols + col_base);
-            // 128 accumulators per thread leave no room for 32 more load registers at the
-            // 168-register limit of 10+ warps per CTA: drain those 16 columns at a time
-            if constexpr (Cfg::kThreadCols % 32 == 0 && Cfg::kThreadCols < 128) {
+            if constexpr (Cfg::kRegSplit && Cfg::kThreadCols % 64 == 0) {
+              // two 32-column loads in flight per wait
+#pragma unroll
+              for (int pc = 0; pc < Cfg::kThreadCols / 64; ++pc) {
+                uint32_t v0[32], v1[32];
+                ptx::tmem_ld_x32(t_buf + static_cast<uint32_t>(pc * 64), v0);
+                ptx::tmem_ld_x32(t_buf + static_cast<uint32_t>(pc * 64 + 32), v1);
+                ptx::tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                  acc[pc * 64 + j] += __uint_as_float(v0[j]);
+                  acc[pc * 64 + 32 + j] += __uint_as_float(v1[j]);
+                }
+              }
+            } else if constexpr (Cfg::kThreadCols % 32 == 0 && Cfg::kThreadCols < 128) {
+              // 128 accumulators per thread leave no room for 32 more load registers at
+              // the 168-register limit of 10+ warps: those drain 16 columns at a time
 #pragma unroll
               for (int pc = 0; pc < Cfg::kThreadCols / 32; ++pc) {
                 uint32_t v[32];

@@ -34,6 +34,7 @@ struct VariantInfo {
   int act_rows;   // activation rows per tile
   int w_rows;     // weight rows per tile
   int partial_bytes;  // fp32 partial sums of one tile (a split tile's piece)
+  int launch_regs;    // registers per thread the kernel must be built with (0: any)
   LaunchFn launch;
   AttrFn set_attr;
   OccupancyFn occupancy;
@@ -73,7 +74,8 @@ constexpr VariantInfo make_variant(const char* name) {
   return VariantInfo{name,          Cfg::kTileN,   Cfg::kStages,  Cfg::kSwap,
                      Cfg::kTma,     Cfg::kDynamic, Cfg::kThreads, Cfg::kSmemBytes,
                      Cfg::kActRows, Cfg::kWRows,   Cfg::kEpiWarps * 32 * Cfg::kThreadCols * 4,
-                     &launch_variant<Cfg>, &set_attr_variant<Cfg>, &occupancy_variant<Cfg>};
+                     Cfg::kLaunchRegs, &launch_variant<Cfg>, &set_attr_variant<Cfg>,
+                     &occupancy_variant<Cfg>};
 }
 
 // Defined in mslkb.cu, for the allocation-free entry point in mslkb_noalloc.cu.

@@ -204,6 +204,10 @@ mslkb_status ensure_attr(DeviceState* st, int vi) {
   e = variant(vi)->occupancy(&blocks, &regs);
   if (e != cudaSuccess) return cuda_fail(e);
   if (blocks < 1) return cuda_fail(cudaErrorLaunchOutOfResources);
+  // a kernel that moves registers between warpgroups must start with exactly the budget
+  // its split adds up to; with fewer, the warps asking for more would never get them
+  if (variant(vi)->launch_regs != 0 && regs != variant(vi)->launch_regs)
+    return cuda_fail(cudaErrorInvalidConfiguration);
   std::lock_guard<std::mutex> lock(g_mutex);
   st->attr_done[vi >> 6] |= bit;
   return MSLKB_OK;
