@@ -254,9 +254,9 @@ def sweep_shape(fx, wl, pk, device):
             for i in range(n_sets):
                 run_call(fx, sets[i], outs[i], wl, sp)
             stream.synchronize()
-    # calls per replay: enough for ~2 ms of work, a multiple of the set count
+    # calls per replay: ~10 ms of work and at least 16 calls, a multiple of the set count
     t_est = max(roofline_times(wl, pk)) * 1.5 + 3e-6
-    reps = max(1, min(200, int(2e-3 / t_est) // n_sets)) * n_sets
+    reps = max(16 // n_sets + 1, min(400, int(1e-2 / t_est) // n_sets)) * n_sets
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=stream):
         for r in range(reps):

@@ -433,6 +433,12 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     ptx::tmem_alloc(ptx::smem_addr(tmem_holder), Cfg::kTmemCols);
     ptx::tmem_relinquish();
   }
+  // Everything above is CTA-local.  With programmatic dependent launch the next kernel on
+  // the stream may begin launching now; this kernel's first global-memory access (the
+  // metadata, operands, scales, output, split workspace, status word) waits below until
+  // the kernels it depends on have completed.
+  if (threadIdx.x == 0) ptx::griddep_launch_dependents();
+  ptx::griddep_wait();
   if (warp == Cfg::kEpiWarp0) build_sched<Cfg>(p, rowinfo, tile_pre, lane);
   ptx::tc_fence_before_sync();
   __syncthreads();

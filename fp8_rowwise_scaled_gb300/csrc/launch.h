@@ -47,8 +47,13 @@ cudaError_t launch_variant(const LaunchArgs& a) {
   cfg.blockDim = dim3(Cfg::kThreads, 1, 1);
   cfg.dynamicSmemBytes = Cfg::kSmemBytes;
   cfg.stream = a.stream;
-  cfg.attrs = nullptr;
-  cfg.numAttrs = 0;
+  // programmatic dependent launch: the kernel waits (griddepcontrol.wait) before touching
+  // global memory, so it may start launching while the previous kernel on the stream ends
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<Cfg>, a.params, a.tmA, a.tmB, a.tmC);
 }
 

@@ -222,6 +222,15 @@ __device__ __forceinline__ void tmem_ld_x32(uint32_t taddr, uint32_t (&r)[32]) {
       : "r"(taddr));
 }
 
+// Programmatic dependent launch: let the next kernel on the stream start launching, and
+// wait until the kernels this one depends on have completed and their writes are visible.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // Move registers between warpgroups of a CTA (all four warps of a warpgroup execute it).
 template <uint32_t kRegs>
 __device__ __forceinline__ void setmaxnreg_dec() {

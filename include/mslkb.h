@@ -230,8 +230,10 @@ MSLKB_API mslkb_status mslkb_set_split_k(int32_t enable);
  * 1e-6 * sum|terms|.  So the kernel lets the tensor core sum at most `kblocks` blocks of
  * 128 K elements into one TMEM buffer, and its epilogue adds each such partial sum into
  * fp32 registers with round-to-nearest (the accumulator is still fp32 and is never
- * rounded to a narrower type before the scales are applied).  Default 4 (512 K elements);
- * 0 lets the tensor core accumulate the whole K.  Applies to every following call from
+ * rounded to a narrower type before the scales are applied).  Default 8 (1024 K
+ * elements): partial sums built to cancel inside every chunk then stay within half the
+ * tolerance on GB300 (4 K-blocks: a quarter; 16: just over it); 0 lets the tensor core
+ * accumulate the whole K.  Applies to every following call from
  * any thread; a tuning and test hook.  Negative values give MSLKB_ERR_SHAPE.
  */
 MSLKB_API mslkb_status mslkb_set_accumulation_chunk(int32_t kblocks);

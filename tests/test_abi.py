@@ -103,7 +103,7 @@ def test_argument_errors_layout_specific(L):
 
 def test_accumulation_chunk_setting(L):
     old = fx.mslkb_accumulation_chunk()
-    assert old == 4
+    assert old == 8
     try:
         fx.mslkb_set_accumulation_chunk(0)
         assert fx.mslkb_accumulation_chunk() == 0

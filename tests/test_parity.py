@@ -310,10 +310,12 @@ def test_accumulator_cancellation(orc):
 
 
 def test_accumulator_cancellation_inside_chunks(orc):
-    """The same stress at the scale of one accumulation chunk: every 512 K elements (the
-    default chunk) the second 256 products mirror the first 256 with the opposite sign,
-    so each chunk's own partial sums climb and cancel, and the chunk totals are ~0."""
-    K, N, M, half = 16384, 128, 24, 256
+    """The same stress at the scale of one accumulation chunk (the library's current
+    chunk length): in every chunk the second half of the products mirrors the first with
+    the opposite sign, so each chunk's own partial sums climb and cancel, and the chunk
+    totals are ~0 -- the worst case for the tensor core's round-toward-zero adds."""
+    half = 64 * fx.mslkb_accumulation_chunk()  # a chunk is 128 K elements per K-block
+    K, N, M = 16384, 128, 24
     g = torch.Generator().manual_seed(23)
     a = random_codes((M, K), g).numpy() & 0x7F
     b = random_codes((1, N, K), g).numpy() & 0x7F
