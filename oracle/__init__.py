@@ -89,6 +89,10 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_dynamic_rows.argtypes = [p, p, p, p, p, i64, i64, i64, i64, p, i64, p,
                                         ctypes.c_int]
     lib.oracle_dynamic_rows.restype = None
+    lib.oracle_offsets.argtypes = [p, p, p, p, p, i64, i64, i64, i64, p, ctypes.c_int]
+    lib.oracle_offsets.restype = ctypes.c_int
+    lib.oracle_batched.argtypes = [p, p, p, p, i64, i64, i64, i64, p, ctypes.c_int]
+    lib.oracle_batched.restype = None
     lib.oracle_dot_int.argtypes = [p, p, i64]
     lib.oracle_dot_int.restype = ctypes.c_int64
     lib.oracle_dot.argtypes = [p, p, i64]
@@ -211,6 +215,40 @@ class Oracle:
         out = np.full((G * E, N), 0xABCD, dtype=np.uint16)
         self.lib.oracle_dynamic(_ptr(A), _ptr(B), _ptr(sa), _ptr(sb), _ptr(z), G, E, N, K,
                                 _ptr(out), int(threads))
+        return out
+
+    def offsets(self, A, B, scale_a, scale_b, offsets, total_M=None, out=None,
+                threads: int = 0):
+        """Offsets layout: offsets [G] int32 inclusive prefix (group g owns rows
+        [offsets[g-1], offsets[g])).  Returns (out [total_M, N] u16, clamped)."""
+        A = _c(A, np.uint8)
+        B = _c(B, np.uint8)
+        G, N, K = B.shape
+        if total_M is None:
+            total_M = A.shape[0]
+        sa = _c(scale_a, np.float32)
+        sb = _c(scale_b, np.float32).reshape(G, N)
+        o = _c(offsets, np.int32)
+        assert o.size == G and A.shape == (total_M, K) and sa.size == total_M
+        out = np.zeros((total_M, N), dtype=np.uint16) if out is None else \
+            _c(out, np.uint16).copy()
+        clamped = self.lib.oracle_offsets(_ptr(A), _ptr(B), _ptr(sa), _ptr(sb), _ptr(o), G, N,
+                                          K, int(total_M), _ptr(out), int(threads))
+        return out, bool(clamped)
+
+    def batched(self, A, B, scale_a, scale_b, threads: int = 0):
+        """Batched layout: A [G*M, K] (or [G, M, K]), every row of every slab computed.
+        Returns out [G*M, N] u16."""
+        B = _c(B, np.uint8)
+        G, N, K = B.shape
+        sa = _c(scale_a, np.float32)
+        M = sa.size // G if G else 0
+        A = _c(A, np.uint8).reshape(G * M, K)
+        sb = _c(scale_b, np.float32).reshape(G, N)
+        assert A.shape[0] == G * M and sa.size == G * M
+        out = np.full((G * M, N), 0xABCD, dtype=np.uint16)
+        self.lib.oracle_batched(_ptr(A), _ptr(B), _ptr(sa), _ptr(sb), G, M, N, K, _ptr(out),
+                                int(threads))
         return out
 
     def dynamic_rows(self, A, B, scale_a, scale_b, zsi, expected_m: int, rows,

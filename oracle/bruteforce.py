@@ -119,3 +119,16 @@ def dynamic(A, B, scale_a, scale_b, zsi, expected_m):
                 else:
                     out[(row, n)] = 0x0000
     return out
+
+
+def offsets(A, B, scale_a, scale_b, offsets_incl, total_M):
+    """Group g owns rows [offsets[g-1], offsets[g]) (offsets[-1] = 0): the row counts are
+    the steps between successive inclusive offsets."""
+    counts = [int(offsets_incl[g]) - (int(offsets_incl[g - 1]) if g else 0)
+              for g in range(len(offsets_incl))]
+    return stacked(A, B, scale_a, scale_b, counts, total_M)
+
+
+def batched(A, B, scale_a, scale_b, M):
+    G = len(B)
+    return dynamic(A, B, scale_a, scale_b, [M] * G, M)

@@ -403,6 +403,54 @@ void oracle_dynamic_rows(const uint8_t *A, const uint8_t *B, const float *scale_
     }
 }
 
+/* ------------------------------------------------------------------------------ */
+/* Offsets layout (2D-3D, the torch-native grouped mm addressing; MSLK #471, commit  */
+/* decoding group boundaries from an int32 inclusive prefix sum): offsets[g] is the  */
+/* end row of group g, so group g owns rows [offsets[g-1], offsets[g]) with          */
+/* offsets[-1] = 0 -- a row count is the step between successive offsets.  Counts    */
+/* then follow the stacked rules (a negative step owns no rows; rows past total_M    */
+/* are clamped).  Returns the stacked clamp flag.                                    */
+/* ------------------------------------------------------------------------------ */
+int oracle_offsets(const uint8_t *A, const uint8_t *B, const float *scale_a,
+                   const float *scale_b, const int32_t *offsets, int64_t G, int64_t N,
+                   int64_t K, int64_t total_M, uint16_t *out, int nthreads)
+{
+    int64_t *m = (int64_t *)malloc(sizeof(int64_t) * (size_t)(G > 0 ? G : 1));
+    if (!m) return -1;
+    for (int64_t g = 0; g < G; ++g)
+        m[g] = (int64_t)offsets[g] - (g > 0 ? (int64_t)offsets[g - 1] : 0);
+    int clamped = oracle_stacked(A, B, scale_a, scale_b, m, G, N, K, total_M, out, nthreads);
+    free(m);
+    return clamped;
+}
+
+/* ------------------------------------------------------------------------------ */
+/* Batched layout (3D-3D; MSLK #471, commit adding the layout whose groups all carry */
+/* their full complement of rows): group g owns the whole slab [g*M, (g+1)*M), every */
+/* row computed, and no metadata is read.                                           */
+/* ------------------------------------------------------------------------------ */
+void oracle_batched(const uint8_t *A, const uint8_t *B, const float *scale_a,
+                    const float *scale_b, int64_t G, int64_t M, int64_t N, int64_t K,
+                    uint16_t *out, int nthreads)
+{
+    double lut[256];
+    fill_lut(lut);
+    int64_t rows = G * M;
+#ifdef _OPENMP
+    if (nthreads <= 0) nthreads = omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads)
+#else
+    (void)nthreads;
+#endif
+    for (int64_t row = 0; row < rows; ++row) {
+        int64_t g = row / M;
+        const uint8_t *arow = A + (size_t)row * (size_t)K;
+        uint16_t *o = out + (size_t)row * (size_t)N;
+        for (int64_t n = 0; n < N; ++n)
+            o[n] = element_gn(arow, B, scale_b, g, n, N, K, scale_a[row], lut);
+    }
+}
+
 /* Exact unscaled dot products as integers: S * 2^18 for one (row, n) pair, using   */
 /* the integer form of each code (value * 2^9).  Lets a test check the fp64 sum     */
 /* against integer arithmetic.  NaN codes yield INT64_MIN.                          */

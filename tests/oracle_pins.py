@@ -417,10 +417,47 @@ def pin_sampled_rows(orc, seed=41):
     assert np.array_equal(orc.dynamic_rows(Ad, B, sad, sb, [3, 7, 0], E, rows), dy[rows])
 
 
+def pin_offsets_layout(orc, cases=20, seed=43):
+    """Offsets layout: brute force on tiny cases, and bit-equal to the stacked layout fed
+    the steps between successive offsets."""
+    rng = _rng(seed)
+    for i in range(cases):
+        A, B, sa, sb, m, total = _tiny_stacked_case(rng)
+        incl = np.cumsum(m).astype(np.int32)
+        out, _ = orc.offsets(A, B, sa, sb, incl, total_M=total,
+                             out=np.full((total, B.shape[1]), 0xDEAD, np.uint16))
+        ref = bf.offsets(A.tolist(), B.tolist(), sa.tolist(), sb.tolist(), incl.tolist(), total)
+        for (r, n), bits in ref.items():
+            got = int(out[r, n])
+            assert got == bits or (bits == 0 and got == 0x8000), f"case {i} ({r},{n})"
+        st, _ = orc.stacked(A, B, sa, sb, m, total_M=total,
+                            out=np.full((total, B.shape[1]), 0xDEAD, np.uint16))
+        assert np.array_equal(out, st), f"case {i}: offsets != stacked"
+
+
+def pin_batched_layout(orc, cases=15, seed=47):
+    """Batched layout: brute force on tiny cases, and bit-equal to the dynamic layout with
+    every slab full."""
+    rng = _rng(seed)
+    for i in range(cases):
+        G, M = int(rng.integers(1, 4)), int(rng.integers(1, 5))
+        N, K = int(rng.integers(1, 7)), int(rng.choice([0, 1, 9, 32]))
+        A = _random_codes(rng, (G * M, K))
+        B = _random_codes(rng, (G, N, K))
+        sa = _random_scales(rng, G * M)
+        sb = _random_scales(rng, G * N).reshape(G, N)
+        out = orc.batched(A, B, sa, sb)
+        ref = bf.batched(A.tolist(), B.tolist(), sa.tolist(), sb.tolist(), M)
+        for (r, n), bits in ref.items():
+            got = int(out[r, n])
+            assert got == bits or (bits == 0 and got == 0x8000), f"case {i} ({r},{n})"
+        assert np.array_equal(out, orc.dynamic(A, B, sa, sb, [M] * G, M)), f"case {i}"
+
+
 PINS = [
     pin_decode_vs_torch, pin_decode_golden, pin_bf16_golden, pin_bf16_vs_torch,
     pin_dot_exact, pin_closed_form_k1, pin_closed_form_all_ones, pin_closed_form_identity,
     pin_coherent_groups, pin_golden_tiny, pin_bruteforce_stacked, pin_bruteforce_dynamic,
     pin_scale_factoring, pin_stacked_ownership, pin_padding_zero, pin_layout_agreement,
-    pin_k_zero, pin_sampled_rows,
+    pin_k_zero, pin_sampled_rows, pin_offsets_layout, pin_batched_layout,
 ]
