@@ -42,7 +42,8 @@ METRIC = "FP8 grouped GEMM TFLOPS, µs/call, % of roofline (FP8 peak or HBM) per
 UNIT = "TFLOPS"
 HEADLINE = "c4_llama405b"
 SWEEP = ["c2a_dsv3_gate_up", "c2b_dsv3_down", "c3_llama70b_m1", "c3_llama70b_m16",
-         "c3_llama70b_m128", "c3_llama70b_m1024", "c3_llama70b_m8192"]
+         "c3_llama70b_m128", "c3_llama70b_m1024", "c3_llama70b_m8192",
+         "n1_batched_llama70b_m512", "n2_offsets_llama70b_m8192"]
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 FP8_OVER_BF16 = 2.0  # nominal dense ratio (4.5 / 2.25 PFLOP/s)
@@ -215,6 +216,16 @@ def run_call(fx, inp, out, wl, stream_ptr):
             inp["A"].data_ptr(), inp["B"].data_ptr(), inp["scale_a"].data_ptr(),
             inp["scale_b"].data_ptr(), inp["meta"].data_ptr(), out.data_ptr(), wl.rows, wl.G,
             wl.N, wl.K, stream_ptr)
+    elif wl.layout == "offsets":
+        s = fx.mslkb_f8f8bf16_rowwise_grouped_offsets(
+            inp["A"].data_ptr(), inp["B"].data_ptr(), inp["scale_a"].data_ptr(),
+            inp["scale_b"].data_ptr(), inp["meta"].data_ptr(), out.data_ptr(), wl.rows, wl.G,
+            wl.N, wl.K, stream_ptr)
+    elif wl.layout == "batched":
+        s = fx.mslkb_f8f8bf16_rowwise_grouped_batched(
+            inp["A"].data_ptr(), inp["B"].data_ptr(), inp["scale_a"].data_ptr(),
+            inp["scale_b"].data_ptr(), out.data_ptr(), wl.G, wl.expected_m, wl.N, wl.K,
+            stream_ptr)
     else:
         s = fx.mslkb_f8f8bf16_rowwise_grouped_dynamic(
             inp["A"].data_ptr(), inp["B"].data_ptr(), inp["scale_a"].data_ptr(),
@@ -231,9 +242,8 @@ def roofline_times(wl, pk):
 
 
 def plan_for(fx, wl, sms):
-    return fx.mslkb_plan(0 if wl.layout == "stacked" else 1,
-                         wl.rows if wl.layout == "stacked" else wl.expected_m, wl.G, wl.N,
-                         wl.K, sms)
+    return fx.mslkb_plan(1 if wl.slabs else 0, wl.expected_m if wl.slabs else wl.rows, wl.G,
+                         wl.N, wl.K, sms)
 
 
 def sweep_shape(fx, wl, pk, device):

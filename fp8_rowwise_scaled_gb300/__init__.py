@@ -78,6 +78,12 @@ def lib() -> ctypes.CDLL:
                 fn = getattr(L, name)
                 fn.argtypes = [p, p, p, p, p, p, i64, i64, i64, i64, p]
                 fn.restype = ctypes.c_int
+            L.mslkb_f8f8bf16_rowwise_grouped_offsets.argtypes = [p, p, p, p, p, p, i64, i64,
+                                                                 i64, i64, p]
+            L.mslkb_f8f8bf16_rowwise_grouped_offsets.restype = ctypes.c_int
+            L.mslkb_f8f8bf16_rowwise_grouped_batched.argtypes = [p, p, p, p, p, i64, i64, i64,
+                                                                 i64, p]
+            L.mslkb_f8f8bf16_rowwise_grouped_batched.restype = ctypes.c_int
             L.mslkb_status_string.argtypes = [ctypes.c_int]
             L.mslkb_status_string.restype = ctypes.c_char_p
             L.mslkb_last_cuda_error.argtypes = []
@@ -130,6 +136,18 @@ def mslkb_f8f8bf16_rowwise_grouped_stacked_noalloc(A, B, scale_a, scale_b, m_siz
     nothing (for callers recording CUDA graphs or whose framework owns all memory)."""
     return lib().mslkb_f8f8bf16_rowwise_grouped_stacked_noalloc(
         A, B, scale_a, scale_b, m_sizes, out, total_M, G, N, K, stream)
+
+
+def mslkb_f8f8bf16_rowwise_grouped_offsets(A, B, scale_a, scale_b, offsets, out, total_M, G,
+                                           N, K, stream=0) -> int:
+    return lib().mslkb_f8f8bf16_rowwise_grouped_offsets(A, B, scale_a, scale_b, offsets, out,
+                                                        total_M, G, N, K, stream)
+
+
+def mslkb_f8f8bf16_rowwise_grouped_batched(A, B, scale_a, scale_b, out, G, M, N, K,
+                                           stream=0) -> int:
+    return lib().mslkb_f8f8bf16_rowwise_grouped_batched(A, B, scale_a, scale_b, out, G, M, N,
+                                                        K, stream)
 
 
 def mslkb_status_string(status: int) -> str:
@@ -300,6 +318,57 @@ def f8f8bf16_rowwise_grouped_dynamic(XQ, WQ, x_scale, w_scale, zero_start_index_
         zero_start_index_M.data_ptr(), out.data_ptr(), G, E, N, K, _stream_ptr(stream))
     if s != MSLKB_OK:
         raise MslkbError(s, "f8f8bf16_rowwise_grouped_dynamic")
+    return out
+
+
+def f8f8bf16_rowwise_grouped_offsets(XQ, WQ, x_scale, w_scale, offsets, out=None,
+                                     stream=None):
+    """XQ [total_M, K] e4m3, WQ [G, N, K] e4m3, x_scale [total_M], w_scale [G, N] fp32,
+    offsets [G] int32 inclusive prefix (group g owns rows [offsets[g-1], offsets[g]))
+    -> out [total_M, N] bf16 (rows past offsets[G-1] zeroed when out is allocated here)."""
+    import torch
+    _check(XQ, "XQ", _fp8_types(), 2)
+    _check(WQ, "WQ", _fp8_types(), 3)
+    _check(x_scale, "x_scale", (torch.float32,))
+    _check(w_scale, "w_scale", (torch.float32,))
+    _check(offsets, "offsets", (torch.int32,), 1)
+    total_M, K = XQ.shape
+    G, N, K2 = WQ.shape
+    if K2 != K or x_scale.numel() != total_M or w_scale.numel() != G * N or offsets.numel() != G:
+        raise ValueError("inconsistent shapes")
+    if out is None:
+        out = torch.zeros((total_M, N), dtype=torch.bfloat16, device=XQ.device)
+    else:
+        _check(out, "out", (torch.bfloat16,), 2)
+    s = mslkb_f8f8bf16_rowwise_grouped_offsets(
+        XQ.data_ptr(), WQ.data_ptr(), x_scale.data_ptr(), w_scale.data_ptr(),
+        offsets.data_ptr(), out.data_ptr(), total_M, G, N, K, _stream_ptr(stream))
+    if s != MSLKB_OK:
+        raise MslkbError(s, "f8f8bf16_rowwise_grouped_offsets")
+    return out
+
+
+def f8f8bf16_rowwise_grouped_batched(XQ, WQ, x_scale, w_scale, out=None, stream=None):
+    """XQ [G, M, K] e4m3, WQ [G, N, K] e4m3, x_scale [G, M], w_scale [G, N] fp32
+    -> out [G, M, N] bf16; every row of every slab computed."""
+    import torch
+    _check(XQ, "XQ", _fp8_types(), 3)
+    _check(WQ, "WQ", _fp8_types(), 3)
+    _check(x_scale, "x_scale", (torch.float32,))
+    _check(w_scale, "w_scale", (torch.float32,))
+    G, M, K = XQ.shape
+    G2, N, K2 = WQ.shape
+    if G2 != G or K2 != K or x_scale.numel() != G * M or w_scale.numel() != G * N:
+        raise ValueError("inconsistent shapes")
+    if out is None:
+        out = torch.empty((G, M, N), dtype=torch.bfloat16, device=XQ.device)
+    else:
+        _check(out, "out", (torch.bfloat16,))
+    s = mslkb_f8f8bf16_rowwise_grouped_batched(
+        XQ.data_ptr(), WQ.data_ptr(), x_scale.data_ptr(), w_scale.data_ptr(), out.data_ptr(),
+        G, M, N, K, _stream_ptr(stream))
+    if s != MSLKB_OK:
+        raise MslkbError(s, "f8f8bf16_rowwise_grouped_batched")
     return out
 
 

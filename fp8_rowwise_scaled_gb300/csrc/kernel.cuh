@@ -56,6 +56,8 @@ struct GemmParams {
   int32_t E;               // expected_m (dynamic only)
   int32_t num_kb;          // ceil(K / 128)
   int32_t copy_width;      // cp.async loader: bytes per copy (16, 8, 4) or 1 (byte loads)
+  int32_t meta_kind;       // stacked: 0 int64 m_sizes, 1 int32 inclusive offsets;
+                           // dynamic: 0 int64 zero_start_index_M, 2 none (full slabs)
   int32_t kb_per_chunk;    // K blocks the tensor core sums before the epilogue takes over
   int32_t split_k;         // 1: split the last waves' tiles along K over all CTAs
   float* sk_ws;            // split tiles: fp32 partial sums, 2 slots per CTA
@@ -304,22 +306,31 @@ __device__ void build_sched(const GemmParams& p, int32_t* rowinfo, int32_t* tile
   bool clamped = false;
   if constexpr (Cfg::kDynamic) {
     for (int32_t g = g0; g < g1; ++g) {
-      int64_t v = p.meta[g];
+      // full slabs (batched layout) read no metadata
+      int64_t v = p.meta_kind == 2 ? p.E : p.meta[g];
       v = v < 0 ? 0 : (v > p.E ? p.E : v);
       rowinfo[g] = static_cast<int32_t>(v);
     }
   } else {
+    // rows of group g: m_sizes[g], or the step between successive int32 inclusive
+    // offsets (offsets[-1] = 0)
+    const int32_t* offs = reinterpret_cast<const int32_t*>(p.meta);
+    auto count = [&](int32_t g) -> int64_t {
+      if (p.meta_kind == 1)
+        return static_cast<int64_t>(offs[g]) - (g > 0 ? static_cast<int64_t>(offs[g - 1]) : 0);
+      return p.meta[g];
+    };
     // clamped exclusive prefix: off_g = min(sum_{h<g} max(m_h, 0), total_M)
     int64_t my_sum = 0;
     for (int32_t g = g0; g < g1; ++g) {
-      const int64_t m = p.meta[g];
+      const int64_t m = count(g);
       if (m < 0) clamped = true;
       my_sum += m < 0 ? 0 : m;
     }
     const int64_t total = p.rows;
     int64_t run = warp_incl_scan(my_sum, lane) - my_sum;
     for (int32_t g = g0; g < g1; ++g) {
-      const int64_t m = p.meta[g];
+      const int64_t m = count(g);
       rowinfo[g] = static_cast<int32_t>(run < total ? run : total);
       run += m < 0 ? 0 : m;
     }

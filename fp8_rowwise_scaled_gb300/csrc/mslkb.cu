@@ -381,12 +381,15 @@ mslkb_status check_sizes(int64_t rows, int64_t G, int64_t N, int64_t K) {
   return MSLKB_OK;
 }
 
+// meta_kind: stacked 0 (int64 m_sizes) / 1 (int32 inclusive offsets); dynamic 0 (int64
+// zero_start_index_M) / 2 (no metadata: every slab full)
 mslkb_status run(int layout, const void* A, const void* B, const float* scale_a,
-                 const float* scale_b, const int64_t* meta, void* out, int64_t rows, int64_t G,
-                 int64_t E, int64_t N, int64_t K, void* stream) {
+                 const float* scale_b, const void* meta, void* out, int64_t rows, int64_t G,
+                 int64_t E, int64_t N, int64_t K, void* stream, int meta_kind = 0) {
   // rows: total_M (stacked) or G * E (dynamic)
   if (rows == 0 || N == 0 || G == 0) return MSLKB_OK;  // nothing is owned or written
-  if (out == nullptr || meta == nullptr || scale_a == nullptr || scale_b == nullptr)
+  if (out == nullptr || (meta == nullptr && meta_kind != 2) || scale_a == nullptr ||
+      scale_b == nullptr)
     return MSLKB_ERR_NULL;
   if (K > 0 && (A == nullptr || B == nullptr)) return MSLKB_ERR_NULL;
   if (reinterpret_cast<uintptr_t>(out) % 16 != 0) return MSLKB_ERR_ALIGN;
@@ -410,7 +413,8 @@ mslkb_status run(int layout, const void* A, const void* B, const float* scale_a,
   p.B = static_cast<const uint8_t*>(B);
   p.scale_a = scale_a;
   p.scale_b = scale_b;
-  p.meta = meta;
+  p.meta = static_cast<const int64_t*>(meta);
+  p.meta_kind = meta_kind;
   p.out = static_cast<uint16_t*>(out);
   p.status = st->status_ptr;
   p.rows = static_cast<int32_t>(rows);
@@ -558,6 +562,27 @@ mslkb_status mslkb_f8f8bf16_rowwise_grouped_dynamic(const void* A, const void* B
   if (expected_m > 0 && G > MSLKB_MAX_DIM / expected_m) return MSLKB_ERR_SHAPE;
   return run(1, A, B, scale_a, scale_b, zero_start_index_M, out, G * expected_m, G, expected_m, N,
              K, stream);
+}
+
+mslkb_status mslkb_f8f8bf16_rowwise_grouped_offsets(const void* A, const void* B,
+                                                    const float* scale_a, const float* scale_b,
+                                                    const int32_t* offsets, void* out,
+                                                    int64_t total_M, int64_t G, int64_t N,
+                                                    int64_t K, void* stream) {
+  mslkb_status s = check_sizes(total_M, G, N, K);
+  if (s != MSLKB_OK) return s;
+  return run(0, A, B, scale_a, scale_b, offsets, out, total_M, G, 0, N, K, stream, 1);
+}
+
+mslkb_status mslkb_f8f8bf16_rowwise_grouped_batched(const void* A, const void* B,
+                                                    const float* scale_a, const float* scale_b,
+                                                    void* out, int64_t G, int64_t M, int64_t N,
+                                                    int64_t K, void* stream) {
+  if (M < 0) return MSLKB_ERR_SHAPE;
+  mslkb_status s = check_sizes(0, G, N, K);
+  if (s != MSLKB_OK) return s;
+  if (M > 0 && G > MSLKB_MAX_DIM / M) return MSLKB_ERR_SHAPE;
+  return run(1, A, B, scale_a, scale_b, nullptr, out, G * M, G, M, N, K, stream, 2);
 }
 
 const char* mslkb_status_string(mslkb_status status) {

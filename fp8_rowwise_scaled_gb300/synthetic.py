@@ -71,12 +71,13 @@ def multinomial_counts(seed: int, total: int, probs: list[float]) -> list[int]:
 class Workload:
     """One problem: layout, sizes and group metadata (m_sizes or zero_start_index_M)."""
     name: str
-    layout: str            # "stacked" or "dynamic"
+    layout: str            # "stacked", "dynamic", "offsets" or "batched"
     G: int
     N: int
     K: int
     rows: int              # total_M (stacked) or G * expected_m (dynamic)
-    meta: tuple            # m_sizes (stacked) or zero_start_index_M (dynamic)
+    meta: tuple            # m_sizes (stacked), zero_start_index_M (dynamic), int32
+                           # inclusive offsets (offsets); empty (batched)
     seed: int
     expected_m: int = 0    # dynamic only
     note: str = ""
@@ -86,15 +87,27 @@ class Workload:
     def total_M(self) -> int:
         return self.rows
 
-    def valid_rows(self) -> int:
+    def counts(self) -> list:
+        """Rows of each group."""
         if self.layout == "stacked":
-            return sum(self.meta)
-        return sum(max(0, min(v, self.expected_m)) for v in self.meta)
+            return [max(0, m) for m in self.meta]
+        if self.layout == "offsets":
+            return [max(0, self.meta[g] - (self.meta[g - 1] if g else 0))
+                    for g in range(self.G)]
+        if self.layout == "batched":
+            return [self.expected_m] * self.G
+        return [max(0, min(v, self.expected_m)) for v in self.meta]
+
+    @property
+    def slabs(self) -> bool:
+        """True for the layouts whose groups own fixed slabs of expected_m rows."""
+        return self.layout in ("dynamic", "batched")
+
+    def valid_rows(self) -> int:
+        return sum(self.counts())
 
     def nonempty_groups(self) -> int:
-        if self.layout == "stacked":
-            return sum(1 for m in self.meta if m > 0)
-        return sum(1 for v in self.meta if min(v, self.expected_m) > 0)
+        return sum(1 for c in self.counts() if c > 0)
 
     def flops(self) -> int:
         """Algorithmic flops: 2 * (valid rows) * N * K."""
@@ -108,10 +121,10 @@ class Workload:
         v = self.valid_rows()
         nz = self.nonempty_groups()
         b = v * self.K + 4 * v + nz * self.N * self.K + 4 * nz * self.N + 8 * self.G
-        if self.layout == "stacked":
-            b += 2 * v * self.N
-        else:
+        if self.slabs:
             b += 2 * self.G * self.expected_m * self.N
+        else:
+            b += 2 * v * self.N
         return b
 
 
@@ -152,6 +165,21 @@ def workloads() -> dict[str, Workload]:
         nm = f"c3_llama70b_m{tm}"
         w[nm] = _stacked(nm, 3, i, 16, 8192, 8192, m3,
                          f"llama3-70b: G=16, N=K=8192, total_M={tm} uniform", ("perf",))
+    # NEXT rows: the same llama3-70b total_M = 8192 routing given as int32 inclusive
+    # offsets, and a batched (every slab full) problem of the same size
+    m3 = w["c3_llama70b_m8192"].meta
+    incl, acc = [], 0
+    for m in m3:
+        acc += m
+        incl.append(acc)
+    w["n2_offsets_llama70b_m8192"] = Workload(
+        name="n2_offsets_llama70b_m8192", layout="offsets", G=16, N=8192, K=8192, rows=acc,
+        meta=tuple(incl), seed=1000 * 3 + 4,
+        note="llama3-70b total_M=8192 routing as int32 inclusive offsets", tags=("perf",))
+    w["n1_batched_llama70b_m512"] = Workload(
+        name="n1_batched_llama70b_m512", layout="batched", G=16, N=8192, K=8192,
+        rows=16 * 512, meta=(), seed=1000 * 5 + 0, expected_m=512,
+        note="batched: G=16 full slabs of 512 rows, N=K=8192", tags=("perf",))
     # 4: llama3-405b-shaped
     m4 = multinomial_counts(1000 * 4 + 0, 16384, [1.0 / 16] * 16)
     w["c4_llama405b"] = _stacked("c4_llama405b", 4, 0, 16, 16384, 16384, m4,
@@ -199,7 +227,8 @@ def make_inputs(wl: Workload, device="cpu", chunk_rows: int = 8192):
             n1 = min(N, n0 + chunk_rows)
             x = torch.randn((n1 - n0, K), generator=gen, device=device, dtype=torch.float32)
             B[g, n0:n1], sb[g, n0:n1] = quantize_rows(x)
-    meta = torch.tensor(list(wl.meta), dtype=torch.int64, device=device)
+    mdt = torch.int32 if wl.layout == "offsets" else torch.int64
+    meta = torch.tensor(list(wl.meta), dtype=mdt, device=device)
     return {"A": A, "B": B, "scale_a": sa, "scale_b": sb, "meta": meta}
 
 

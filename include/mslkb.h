@@ -125,6 +125,40 @@ MSLKB_API mslkb_status mslkb_f8f8bf16_rowwise_grouped_dynamic(
     int64_t N, int64_t K, void *stream);
 
 /*
+ * Offsets layout (2D-3D, the torch-native grouped-mm addressing; MSLK #471, commits
+ * decoding group boundaries from an int32 inclusive prefix sum and binding the `_mm` op's
+ * 2D-3D rank combination).  As the stacked call, but the groups are given as
+ *
+ *   offsets  device, int32 [G]   inclusive prefix: group g owns rows
+ *                                [offsets[g-1], offsets[g]) with offsets[-1] = 0
+ *
+ * A row count is the step between successive offsets; a negative step owns no rows and
+ * steps past total_M are clamped (both set MSLKB_DEV_MSIZES_CLAMPED), as for m_sizes.
+ */
+MSLKB_API mslkb_status mslkb_f8f8bf16_rowwise_grouped_offsets(
+    const void *A, const void *B, const float *scale_a, const float *scale_b,
+    const int32_t *offsets, void *out, int64_t total_M, int64_t G, int64_t N, int64_t K,
+    void *stream);
+
+/*
+ * Batched layout (3D-3D; MSLK #471, commit adding the layout whose groups all carry their
+ * full complement of rows, and the one eliding its retire guard).  Every group owns a full
+ * slab of M rows and no metadata is read:
+ *
+ *   A        device, e4m3 codes [G, M, K]
+ *   B        device, e4m3 codes [G, N, K]
+ *   scale_a  device, fp32 [G, M]
+ *   scale_b  device, fp32 [G, N]
+ *   out      device, bf16 [G, M, N], 16-byte aligned
+ *
+ * M need not divide the tile height: rows past a slab are never written (the next slab's
+ * rows belong to the next group).  K and N rules as for the stacked layout.
+ */
+MSLKB_API mslkb_status mslkb_f8f8bf16_rowwise_grouped_batched(
+    const void *A, const void *B, const float *scale_a, const float *scale_b, void *out,
+    int64_t G, int64_t M, int64_t N, int64_t K, void *stream);
+
+/*
  * Allocation-free stacked call (no counterpart on the pages: an addition of this library).
  *
  * For callers that must not allocate device memory: code recording a CUDA graph (memory

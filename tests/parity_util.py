@@ -82,8 +82,12 @@ class Problem:
     def from_numpy(cls, layout, A, B, sa, sb, meta, expected_m=0, device="cuda"):
         def T(x, dt):
             return torch.from_numpy(np.ascontiguousarray(x)).to(device=device, dtype=dt)
+        if layout == "offsets":
+            m = T(np.asarray(meta, np.int32), torch.int32)
+        else:
+            m = T(np.asarray(meta, np.int64), torch.int64)
         return cls(layout, T(A, torch.uint8), T(B, torch.uint8), T(sa, torch.float32),
-                   T(sb, torch.float32), T(np.asarray(meta, np.int64), torch.int64), expected_m)
+                   T(sb, torch.float32), m, expected_m)
 
     @classmethod
     def from_inputs(cls, wl, inp):
@@ -105,6 +109,15 @@ class Problem:
             if self.layout == "stacked":
                 return fx.f8f8bf16_rowwise_grouped_stacked(self.A, self.B, self.sa, self.sb,
                                                            self.meta, out=out)
+            if self.layout == "offsets":
+                return fx.f8f8bf16_rowwise_grouped_offsets(self.A, self.B, self.sa, self.sb,
+                                                           self.meta, out=out)
+            if self.layout == "batched":
+                E = self.expected_m
+                res = fx.f8f8bf16_rowwise_grouped_batched(
+                    self.A.view(self.G, E, self.K), self.B, self.sa, self.sb,
+                    out=None if out is None else out.view(self.G, E, self.N))
+                return res.view(self.G * E, self.N)
             return fx.f8f8bf16_rowwise_grouped_dynamic(self.A, self.B, self.sa, self.sb,
                                                        self.meta, out=out)
         finally:
@@ -114,7 +127,16 @@ class Problem:
     # -- the oracle ---------------------------------------------------------------------
     def oracle_full(self, orc, poison=None):
         h = self.host()
-        if self.layout == "stacked":
+        if self.layout == "offsets":
+            ref, _ = orc.offsets(h["A"], h["B"], h["sa"], h["sb"], h["meta"], total_M=self.rows,
+                                 out=poison)
+            ab, _ = orc.offsets(abs_codes(h["A"]), abs_codes(h["B"]), np.abs(h["sa"]),
+                                np.abs(h["sb"]), h["meta"], total_M=self.rows)
+        elif self.layout == "batched":
+            ref = orc.batched(h["A"], h["B"], h["sa"], h["sb"])
+            ab = orc.batched(abs_codes(h["A"]), abs_codes(h["B"]), np.abs(h["sa"]),
+                             np.abs(h["sb"]))
+        elif self.layout == "stacked":
             ref, _ = orc.stacked(h["A"], h["B"], h["sa"], h["sb"], h["meta"], total_M=self.rows,
                                  out=poison)
             ab, _ = orc.stacked(abs_codes(h["A"]), abs_codes(h["B"]), np.abs(h["sa"]),
@@ -127,24 +149,35 @@ class Problem:
 
     def oracle_rows(self, orc, rows):
         h = self.host()
-        if self.layout == "stacked":
-            ref = orc.stacked_rows(h["A"], h["B"], h["sa"], h["sb"], h["meta"], rows)
+        if self.layout in ("stacked", "offsets"):
+            # sampled rows via the stacked oracle on the groups' row counts (the offsets
+            # pin checks the two layouts agree bit for bit)
+            cnt = np.array(self.counts(), np.int64)
+            ref = orc.stacked_rows(h["A"], h["B"], h["sa"], h["sb"], cnt, rows)
             ab = orc.stacked_rows(abs_codes(h["A"]), abs_codes(h["B"]), np.abs(h["sa"]),
-                                  np.abs(h["sb"]), h["meta"], rows)
+                                  np.abs(h["sb"]), cnt, rows)
         else:
-            ref = orc.dynamic_rows(h["A"], h["B"], h["sa"], h["sb"], h["meta"],
-                                   self.expected_m, rows)
+            zsi = h["meta"] if self.layout == "dynamic" else \
+                np.full(self.G, self.expected_m, np.int64)
+            ref = orc.dynamic_rows(h["A"], h["B"], h["sa"], h["sb"], zsi, self.expected_m, rows)
             ab = orc.dynamic_rows(abs_codes(h["A"]), abs_codes(h["B"]), np.abs(h["sa"]),
-                                  np.abs(h["sb"]), h["meta"], self.expected_m, rows)
+                                  np.abs(h["sb"]), zsi, self.expected_m, rows)
         return ref, ab
 
-    def owned_rows_mask(self):
+    def counts(self):
+        """Rows of each group before clamping (stacked-like layouts)."""
         h = self.host()
+        if self.layout == "offsets":
+            o = [int(x) for x in h["meta"]]
+            return [o[g] - (o[g - 1] if g else 0) for g in range(len(o))]
+        return [int(x) for x in h["meta"]]
+
+    def owned_rows_mask(self):
         mask = np.zeros(self.rows, dtype=bool)
-        if self.layout == "stacked":
+        if self.layout in ("stacked", "offsets"):
             off = 0
-            for m in h["meta"]:
-                m = max(0, min(int(m), self.rows - off))
+            for m in self.counts():
+                m = max(0, min(m, self.rows - off))
                 mask[off:off + m] = True
                 off += m
         else:
@@ -156,9 +189,9 @@ class Problem:
         rng = np.random.default_rng(seed)
         h = self.host()
         rows = []
-        if self.layout == "stacked":
+        if self.layout in ("stacked", "offsets"):
             off = 0
-            for m in h["meta"]:
+            for m in self.counts():
                 m = max(0, min(int(m), self.rows - off))
                 if m > 0:
                     rows += [off, off + m - 1]
@@ -166,7 +199,8 @@ class Problem:
                 off += m
         else:
             E = self.expected_m
-            for g, v in enumerate(h["meta"]):
+            zsi = h["meta"] if self.layout == "dynamic" else [E] * self.G
+            for g, v in enumerate(zsi):
                 v = max(0, min(int(v), E))
                 rows += [g * E, g * E + E - 1]
                 if v > 0:

@@ -101,6 +101,20 @@ def test_argument_errors_layout_specific(L):
     assert _stacked(A=0, B=0, K=0, G=0) == fx.MSLKB_OK
 
 
+def test_offsets_and_batched_argument_errors(L):
+    off = lambda **kw: fx.mslkb_f8f8bf16_rowwise_grouped_offsets(
+        *[kw.get(k, d) for k, d in (("A", 16), ("B", 16), ("sa", 16), ("sb", 16), ("o", 16),
+                                     ("out", 256), ("M", 4), ("G", 2), ("N", 8), ("K", 16))], 0)
+    bat = lambda **kw: fx.mslkb_f8f8bf16_rowwise_grouped_batched(
+        *[kw.get(k, d) for k, d in (("A", 16), ("B", 16), ("sa", 16), ("sb", 16),
+                                     ("out", 256), ("G", 2), ("M", 4), ("N", 8), ("K", 16))], 0)
+    assert off(N=12) == fx.MSLKB_ERR_SHAPE and bat(N=12) == fx.MSLKB_ERR_SHAPE
+    assert off(o=0) == fx.MSLKB_ERR_NULL
+    assert off(out=264) == fx.MSLKB_ERR_ALIGN and bat(out=264) == fx.MSLKB_ERR_ALIGN
+    assert bat(sa=0) == fx.MSLKB_ERR_NULL and bat(M=-1) == fx.MSLKB_ERR_SHAPE
+    assert off(M=0) == fx.MSLKB_OK and bat(M=0) == fx.MSLKB_OK and bat(G=0) == fx.MSLKB_OK
+
+
 def test_accumulation_chunk_setting(L):
     old = fx.mslkb_accumulation_chunk()
     assert old == 8

@@ -15,7 +15,8 @@ from parity_util import Problem, bits_of, compare
 pytestmark = pytest.mark.gpu
 
 FULL = ["c2a_dsv3_gate_up", "c2b_dsv3_down", "c3_llama70b_m1", "c3_llama70b_m16",
-        "c3_llama70b_m128", "c3_llama70b_m1024", "c3_llama70b_m8192", "c4_llama405b"]
+        "c3_llama70b_m128", "c3_llama70b_m1024", "c3_llama70b_m8192", "c4_llama405b",
+        "n1_batched_llama70b_m512", "n2_offsets_llama70b_m8192"]
 
 
 @pytest.fixture(scope="module", autouse=True)
