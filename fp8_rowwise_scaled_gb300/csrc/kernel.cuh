@@ -22,10 +22,19 @@
 // generates no tile.  Within a group tiles run n-major (all m-tiles of one weight
 // n-tile are consecutive), so concurrently running CTAs share a weight tile in L2.
 //
-// Two tile shapes:
+// Tile shapes:
 //   normal  (kSwap = false): MMA M = 128 activation rows, MMA N = kTileN weight rows.
 //   swap-AB (kSwap = true) : MMA M = 128 weight rows, MMA N = kTileN activation rows;
 //                            for few rows per group the weights fill the 128-row side.
+//   CTA pair (kPair = true): a cluster of two CTAs on two SMs computes a 256 x 256 tile
+//                            with one cta_group::2 MMA of M = 256 issued by the leader
+//                            (rank 0).  Each CTA loads its own 128 activation rows and
+//                            half of the 256 weight rows per K block -- 32 KB instead of
+//                            the 48 KB a 128 x 256 tile needs per SM -- and its TMEM gets
+//                            the 128 x 256 accumulator of its own rows.  Both CTAs' loads
+//                            complete on the leader's full barrier; the leader's commits
+//                            arrive on both CTAs' barriers; both epilogues arrive on the
+//                            leader's accumulator-empty barrier.
 #pragma once
 
 #include <cstdint>
@@ -65,19 +74,28 @@ struct GemmParams {
   uint64_t timeout_ns;     // give-up time of one pipeline wait
 };
 
-template <int kTileN_, int kStages_, bool kSwap_, bool kTma_, bool kDynamic_, int kEpiWarps_ = 4>
+template <int kTileN_, int kStages_, bool kSwap_, bool kTma_, bool kDynamic_, int kEpiWarps_ = 4,
+          bool kPair_ = false>
 struct KernelCfg {
   static constexpr int kTileN = kTileN_;     // MMA N
   static constexpr int kStages = kStages_;
   static constexpr bool kSwap = kSwap_;
   static constexpr bool kTma = kTma_;
   static constexpr bool kDynamic = kDynamic_;
-  static constexpr int kMmaM = 128;
-  static constexpr int kActRows = kSwap ? kTileN : kMmaM;  // activation rows per tile
-  static constexpr int kWRows = kSwap ? kMmaM : kTileN;    // weight rows per tile
+  // CTA pair (cluster of two, cta_group::2): the leader CTA issues one MMA of M = 256
+  // rows whose A rows and B (weight) rows are split in halves over the two CTAs' shared
+  // memory; each CTA's TMEM receives the 128 x kTileN accumulator of its own rows.  Each
+  // SM then loads half of the weight tile per K block instead of all of it.
+  static constexpr bool kPair = kPair_;
+  static constexpr int kCtas = kPair ? 2 : 1;
+  static constexpr int kMmaM = 128;                           // accumulator rows per CTA
+  static constexpr int kActRows = kSwap ? kTileN : kMmaM;     // activation rows per CTA
+  static constexpr int kWRows = kSwap ? kMmaM : kTileN / kCtas;  // weight rows per CTA
+  static constexpr int kTileAct = kActRows * kCtas;  // activation rows per output tile
+  static constexpr int kTileW = kWRows * kCtas;      // weight rows (columns) per output tile
   static constexpr int kActBytes = kActRows * kBK;
   static constexpr int kWBytes = kWRows * kBK;
-  static constexpr int kStageBytes = kActBytes + kWBytes;
+  static constexpr int kStageBytes = kActBytes + kWBytes;  // one CTA's bytes per stage
   static constexpr int kLoaderWarps = kTma ? 1 : 4;
   static constexpr int kLoaderThreads = 32 * kLoaderWarps;
   static constexpr int kMmaWarp = kLoaderWarps;
@@ -104,7 +122,7 @@ struct KernelCfg {
                                    : (2 * kAccCols <= 256) ? 256
                                                            : 512;
   static constexpr int kCpLag = kStages - 2;  // cp.async groups kept in flight per thread
-  static constexpr uint32_t kIdesc = ptx::idesc_e4m3_f32(kMmaM, kTileN);
+  static constexpr uint32_t kIdesc = ptx::idesc_e4m3_f32(kMmaM * kCtas, kTileN);
 
   // 128-row tiles write the output through shared memory and TMA stores: each epilogue
   // warp stages 32 rows x 32 columns of bf16 (2 KB, 64-byte swizzle) at a time
@@ -129,6 +147,7 @@ struct KernelCfg {
   static_assert(kSmemBytes <= 232448, "shared memory per CTA");
   static_assert(2 * kAccCols <= 512, "two accumulators must fit TMEM");
   static_assert(kEpiWarps == 4 || (kEpiWarps == 8 && !kSwap), "epilogue warp split");
+  static_assert(!kPair || (kTma && !kSwap && kTileN == 256), "CTA pairs: 256 x 256 tiles, TMA");
   static_assert(kThreadCols % 16 == 0, "TMEM load granularity");
   static_assert(!kRegSplit || (kThreads == 384 && kEpiWarp0 == 4 &&
                                128 * kRegsLow + 256 * kRegsHigh == kThreads * kLaunchRegs),
@@ -162,8 +181,10 @@ __device__ __forceinline__ int32_t group_rows(const Sched& s, int32_t g) {
   else return s.rowinfo[g + 1] - s.rowinfo[g];
 }
 
+// crank: this CTA's rank in its pair (0 without pairs); a pair's output tile spans
+// kTileAct rows, of which CTA r owns [m0 + r * kActRows, m0 + (r + 1) * kActRows).
 template <class Cfg>
-__device__ __forceinline__ TileCoord decode_tile(const Sched& s, int32_t t) {
+__device__ __forceinline__ TileCoord decode_tile(const Sched& s, int32_t t, uint32_t crank) {
   // largest g with tile_pre[g] <= t  (tile_pre[0] = 0 <= t < tile_pre[G] = total)
   int32_t lo = 0, hi = s.G;
   while (hi - lo > 1) {
@@ -173,15 +194,15 @@ __device__ __forceinline__ TileCoord decode_tile(const Sched& s, int32_t t) {
   }
   const int32_t g = lo;
   const int32_t cnt = group_rows<Cfg>(s, g);
-  const int32_t mt = (cnt + Cfg::kActRows - 1) / Cfg::kActRows;
+  const int32_t mt = (cnt + Cfg::kTileAct - 1) / Cfg::kTileAct;
   const int32_t local = t - s.tile_pre[g];
   const int32_t n_idx = local / mt;
   const int32_t m_idx = local - n_idx * mt;
   TileCoord c;
   c.g = g;
   const int32_t base = Cfg::kDynamic ? g * s.E : s.rowinfo[g];
-  c.m0 = base + m_idx * Cfg::kActRows;
-  c.n0 = n_idx * Cfg::kWRows;
+  c.m0 = base + m_idx * Cfg::kTileAct + static_cast<int32_t>(crank) * Cfg::kActRows;
+  c.n0 = n_idx * Cfg::kTileW;
   c.valid_end = base + cnt;
   c.zero_end = Cfg::kDynamic ? base + s.E : base + cnt;
   return c;
@@ -213,9 +234,9 @@ struct Item {
   int32_t sk_tile;   // index of a tile shared with other CTAs, else -1
 };
 
-__device__ __forceinline__ Work make_work(int32_t T, int32_t nkb, bool split) {
-  const int32_t P = gridDim.x;
-  const int32_t c = blockIdx.x;
+// c: this worker (a CTA, or a CTA pair), P: the number of workers
+__device__ __forceinline__ Work make_work(int32_t T, int32_t nkb, bool split, int32_t c,
+                                          int32_t P) {
   Work w;
   w.nkb = nkb;
   int32_t dp = T;
@@ -233,10 +254,10 @@ __device__ __forceinline__ Work make_work(int32_t T, int32_t nkb, bool split) {
   return w;
 }
 
-__device__ __forceinline__ Item work_item(const Work& w, int32_t i) {
+__device__ __forceinline__ Item work_item(const Work& w, int32_t i, int32_t c, int32_t P) {
   Item it;
   if (i < w.n_dp) {
-    it.tile = blockIdx.x + i * gridDim.x;
+    it.tile = c + i * P;
     it.kb0 = 0;
     it.kb1 = w.nkb;
     it.sk_tile = -1;
@@ -259,13 +280,18 @@ __device__ __forceinline__ int32_t unit_owner(const Work& w, int64_t u) {
 }
 
 // Bounded mbarrier wait: false if the CTA is aborting or the wait gave up, in which
-// case the abort flag and the device status word are set.
+// case the abort flag and the device status word are set.  kCluster: acquire at cluster
+// scope (a barrier that the other CTA of a pair arrives on).
+template <bool kCluster = false>
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile uint32_t* abort,
                                          uint32_t* status, uint64_t timeout_ns) {
-  if (ptx::mbar_try_wait(bar, parity)) return true;
+  auto try_wait = [&]() {
+    return kCluster ? ptx::mbar_try_wait_cluster(bar, parity) : ptx::mbar_try_wait(bar, parity);
+  };
+  if (try_wait()) return true;
   const uint64_t t0 = ptx::globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
-    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if (try_wait()) return true;
     if ((it & 255u) == 0) {
       if (*abort) return false;
       if (ptx::globaltimer_ns() - t0 > timeout_ns) {
@@ -302,7 +328,7 @@ __device__ void build_sched(const GemmParams& p, int32_t* rowinfo, int32_t* tile
   const int32_t per = (G + 31) / 32;
   const int32_t g0 = min(G, static_cast<int32_t>(lane) * per);
   const int32_t g1 = min(G, g0 + per);
-  const int64_t ntn = (p.N + Cfg::kWRows - 1) / Cfg::kWRows;
+  const int64_t ntn = (p.N + Cfg::kTileW - 1) / Cfg::kTileW;
   bool clamped = false;
   if constexpr (Cfg::kDynamic) {
     for (int32_t g = g0; g < g1; ++g) {
@@ -345,7 +371,7 @@ __device__ void build_sched(const GemmParams& p, int32_t* rowinfo, int32_t* tile
     int64_t cnt;
     if constexpr (Cfg::kDynamic) cnt = rowinfo[g];
     else cnt = static_cast<int64_t>(rowinfo[g + 1]) - rowinfo[g];
-    my_tiles += ((cnt + Cfg::kActRows - 1) / Cfg::kActRows) * ntn;
+    my_tiles += ((cnt + Cfg::kTileAct - 1) / Cfg::kTileAct) * ntn;
   }
   const int64_t incl = warp_incl_scan(my_tiles, lane);
   int64_t tp = incl - my_tiles;
@@ -354,7 +380,7 @@ __device__ void build_sched(const GemmParams& p, int32_t* rowinfo, int32_t* tile
     int64_t cnt;
     if constexpr (Cfg::kDynamic) cnt = rowinfo[g];
     else cnt = static_cast<int64_t>(rowinfo[g + 1]) - rowinfo[g];
-    tp += ((cnt + Cfg::kActRows - 1) / Cfg::kActRows) * ntn;
+    tp += ((cnt + Cfg::kTileAct - 1) / Cfg::kTileAct) * ntn;
   }
   if (lane == 31) tile_pre[G] = static_cast<int32_t>(incl);
   const bool any_clamped = __any_sync(0xffffffffu, clamped);
@@ -420,6 +446,10 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
 
   const uint32_t warp = threadIdx.x >> 5;
   const uint32_t lane = threadIdx.x & 31u;
+  // CTA pairs: this CTA's rank in its pair; work is divided among pairs
+  const uint32_t crank = Cfg::kPair ? ptx::cluster_ctarank() : 0u;
+  const int32_t worker = static_cast<int32_t>(blockIdx.x) / Cfg::kCtas;
+  const int32_t workers = static_cast<int32_t>(gridDim.x) / Cfg::kCtas;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < Cfg::kStages; ++s) {
@@ -428,7 +458,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(tfull_bar(b), 1u);
-      ptx::mbar_init(tempty_bar(b), static_cast<uint32_t>(Cfg::kEpiWarps));
+      // pairs: the leader's MMA waits for the epilogue warps of both CTAs
+      ptx::mbar_init(tempty_bar(b), static_cast<uint32_t>(Cfg::kEpiWarps * Cfg::kCtas));
     }
     *abort_flag = 0u;
     ptx::fence_mbar_init();
@@ -441,8 +472,19 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     }
   }
   if (warp == Cfg::kMmaWarp) {
-    ptx::tmem_alloc(ptx::smem_addr(tmem_holder), Cfg::kTmemCols);
-    ptx::tmem_relinquish();
+    if constexpr (Cfg::kPair) {
+      ptx::tmem_alloc_pair(ptx::smem_addr(tmem_holder), Cfg::kTmemCols);
+      ptx::tmem_relinquish_pair();
+    } else {
+      ptx::tmem_alloc(ptx::smem_addr(tmem_holder), Cfg::kTmemCols);
+      ptx::tmem_relinquish();
+    }
+  }
+  if constexpr (Cfg::kPair) {
+    // the peer signals this CTA's barriers only after both have initialised theirs
+    ptx::tc_fence_before_sync();
+    ptx::cluster_sync();
+    ptx::tc_fence_after_sync();
   }
   // Everything above is CTA-local.  With programmatic dependent launch the next kernel on
   // the stream may begin launching now; this kernel's first global-memory access (the
@@ -466,7 +508,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
   const bool has_k = p.num_kb > 0;
   // the work split lives in shared memory: every role reads it, none keeps it in registers
   Work* work_smem = reinterpret_cast<Work*>(smem + Cfg::kOffWork);
-  if (threadIdx.x == 0) *work_smem = make_work(sched.total, p.num_kb, p.split_k != 0);
+  if (threadIdx.x == 0)
+    *work_smem = make_work(sched.total, p.num_kb, p.split_k != 0 && !Cfg::kPair, worker, workers);
   __syncthreads();
   const Work& work = *work_smem;
 
@@ -481,18 +524,27 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         uint32_t phase = 0;
         bool ok = true;
         for (int32_t i = 0; ok && i < work.n_items; ++i) {
-          const Item it = work_item(work, i);
-          const TileCoord c = decode_tile<Cfg>(sched, it.tile);
+          const Item it = work_item(work, i, worker, workers);
+          const TileCoord c = decode_tile<Cfg>(sched, it.tile, crank);
           for (int32_t kb = it.kb0; kb < it.kb1; ++kb) {
             if (!wait_bar(empty_bar(stage), phase ^ 1u, abort_flag, p.status, p.timeout_ns)) {
               ok = false;
               break;
             }
-            ptx::mbar_arrive_expect_tx(full_bar(stage), Cfg::kStageBytes);
-            ptx::tma_load_2d(s_act + stage * Cfg::kActBytes, &tmA, full_bar(stage), kb * kBK,
-                             c.m0);
-            ptx::tma_load_3d(s_w + stage * Cfg::kWBytes, &tmB, full_bar(stage), kb * kBK, c.n0,
-                             c.g);
+            if constexpr (Cfg::kPair) {
+              // both CTAs' bytes complete on the leader's full barrier, which expects them all
+              const uint32_t fb = ptx::mapa_shared(full_bar(stage), 0u);
+              if (crank == 0) ptx::mbar_arrive_expect_tx(full_bar(stage), 2 * Cfg::kStageBytes);
+              ptx::tma_load_2d_pair(s_act + stage * Cfg::kActBytes, &tmA, fb, kb * kBK, c.m0);
+              ptx::tma_load_3d_pair(s_w + stage * Cfg::kWBytes, &tmB, fb, kb * kBK,
+                                    c.n0 + static_cast<int32_t>(crank) * Cfg::kWRows, c.g);
+            } else {
+              ptx::mbar_arrive_expect_tx(full_bar(stage), Cfg::kStageBytes);
+              ptx::tma_load_2d(s_act + stage * Cfg::kActBytes, &tmA, full_bar(stage), kb * kBK,
+                               c.m0);
+              ptx::tma_load_3d(s_w + stage * Cfg::kWBytes, &tmB, full_bar(stage), kb * kBK, c.n0,
+                               c.g);
+            }
             if (++stage == Cfg::kStages) {
               stage = 0;
               phase ^= 1u;
@@ -516,8 +568,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         int64_t fills = 0;  // stages issued by this thread
         bool ok = true;
         for (int32_t i = 0; ok && i < work.n_items; ++i) {
-          const Item it = work_item(work, i);
-          const TileCoord c = decode_tile<Cfg>(sched, it.tile);
+          const Item it = work_item(work, i, worker, workers);
+          const TileCoord c = decode_tile<Cfg>(sched, it.tile, crank);
           const uint8_t* b_group = p.B + static_cast<size_t>(c.g) * p.N * p.K;
           for (int32_t kb = it.kb0; kb < it.kb1; ++kb) {
             if (!wait_bar(empty_bar(stage), phase ^ 1u, abort_flag, p.status, p.timeout_ns)) {
@@ -582,18 +634,20 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     // The tensor core sums at most kb_per_chunk K blocks into one TMEM chunk buffer
     // (two buffers, alternating); the epilogue adds every chunk into fp32 registers with
     // round-to-nearest, so the tensor core's own accumulation only ever spans a chunk.
-    if (lane == 0 && has_k) {
+    // A pair's MMAs are issued by its leader (rank 0) alone.
+    if (lane == 0 && has_k && crank == 0) {
       int stage = 0;
       uint32_t phase = 0;
       uint32_t chunk = 0;  // chunks issued by this CTA: buffer = chunk & 1
       bool ok = true;
       const int32_t kpc = p.kb_per_chunk;
       for (int32_t i = 0; ok && i < work.n_items; ++i) {
-        const Item it = work_item(work, i);
+        const Item it = work_item(work, i, worker, workers);
         for (int32_t kb0 = it.kb0; ok && kb0 < it.kb1; kb0 += kpc) {
           const int buf = static_cast<int>(chunk & 1u);
           const uint32_t use = chunk >> 1;  // how often this buffer was used before
-          if (!wait_bar(tempty_bar(buf), (use & 1u) ^ 1u, abort_flag, p.status, p.timeout_ns)) {
+          if (!wait_bar<Cfg::kPair>(tempty_bar(buf), (use & 1u) ^ 1u, abort_flag, p.status,
+                                    p.timeout_ns)) {
             ok = false;
             break;
           }
@@ -613,17 +667,24 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
 #pragma unroll
             for (int k = 0; k < kBK / 32; ++k) {
               // advance 32 bytes of K inside the 128-byte swizzled row: +2 in 16-byte units
-              ptx::mma_f8f6f4(d_tmem, a_desc + 2u * k, b_desc + 2u * k, Cfg::kIdesc,
-                              (kb > kb0 || k > 0) ? 1u : 0u);
+              if constexpr (Cfg::kPair)
+                ptx::mma_f8f6f4_pair(d_tmem, a_desc + 2u * k, b_desc + 2u * k, Cfg::kIdesc,
+                                     (kb > kb0 || k > 0) ? 1u : 0u);
+              else
+                ptx::mma_f8f6f4(d_tmem, a_desc + 2u * k, b_desc + 2u * k, Cfg::kIdesc,
+                                (kb > kb0 || k > 0) ? 1u : 0u);
             }
-            ptx::mma_commit(empty_bar(stage));
+            // pairs: the stage is free in both CTAs once the MMAs reading it complete
+            if constexpr (Cfg::kPair) ptx::mma_commit_pair(empty_bar(stage), 0x3);
+            else ptx::mma_commit(empty_bar(stage));
             if (++stage == Cfg::kStages) {
               stage = 0;
               phase ^= 1u;
             }
           }
           if (!ok) break;
-          ptx::mma_commit(tfull_bar(buf));
+          if constexpr (Cfg::kPair) ptx::mma_commit_pair(tfull_bar(buf), 0x3);
+          else ptx::mma_commit(tfull_bar(buf));
           ++chunk;
         }
       }
@@ -642,7 +703,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
       const int32_t nw = gridDim.x * Cfg::kEpiWarps;
       for (int32_t g = 0; g < p.G; ++g) {
         const int32_t v = rowinfo[g];
-        const int32_t covered = ((v + Cfg::kActRows - 1) / Cfg::kActRows) * Cfg::kActRows;
+        const int32_t covered = ((v + Cfg::kTileAct - 1) / Cfg::kTileAct) * Cfg::kTileAct;
         const int32_t z0 = g * p.E + (covered < p.E ? covered : p.E);
         const int32_t z1 = (g + 1) * p.E;
         for (int32_t r = z0 + gw; r < z1; r += nw) {
@@ -656,8 +717,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     bool ok = true;
     const int32_t kpc = p.kb_per_chunk;
     for (int32_t i = 0; ok && i < work.n_items; ++i) {
-      const Item it = work_item(work, i);
-      TileCoord c = decode_tile<Cfg>(sched, it.tile);
+      const Item it = work_item(work, i, worker, workers);
+      TileCoord c = decode_tile<Cfg>(sched, it.tile, crank);
       // an empty reduction (K = 0) writes +0.0 to every owned row, whatever the scales
       if (!has_k) c.valid_end = c.m0;
       // scales this thread needs, loaded before the chunk waits so their latency hides
@@ -736,7 +797,10 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
           }
           ptx::tc_fence_before_sync();
           __syncwarp();
-          if (lane == 0) ptx::mbar_arrive(tempty_bar(buf));
+          if (lane == 0) {
+            if constexpr (Cfg::kPair) ptx::mbar_arrive_cluster(ptx::mapa_shared(tempty_bar(buf), 0u));
+            else ptx::mbar_arrive(tempty_bar(buf));
+          }
           ++chunk;
         }
         if (!ok) break;
@@ -891,14 +955,25 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
   // ------------------------------------------------------------------ teardown
   ptx::tc_fence_before_sync();
   __syncthreads();
-  if (*abort_flag) {
+  bool aborting = *abort_flag != 0u;
+  if constexpr (Cfg::kPair) {
+    // neither CTA of a pair leaves while the other may still signal its barriers or read
+    // its shared memory, and both wait out in-flight work if either gave up
+    ptx::cluster_sync();
+    const uint32_t peer_abort = ptx::ld_shared_cluster_u32(
+        ptx::mapa_shared(ptx::smem_addr(smem + Cfg::kOffMisc + 4), crank ^ 1u));
+    aborting = aborting || peer_abort != 0u;
+    ptx::cluster_sync();
+  }
+  if (aborting) {
     // let any copy or MMA still in flight land before the memory is released
     const uint64_t t0 = ptx::globaltimer_ns();
     while (ptx::globaltimer_ns() - t0 < 2000000ull) ptx::nanosleep(1000);
   }
   if (warp == static_cast<uint32_t>(Cfg::kMmaWarp)) {
     ptx::tc_fence_after_sync();
-    ptx::tmem_dealloc(tmem_base, Cfg::kTmemCols);
+    if constexpr (Cfg::kPair) ptx::tmem_dealloc_pair(tmem_base, Cfg::kTmemCols);
+    else ptx::tmem_dealloc(tmem_base, Cfg::kTmemCols);
   }
 }
 

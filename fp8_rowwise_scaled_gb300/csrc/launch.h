@@ -11,8 +11,8 @@ namespace mslkb {
 
 struct LaunchArgs {
   GemmParams params;
-  CUtensorMap tmA;   // activation tiles [rows, K], box (128 B, act_rows)
-  CUtensorMap tmB;   // weight tiles [G, N, K], box (128 B, w_rows, 1)
+  CUtensorMap tmA;   // activation tiles [rows, K], box (128 B, box_act)
+  CUtensorMap tmB;   // weight tiles [G, N, K], box (128 B, box_w, 1)
   CUtensorMap tmC;   // output [rows, N] bf16, box (32, 32), 64-byte swizzle (128-row tiles)
   dim3 grid;
   cudaStream_t stream;
@@ -20,7 +20,8 @@ struct LaunchArgs {
 
 using LaunchFn = cudaError_t (*)(const LaunchArgs&);
 using AttrFn = cudaError_t (*)();
-using OccupancyFn = cudaError_t (*)(int* blocks_per_sm, int* regs_per_thread);
+using OccupancyFn = cudaError_t (*)(int* blocks_per_sm, int* regs_per_thread,
+                                    int* cluster_ctas);
 
 struct VariantInfo {
   const char* name;
@@ -31,8 +32,11 @@ struct VariantInfo {
   bool dynamic;
   int threads;
   int smem;
-  int act_rows;   // activation rows per tile
-  int w_rows;     // weight rows per tile
+  int act_rows;   // activation rows per output tile
+  int w_rows;     // weight rows (output columns) per output tile
+  int box_act;    // activation rows one CTA loads per stage (TMA box height)
+  int box_w;      // weight rows one CTA loads per stage
+  int cluster;    // CTAs per cluster: 2 for CTA pairs (cta_group::2), else 1
   int partial_bytes;  // fp32 partial sums of one tile (a split tile's piece)
   int launch_regs;    // registers per thread the kernel must be built with (0: any)
   LaunchFn launch;
@@ -49,11 +53,18 @@ cudaError_t launch_variant(const LaunchArgs& a) {
   cfg.stream = a.stream;
   // programmatic dependent launch: the kernel waits (griddepcontrol.wait) before touching
   // global memory, so it may start launching while the previous kernel on the stream ends
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  if constexpr (Cfg::kPair) {  // CTA pairs: clusters of two along x
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 2;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.numAttrs = 2;
+  }
   return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<Cfg>, a.params, a.tmA, a.tmB, a.tmC);
 }
 
@@ -64,21 +75,46 @@ cudaError_t set_attr_variant() {
 }
 
 // CTAs of this variant that fit on one SM (needs the shared-memory attribute set first)
+// and, for CTA pairs, how many CTAs of the device can run at once in whole clusters
+// (SMs left over in a GPC hold no pair); 0 for single-CTA variants.
 template <class Cfg>
-cudaError_t occupancy_variant(int* blocks_per_sm, int* regs_per_thread) {
+cudaError_t occupancy_variant(int* blocks_per_sm, int* regs_per_thread, int* cluster_ctas) {
   cudaFuncAttributes fa;
   cudaError_t e = cudaFuncGetAttributes(&fa, grouped_gemm_kernel<Cfg>);
   if (e != cudaSuccess) return e;
   *regs_per_thread = fa.numRegs;
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, grouped_gemm_kernel<Cfg>,
-                                                       Cfg::kThreads, Cfg::kSmemBytes);
+  *cluster_ctas = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, grouped_gemm_kernel<Cfg>,
+                                                    Cfg::kThreads, Cfg::kSmemBytes);
+  if (e != cudaSuccess || !Cfg::kPair) return e;
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+    return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(sms & ~1), 1, 1);
+  cfg.blockDim = dim3(Cfg::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = Cfg::kSmemBytes;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int clusters = 0;
+  e = cudaOccupancyMaxActiveClusters(&clusters, grouped_gemm_kernel<Cfg>, &cfg);
+  if (e != cudaSuccess) return e;
+  *cluster_ctas = 2 * clusters;
+  return cudaSuccess;
 }
 
 template <class Cfg>
 constexpr VariantInfo make_variant(const char* name) {
-  return VariantInfo{name,          Cfg::kTileN,   Cfg::kStages,  Cfg::kSwap,
-                     Cfg::kTma,     Cfg::kDynamic, Cfg::kThreads, Cfg::kSmemBytes,
-                     Cfg::kActRows, Cfg::kWRows,   Cfg::kEpiWarps * 32 * Cfg::kThreadCols * 4,
+  return VariantInfo{name,           Cfg::kTileN,   Cfg::kStages,  Cfg::kSwap,
+                     Cfg::kTma,      Cfg::kDynamic, Cfg::kThreads, Cfg::kSmemBytes,
+                     Cfg::kTileAct,  Cfg::kTileW,   Cfg::kActRows, Cfg::kWRows,
+                     Cfg::kCtas,     Cfg::kEpiWarps * 32 * Cfg::kThreadCols * 4,
                      Cfg::kLaunchRegs, &launch_variant<Cfg>, &set_attr_variant<Cfg>,
                      &occupancy_variant<Cfg>};
 }

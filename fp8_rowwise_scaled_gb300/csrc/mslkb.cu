@@ -63,10 +63,12 @@ const VariantInfo* variant(int i) {
   return nullptr;
 }
 
-int find_variant(bool dynamic, bool tma, bool swap, int tile_n) {
+int find_variant(bool dynamic, bool tma, bool swap, int tile_n, int cluster = 1) {
   for (int i = 0; i < num_variants(); ++i) {
     const VariantInfo* v = variant(i);
-    if (v->dynamic == dynamic && v->tma == tma && v->swap == swap && v->tile_n == tile_n) return i;
+    if (v->dynamic == dynamic && v->tma == tma && v->swap == swap && v->tile_n == tile_n &&
+        v->cluster == cluster)
+      return i;
   }
   return -1;
 }
@@ -80,6 +82,7 @@ struct DeviceState {
   int sm_count = 0;
   uint32_t* status_ptr = nullptr;
   uint64_t attr_done[2] = {0, 0};  // one bit per variant
+  int cluster_ctas[128] = {};       // CTA-pair variants: CTAs that run at once in pairs
 };
 
 std::mutex g_mutex;
@@ -203,17 +206,31 @@ mslkb_status ensure_attr(DeviceState* st, int vi) {
   cudaError_t e = variant(vi)->set_attr();
   if (e != cudaSuccess) return cuda_fail(e);
   // a variant that cannot place one CTA on an SM is reported here, not at launch
-  int blocks = 0, regs = 0;
-  e = variant(vi)->occupancy(&blocks, &regs);
+  int blocks = 0, regs = 0, cluster_ctas = 0;
+  e = variant(vi)->occupancy(&blocks, &regs, &cluster_ctas);
   if (e != cudaSuccess) return cuda_fail(e);
   if (blocks < 1) return cuda_fail(cudaErrorLaunchOutOfResources);
+  if (variant(vi)->cluster > 1 && cluster_ctas < variant(vi)->cluster)
+    return cuda_fail(cudaErrorLaunchOutOfResources);
   // a kernel that moves registers between warpgroups must start with exactly the budget
   // its split adds up to; with fewer, the warps asking for more would never get them
   if (variant(vi)->launch_regs != 0 && regs != variant(vi)->launch_regs)
     return cuda_fail(cudaErrorInvalidConfiguration);
   std::lock_guard<std::mutex> lock(g_mutex);
+  st->cluster_ctas[vi & 127] = cluster_ctas;
   st->attr_done[vi >> 6] |= bit;
   return MSLKB_OK;
+}
+
+// The planned grid, for CTA pairs cut to the CTAs that run at once in whole clusters (a
+// persistent grid must not queue a second partial wave).
+unsigned launch_grid(const DeviceState* st, int vi, int64_t planned) {
+  const VariantInfo* v = variant(vi);
+  if (v->cluster > 1) {
+    const int64_t fit = st->cluster_ctas[vi & 127];
+    if (planned > fit) planned = (fit / v->cluster) * v->cluster;
+  }
+  return static_cast<unsigned>(planned);
 }
 
 // ---------------------------------------------------------------------------------
@@ -278,15 +295,18 @@ mslkb_status plan(int layout, int64_t rows, int64_t G, int64_t N, int64_t K, int
   // Measured on GB300: splitting speeds up the swap-AB plans at small M (more SMs stream
   // weights) but slows the 128-row-tile plans by 4-9% (128 KB of partial sums per piece).
   const int policy = g_split_k.load();
-  const bool split = nkb > 0 && (policy == 2 || (policy == 1 && v->swap));
+  // CTA pairs run whole tiles only (one pair per tile)
+  const bool split = nkb > 0 && v->cluster == 1 && (policy == 2 || (policy == 1 && v->swap));
   // with splitting every CTA gets K work as long as there are units to share
-  const int64_t work = split ? bound * nkb : bound;
-  int64_t grid = work < num_sms ? work : num_sms;
+  const int64_t work = (split ? bound * nkb : bound) * v->cluster;
+  const int64_t max_ctas = (num_sms / v->cluster) * v->cluster;
+  int64_t grid = work < max_ctas ? work : max_ctas;
   if (dynamic) {  // padding rows are zeroed by every CTA's epilogue warps
     const int64_t zero_ctas = ceil_div(G * rows, 32);
     if (grid < zero_ctas) grid = zero_ctas < num_sms ? zero_ctas : num_sms;
   }
-  if (grid < 1) grid = 1;
+  if (v->cluster > 1) grid = (grid / v->cluster) * v->cluster;
+  if (grid < v->cluster) grid = v->cluster;
   std::memset(info, 0, sizeof(*info));
   info->variant = vi;
   info->swap_ab = v->swap;
@@ -342,7 +362,7 @@ mslkb_status encode_maps(LaunchArgs* la, const VariantInfo* v, const void* A, co
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K)};
     const cuuint32_t box[2] = {static_cast<cuuint32_t>(mslkb::kBK),
-                               static_cast<cuuint32_t>(v->act_rows)};
+                               static_cast<cuuint32_t>(v->box_act)};
     CUresult r = g_encode(&la->tmA, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(A), dims,
                           strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -357,7 +377,7 @@ mslkb_status encode_maps(LaunchArgs* la, const VariantInfo* v, const void* A, co
                                 static_cast<cuuint64_t>(G)};
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(N * K)};
     const cuuint32_t box[3] = {static_cast<cuuint32_t>(mslkb::kBK),
-                               static_cast<cuuint32_t>(v->w_rows), 1};
+                               static_cast<cuuint32_t>(v->box_w), 1};
     CUresult r = g_encode(&la->tmB, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(B), dims,
                           strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -441,7 +461,7 @@ mslkb_status run(int layout, const void* A, const void* B, const float* scale_a,
   }
   if ((s = encode_maps(&la, v, A, B, rows, G, N, K)) != MSLKB_OK) return s;
   if ((s = encode_out_map(&la, v, out, rows, N)) != MSLKB_OK) return s;
-  la.grid = dim3(static_cast<unsigned>(info.grid), 1, 1);
+  la.grid = dim3(launch_grid(st, info.variant, info.grid), 1, 1);
   la.stream = static_cast<cudaStream_t>(stream);
   cudaError_t e = v->launch(la);
   if (e != cudaSuccess) return cuda_fail(e);
@@ -528,7 +548,7 @@ mslkb_status run_stacked_with_scratch(const void* A, const void* B, const float*
   }
   if ((s = encode_maps(&la, v, A, B, total_M, G, N, K)) != MSLKB_OK) return s;
   if ((s = encode_out_map(&la, v, out, total_M, N)) != MSLKB_OK) return s;
-  la.grid = dim3(static_cast<unsigned>(info.grid), 1, 1);
+  la.grid = dim3(launch_grid(st, info.variant, info.grid), 1, 1);
   la.stream = cs;
   cudaError_t e = v->launch(la);
   if (e != cudaSuccess) return cuda_fail(e);
@@ -650,8 +670,8 @@ mslkb_status mslkb_variant_resources(int32_t i, int32_t* blocks_per_sm, int32_t*
   if (s != MSLKB_OK) return s;
   cudaError_t e = v->set_attr();
   if (e != cudaSuccess) return cuda_fail(e);
-  int blocks = 0, regs = 0;
-  e = v->occupancy(&blocks, &regs);
+  int blocks = 0, regs = 0, cluster_ctas = 0;
+  e = v->occupancy(&blocks, &regs, &cluster_ctas);
   if (e != cudaSuccess) return cuda_fail(e);
   *blocks_per_sm = blocks;
   *regs_per_thread = regs;

@@ -192,6 +192,27 @@ def test_plan_forced_variant(L):
         fx.mslkb_force_variant(-1)
 
 
+def test_plan_pair_variant(L):
+    # CTA pairs: 256 x 256 output tiles, two CTAs per tile (an even grid), never split
+    try:
+        fx.mslkb_force_variant(fx.variant_index("stacked_pair256x256_tma"))
+        fx.mslkb_set_split_k(2)
+        i = fx.mslkb_plan(0, 16384, 16, 16384, 16384, 152)
+        assert (i.tile_m, i.tile_n, i.split_k, i.grid, i.threads) == (256, 256, 0, 152, 384)
+        i = fx.mslkb_plan(0, 300, 1, 512, 1024, 152)   # 2 x 2 tiles: 4 pairs
+        assert (i.tiles_bound, i.grid) == (4, 8)
+        i = fx.mslkb_plan(0, 300, 1, 512, 1024, 7)     # 7 SMs hold 3 pairs
+        assert i.grid == 6
+        with pytest.raises(fx.MslkbError):             # a stacked kernel for the dynamic layout
+            fx.mslkb_plan(1, 128, 4, 256, 512, 152)
+        fx.mslkb_force_variant(fx.variant_index("dynamic_pair256x256_tma"))
+        i = fx.mslkb_plan(1, 600, 8, 1024, 512, 152)   # 8 slabs x 3 x 4 tiles
+        assert (i.tiles_bound, i.grid) == (96, 152)
+    finally:
+        fx.mslkb_force_variant(-1)
+        fx.mslkb_set_split_k(1)
+
+
 def test_plan_grid_bounds(L):
     # tiles bound for stacked: (total_M + nz * (tile_m - 1)) / tile_m * ceil(N / tile_n)
     try:

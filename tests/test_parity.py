@@ -131,6 +131,28 @@ def test_dynamic_variant_ragged(orc, variant):
         assert np.all(gb[g * 200 + v[g]:(g + 1) * 200] == 0)
 
 
+@pytest.mark.parametrize("layout", ["stacked", "dynamic"])
+def test_pair_tiles_many_waves(orc, layout):
+    # CTA pairs (256 x 256 output tiles from one cta_group::2 MMA): more tiles than pairs
+    # fit on the GPU, so each pair runs several tiles and reuses its TMEM accumulators;
+    # groups end inside the leader's rows, inside the peer's rows, or leave the peer none
+    if layout == "stacked":
+        meta = [520, 3, 0, 700, 256, 129, 511, 520]
+        prob = _rand_problem("stacked", 8, 1024, 512, meta, seed=11, total_extra=5)
+    else:
+        meta = [520, 3, 0, 600, 256, 129, 511, 520]
+        prob = _rand_problem("dynamic", 8, 1024, 512, meta, E=600, seed=12)
+    v = f"{layout}_pair256x256_tma"
+    for kpc in (8, 1):   # one chunk per tile; a chunk per K block
+        fx.mslkb_set_accumulation_chunk(kpc)
+        try:
+            _check_full(prob, orc, variant=v, poison_value=0x5A5A if layout == "stacked" else None,
+                        what=f"{v} chunk {kpc}")
+        finally:
+            fx.mslkb_set_accumulation_chunk(8)
+    assert fx.device_status() == 0
+
+
 @pytest.mark.parametrize("tile", ["tile128x128", "swap_w128xa16"])
 @pytest.mark.parametrize("layout", ["stacked", "dynamic"])
 def test_cpasync_bit_identical_to_tma(orc, tile, layout):
