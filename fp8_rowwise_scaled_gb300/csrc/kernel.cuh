@@ -123,6 +123,8 @@ struct KernelCfg {
                                                            : 512;
   static constexpr int kCpLag = kStages - 2;  // cp.async groups kept in flight per thread
   static constexpr uint32_t kIdesc = ptx::idesc_e4m3_f32(kMmaM * kCtas, kTileN);
+  // CTA pairs, a group's last <= 128 rows: one M = 128 MMA over both CTAs (64 rows each)
+  static constexpr uint32_t kIdescHalf = ptx::idesc_e4m3_f32(kMmaM, kTileN);
 
   // 128-row tiles write the output through shared memory and TMA stores: each epilogue
   // warp stages 32 rows x 32 columns of bf16 (2 KB, 64-byte swizzle) at a time
@@ -156,11 +158,25 @@ struct KernelCfg {
 
 struct TileCoord {
   int32_t g;          // group
-  int32_t m0;         // first activation row (global row index)
+  int32_t m0;         // first activation row of this CTA (global row index)
   int32_t n0;         // first weight row / output column
   int32_t valid_end;  // rows < valid_end get the product
   int32_t zero_end;   // rows in [valid_end, zero_end) get +0.0 (padding)
+  bool half;          // CTA pairs: a 128-row tile (64 rows per CTA, M = 128 MMA)
 };
+
+// CTA pairs: a group's rows run in 256-row tiles, except that a last piece of at most 128
+// rows runs as a 128-row tile (64 rows per CTA), so short remainders cost half a tile.
+// Rows [0, cover) of a group of `cnt` rows lie inside its tiles.
+template <class Cfg>
+__device__ __forceinline__ int32_t tile_cover(int32_t cnt) {
+  const int32_t full = (cnt + Cfg::kTileAct - 1) / Cfg::kTileAct * Cfg::kTileAct;
+  if constexpr (Cfg::kPair) {
+    const int32_t rem = cnt % Cfg::kTileAct;
+    if (rem > 0 && rem <= Cfg::kTileAct / 2) return full - Cfg::kTileAct / 2;
+  }
+  return full;
+}
 
 // Shared-memory scheduler tables.
 //   rowinfo[g]: stacked -> first row of group g (G + 1 entries, clamped prefix);
@@ -201,7 +217,13 @@ __device__ __forceinline__ TileCoord decode_tile(const Sched& s, int32_t t, uint
   TileCoord c;
   c.g = g;
   const int32_t base = Cfg::kDynamic ? g * s.E : s.rowinfo[g];
-  c.m0 = base + m_idx * Cfg::kTileAct + static_cast<int32_t>(crank) * Cfg::kActRows;
+  c.half = false;
+  if constexpr (Cfg::kPair) {
+    const int32_t rem = cnt - m_idx * Cfg::kTileAct;  // rows from this tile's first on
+    c.half = rem <= Cfg::kTileAct / 2;
+  }
+  const int32_t cta_rows = c.half ? Cfg::kActRows / 2 : Cfg::kActRows;
+  c.m0 = base + m_idx * Cfg::kTileAct + static_cast<int32_t>(crank) * cta_rows;
   c.n0 = n_idx * Cfg::kTileW;
   c.valid_end = base + cnt;
   c.zero_end = Cfg::kDynamic ? base + s.E : base + cnt;
@@ -643,6 +665,10 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
       const int32_t kpc = p.kb_per_chunk;
       for (int32_t i = 0; ok && i < work.n_items; ++i) {
         const Item it = work_item(work, i, worker, workers);
+        uint32_t idesc = Cfg::kIdesc;
+        if constexpr (Cfg::kPair) {
+          if (decode_tile<Cfg>(sched, it.tile, 0u).half) idesc = Cfg::kIdescHalf;
+        }
         for (int32_t kb0 = it.kb0; ok && kb0 < it.kb1; kb0 += kpc) {
           const int buf = static_cast<int>(chunk & 1u);
           const uint32_t use = chunk >> 1;  // how often this buffer was used before
@@ -668,7 +694,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
             for (int k = 0; k < kBK / 32; ++k) {
               // advance 32 bytes of K inside the 128-byte swizzled row: +2 in 16-byte units
               if constexpr (Cfg::kPair)
-                ptx::mma_f8f6f4_pair(d_tmem, a_desc + 2u * k, b_desc + 2u * k, Cfg::kIdesc,
+                ptx::mma_f8f6f4_pair(d_tmem, a_desc + 2u * k, b_desc + 2u * k, idesc,
                                      (kb > kb0 || k > 0) ? 1u : 0u);
               else
                 ptx::mma_f8f6f4(d_tmem, a_desc + 2u * k, b_desc + 2u * k, Cfg::kIdesc,
@@ -703,7 +729,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
       const int32_t nw = gridDim.x * Cfg::kEpiWarps;
       for (int32_t g = 0; g < p.G; ++g) {
         const int32_t v = rowinfo[g];
-        const int32_t covered = ((v + Cfg::kTileAct - 1) / Cfg::kTileAct) * Cfg::kTileAct;
+        const int32_t covered = tile_cover<Cfg>(v);
         const int32_t z0 = g * p.E + (covered < p.E ? covered : p.E);
         const int32_t z1 = (g + 1) * p.E;
         for (int32_t r = z0 + gw; r < z1; r += nw) {
@@ -721,19 +747,33 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
       TileCoord c = decode_tile<Cfg>(sched, it.tile, crank);
       // an empty reduction (K = 0) writes +0.0 to every owned row, whatever the scales
       if (!has_k) c.valid_end = c.m0;
+      // this warp's rows (row_off from c.m0) and output columns (ocol from c.n0).  A CTA
+      // pair's 128-row tile leaves each CTA 64 rows x 256 columns, folded into TMEM as
+      // lanes 0-63 = columns 0-127 and lanes 64-127 = columns 128-255 (TMEM columns
+      // 0-127): the four warps of column slice 0 hold it all, the others sit out.
+      int32_t row_off = static_cast<int32_t>(32u * q);
+      int32_t ocol = col_base;
+      bool active = true;
+      if constexpr (Cfg::kPair) {
+        if (c.half) {
+          row_off = static_cast<int32_t>(32u * (q & 1u));
+          ocol = static_cast<int32_t>(q >> 1) * (Cfg::kTileN / 2);
+          active = col_base == 0;
+        }
+      }
       // scales this thread needs, loaded before the chunk waits so their latency hides
       // behind the MMA: scale_a of its row, and scale_b of column (col0 + lane) for each
       // 32-column piece, broadcast by shuffle when the piece is stored
       float sa_pre = 0.0f;
       float sb_pre[Cfg::kSwap ? 1 : Cfg::kThreadCols / 32];
       if constexpr (!Cfg::kSwap) {
-        const int32_t R = c.m0 + static_cast<int32_t>(32u * q + lane);
-        if (R < c.valid_end) sa_pre = __ldg(p.scale_a + R);
+        const int32_t R = c.m0 + row_off + static_cast<int32_t>(lane);
+        if (active && R < c.valid_end) sa_pre = __ldg(p.scale_a + R);
         const float* sb_g = p.scale_b + static_cast<size_t>(c.g) * p.N;
 #pragma unroll
         for (int pc = 0; pc < Cfg::kThreadCols / 32; ++pc) {
-          const int32_t col = c.n0 + col_base + pc * 32 + static_cast<int32_t>(lane);
-          sb_pre[pc] = col < p.N ? __ldg(sb_g + col) : 0.0f;
+          const int32_t col = c.n0 + ocol + pc * 32 + static_cast<int32_t>(lane);
+          sb_pre[pc] = (active && col < p.N) ? __ldg(sb_g + col) : 0.0f;
         }
       }
       // fp32 accumulator of this thread (round-to-nearest adds of the TMEM chunks)
@@ -743,7 +783,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
       // TMEM data is needed only when this warp's lanes hold rows with computed values
       bool warp_any;
       if constexpr (!Cfg::kSwap) {
-        warp_any = c.m0 + static_cast<int32_t>(32u * q) < c.valid_end;  // lane 0's row
+        warp_any = active && c.m0 + row_off < c.valid_end;  // lane 0's row
       } else {
         warp_any = c.n0 + static_cast<int32_t>(32u * q) < p.N && c.m0 < c.valid_end;
       }
@@ -848,12 +888,13 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         }
         if (lane == 0) *cnt = 0u;  // ready for the next call
       }
+      if (!active) continue;
       if constexpr (!Cfg::kSwap) {
         // thread = one activation row
-        const int32_t R = c.m0 + static_cast<int32_t>(32u * q + lane);
+        const int32_t R = c.m0 + row_off + static_cast<int32_t>(lane);
         const bool row_val = R < c.valid_end;
         const bool row_zero = !row_val && R < c.zero_end;
-        const int32_t R_first = c.m0 + static_cast<int32_t>(32u * q);
+        const int32_t R_first = c.m0 + row_off;
         if (Cfg::kTmaStore && R_first + 31 < c.zero_end) {
           // all 32 rows of this warp are owned: stage 32 x 32 bf16 blocks in shared memory
           // (64-byte swizzle: 16-byte chunk j of row r sits at chunk j ^ ((r >> 1) & 3))
@@ -861,7 +902,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
           const uint32_t stg = s_out + ew * Cfg::kStageOutBytes;
 #pragma unroll
           for (int pc = 0; pc < Cfg::kThreadCols / 32; ++pc) {
-            const int32_t col0 = c.n0 + col_base + pc * 32;
+            const int32_t col0 = c.n0 + ocol + pc * 32;
             const float sb_l = sb_pre[pc];
             if (lane == 0) ptx::bulk_wait_read_all();  // staging buffer free again
             __syncwarp();
@@ -893,7 +934,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
           uint16_t* orow = p.out + static_cast<size_t>(row_val || row_zero ? R : 0) * p.N;
 #pragma unroll
           for (int pc = 0; pc < Cfg::kThreadCols / 32; ++pc) {
-            const int32_t col0 = c.n0 + col_base + pc * 32;
+            const int32_t col0 = c.n0 + ocol + pc * 32;
             const float sb_l = sb_pre[pc];
 #pragma unroll
             for (int j8 = 0; j8 < 4; ++j8) {

@@ -268,6 +268,7 @@ mslkb_status plan(int layout, int64_t rows, int64_t G, int64_t N, int64_t K, int
   if (!dynamic && G > 0 && rows > 0) per_group = rows / (G < rows ? G : rows);
   bool swap;
   int tile_n;
+  int cluster = 1;
   if (per_group <= 16) {
     swap = true;
     tile_n = 16;
@@ -280,11 +281,19 @@ mslkb_status plan(int layout, int64_t rows, int64_t G, int64_t N, int64_t K, int
     if (tma) {
       const int wide = find_variant(dynamic, true, false, 256);
       if (wide >= 0 && tiles_bound(variant(wide), layout, rows, G, N) >= num_sms) tile_n = 256;
+      // CTA pairs (256 x 256 tiles, half the weight bytes per SM and K block): measured on
+      // GB300 ~5% ahead of 128 x 256 tiles on full 512-row slabs and level on 1024-row
+      // groups, behind on shorter or ragged groups and on HBM-bound shapes; taken for
+      // long groups with at least four waves of pairs
+      const int pair = find_variant(dynamic, true, false, 256, 2);
+      if (tile_n == 256 && pair >= 0 && per_group >= (dynamic ? 512 : 1024) &&
+          tiles_bound(variant(pair), layout, rows, G, N) >= 4 * (num_sms / 2))
+        cluster = 2;
     }
   }
   int vi = g_forced_variant.load();
   if (vi < 0) {
-    vi = find_variant(dynamic, tma, swap, tile_n);
+    vi = find_variant(dynamic, tma, swap, tile_n, cluster);
     if (vi < 0 && !tma) vi = find_variant(dynamic, false, false, 128);
   }
   const VariantInfo* v = variant(vi);

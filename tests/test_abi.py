@@ -153,12 +153,14 @@ GB300_SMS = 152
     ("c3_llama70b_m128", "stacked_swap_w128xa16_tma"),
     ("c3_llama70b_m1024", "stacked_tile128x256_tma"),
     ("c3_llama70b_m8192", "stacked_tile128x256_tma"),
-    ("c4_llama405b", "stacked_tile128x256_tma"),
+    ("c4_llama405b", "stacked_pair256x256_tma"),
+    ("n1_batched_llama70b_m512", "dynamic_pair256x256_tma"),
+    ("n2_offsets_llama70b_m8192", "stacked_tile128x256_tma"),
 ])
 def test_plan_per_workload(L, name, expect):
     wl = workloads()[name]
-    layout = 0 if wl.layout == "stacked" else 1
-    rows = wl.rows if layout == 0 else wl.expected_m
+    layout = 1 if wl.slabs else 0   # offsets plan as stacked, batched as dynamic
+    rows = wl.expected_m if wl.slabs else wl.rows
     info = fx.mslkb_plan(layout, rows, wl.G, wl.N, wl.K, GB300_SMS)
     assert fx.variant_name(info.variant) == expect
     assert 1 <= info.grid <= GB300_SMS
@@ -224,13 +226,14 @@ def test_plan_grid_bounds(L):
         fx.mslkb_set_split_k(1)  # auto: swap-AB plans split, every SM gets K work
         i = fx.mslkb_plan(0, 1, 16, 8192, 8192, 152)
         assert i.tiles_bound == 64 and i.grid == 152 and i.split_k == 1
-        i = fx.mslkb_plan(0, 16384, 16, 16384, 16384, 152)  # 128-row tiles: whole
-        assert i.grid == 152 and i.tiles_bound == (16384 + 16 * 127) // 128 * 64
-        assert i.split_k == 0
+        i = fx.mslkb_plan(0, 16384, 64, 16384, 16384, 152)  # 128-row tiles: whole
+        assert i.grid == 152 and i.tiles_bound == (16384 + 64 * 127) // 128 * 64
+        assert i.split_k == 0 and i.tile_m == 128
         i = fx.mslkb_plan(0, 64, 4, 256, 0, 152)  # K = 0: nothing to split
         assert i.split_k == 0
         fx.mslkb_set_split_k(2)  # every plan
-        assert fx.mslkb_plan(0, 16384, 16, 16384, 16384, 152).split_k == 1
+        assert fx.mslkb_plan(0, 16384, 64, 16384, 16384, 152).split_k == 1
+        assert fx.mslkb_plan(0, 16384, 16, 16384, 16384, 152).split_k == 0  # pairs: whole
         assert fx.mslkb_plan(0, 512, 2, 4096, 64, 152).grid == 152
         with pytest.raises(fx.MslkbError):
             fx.mslkb_set_split_k(3)
