@@ -1,4 +1,5 @@
-"""CPU oracle for the FP8 rowwise-scaled grouped GEMM (stacked and dynamic layouts).
+"""CPU oracle for the FP8 rowwise-scaled grouped GEMM (stacked, dynamic, offsets, batched,
+ragged-N and ragged-K layouts).
 
 TEST INFRASTRUCTURE ONLY: the tests, the smoke check and the benchmark's CPU-baseline
 leg are the only callers.  Nothing here imports the CUDA library or its package, and
@@ -45,6 +46,8 @@ MUTANTS = {
     8: "dynamic padding rows not written",
     9: "bf16 ties rounded away from zero",
     10: "scale_b not applied",
+    11: "ragged-N: the slab of group 0 used for every group",
+    12: "ragged-K: every group's slice read from k = 0",
 }
 
 
@@ -93,6 +96,10 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_offsets.restype = ctypes.c_int
     lib.oracle_batched.argtypes = [p, p, p, p, i64, i64, i64, i64, p, ctypes.c_int]
     lib.oracle_batched.restype = None
+    lib.oracle_n_offsets.argtypes = [p, p, p, p, p, i64, i64, i64, i64, p, i64, p, ctypes.c_int]
+    lib.oracle_n_offsets.restype = ctypes.c_int
+    lib.oracle_k_offsets.argtypes = [p, p, p, p, p, i64, i64, i64, i64, p, i64, p, ctypes.c_int]
+    lib.oracle_k_offsets.restype = ctypes.c_int
     lib.oracle_dot_int.argtypes = [p, p, i64]
     lib.oracle_dot_int.restype = ctypes.c_int64
     lib.oracle_dot.argtypes = [p, p, i64]
@@ -265,6 +272,53 @@ class Oracle:
         self.lib.oracle_dynamic_rows(_ptr(A), _ptr(B), _ptr(sa), _ptr(sb), _ptr(z), G, E,
                                      N, K, _ptr(r), r.size, _ptr(out), int(threads))
         return out
+
+    def n_offsets(self, A, B, scale_a, scale_b, offsets, rows=None, out=None,
+                  threads: int = 0):
+        """Ragged-N layout: A [G, M, K] u8, B [total_N, K] u8, scale_a [G, M] f32,
+        scale_b [total_N] f32, offsets [G] int32 inclusive prefix over N.  Returns
+        (out [M, total_N] u16 -- or the chosen ``rows`` of it --, clamped).  Columns past
+        the last group keep the contents of ``out`` (zeros if None)."""
+        B = _c(B, np.uint8)
+        total_N, K = B.shape
+        o = _c(offsets, np.int32)
+        G = o.size
+        sa = _c(scale_a, np.float32).ravel()
+        M = sa.size // G if G else 0
+        A = _c(A, np.uint8).reshape(G * M, K)
+        sb = _c(scale_b, np.float32).ravel()
+        assert sb.size == total_N and sa.size == G * M
+        r = None if rows is None else _c(rows, np.int64)
+        n_out = M if r is None else r.size
+        if out is None:
+            out = np.zeros((n_out, total_N), dtype=np.uint16)
+        else:
+            out = _c(out, np.uint16).reshape(n_out, total_N).copy()
+        clamped = self.lib.oracle_n_offsets(_ptr(A), _ptr(B), _ptr(sa), _ptr(sb), _ptr(o), G, M,
+                                            total_N, K, 0 if r is None else _ptr(r),
+                                            0 if r is None else r.size, _ptr(out), int(threads))
+        return out, bool(clamped)
+
+    def k_offsets(self, A, B, scale_a, scale_b, offsets, rows=None, threads: int = 0):
+        """Ragged-K layout: A [M, total_K] u8, B [N, total_K] u8, scale_a [G, M] f32,
+        scale_b [G, N] f32, offsets [G] int32 inclusive prefix over K.  Returns (out
+        [G*M, N] u16 -- or the chosen slab ``rows`` of it --, clamped)."""
+        A = _c(A, np.uint8)
+        B = _c(B, np.uint8)
+        M, total_K = A.shape
+        N = B.shape[0]
+        o = _c(offsets, np.int32)
+        G = o.size
+        sa = _c(scale_a, np.float32).ravel()
+        sb = _c(scale_b, np.float32).ravel()
+        assert B.shape == (N, total_K) and sa.size == G * M and sb.size == G * N
+        r = None if rows is None else _c(rows, np.int64)
+        n_out = G * M if r is None else r.size
+        out = np.full((n_out, N), 0xABCD, dtype=np.uint16)
+        clamped = self.lib.oracle_k_offsets(_ptr(A), _ptr(B), _ptr(sa), _ptr(sb), _ptr(o), G, M,
+                                            N, total_K, 0 if r is None else _ptr(r),
+                                            0 if r is None else r.size, _ptr(out), int(threads))
+        return out, bool(clamped)
 
 
 def bf16_bits_to_float(bits: np.ndarray) -> np.ndarray:

@@ -132,3 +132,42 @@ def offsets(A, B, scale_a, scale_b, offsets_incl, total_M):
 def batched(A, B, scale_a, scale_b, M):
     G = len(B)
     return dynamic(A, B, scale_a, scale_b, [M] * G, M)
+
+
+def _bounds(offsets_incl, total):
+    """Group ranges from an int32 inclusive prefix: the steps between successive offsets
+    (offsets[-1] = 0), each clamped into [0, total - start]."""
+    out, start = [], 0
+    for g in range(len(offsets_incl)):
+        c = int(offsets_incl[g]) - (int(offsets_incl[g - 1]) if g else 0)
+        c = max(0, min(c, total - start))
+        out.append((start, start + c))
+        start += c
+    return out
+
+
+def n_offsets(A, B, scale_a, scale_b, offsets_incl, total_N):
+    """Ragged N: A[g][m] rows (G slabs of M), B[n] rows (total_N), scale_a[g][m],
+    scale_b[n]; group g owns output columns [c_g, c_{g+1}); out {(m, n): bits}."""
+    G = len(A)
+    M = len(A[0]) if G else 0
+    out = {}
+    for g, (c0, c1) in enumerate(_bounds(offsets_incl, total_N)):
+        for m in range(M):
+            for n in range(c0, c1):
+                out[(m, n)] = element(A[g][m], B[n], scale_a[g][m], scale_b[n])
+    return out
+
+
+def k_offsets(A, B, scale_a, scale_b, offsets_incl, total_K):
+    """Ragged K: A[m] and B[n] rows of total_K codes, scale_a[g][m], scale_b[g][n]; group
+    g contracts over k in [k_g, k_{g+1}); out {(g*M + m, n): bits}."""
+    M = len(A)
+    N = len(B)
+    out = {}
+    for g, (k0, k1) in enumerate(_bounds(offsets_incl, total_K)):
+        for m in range(M):
+            for n in range(N):
+                out[(g * M + m, n)] = element(list(A[m])[k0:k1], list(B[n])[k0:k1],
+                                              scale_a[g][m], scale_b[g][n])
+    return out

@@ -1,6 +1,7 @@
 /*
  * oracle.c -- plain, slow, obviously correct CPU oracle for the FP8 rowwise-scaled
- * grouped GEMM f8f8bf16_rowwise_grouped, stacked and dynamic layouts.
+ * grouped GEMM f8f8bf16_rowwise_grouped: stacked, dynamic, offsets, batched, ragged-N
+ * and ragged-K layouts.
  *
  * TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the CPU-baseline leg
  * of the benchmark may build, load or call this file.  It shares no code, header,
@@ -449,6 +450,109 @@ void oracle_batched(const uint8_t *A, const uint8_t *B, const float *scale_a,
         for (int64_t n = 0; n < N; ++n)
             o[n] = element_gn(arow, B, scale_b, g, n, N, K, scale_a[row], lut);
     }
+}
+
+/* ------------------------------------------------------------------------------ */
+/* Ragged-N layout (3D-2D; MSLK #471, commit adding the form whose weights are one    */
+/* [total_N, K] matrix that the groups partition by row, results packed side by side */
+/* into [M, total_N]).  A [G, M, K] (one slab of M rows per group), scale_a [G, M],    */
+/* B [total_N, K], scale_b [total_N], offsets [G] int32 inclusive prefix over N:       */
+/* group g owns the output columns [c_g, c_{g+1}), where the column counts are the     */
+/* steps offsets[g] - offsets[g-1] (offsets[-1] = 0) under the stacked clamping rules. */
+/*   out[m, n] = bf16(sa[g, m] * sb[n] * sum_k A[g, m, k] * B[n, k]),  n in group g    */
+/* Columns past the last group are left untouched.  Returns the clamp flag.           */
+/* ------------------------------------------------------------------------------ */
+static int counts_from_offsets(const int32_t *offsets, int64_t G, int64_t total, int64_t *bound)
+{
+    int64_t *cnt = (int64_t *)malloc(sizeof(int64_t) * (size_t)(G > 0 ? G : 1));
+    if (!cnt) return -1;
+    for (int64_t g = 0; g < G; ++g)
+        cnt[g] = (int64_t)offsets[g] - (g > 0 ? (int64_t)offsets[g - 1] : 0);
+    int clamped = oracle_stacked_offsets(cnt, G, total, bound);
+    free(cnt);
+    return clamped;
+}
+
+int oracle_n_offsets(const uint8_t *A, const uint8_t *B, const float *scale_a,
+                     const float *scale_b, const int32_t *offsets, int64_t G, int64_t M,
+                     int64_t total_N, int64_t K, const int64_t *rows, int64_t nrows,
+                     uint16_t *out, int nthreads)
+{
+    /* rows == NULL: all M output rows into out [M, total_N]; else out row i = row rows[i] */
+    double lut[256];
+    fill_lut(lut);
+    int64_t *col = (int64_t *)malloc(sizeof(int64_t) * (size_t)(G + 1));
+    if (!col) return -1;
+    int clamped = counts_from_offsets(offsets, G, total_N, col);
+    int64_t n_out = rows ? nrows : M;
+#ifdef _OPENMP
+    if (nthreads <= 0) nthreads = omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads)
+#else
+    (void)nthreads;
+#endif
+    for (int64_t i = 0; i < n_out; ++i) {
+        int64_t m = rows ? rows[i] : i;
+        uint16_t *o = out + (size_t)i * (size_t)total_N;
+        for (int64_t g = 0; g < G; ++g) {
+#if ORACLE_MUTANT == 11
+            const uint8_t *arow = A + (size_t)m * (size_t)K; /* mutant: slab of group 0 */
+#else
+            const uint8_t *arow = A + ((size_t)g * (size_t)M + (size_t)m) * (size_t)K;
+#endif
+            float sa = scale_a[g * M + m];
+            for (int64_t n = col[g]; n < col[g + 1]; ++n)
+                o[n] = oracle_element(arow, B + (size_t)n * (size_t)K, K, sa, scale_b[n], lut);
+        }
+    }
+    free(col);
+    return clamped;
+}
+
+/* ------------------------------------------------------------------------------ */
+/* Ragged-K layout (2D-2D; MSLK #471, commit adding the layout whose groups slice K):   */
+/* A [M, total_K], B [N, total_K], scale_a [G, M], scale_b [G, N], offsets [G] int32   */
+/* inclusive prefix over K: group g contracts over k in [k_g, k_{g+1}) (counts and     */
+/* clamping as above) and produces a whole [M, N] slab:                                 */
+/*   out[g, m, n] = bf16(sa[g, m] * sb[g, n] * sum_{k_g <= k < k_{g+1}} A[m, k] B[n, k]) */
+/* A group contracting over nothing gets +0.0 (the empty sum).  out is [G*M, N]; with   */
+/* rows != NULL, out row i is slab row rows[i] (in [0, G*M)).  Returns the clamp flag.  */
+/* ------------------------------------------------------------------------------ */
+int oracle_k_offsets(const uint8_t *A, const uint8_t *B, const float *scale_a,
+                     const float *scale_b, const int32_t *offsets, int64_t G, int64_t M,
+                     int64_t N, int64_t total_K, const int64_t *rows, int64_t nrows,
+                     uint16_t *out, int nthreads)
+{
+    double lut[256];
+    fill_lut(lut);
+    int64_t *ks = (int64_t *)malloc(sizeof(int64_t) * (size_t)(G + 1));
+    if (!ks) return -1;
+    int clamped = counts_from_offsets(offsets, G, total_K, ks);
+    int64_t n_out = rows ? nrows : G * M;
+#ifdef _OPENMP
+    if (nthreads <= 0) nthreads = omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads)
+#else
+    (void)nthreads;
+#endif
+    for (int64_t i = 0; i < n_out; ++i) {
+        int64_t row = rows ? rows[i] : i;
+        int64_t g = row / M;
+        int64_t m = row - g * M;
+#if ORACLE_MUTANT == 12
+        int64_t k0 = 0, len = ks[g + 1] - ks[g]; /* mutant: every slice starts at k = 0 */
+#else
+        int64_t k0 = ks[g], len = ks[g + 1] - ks[g];
+#endif
+        const uint8_t *arow = A + (size_t)m * (size_t)total_K + (size_t)k0;
+        float sa = scale_a[g * M + m];
+        uint16_t *o = out + (size_t)i * (size_t)N;
+        for (int64_t n = 0; n < N; ++n)
+            o[n] = oracle_element(arow, B + (size_t)n * (size_t)total_K + (size_t)k0, len, sa,
+                                  scale_b[g * N + n], lut);
+    }
+    free(ks);
+    return clamped;
 }
 
 /* Exact unscaled dot products as integers: S * 2^18 for one (row, n) pair, using   */

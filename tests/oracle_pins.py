@@ -454,10 +454,111 @@ def pin_batched_layout(orc, cases=15, seed=47):
         assert np.array_equal(out, orc.dynamic(A, B, sa, sb, [M] * G, M)), f"case {i}"
 
 
+def _ragged_offsets(rng, G, total, step=1, over=False):
+    """Random int32 inclusive offsets over `total` (multiples of `step`): some empty
+    groups, optionally a last offset past `total` (clamped) or a decreasing step."""
+    cuts = np.sort(rng.integers(0, total // step + 1, size=G)) * step
+    if G > 1 and rng.random() < 0.5:
+        cuts[rng.integers(0, G - 1)] = cuts[rng.integers(0, G - 1)]  # a repeated offset
+    if over:
+        cuts[-1] = total + step
+    return cuts.astype(np.int32)
+
+
+def pin_n_offsets_layout(orc, cases=20, seed=53):
+    """Ragged-N layout: brute force on tiny cases (empty groups, columns past the last
+    group untouched, clamping at total_N), and each group's columns bit-equal to the
+    stacked layout with that group alone (A = the group's slab, B = its rows of B)."""
+    rng = _rng(seed)
+    for i in range(cases):
+        G, M = int(rng.integers(1, 4)), int(rng.integers(1, 5))
+        TN, K = int(rng.integers(1, 10)), int(rng.choice([0, 1, 9, 32]))
+        A = _random_codes(rng, (G, M, K))
+        B = _random_codes(rng, (TN, K))
+        sa = _random_scales(rng, G * M).reshape(G, M)
+        sb = _random_scales(rng, TN)
+        off = _ragged_offsets(rng, G, TN, over=(i % 5 == 4))
+        out, clamped = orc.n_offsets(A, B, sa, sb, off, out=np.full((M, TN), 0xDEAD, np.uint16))
+        ref = bf.n_offsets(A.tolist(), B.tolist(), sa.tolist(), sb.tolist(), off.tolist(), TN)
+        for (m, n), bits in ref.items():
+            got = int(out[m, n])
+            assert got == bits or (bits == 0 and got == 0x8000), f"case {i} ({m},{n})"
+        owned = {n for (_, n) in ref}
+        for n in range(TN):
+            if n not in owned:
+                assert np.all(out[:, n] == 0xDEAD), f"case {i}: column {n} written"
+        assert clamped == (i % 5 == 4 and int(off[-1]) > TN), f"case {i}: clamp flag"
+        start = 0
+        for g in range(G):
+            end = min(max(int(off[g]), start), TN)
+            if end > start:
+                st, _ = orc.stacked(A[g], B[start:end][None], sa[g], sb[start:end][None], [M],
+                                    total_M=M)
+                assert np.array_equal(out[:, start:end], st), f"case {i} group {g}"
+            start = end
+
+
+def pin_k_offsets_layout(orc, cases=20, seed=59):
+    """Ragged-K layout: brute force on tiny cases (empty slices give +0.0, clamping at
+    total_K), and each group's slab bit-equal to the stacked layout over its K slice; one
+    group over all of K is the plain GEMM."""
+    rng = _rng(seed)
+    for i in range(cases):
+        G, M, N = int(rng.integers(1, 4)), int(rng.integers(1, 5)), int(rng.integers(1, 6))
+        TK = int(rng.choice([0, 16, 48, 64]))
+        A = _random_codes(rng, (M, TK))
+        B = _random_codes(rng, (N, TK))
+        sa = _random_scales(rng, G * M).reshape(G, M)
+        sb = _random_scales(rng, G * N).reshape(G, N)
+        off = _ragged_offsets(rng, G, TK, step=int(rng.choice([1, 16])), over=(i % 5 == 4))
+        out, clamped = orc.k_offsets(A, B, sa, sb, off)
+        ref = bf.k_offsets(A.tolist(), B.tolist(), sa.tolist(), sb.tolist(), off.tolist(), TK)
+        assert len(ref) == out.size
+        for (r, n), bits in ref.items():
+            got = int(out[r, n])
+            assert got == bits or (bits == 0 and got == 0x8000), f"case {i} ({r},{n})"
+        assert clamped == (i % 5 == 4 and int(off[-1]) > TK), f"case {i}: clamp flag"
+        start = 0
+        for g in range(G):
+            end = min(max(int(off[g]), start), TK)
+            st, _ = orc.stacked(A[:, start:end], B[None, :, start:end], sa[g], sb[g][None],
+                                [M], total_M=M)
+            assert np.array_equal(out[g * M:(g + 1) * M], st), f"case {i} group {g}"
+            start = end
+    # one group over all of K: the plain (dense) product
+    A = _random_codes(rng, (3, 64))
+    B = _random_codes(rng, (5, 64))
+    sa, sb = _random_scales(rng, 3), _random_scales(rng, 5)
+    out, _ = orc.k_offsets(A, B, sa, sb, [64])
+    st, _ = orc.stacked(A, B[None], sa, sb[None], [3], total_M=3)
+    assert np.array_equal(out, st)
+
+
+def pin_ragged_sampled_rows(orc, seed=61):
+    """The row-sampling forms of the ragged layouts equal rows of the full results."""
+    rng = _rng(seed)
+    A = _random_codes(rng, (3, 6, 32))
+    B = _random_codes(rng, (11, 32))
+    sa, sb = _random_scales(rng, 18).reshape(3, 6), _random_scales(rng, 11)
+    off = np.array([4, 4, 11], np.int32)
+    full, _ = orc.n_offsets(A, B, sa, sb, off)
+    rows = np.array([5, 0, 3])
+    part, _ = orc.n_offsets(A, B, sa, sb, off, rows=rows)
+    assert np.array_equal(part, full[rows])
+    A2, B2 = _random_codes(rng, (6, 64)), _random_codes(rng, (7, 64))
+    sa2, sb2 = _random_scales(rng, 18).reshape(3, 6), _random_scales(rng, 21).reshape(3, 7)
+    off2 = np.array([16, 48, 64], np.int32)
+    full2, _ = orc.k_offsets(A2, B2, sa2, sb2, off2)
+    rows2 = np.array([17, 0, 11, 6])
+    part2, _ = orc.k_offsets(A2, B2, sa2, sb2, off2, rows=rows2)
+    assert np.array_equal(part2, full2[rows2])
+
+
 PINS = [
     pin_decode_vs_torch, pin_decode_golden, pin_bf16_golden, pin_bf16_vs_torch,
     pin_dot_exact, pin_closed_form_k1, pin_closed_form_all_ones, pin_closed_form_identity,
     pin_coherent_groups, pin_golden_tiny, pin_bruteforce_stacked, pin_bruteforce_dynamic,
     pin_scale_factoring, pin_stacked_ownership, pin_padding_zero, pin_layout_agreement,
     pin_k_zero, pin_sampled_rows, pin_offsets_layout, pin_batched_layout,
+    pin_n_offsets_layout, pin_k_offsets_layout, pin_ragged_sampled_rows,
 ]
