@@ -29,6 +29,7 @@ MSLKB_ERR_TOO_LARGE = 6
 NOALLOC_SCRATCH_BYTES = 8 << 20
 MSLKB_DEV_TIMEOUT = 0x1
 MSLKB_DEV_MSIZES_CLAMPED = 0x2
+MSLKB_DEV_BAD_SLICE = 0x4
 MAX_GROUPS = 1024
 
 _lib = None
@@ -84,6 +85,11 @@ def lib() -> ctypes.CDLL:
             L.mslkb_f8f8bf16_rowwise_grouped_batched.argtypes = [p, p, p, p, p, i64, i64, i64,
                                                                  i64, p]
             L.mslkb_f8f8bf16_rowwise_grouped_batched.restype = ctypes.c_int
+            for name in ("mslkb_f8f8bf16_rowwise_grouped_n_offsets",
+                         "mslkb_f8f8bf16_rowwise_grouped_k_offsets"):
+                fn = getattr(L, name)
+                fn.argtypes = [p, p, p, p, p, p, i64, i64, i64, i64, p]
+                fn.restype = ctypes.c_int
             L.mslkb_status_string.argtypes = [ctypes.c_int]
             L.mslkb_status_string.restype = ctypes.c_char_p
             L.mslkb_last_cuda_error.argtypes = []
@@ -148,6 +154,18 @@ def mslkb_f8f8bf16_rowwise_grouped_batched(A, B, scale_a, scale_b, out, G, M, N,
                                            stream=0) -> int:
     return lib().mslkb_f8f8bf16_rowwise_grouped_batched(A, B, scale_a, scale_b, out, G, M, N,
                                                         K, stream)
+
+
+def mslkb_f8f8bf16_rowwise_grouped_n_offsets(A, B, scale_a, scale_b, offsets, out, G, M,
+                                             total_N, K, stream=0) -> int:
+    return lib().mslkb_f8f8bf16_rowwise_grouped_n_offsets(A, B, scale_a, scale_b, offsets, out,
+                                                          G, M, total_N, K, stream)
+
+
+def mslkb_f8f8bf16_rowwise_grouped_k_offsets(A, B, scale_a, scale_b, offsets, out, G, M, N,
+                                             total_K, stream=0) -> int:
+    return lib().mslkb_f8f8bf16_rowwise_grouped_k_offsets(A, B, scale_a, scale_b, offsets, out,
+                                                          G, M, N, total_K, stream)
 
 
 def mslkb_status_string(status: int) -> str:
@@ -369,6 +387,64 @@ def f8f8bf16_rowwise_grouped_batched(XQ, WQ, x_scale, w_scale, out=None, stream=
         G, M, N, K, _stream_ptr(stream))
     if s != MSLKB_OK:
         raise MslkbError(s, "f8f8bf16_rowwise_grouped_batched")
+    return out
+
+
+def f8f8bf16_rowwise_grouped_n_offsets(XQ, WQ, x_scale, w_scale, offsets, out=None,
+                                       stream=None):
+    """Ragged N (3D-2D): XQ [G, M, K] e4m3, WQ [total_N, K] e4m3, x_scale [G, M] fp32,
+    w_scale [total_N] fp32, offsets [G] int32 inclusive prefix over N -> out [M, total_N]
+    bf16 (columns past offsets[G-1] zeroed when out is allocated here)."""
+    import torch
+    _check(XQ, "XQ", _fp8_types(), 3)
+    _check(WQ, "WQ", _fp8_types(), 2)
+    _check(x_scale, "x_scale", (torch.float32,))
+    _check(w_scale, "w_scale", (torch.float32,))
+    _check(offsets, "offsets", (torch.int32,), 1)
+    G, M, K = XQ.shape
+    total_N, K2 = WQ.shape
+    if K2 != K or x_scale.numel() != G * M or w_scale.numel() != total_N or offsets.numel() != G:
+        raise ValueError("inconsistent shapes")
+    if out is None:
+        out = torch.zeros((M, total_N), dtype=torch.bfloat16, device=XQ.device)
+    else:
+        _check(out, "out", (torch.bfloat16,), 2)
+        if tuple(out.shape) != (M, total_N):
+            raise ValueError("out has the wrong shape")
+    s = mslkb_f8f8bf16_rowwise_grouped_n_offsets(
+        XQ.data_ptr(), WQ.data_ptr(), x_scale.data_ptr(), w_scale.data_ptr(),
+        offsets.data_ptr(), out.data_ptr(), G, M, total_N, K, _stream_ptr(stream))
+    if s != MSLKB_OK:
+        raise MslkbError(s, "f8f8bf16_rowwise_grouped_n_offsets")
+    return out
+
+
+def f8f8bf16_rowwise_grouped_k_offsets(XQ, WQ, x_scale, w_scale, offsets, out=None,
+                                       stream=None):
+    """Ragged K (2D-2D): XQ [M, total_K] e4m3, WQ [N, total_K] e4m3, x_scale [G, M] fp32,
+    w_scale [G, N] fp32, offsets [G] int32 inclusive prefix over K -> out [G, M, N] bf16."""
+    import torch
+    _check(XQ, "XQ", _fp8_types(), 2)
+    _check(WQ, "WQ", _fp8_types(), 2)
+    _check(x_scale, "x_scale", (torch.float32,))
+    _check(w_scale, "w_scale", (torch.float32,))
+    _check(offsets, "offsets", (torch.int32,), 1)
+    M, total_K = XQ.shape
+    N, K2 = WQ.shape
+    G = offsets.numel()
+    if K2 != total_K or x_scale.numel() != G * M or w_scale.numel() != G * N:
+        raise ValueError("inconsistent shapes")
+    if out is None:
+        out = torch.empty((G, M, N), dtype=torch.bfloat16, device=XQ.device)
+    else:
+        _check(out, "out", (torch.bfloat16,))
+        if out.numel() != G * M * N:
+            raise ValueError("out has the wrong size")
+    s = mslkb_f8f8bf16_rowwise_grouped_k_offsets(
+        XQ.data_ptr(), WQ.data_ptr(), x_scale.data_ptr(), w_scale.data_ptr(),
+        offsets.data_ptr(), out.data_ptr(), G, M, N, total_K, _stream_ptr(stream))
+    if s != MSLKB_OK:
+        raise MslkbError(s, "f8f8bf16_rowwise_grouped_k_offsets")
     return out
 
 

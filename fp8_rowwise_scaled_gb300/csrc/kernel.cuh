@@ -49,20 +49,23 @@ constexpr int kMaxGroups = 1024;
 constexpr int kBK = 128;  // bytes (= e4m3 elements) of K per pipeline stage
 constexpr uint32_t kStatusTimeout = 1u;
 constexpr uint32_t kStatusClamped = 2u;
+constexpr uint32_t kStatusBadSlice = 4u;  // ragged K: a slice bound not on 16 elements
 
 struct GemmParams {
   const uint8_t* A;        // [rows, K] e4m3
   const uint8_t* B;        // [G, N, K] e4m3
   const float* scale_a;    // [rows]
   const float* scale_b;    // [G, N]
-  const int64_t* meta;     // [G] m_sizes (stacked) or zero_start_index_M (dynamic)
+  const int64_t* meta;     // [G] m_sizes (stacked), zero_start_index_M (dynamic), or int32
+                           // inclusive offsets (offsets layout; ragged N / K over N / K)
   uint16_t* out;           // [rows, N] bf16 bits
   uint32_t* status;        // device status word
-  int32_t rows;            // total_M (stacked) or G * E (dynamic)
+  int32_t rows;            // rows of A: total_M (stacked), G * E (dynamic, ragged N), M
+                           // (ragged K)
   int32_t G;
-  int32_t N;
-  int32_t K;
-  int32_t E;               // expected_m (dynamic only)
+  int32_t N;               // columns of the output (total_N for ragged N)
+  int32_t K;               // row length of A and B (total_K for ragged K)
+  int32_t E;               // slab height: expected_m (dynamic), M (ragged N / K)
   int32_t num_kb;          // ceil(K / 128)
   int32_t copy_width;      // cp.async loader: bytes per copy (16, 8, 4) or 1 (byte loads)
   int32_t meta_kind;       // stacked: 0 int64 m_sizes, 1 int32 inclusive offsets;
@@ -75,7 +78,7 @@ struct GemmParams {
 };
 
 template <int kTileN_, int kStages_, bool kSwap_, bool kTma_, bool kDynamic_, int kEpiWarps_ = 4,
-          bool kPair_ = false>
+          bool kPair_ = false, int kRagged_ = 0>
 struct KernelCfg {
   static constexpr int kTileN = kTileN_;     // MMA N
   static constexpr int kStages = kStages_;
@@ -88,6 +91,12 @@ struct KernelCfg {
   // SM then loads half of the weight tile per K block instead of all of it.
   static constexpr bool kPair = kPair_;
   static constexpr int kCtas = kPair ? 2 : 1;
+  // Ragged layouts (MSLK #471, grouped-mm commits): 1 = groups partition N (A [G, M, K],
+  // B [total_N, K], out [M, total_N]); 2 = groups slice K (A [M, total_K], B [N, total_K],
+  // out [G, M, N]).  Group ranges come from int32 inclusive offsets.
+  static constexpr bool kRagN = kRagged_ == 1;
+  static constexpr bool kRagK = kRagged_ == 2;
+  static constexpr bool kRagged = kRagged_ != 0;
   static constexpr int kMmaM = 128;                           // accumulator rows per CTA
   static constexpr int kActRows = kSwap ? kTileN : kMmaM;     // activation rows per CTA
   static constexpr int kWRows = kSwap ? kMmaM : kTileN / kCtas;  // weight rows per CTA
@@ -150,6 +159,7 @@ struct KernelCfg {
   static_assert(2 * kAccCols <= 512, "two accumulators must fit TMEM");
   static_assert(kEpiWarps == 4 || (kEpiWarps == 8 && !kSwap), "epilogue warp split");
   static_assert(!kPair || (kTma && !kSwap && kTileN == 256), "CTA pairs: 256 x 256 tiles, TMA");
+  static_assert(!kRagged || (kTma && !kPair && !kDynamic), "ragged layouts: TMA, single CTAs");
   static_assert(kThreadCols % 16 == 0, "TMEM load granularity");
   static_assert(!kRegSplit || (kThreads == 384 && kEpiWarp0 == 4 &&
                                128 * kRegsLow + 256 * kRegsHigh == kThreads * kLaunchRegs),
@@ -163,6 +173,15 @@ struct TileCoord {
   int32_t valid_end;  // rows < valid_end get the product
   int32_t zero_end;   // rows in [valid_end, zero_end) get +0.0 (padding)
   bool half;          // CTA pairs: a 128-row tile (64 rows per CTA, M = 128 MMA)
+  int32_t orow_delta; // output row = A row + orow_delta
+  int32_t srow_delta; // scale_a index = A row + srow_delta
+  int32_t n_begin;    // columns in [n_begin, n_end) belong to the tile's group
+  int32_t n_end;
+  int32_t bz;         // third coordinate of the weight tensor map
+  int32_t sb_off;     // scale_b index of column 0 of the group
+  int32_t k0;         // first K element of the contraction
+  int32_t k_len;      // K elements of the contraction
+  int32_t nkb;        // K blocks of the contraction
 };
 
 // CTA pairs: a group's rows run in 256-row tiles, except that a last piece of at most 128
@@ -180,7 +199,8 @@ __device__ __forceinline__ int32_t tile_cover(int32_t cnt) {
 
 // Shared-memory scheduler tables.
 //   rowinfo[g]: stacked -> first row of group g (G + 1 entries, clamped prefix);
-//               dynamic -> valid rows v_g of slab g.
+//               dynamic -> valid rows v_g of slab g;
+//               ragged N / K -> first column / first K element of group g (G + 1 entries).
 //   tile_pre[g]: exclusive prefix of output tiles over groups (G + 1 entries).
 struct Sched {
   const int32_t* rowinfo;
@@ -189,7 +209,30 @@ struct Sched {
   int32_t E;
   int32_t n_tiles_n;
   int32_t total;
+  int32_t N;
+  int32_t K;
+  int32_t num_kb;
 };
+
+// Output tiles of group g (ntn: weight tiles across N).
+template <class Cfg>
+__device__ __forceinline__ int64_t group_tiles(const int32_t* rowinfo, int32_t g, int32_t E,
+                                               int64_t ntn) {
+  if constexpr (Cfg::kRagN) {
+    // every slab row, over the group's own columns; the group's tiles start on the 8-column
+    // grid below its first column, so that every output store is 16-byte aligned
+    const int32_t c0 = rowinfo[g], c1 = rowinfo[g + 1];
+    const int64_t cols = c1 > c0 ? static_cast<int64_t>(c1) - (c0 & ~7) : 0;
+    return ((E + Cfg::kTileAct - 1) / Cfg::kTileAct) * ((cols + Cfg::kTileW - 1) / Cfg::kTileW);
+  } else if constexpr (Cfg::kRagK) {  // a whole [M, N] slab per group
+    return ((E + Cfg::kTileAct - 1) / Cfg::kTileAct) * ntn;
+  } else {
+    int64_t cnt;
+    if constexpr (Cfg::kDynamic) cnt = rowinfo[g];
+    else cnt = static_cast<int64_t>(rowinfo[g + 1]) - rowinfo[g];
+    return ((cnt + Cfg::kTileAct - 1) / Cfg::kTileAct) * ntn;
+  }
+}
 
 template <class Cfg>
 __device__ __forceinline__ int32_t group_rows(const Sched& s, int32_t g) {
@@ -209,15 +252,61 @@ __device__ __forceinline__ TileCoord decode_tile(const Sched& s, int32_t t, uint
     else hi = mid;
   }
   const int32_t g = lo;
+  TileCoord c;
+  c.g = g;
+  c.half = false;
+  if constexpr (Cfg::kRagged) {
+    const int32_t mt = (s.E + Cfg::kTileAct - 1) / Cfg::kTileAct;
+    const int32_t local = t - s.tile_pre[g];
+    const int32_t n_idx = local / mt;
+    const int32_t m_idx = local - n_idx * mt;
+    const int32_t lo_g = s.rowinfo[g], hi_g = s.rowinfo[g + 1];
+    if constexpr (Cfg::kRagN) {
+      // A rows of slab g; output rows are slab-local; columns of the group only
+      c.m0 = g * s.E + m_idx * Cfg::kTileAct;
+      c.valid_end = c.zero_end = g * s.E + s.E;
+      c.orow_delta = -g * s.E;
+      c.srow_delta = 0;
+      c.n0 = (lo_g & ~7) + n_idx * Cfg::kTileW;  // on the 8-column grid (16-byte stores)
+      c.n_begin = lo_g;
+      c.n_end = hi_g;
+      c.sb_off = 0;
+      c.k0 = 0;
+      c.k_len = s.K;
+      c.nkb = s.num_kb;
+    } else {
+      // A rows shared by the groups; output slab g and scales of group g; the K slice
+      c.m0 = m_idx * Cfg::kTileAct;
+      c.valid_end = c.zero_end = s.E;
+      c.orow_delta = g * s.E;
+      c.srow_delta = g * s.E;
+      c.n0 = n_idx * Cfg::kTileW;
+      c.n_begin = 0;
+      c.n_end = s.N;
+      c.sb_off = g * s.N;
+      c.k0 = lo_g;
+      // a slice whose bounds are off the 16-element TMA grid is not computed (+0.0)
+      c.k_len = ((lo_g | hi_g) & 15) ? 0 : hi_g - lo_g;
+      c.nkb = (c.k_len + kBK - 1) / kBK;
+    }
+    c.bz = 0;
+    return c;
+  }
   const int32_t cnt = group_rows<Cfg>(s, g);
   const int32_t mt = (cnt + Cfg::kTileAct - 1) / Cfg::kTileAct;
   const int32_t local = t - s.tile_pre[g];
   const int32_t n_idx = local / mt;
   const int32_t m_idx = local - n_idx * mt;
-  TileCoord c;
-  c.g = g;
+  c.orow_delta = 0;
+  c.srow_delta = 0;
+  c.n_begin = 0;
+  c.n_end = s.N;
+  c.bz = g;
+  c.sb_off = g * s.N;
+  c.k0 = 0;
+  c.k_len = s.K;
+  c.nkb = s.num_kb;
   const int32_t base = Cfg::kDynamic ? g * s.E : s.rowinfo[g];
-  c.half = false;
   if constexpr (Cfg::kPair) {
     const int32_t rem = cnt - m_idx * Cfg::kTileAct;  // rows from this tile's first on
     c.half = rem <= Cfg::kTileAct / 2;
@@ -375,7 +464,8 @@ __device__ void build_sched(const GemmParams& p, int32_t* rowinfo, int32_t* tile
       if (m < 0) clamped = true;
       my_sum += m < 0 ? 0 : m;
     }
-    const int64_t total = p.rows;
+    // ragged layouts partition the columns (N) or the contraction (K) instead of the rows
+    const int64_t total = Cfg::kRagN ? p.N : (Cfg::kRagK ? p.K : p.rows);
     int64_t run = warp_incl_scan(my_sum, lane) - my_sum;
     for (int32_t g = g0; g < g1; ++g) {
       const int64_t m = count(g);
@@ -389,24 +479,22 @@ __device__ void build_sched(const GemmParams& p, int32_t* rowinfo, int32_t* tile
   }
   __syncwarp();
   int64_t my_tiles = 0;
+  bool bad_slice = false;
   for (int32_t g = g0; g < g1; ++g) {
-    int64_t cnt;
-    if constexpr (Cfg::kDynamic) cnt = rowinfo[g];
-    else cnt = static_cast<int64_t>(rowinfo[g + 1]) - rowinfo[g];
-    my_tiles += ((cnt + Cfg::kTileAct - 1) / Cfg::kTileAct) * ntn;
+    my_tiles += group_tiles<Cfg>(rowinfo, g, p.E, ntn);
+    if constexpr (Cfg::kRagK) bad_slice |= ((rowinfo[g] | rowinfo[g + 1]) & 15) != 0;
   }
   const int64_t incl = warp_incl_scan(my_tiles, lane);
   int64_t tp = incl - my_tiles;
   for (int32_t g = g0; g < g1; ++g) {
     tile_pre[g] = static_cast<int32_t>(tp);
-    int64_t cnt;
-    if constexpr (Cfg::kDynamic) cnt = rowinfo[g];
-    else cnt = static_cast<int64_t>(rowinfo[g + 1]) - rowinfo[g];
-    tp += ((cnt + Cfg::kTileAct - 1) / Cfg::kTileAct) * ntn;
+    tp += group_tiles<Cfg>(rowinfo, g, p.E, ntn);
   }
   if (lane == 31) tile_pre[G] = static_cast<int32_t>(incl);
   const bool any_clamped = __any_sync(0xffffffffu, clamped);
   if (any_clamped && lane == 0 && blockIdx.x == 0) atomicOr(p.status, kStatusClamped);
+  const bool any_bad = __any_sync(0xffffffffu, bad_slice);
+  if (any_bad && lane == 0 && blockIdx.x == 0) atomicOr(p.status, kStatusBadSlice);
 }
 
 // cp.async loader: one 16-byte chunk of a swizzled tile row.
@@ -527,11 +615,15 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
   sched.E = p.E;
   sched.n_tiles_n = (p.N + Cfg::kWRows - 1) / Cfg::kWRows;
   sched.total = tile_pre[p.G];
+  sched.N = p.N;
+  sched.K = p.K;
+  sched.num_kb = p.num_kb;
   const bool has_k = p.num_kb > 0;
   // the work split lives in shared memory: every role reads it, none keeps it in registers
   Work* work_smem = reinterpret_cast<Work*>(smem + Cfg::kOffWork);
   if (threadIdx.x == 0)
-    *work_smem = make_work(sched.total, p.num_kb, p.split_k != 0 && !Cfg::kPair, worker, workers);
+    *work_smem = make_work(sched.total, p.num_kb, p.split_k != 0 && !Cfg::kPair && !Cfg::kRagged,
+                           worker, workers);
   __syncthreads();
   const Work& work = *work_smem;
 
@@ -548,7 +640,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         for (int32_t i = 0; ok && i < work.n_items; ++i) {
           const Item it = work_item(work, i, worker, workers);
           const TileCoord c = decode_tile<Cfg>(sched, it.tile, crank);
-          for (int32_t kb = it.kb0; kb < it.kb1; ++kb) {
+          const int32_t kb_end = Cfg::kRagK ? c.nkb : it.kb1;  // a ragged-K tile's own K
+          for (int32_t kb = it.kb0; kb < kb_end; ++kb) {
             if (!wait_bar(empty_bar(stage), phase ^ 1u, abort_flag, p.status, p.timeout_ns)) {
               ok = false;
               break;
@@ -562,10 +655,11 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                                     c.n0 + static_cast<int32_t>(crank) * Cfg::kWRows, c.g);
             } else {
               ptx::mbar_arrive_expect_tx(full_bar(stage), Cfg::kStageBytes);
-              ptx::tma_load_2d(s_act + stage * Cfg::kActBytes, &tmA, full_bar(stage), kb * kBK,
-                               c.m0);
-              ptx::tma_load_3d(s_w + stage * Cfg::kWBytes, &tmB, full_bar(stage), kb * kBK, c.n0,
-                               c.g);
+              // k0: a ragged-K slice starts on a multiple of 16 elements (16 bytes)
+              ptx::tma_load_2d(s_act + stage * Cfg::kActBytes, &tmA, full_bar(stage),
+                               c.k0 + kb * kBK, c.m0);
+              ptx::tma_load_3d(s_w + stage * Cfg::kWBytes, &tmB, full_bar(stage),
+                               c.k0 + kb * kBK, c.n0, c.bz);
             }
             if (++stage == Cfg::kStages) {
               stage = 0;
@@ -669,7 +763,14 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         if constexpr (Cfg::kPair) {
           if (decode_tile<Cfg>(sched, it.tile, 0u).half) idesc = Cfg::kIdescHalf;
         }
-        for (int32_t kb0 = it.kb0; ok && kb0 < it.kb1; kb0 += kpc) {
+        int32_t kb_end = it.kb1;
+        int32_t k_len = 0;
+        if constexpr (Cfg::kRagK) {
+          const TileCoord c = decode_tile<Cfg>(sched, it.tile, 0u);
+          kb_end = c.nkb;
+          k_len = c.k_len;
+        }
+        for (int32_t kb0 = it.kb0; ok && kb0 < kb_end; kb0 += kpc) {
           const int buf = static_cast<int>(chunk & 1u);
           const uint32_t use = chunk >> 1;  // how often this buffer was used before
           if (!wait_bar<Cfg::kPair>(tempty_bar(buf), (use & 1u) ^ 1u, abort_flag, p.status,
@@ -679,7 +780,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
           }
           ptx::tc_fence_after_sync();
           const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * Cfg::kAccCols);
-          const int32_t kb1 = min(it.kb1, kb0 + kpc);
+          const int32_t kb1 = min(kb_end, kb0 + kpc);
           for (int32_t kb = kb0; kb < kb1; ++kb) {
             if (!wait_bar(full_bar(stage), phase, abort_flag, p.status, p.timeout_ns)) {
               ok = false;
@@ -690,8 +791,32 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
             const uint64_t w_desc = ptx::sw128_kmajor_desc(s_w + stage * Cfg::kWBytes);
             const uint64_t a_desc = Cfg::kSwap ? w_desc : act_desc;
             const uint64_t b_desc = Cfg::kSwap ? act_desc : w_desc;
+            int nmma = kBK / 32;
+            if constexpr (Cfg::kRagK) {
+              // the last block of a K slice: the bytes past the slice belong to the next
+              // group (or are TMA zero fill past total_K).  Whole 32-byte steps past it are
+              // not issued; in a half-used step the unused 16 bytes of every row of both
+              // operands are zeroed first (the slice ends on a 16-element boundary).
+              const int32_t r = k_len - kb * kBK;
+              if (r < kBK) {
+                nmma = (r + 31) / 32;
+                if (r & 16) {
+                  const uint32_t chunk = static_cast<uint32_t>(r >> 4);
+                  const uint32_t sa_base = s_act + stage * Cfg::kActBytes;
+                  const uint32_t sw_base = s_w + stage * Cfg::kWBytes;
+                  for (int row = 0; row < Cfg::kActRows; ++row)
+                    ptx::st_shared_v4(sa_base + row * 128u + ((chunk ^ (row & 7u)) << 4), 0u,
+                                      0u, 0u, 0u);
+                  for (int row = 0; row < Cfg::kWRows; ++row)
+                    ptx::st_shared_v4(sw_base + row * 128u + ((chunk ^ (row & 7u)) << 4), 0u,
+                                      0u, 0u, 0u);
+                  ptx::fence_proxy_async_smem();
+                }
+              }
+            }
 #pragma unroll
             for (int k = 0; k < kBK / 32; ++k) {
+              if (k >= nmma) break;
               // advance 32 bytes of K inside the 128-byte swizzled row: +2 in 16-byte units
               if constexpr (Cfg::kPair)
                 ptx::mma_f8f6f4_pair(d_tmem, a_desc + 2u * k, b_desc + 2u * k, idesc,
@@ -747,6 +872,9 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
       TileCoord c = decode_tile<Cfg>(sched, it.tile, crank);
       // an empty reduction (K = 0) writes +0.0 to every owned row, whatever the scales
       if (!has_k) c.valid_end = c.m0;
+      // a ragged-K tile contracting over nothing (an empty or skipped slice) is all +0.0
+      const int32_t kb_end = Cfg::kRagK ? c.nkb : it.kb1;
+      if (Cfg::kRagK && c.nkb == 0) c.valid_end = c.m0;
       // this warp's rows (row_off from c.m0) and output columns (ocol from c.n0).  A CTA
       // pair's 128-row tile leaves each CTA 64 rows x 256 columns, folded into TMEM as
       // lanes 0-63 = columns 0-127 and lanes 64-127 = columns 128-255 (TMEM columns
@@ -768,12 +896,12 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
       float sb_pre[Cfg::kSwap ? 1 : Cfg::kThreadCols / 32];
       if constexpr (!Cfg::kSwap) {
         const int32_t R = c.m0 + row_off + static_cast<int32_t>(lane);
-        if (active && R < c.valid_end) sa_pre = __ldg(p.scale_a + R);
-        const float* sb_g = p.scale_b + static_cast<size_t>(c.g) * p.N;
+        if (active && R < c.valid_end) sa_pre = __ldg(p.scale_a + (R + c.srow_delta));
+        const float* sb_g = p.scale_b + c.sb_off;
 #pragma unroll
         for (int pc = 0; pc < Cfg::kThreadCols / 32; ++pc) {
           const int32_t col = c.n0 + ocol + pc * 32 + static_cast<int32_t>(lane);
-          sb_pre[pc] = (active && col < p.N) ? __ldg(sb_g + col) : 0.0f;
+          sb_pre[pc] = (active && col < c.n_end) ? __ldg(sb_g + col) : 0.0f;
         }
       }
       // fp32 accumulator of this thread (round-to-nearest adds of the TMEM chunks)
@@ -788,7 +916,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         warp_any = c.n0 + static_cast<int32_t>(32u * q) < p.N && c.m0 < c.valid_end;
       }
       if (has_k) {
-        for (int32_t kb0 = it.kb0; kb0 < it.kb1; kb0 += kpc) {
+        for (int32_t kb0 = it.kb0; kb0 < kb_end; kb0 += kpc) {
           const int buf = static_cast<int>(chunk & 1u);
           const uint32_t use = chunk >> 1;
           if (!wait_bar(tfull_bar(buf), use & 1u, abort_flag, p.status, p.timeout_ns)) {
@@ -895,7 +1023,10 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         const bool row_val = R < c.valid_end;
         const bool row_zero = !row_val && R < c.zero_end;
         const int32_t R_first = c.m0 + row_off;
-        if (Cfg::kTmaStore && R_first + 31 < c.zero_end) {
+        // TMA stores clip at the output's last column only: a block that reaches outside a
+        // ragged-N group's columns takes the predicated path
+        if (Cfg::kTmaStore && R_first + 31 < c.zero_end && c.n0 + ocol >= c.n_begin &&
+            (c.n_end == p.N || c.n0 + ocol + Cfg::kThreadCols <= c.n_end)) {
           // all 32 rows of this warp are owned: stage 32 x 32 bf16 blocks in shared memory
           // (64-byte swizzle: 16-byte chunk j of row r sits at chunk j ^ ((r >> 1) & 3))
           // and let one lane store each block with TMA (whole lines, clipped at N)
@@ -924,14 +1055,15 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
             ptx::fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-              ptx::tma_store_2d(&tmC, stg, col0, R_first);
+              ptx::tma_store_2d(&tmC, stg, col0, R_first + c.orow_delta);
               ptx::bulk_commit();
             }
           }
         } else if (__any_sync(0xffffffffu, row_val || row_zero)) {
           // 8 output columns per 16-byte store, predicated per row and on the last column
           const float sa = sa_pre;
-          uint16_t* orow = p.out + static_cast<size_t>(row_val || row_zero ? R : 0) * p.N;
+          uint16_t* orow =
+              p.out + static_cast<size_t>(row_val || row_zero ? R + c.orow_delta : 0) * p.N;
 #pragma unroll
           for (int pc = 0; pc < Cfg::kThreadCols / 32; ++pc) {
             const int32_t col0 = c.n0 + ocol + pc * 32;
@@ -944,8 +1076,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                 const float sb = __shfl_sync(0xffffffffu, sb_l, j8 * 8 + j);
                 y[j] = (acc[pc * 32 + j8 * 8 + j] * sa) * sb;
               }
-              const int32_t col = col0 + j8 * 8;
-              if (col + 7 < p.N) {
+              const int32_t col = col0 + j8 * 8;  // a multiple of 8: 16-byte aligned
+              if (col + 7 < c.n_end && col >= c.n_begin) {
                 if (row_val) {
                   *reinterpret_cast<uint4*>(orow + col) =
                       make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]),
@@ -953,6 +1085,13 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                 } else if (row_zero) {
                   *reinterpret_cast<uint4*>(orow + col) = make_uint4(0u, 0u, 0u, 0u);
                 }
+              } else if (Cfg::kRagN && row_val && col < c.n_end && col + 7 >= c.n_begin) {
+                // a ragged-N group starting or ending inside these 8 columns: its own
+                // columns one by one
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                  if (col + j >= c.n_begin && col + j < c.n_end)
+                    orow[col + j] = __bfloat16_as_ushort(__float2bfloat16_rn(y[j]));
               }
             }
           }
@@ -960,8 +1099,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
       } else {
         // thread = one weight row (output column n); accumulator columns are activation rows
         const int32_t n = c.n0 + static_cast<int32_t>(32u * q + lane);
-        const bool col_ok = n < p.N;
-        const float sb = col_ok ? __ldg(p.scale_b + static_cast<size_t>(c.g) * p.N + n) : 0.0f;
+        const bool col_ok = n >= c.n_begin && n < c.n_end;
+        const float sb = col_ok ? __ldg(p.scale_b + c.sb_off + n) : 0.0f;
 #pragma unroll
         for (int pc = 0; pc < (Cfg::kTileN + 31) / 32; ++pc) {
           constexpr int kCols = Cfg::kTileN < 32 ? Cfg::kTileN : 32;
@@ -970,7 +1109,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
           // lane j holds scale_a of row m_first + j
           const int32_t Rl = m_first + static_cast<int32_t>(lane);
           const float sa_l = (lane < static_cast<uint32_t>(kCols) && Rl < c.valid_end)
-                                 ? __ldg(p.scale_a + Rl) : 0.0f;
+                                 ? __ldg(p.scale_a + (Rl + c.srow_delta)) : 0.0f;
 #pragma unroll
           for (int j = 0; j < kCols; ++j) {
             const float sa = __shfl_sync(0xffffffffu, sa_l, j);
@@ -978,10 +1117,10 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
             if (R < c.valid_end) {
               const float y = (acc[pc * 32 + j] * sa) * sb;
               if (col_ok)
-                p.out[static_cast<size_t>(R) * p.N + n] =
+                p.out[static_cast<size_t>(R + c.orow_delta) * p.N + n] =
                     __bfloat16_as_ushort(__float2bfloat16_rn(y));
             } else if (R < c.zero_end) {
-              if (col_ok) p.out[static_cast<size_t>(R) * p.N + n] = 0;
+              if (col_ok) p.out[static_cast<size_t>(R + c.orow_delta) * p.N + n] = 0;
             }
           }
         }

@@ -37,6 +37,7 @@ struct VariantInfo {
   int box_act;    // activation rows one CTA loads per stage (TMA box height)
   int box_w;      // weight rows one CTA loads per stage
   int cluster;    // CTAs per cluster: 2 for CTA pairs (cta_group::2), else 1
+  int ragged;     // 0 grouped rows (stacked / dynamic), 1 ragged N, 2 ragged K
   int partial_bytes;  // fp32 partial sums of one tile (a split tile's piece)
   int launch_regs;    // registers per thread the kernel must be built with (0: any)
   LaunchFn launch;
@@ -114,7 +115,8 @@ constexpr VariantInfo make_variant(const char* name) {
   return VariantInfo{name,           Cfg::kTileN,   Cfg::kStages,  Cfg::kSwap,
                      Cfg::kTma,      Cfg::kDynamic, Cfg::kThreads, Cfg::kSmemBytes,
                      Cfg::kTileAct,  Cfg::kTileW,   Cfg::kActRows, Cfg::kWRows,
-                     Cfg::kCtas,     Cfg::kEpiWarps * 32 * Cfg::kThreadCols * 4,
+                     Cfg::kCtas,     Cfg::kRagN ? 1 : (Cfg::kRagK ? 2 : 0),
+                     Cfg::kEpiWarps * 32 * Cfg::kThreadCols * 4,
                      Cfg::kLaunchRegs, &launch_variant<Cfg>, &set_attr_variant<Cfg>,
                      &occupancy_variant<Cfg>};
 }
@@ -138,5 +140,9 @@ extern const VariantInfo kVariantsDynamicTma[];
 extern const int kNumVariantsDynamicTma;
 extern const VariantInfo kVariantsCpAsync[];
 extern const int kNumVariantsCpAsync;
+extern const VariantInfo kVariantsRaggedN[];
+extern const int kNumVariantsRaggedN;
+extern const VariantInfo kVariantsRaggedK[];
+extern const int kNumVariantsRaggedK;
 
 }  // namespace mslkb

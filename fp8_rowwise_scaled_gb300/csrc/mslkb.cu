@@ -50,7 +50,7 @@ std::atomic<int> g_split_k{1};
 // ---------------------------------------------------------------------------------
 int num_variants() {
   return mslkb::kNumVariantsStackedTma + mslkb::kNumVariantsDynamicTma +
-         mslkb::kNumVariantsCpAsync;
+         mslkb::kNumVariantsCpAsync + mslkb::kNumVariantsRaggedN + mslkb::kNumVariantsRaggedK;
 }
 
 const VariantInfo* variant(int i) {
@@ -60,14 +60,18 @@ const VariantInfo* variant(int i) {
   if (i < mslkb::kNumVariantsDynamicTma) return &mslkb::kVariantsDynamicTma[i];
   i -= mslkb::kNumVariantsDynamicTma;
   if (i < mslkb::kNumVariantsCpAsync) return &mslkb::kVariantsCpAsync[i];
+  i -= mslkb::kNumVariantsCpAsync;
+  if (i < mslkb::kNumVariantsRaggedN) return &mslkb::kVariantsRaggedN[i];
+  i -= mslkb::kNumVariantsRaggedN;
+  if (i < mslkb::kNumVariantsRaggedK) return &mslkb::kVariantsRaggedK[i];
   return nullptr;
 }
 
-int find_variant(bool dynamic, bool tma, bool swap, int tile_n, int cluster = 1) {
+int find_variant(bool dynamic, bool tma, bool swap, int tile_n, int cluster = 1, int ragged = 0) {
   for (int i = 0; i < num_variants(); ++i) {
     const VariantInfo* v = variant(i);
     if (v->dynamic == dynamic && v->tma == tma && v->swap == swap && v->tile_n == tile_n &&
-        v->cluster == cluster)
+        v->cluster == cluster && v->ragged == ragged)
       return i;
   }
   return -1;
@@ -248,6 +252,10 @@ int copy_width_for(int64_t K, int64_t a_align, int64_t b_align) {
 // Upper bound on output tiles for a variant (the kernel's own count never exceeds it).
 int64_t tiles_bound(const VariantInfo* v, int layout, int64_t rows, int64_t G, int64_t N) {
   const int64_t ntn = ceil_div(N, v->w_rows);
+  // ragged N: every group's slab rows over its own columns, from the 8-column grid below
+  // its first one (a partial tile per group at most); ragged K: a whole slab per group
+  if (layout == 2) return ceil_div(rows, v->act_rows) * (ceil_div(N + 7 * G, v->w_rows) + G);
+  if (layout == 3) return G * ceil_div(rows, v->act_rows) * ntn;
   if (layout == 0) {
     const int64_t nz = G < rows ? G : rows;  // non-empty groups
     const int64_t mt = (rows + nz * (v->act_rows - 1)) / v->act_rows;
@@ -258,18 +266,27 @@ int64_t tiles_bound(const VariantInfo* v, int layout, int64_t rows, int64_t G, i
 
 mslkb_status plan(int layout, int64_t rows, int64_t G, int64_t N, int64_t K, int num_sms,
                   int64_t a_align, int64_t b_align, mslkb_plan_info* info) {
-  if (layout != 0 && layout != 1) return MSLKB_ERR_SHAPE;
+  if (layout < 0 || layout > 3) return MSLKB_ERR_SHAPE;
   if (num_sms <= 0 || rows < 0 || G < 0 || N < 0 || K < 0) return MSLKB_ERR_SHAPE;
   const bool dynamic = layout == 1;
+  const int ragged = layout >= 2 ? layout - 1 : 0;
   const bool tma = (K % 16 == 0) && (a_align % 16 == 0) && (b_align % 16 == 0);
+  if (ragged && !tma) return MSLKB_ERR_ALIGN;  // the ragged layouts are TMA-only
   // rows of one group: the slab height (dynamic) or the mean over the groups that can
   // be non-empty (stacked; the counts themselves stay on the device)
   int64_t per_group = rows;
-  if (!dynamic && G > 0 && rows > 0) per_group = rows / (G < rows ? G : rows);
+  if (layout == 0 && G > 0 && rows > 0) per_group = rows / (G < rows ? G : rows);
   bool swap;
   int tile_n;
   int cluster = 1;
-  if (per_group <= 16) {
+  if (ragged) {  // TMA variants: swap-AB 32, 128 x 256, 128 x 128
+    swap = per_group <= 32;
+    tile_n = swap ? 32 : 128;
+    if (!swap) {
+      const int wide = find_variant(false, true, false, 256, 1, ragged);
+      if (wide >= 0 && tiles_bound(variant(wide), layout, rows, G, N) >= num_sms) tile_n = 256;
+    }
+  } else if (per_group <= 16) {
     swap = true;
     tile_n = 16;
   } else if (per_group <= 32 && tma) {
@@ -293,11 +310,12 @@ mslkb_status plan(int layout, int64_t rows, int64_t G, int64_t N, int64_t K, int
   }
   int vi = g_forced_variant.load();
   if (vi < 0) {
-    vi = find_variant(dynamic, tma, swap, tile_n, cluster);
+    vi = find_variant(dynamic, tma, swap, tile_n, cluster, ragged);
     if (vi < 0 && !tma) vi = find_variant(dynamic, false, false, 128);
   }
   const VariantInfo* v = variant(vi);
-  if (v == nullptr || v->dynamic != dynamic || (v->tma && !tma)) return MSLKB_ERR_SHAPE;
+  if (v == nullptr || v->dynamic != dynamic || v->ragged != ragged || (v->tma && !tma))
+    return MSLKB_ERR_SHAPE;
   const int64_t bound = tiles_bound(v, layout, rows, G, N);
   if (bound > INT32_MAX) return MSLKB_ERR_SHAPE;
   const int64_t nkb = ceil_div(K, mslkb::kBK);
@@ -305,7 +323,7 @@ mslkb_status plan(int layout, int64_t rows, int64_t G, int64_t N, int64_t K, int
   // weights) but slows the 128-row-tile plans by 4-9% (128 KB of partial sums per piece).
   const int policy = g_split_k.load();
   // CTA pairs run whole tiles only (one pair per tile)
-  const bool split = nkb > 0 && v->cluster == 1 && (policy == 2 || (policy == 1 && v->swap));
+  const bool split = nkb > 0 && v->cluster == 1 && !ragged && (policy == 2 || (policy == 1 && v->swap));
   // with splitting every CTA gets K work as long as there are units to share
   const int64_t work = (split ? bound * nkb : bound) * v->cluster;
   const int64_t max_ctas = (num_sms / v->cluster) * v->cluster;
@@ -477,6 +495,74 @@ mslkb_status run(int layout, const void* A, const void* B, const float* scale_a,
   return MSLKB_OK;
 }
 
+
+// Ragged layouts: layout 2 (groups partition N: A [G, M, K], B [total_N, K], out [M, total_N])
+// or 3 (groups slice K: A [M, total_K], B [N, total_K], out [G, M, N]).  `n_cols` is the
+// output width (total_N or N) and `k_row` the row length of A and B (K or total_K).
+mslkb_status run_ragged(int layout, const void* A, const void* B, const float* scale_a,
+                        const float* scale_b, const int32_t* offsets, void* out, int64_t G,
+                        int64_t M, int64_t n_cols, int64_t k_row, void* stream) {
+  if (G < 0 || M < 0 || n_cols < 0 || k_row < 0) return MSLKB_ERR_SHAPE;
+  if (G > MSLKB_MAX_GROUPS || n_cols % 8 != 0) return MSLKB_ERR_SHAPE;
+  if (n_cols > MSLKB_MAX_DIM || k_row > MSLKB_MAX_DIM || M > MSLKB_MAX_DIM) return MSLKB_ERR_SHAPE;
+  const int64_t a_rows = layout == 2 ? G * M : M;
+  const int64_t out_rows = layout == 2 ? M : G * M;
+  const int64_t b_rows = n_cols;  // total_N (ragged N) or N (ragged K) rows of B
+  if (a_rows > MSLKB_MAX_DIM || out_rows > MSLKB_MAX_DIM || out_rows * n_cols >= (1ll << 40) ||
+      a_rows * k_row >= (1ll << 40) || b_rows * k_row >= (1ll << 40) || G * M > MSLKB_MAX_DIM ||
+      G * n_cols > MSLKB_MAX_DIM)
+    return MSLKB_ERR_SHAPE;
+  if (M == 0 || G == 0 || n_cols == 0) return MSLKB_OK;  // nothing is owned or written
+  if (out == nullptr || offsets == nullptr || scale_a == nullptr || scale_b == nullptr)
+    return MSLKB_ERR_NULL;
+  if (k_row > 0 && (A == nullptr || B == nullptr)) return MSLKB_ERR_NULL;
+  if (reinterpret_cast<uintptr_t>(out) % 16 != 0) return MSLKB_ERR_ALIGN;
+  if (k_row % 16 != 0 || addr_align(A) % 16 != 0 || addr_align(B) % 16 != 0)
+    return MSLKB_ERR_ALIGN;
+
+  DeviceState* st = nullptr;
+  mslkb_status s = device_state(&st);
+  if (s != MSLKB_OK) return s;
+  mslkb_plan_info info;
+  s = plan(layout, M, G, n_cols, k_row, st->sm_count, addr_align(A), addr_align(B), &info);
+  if (s != MSLKB_OK) return s;
+  const VariantInfo* v = variant(info.variant);
+  if ((s = ensure_attr(st, info.variant)) != MSLKB_OK) return s;
+
+  LaunchArgs la;
+  std::memset(&la, 0, sizeof(la));
+  GemmParams& p = la.params;
+  p.A = static_cast<const uint8_t*>(A);
+  p.B = static_cast<const uint8_t*>(B);
+  p.scale_a = scale_a;
+  p.scale_b = scale_b;
+  p.meta = reinterpret_cast<const int64_t*>(offsets);
+  p.meta_kind = 1;  // int32 inclusive offsets
+  p.out = static_cast<uint16_t*>(out);
+  p.status = st->status_ptr;
+  p.rows = static_cast<int32_t>(a_rows);
+  p.G = static_cast<int32_t>(G);
+  p.N = static_cast<int32_t>(n_cols);
+  p.K = static_cast<int32_t>(k_row);
+  p.E = static_cast<int32_t>(M);
+  p.num_kb = static_cast<int32_t>(ceil_div(k_row, mslkb::kBK));
+  p.copy_width = 16;
+  {
+    const int kpc = g_kb_per_chunk.load();
+    p.kb_per_chunk = (kpc <= 0 || kpc > p.num_kb) ? (p.num_kb > 0 ? p.num_kb : 1) : kpc;
+  }
+  p.timeout_ns = kWaitTimeoutNs;
+  p.split_k = 0;
+  // A [a_rows, k_row]; B as a one-group [1, b_rows, k_row] map; out [out_rows, n_cols]
+  if ((s = encode_maps(&la, v, A, B, a_rows, 1, b_rows, k_row)) != MSLKB_OK) return s;
+  if ((s = encode_out_map(&la, v, out, out_rows, n_cols)) != MSLKB_OK) return s;
+  la.grid = dim3(launch_grid(st, info.variant, info.grid), 1, 1);
+  la.stream = static_cast<cudaStream_t>(stream);
+  cudaError_t e = v->launch(la);
+  if (e != cudaSuccess) return cuda_fail(e);
+  return MSLKB_OK;
+}
+
 }  // namespace
 
 namespace mslkb {
@@ -614,12 +700,31 @@ mslkb_status mslkb_f8f8bf16_rowwise_grouped_batched(const void* A, const void* B
   return run(1, A, B, scale_a, scale_b, nullptr, out, G * M, G, M, N, K, stream, 2);
 }
 
+mslkb_status mslkb_f8f8bf16_rowwise_grouped_n_offsets(const void* A, const void* B,
+                                                      const float* scale_a,
+                                                      const float* scale_b,
+                                                      const int32_t* offsets, void* out,
+                                                      int64_t G, int64_t M, int64_t total_N,
+                                                      int64_t K, void* stream) {
+  return run_ragged(2, A, B, scale_a, scale_b, offsets, out, G, M, total_N, K, stream);
+}
+
+mslkb_status mslkb_f8f8bf16_rowwise_grouped_k_offsets(const void* A, const void* B,
+                                                      const float* scale_a,
+                                                      const float* scale_b,
+                                                      const int32_t* offsets, void* out,
+                                                      int64_t G, int64_t M, int64_t N,
+                                                      int64_t total_K, void* stream) {
+  return run_ragged(3, A, B, scale_a, scale_b, offsets, out, G, M, N, total_K, stream);
+}
+
 const char* mslkb_status_string(mslkb_status status) {
   switch (status) {
     case MSLKB_OK: return "ok";
     case MSLKB_ERR_NULL: return "a required pointer is NULL";
     case MSLKB_ERR_SHAPE: return "unsupported or negative size (N must be a multiple of 8)";
-    case MSLKB_ERR_ALIGN: return "out must be 16-byte aligned";
+    case MSLKB_ERR_ALIGN:
+      return "out must be 16-byte aligned (ragged layouts: A and B too, rows a multiple of 16)";
     case MSLKB_ERR_DEVICE: return "the current device is not sm_103 (GB300)";
     case MSLKB_ERR_CUDA: return "a CUDA call failed (see mslkb_last_cuda_error)";
     case MSLKB_ERR_TOO_LARGE:

@@ -59,7 +59,8 @@ typedef enum mslkb_status {
   MSLKB_OK = 0,
   MSLKB_ERR_NULL = 1,   /* a pointer needed for the given sizes is NULL */
   MSLKB_ERR_SHAPE = 2,  /* a size is negative, too large, or N is not a multiple of 8 */
-  MSLKB_ERR_ALIGN = 3,  /* out is not 16-byte aligned */
+  MSLKB_ERR_ALIGN = 3,  /* out is not 16-byte aligned (ragged layouts: or A / B not
+                           16-byte aligned, or their row length not a multiple of 16) */
   MSLKB_ERR_DEVICE = 4, /* the current device is not sm_103 (GB300 / B300) */
   MSLKB_ERR_CUDA = 5,   /* a CUDA runtime or driver call failed; see mslkb_last_cuda_error */
   MSLKB_ERR_TOO_LARGE = 6 /* needs more scratch than the allocation-free entry point holds */
@@ -68,6 +69,7 @@ typedef enum mslkb_status {
 /* Bits of the device status word (mslkb_get_device_status). */
 #define MSLKB_DEV_TIMEOUT 0x1u        /* a pipeline wait in the kernel gave up (~1 s)  */
 #define MSLKB_DEV_MSIZES_CLAMPED 0x2u /* m_sizes had a negative entry or summed past total_M */
+#define MSLKB_DEV_BAD_SLICE 0x4u      /* ragged K: a slice bound not a multiple of 16 */
 
 /* Limits. */
 #define MSLKB_MAX_GROUPS 1024         /* G (kernel keeps per-group tables in shared memory) */
@@ -159,6 +161,57 @@ MSLKB_API mslkb_status mslkb_f8f8bf16_rowwise_grouped_batched(
     int64_t G, int64_t M, int64_t N, int64_t K, void *stream);
 
 /*
+ * Ragged-N layout (3D-2D; MSLK #471, commit adding the form whose weights are one
+ * [total_N, K] matrix that the groups partition by row, results packed side by side).
+ * Group g owns the output columns [offsets[g-1], offsets[g]) (offsets[-1] = 0):
+ *
+ *   out[m, n] = bf16_rne((acc * scale_a[g, m]) * scale_b[n]),
+ *   acc = sum_k A[g, m, k] * B[n, k]                       for every n of group g
+ *
+ *   A        device, e4m3 codes [G, M, K] (one slab of M rows per group), 16-byte aligned
+ *   B        device, e4m3 codes [total_N, K], 16-byte aligned
+ *   scale_a  device, fp32 [G, M]
+ *   scale_b  device, fp32 [total_N]
+ *   offsets  device, int32 [G]   inclusive prefix over the columns
+ *   out      device, bf16 [M, total_N], 16-byte aligned; columns past offsets[G-1] are
+ *            not written
+ *
+ * K must be a multiple of 16 (TMA rows) and total_N of 8; a group's column count may be
+ * anything (its last columns are stored one by one).  Column counts follow the offsets
+ * rules of mslkb_f8f8bf16_rowwise_grouped_offsets (clamped at total_N, status bit set).
+ * M = 0, G = 0 or total_N = 0: nothing to do.  K = 0: the owned columns are +0.0.
+ */
+MSLKB_API mslkb_status mslkb_f8f8bf16_rowwise_grouped_n_offsets(
+    const void *A, const void *B, const float *scale_a, const float *scale_b,
+    const int32_t *offsets, void *out, int64_t G, int64_t M, int64_t total_N, int64_t K,
+    void *stream);
+
+/*
+ * Ragged-K layout (2D-2D; MSLK #471, commit adding the layout whose groups slice K).
+ * Group g contracts over k in [offsets[g-1], offsets[g]) (offsets[-1] = 0) and writes a
+ * whole [M, N] slab:
+ *
+ *   out[g, m, n] = bf16_rne((acc * scale_a[g, m]) * scale_b[g, n]),
+ *   acc = sum over the slice of A[m, k] * B[n, k]
+ *
+ *   A        device, e4m3 codes [M, total_K], 16-byte aligned
+ *   B        device, e4m3 codes [N, total_K], 16-byte aligned
+ *   scale_a  device, fp32 [G, M]
+ *   scale_b  device, fp32 [G, N]
+ *   offsets  device, int32 [G]   inclusive prefix over K
+ *   out      device, bf16 [G, M, N], 16-byte aligned; every element is written
+ *
+ * total_K must be a multiple of 16, N of 8, and every slice must start and end on a
+ * multiple of 16: a group whose slice does not is not computed -- its slab is written
+ * +0.0 and MSLKB_DEV_BAD_SLICE is set.  An empty slice gives +0.0 (the empty sum).
+ * Slice bounds are clamped into [0, total_K] as row counts are for the offsets layout.
+ */
+MSLKB_API mslkb_status mslkb_f8f8bf16_rowwise_grouped_k_offsets(
+    const void *A, const void *B, const float *scale_a, const float *scale_b,
+    const int32_t *offsets, void *out, int64_t G, int64_t M, int64_t N, int64_t total_K,
+    void *stream);
+
+/*
  * Allocation-free stacked call (no counterpart on the pages: an addition of this library).
  *
  * For callers that must not allocate device memory: code recording a CUDA graph (memory
@@ -201,7 +254,8 @@ MSLKB_API mslkb_status mslkb_get_device_status(void *stream, uint32_t *flags);
 
 /*
  * Kernel variants and the plan the host would choose.  Pure host code: no CUDA call.
- * layout: 0 = stacked (rows = total_M), 1 = dynamic (rows = expected_m per group).
+ * layout: 0 = stacked (rows = total_M), 1 = dynamic (rows = expected_m per group),
+ *         2 = ragged N (rows = M, N = total_N), 3 = ragged K (rows = M, K = total_K).
  * num_sms: streaming multiprocessors of the target device.
  * a_align / b_align: the byte alignment of the A and B base addresses (e.g. 256).
  */

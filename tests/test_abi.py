@@ -115,6 +115,43 @@ def test_offsets_and_batched_argument_errors(L):
     assert off(M=0) == fx.MSLKB_OK and bat(M=0) == fx.MSLKB_OK and bat(G=0) == fx.MSLKB_OK
 
 
+def test_ragged_argument_errors(L):
+    rn = lambda **kw: fx.mslkb_f8f8bf16_rowwise_grouped_n_offsets(
+        *[kw.get(k, d) for k, d in (("A", 256), ("B", 256), ("sa", 16), ("sb", 16), ("o", 16),
+                                     ("out", 256), ("G", 2), ("M", 4), ("N", 16), ("K", 32))], 0)
+    rk = lambda **kw: fx.mslkb_f8f8bf16_rowwise_grouped_k_offsets(
+        *[kw.get(k, d) for k, d in (("A", 256), ("B", 256), ("sa", 16), ("sb", 16), ("o", 16),
+                                     ("out", 256), ("G", 2), ("M", 4), ("N", 16), ("K", 32))], 0)
+    for call in (rn, rk):
+        assert call(N=12) == fx.MSLKB_ERR_SHAPE          # output width not a multiple of 8
+        assert call(G=fx.MAX_GROUPS + 1) == fx.MSLKB_ERR_SHAPE
+        assert call(M=-1) == fx.MSLKB_ERR_SHAPE
+        assert call(o=0) == fx.MSLKB_ERR_NULL and call(sa=0) == fx.MSLKB_ERR_NULL
+        assert call(A=0) == fx.MSLKB_ERR_NULL
+        assert call(out=264) == fx.MSLKB_ERR_ALIGN
+        assert call(K=40) == fx.MSLKB_ERR_ALIGN          # rows of A / B: TMA needs 16-byte steps
+        assert call(A=264) == fx.MSLKB_ERR_ALIGN and call(B=264) == fx.MSLKB_ERR_ALIGN
+        assert call(M=0) == fx.MSLKB_OK and call(G=0) == fx.MSLKB_OK and call(N=0) == fx.MSLKB_OK
+        assert call(A=0, B=0, M=0) == fx.MSLKB_OK
+
+
+def test_plan_ragged(L):
+    # ragged N: tiles over each group's own columns; ragged K: a slab per group; never split
+    i = fx.mslkb_plan(2, 1024, 16, 16384, 8192, 152)
+    assert fx.variant_name(i.variant) == "ragn_tile128x256_tma" and i.split_k == 0
+    assert i.tiles_bound == 8 * (-(-(16384 + 7 * 16) // 256) + 16)
+    i = fx.mslkb_plan(2, 16, 16, 4096, 1024, 152)
+    assert fx.variant_name(i.variant) == "ragn_swap_w128xa32_tma" and i.split_k == 0
+    i = fx.mslkb_plan(3, 4096, 8, 4096, 65536, 152)
+    assert fx.variant_name(i.variant) == "ragk_tile128x256_tma" and i.tiles_bound == 8 * 32 * 16
+    i = fx.mslkb_plan(3, 128, 2, 256, 1024, 152)
+    assert fx.variant_name(i.variant) == "ragk_tile128x128_tma"
+    with pytest.raises(fx.MslkbError):
+        fx.mslkb_plan(3, 128, 2, 256, 1000, 152)   # K not a multiple of 16: TMA only
+    with pytest.raises(fx.MslkbError):
+        fx.mslkb_plan(4, 128, 2, 256, 1024, 152)
+
+
 def test_accumulation_chunk_setting(L):
     old = fx.mslkb_accumulation_chunk()
     assert old == 8
