@@ -43,7 +43,8 @@ UNIT = "TFLOPS"
 HEADLINE = "c4_llama405b"
 SWEEP = ["c2a_dsv3_gate_up", "c2b_dsv3_down", "c3_llama70b_m1", "c3_llama70b_m16",
          "c3_llama70b_m128", "c3_llama70b_m1024", "c3_llama70b_m8192",
-         "n1_batched_llama70b_m512", "n2_offsets_llama70b_m8192"]
+         "n1_batched_llama70b_m512", "n2_offsets_llama70b_m8192", "n3_ragged_n_m1024",
+         "n4_ragged_k_wgrad"]
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 FP8_OVER_BF16 = 2.0  # nominal dense ratio (4.5 / 2.25 PFLOP/s)
@@ -221,6 +222,16 @@ def run_call(fx, inp, out, wl, stream_ptr):
             inp["A"].data_ptr(), inp["B"].data_ptr(), inp["scale_a"].data_ptr(),
             inp["scale_b"].data_ptr(), inp["meta"].data_ptr(), out.data_ptr(), wl.rows, wl.G,
             wl.N, wl.K, stream_ptr)
+    elif wl.layout == "ragged_n":
+        s = fx.mslkb_f8f8bf16_rowwise_grouped_n_offsets(
+            inp["A"].data_ptr(), inp["B"].data_ptr(), inp["scale_a"].data_ptr(),
+            inp["scale_b"].data_ptr(), inp["meta"].data_ptr(), out.data_ptr(), wl.G, wl.rows,
+            wl.N, wl.K, stream_ptr)
+    elif wl.layout == "ragged_k":
+        s = fx.mslkb_f8f8bf16_rowwise_grouped_k_offsets(
+            inp["A"].data_ptr(), inp["B"].data_ptr(), inp["scale_a"].data_ptr(),
+            inp["scale_b"].data_ptr(), inp["meta"].data_ptr(), out.data_ptr(), wl.G, wl.rows,
+            wl.N, wl.K, stream_ptr)
     elif wl.layout == "batched":
         s = fx.mslkb_f8f8bf16_rowwise_grouped_batched(
             inp["A"].data_ptr(), inp["B"].data_ptr(), inp["scale_a"].data_ptr(),
@@ -251,8 +262,15 @@ def roofline_times(wl, pk, sustained=True):
 
 
 def plan_for(fx, wl, sms):
+    if wl.layout in ("ragged_n", "ragged_k"):
+        return fx.mslkb_plan(2 if wl.layout == "ragged_n" else 3, wl.rows, wl.G, wl.N, wl.K, sms)
     return fx.mslkb_plan(1 if wl.slabs else 0, wl.expected_m if wl.slabs else wl.rows, wl.G,
                          wl.N, wl.K, sms)
+
+
+def out_shape(wl):
+    """Rows and columns of the output (ragged K: a slab of M rows per group)."""
+    return (wl.G * wl.rows if wl.layout == "ragged_k" else wl.rows, wl.N)
 
 
 def sweep_shape(fx, wl, pk, device):
@@ -264,7 +282,7 @@ def sweep_shape(fx, wl, pk, device):
     n_sets = max(1, min(16, math.ceil(2 * L2_BYTES / ws_bytes)))
     base = make_inputs(wl, device)
     sets = [base] + [{k: v.clone() for k, v in base.items()} for _ in range(n_sets - 1)]
-    outs = [torch.empty((wl.rows, wl.N), dtype=torch.bfloat16, device=device) for _ in sets]
+    outs = [torch.empty(out_shape(wl), dtype=torch.bfloat16, device=device) for _ in sets]
     stream = torch.cuda.Stream(device=device)
     sp = stream.cuda_stream
     with torch.cuda.stream(stream):
@@ -329,7 +347,7 @@ def gpu_arm(args):
     pk, pk_kind = peaks()
     wl = workloads()[args.workload]
     inp = make_inputs(wl, device)
-    out = torch.empty((wl.rows, wl.N), dtype=torch.bfloat16, device=device)
+    out = torch.empty(out_shape(wl), dtype=torch.bfloat16, device=device)
     stream = torch.cuda.Stream(device=device)
     sp = stream.cuda_stream
     sms = torch.cuda.get_device_properties(device).multi_processor_count

@@ -71,13 +71,14 @@ def multinomial_counts(seed: int, total: int, probs: list[float]) -> list[int]:
 class Workload:
     """One problem: layout, sizes and group metadata (m_sizes or zero_start_index_M)."""
     name: str
-    layout: str            # "stacked", "dynamic", "offsets" or "batched"
+    layout: str            # "stacked", "dynamic", "offsets", "batched", "ragged_n", "ragged_k"
     G: int
-    N: int
-    K: int
-    rows: int              # total_M (stacked) or G * expected_m (dynamic)
+    N: int                 # output columns (total_N for ragged_n)
+    K: int                 # contraction length (total_K for ragged_k)
+    rows: int              # total_M (stacked), G * expected_m (dynamic), M (ragged)
     meta: tuple            # m_sizes (stacked), zero_start_index_M (dynamic), int32
-                           # inclusive offsets (offsets); empty (batched)
+                           # inclusive offsets (offsets; over N for ragged_n, over K for
+                           # ragged_k); empty (batched)
     seed: int
     expected_m: int = 0    # dynamic only
     note: str = ""
@@ -87,8 +88,21 @@ class Workload:
     def total_M(self) -> int:
         return self.rows
 
+    def ranges(self) -> list:
+        """Ragged layouts: each group's [start, end) columns (ragged_n) or K slice
+        (ragged_k), from the inclusive offsets."""
+        out, start = [], 0
+        total = self.N if self.layout == "ragged_n" else self.K
+        for g in range(self.G):
+            c = max(0, min(self.meta[g] - (self.meta[g - 1] if g else 0), total - start))
+            out.append((start, start + c))
+            start += c
+        return out
+
     def counts(self) -> list:
-        """Rows of each group."""
+        """Rows of each group (ragged layouts: the M rows of every group)."""
+        if self.layout in ("ragged_n", "ragged_k"):
+            return [self.rows] * self.G
         if self.layout == "stacked":
             return [max(0, m) for m in self.meta]
         if self.layout == "offsets":
@@ -110,7 +124,11 @@ class Workload:
         return sum(1 for c in self.counts() if c > 0)
 
     def flops(self) -> int:
-        """Algorithmic flops: 2 * (valid rows) * N * K."""
+        """Algorithmic flops: 2 * (valid rows) * N * K; ragged layouts: 2 * M * (owned
+        columns) * K, or 2 * M * N * (sum of the K slices)."""
+        if self.layout in ("ragged_n", "ragged_k"):
+            owned = sum(e - s for s, e in self.ranges())
+            return 2 * self.rows * owned * (self.K if self.layout == "ragged_n" else self.N)
         return 2 * self.valid_rows() * self.N * self.K
 
     def bytes(self) -> int:
@@ -118,6 +136,13 @@ class Workload:
         weights and scales of non-empty groups only, the metadata, and the output
         (owned rows for stacked; the whole slab for dynamic, whose padding is
         written with zeros)."""
+        if self.layout == "ragged_n":   # A slabs, B rows and scales, owned output columns
+            owned = sum(e - s for s, e in self.ranges())
+            return (self.G * self.rows * (self.K + 4) + self.N * (self.K + 4) + 4 * self.G
+                    + 2 * self.rows * owned)
+        if self.layout == "ragged_k":   # A and B once, scales, a whole slab per group
+            return (self.rows * self.K + self.N * self.K + 4 * self.G * (self.rows + self.N)
+                    + 4 * self.G + 2 * self.G * self.rows * self.N)
         v = self.valid_rows()
         nz = self.nonempty_groups()
         b = v * self.K + 4 * v + nz * self.N * self.K + 4 * nz * self.N + 8 * self.G
@@ -132,6 +157,14 @@ def _stacked(name, cfg, sub, G, N, K, m_sizes, note="", tags=()):
     return Workload(name=name, layout="stacked", G=G, N=N, K=K, rows=sum(m_sizes),
                     meta=tuple(int(m) for m in m_sizes), seed=1000 * cfg + sub, note=note,
                     tags=tuple(tags))
+
+
+def _inclusive(counts) -> list:
+    out, acc = [], 0
+    for c in counts:
+        acc += int(c)
+        out.append(acc)
+    return out
 
 
 def workloads() -> dict[str, Workload]:
@@ -180,6 +213,21 @@ def workloads() -> dict[str, Workload]:
         name="n1_batched_llama70b_m512", layout="batched", G=16, N=8192, K=8192,
         rows=16 * 512, meta=(), seed=1000 * 5 + 0, expected_m=512,
         note="batched: G=16 full slabs of 512 rows, N=K=8192", tags=("perf",))
+    # NEXT-3: ragged N (the weights of 16 groups as one [16384, 8192] matrix split by a
+    # uniform multinomial over columns, 1024 rows per group's slab) and ragged K (a
+    # weight-gradient shape: 32768 tokens sliced over 16 groups in steps of 16, M = N =
+    # 4096 per group)
+    cn = multinomial_counts(1000 * 6 + 0, 16384, [1.0 / 16] * 16)
+    w["n3_ragged_n_m1024"] = Workload(
+        name="n3_ragged_n_m1024", layout="ragged_n", G=16, N=16384, K=8192, rows=1024,
+        meta=tuple(_inclusive(cn)), seed=1000 * 6 + 0,
+        note="ragged N: G=16 slabs of M=1024 rows, total_N=16384 multinomial, K=8192",
+        tags=("perf",))
+    ck = [16 * c for c in multinomial_counts(1000 * 7 + 0, 32768 // 16, [1.0 / 16] * 16)]
+    w["n4_ragged_k_wgrad"] = Workload(
+        name="n4_ragged_k_wgrad", layout="ragged_k", G=16, N=4096, K=32768, rows=4096,
+        meta=tuple(_inclusive(ck)), seed=1000 * 7 + 0,
+        note="ragged K: G=16 slices of 32768 (steps of 16), M=N=4096", tags=("perf",))
     # 4: llama3-405b-shaped
     m4 = multinomial_counts(1000 * 4 + 0, 16384, [1.0 / 16] * 16)
     w["c4_llama405b"] = _stacked("c4_llama405b", 4, 0, 16, 16384, 16384, m4,
@@ -213,6 +261,8 @@ def make_inputs(wl: Workload, device="cpu", chunk_rows: int = 8192):
     device = torch.device(device)
     gen = torch.Generator(device=device)
     gen.manual_seed(wl.seed)
+    if wl.layout in ("ragged_n", "ragged_k"):
+        return _make_ragged(wl, device, gen, chunk_rows)
     G, N, K, R = wl.G, wl.N, wl.K, wl.rows
     A = torch.empty((R, K), dtype=torch.uint8, device=device)
     sa = torch.empty((R,), dtype=torch.float32, device=device)
@@ -229,6 +279,43 @@ def make_inputs(wl: Workload, device="cpu", chunk_rows: int = 8192):
             B[g, n0:n1], sb[g, n0:n1] = quantize_rows(x)
     mdt = torch.int32 if wl.layout == "offsets" else torch.int64
     meta = torch.tensor(list(wl.meta), dtype=mdt, device=device)
+    return {"A": A, "B": B, "scale_a": sa, "scale_b": sb, "meta": meta}
+
+
+def _make_ragged(wl: Workload, device, gen, chunk_rows: int):
+    """Ragged layouts.  ragged_n: A [G*M, K] with scale_a [G*M] per row, B [total_N, K]
+    with scale_b [total_N] per row.  ragged_k: each group's K slice of A [M, total_K] and
+    B [N, total_K] quantised on its own, one scale per (group, row): scale_a [G*M],
+    scale_b [G*N].  meta: int32 inclusive offsets."""
+    G, M = wl.G, wl.rows
+    if wl.layout == "ragged_n":
+        A = torch.empty((G * M, wl.K), dtype=torch.uint8, device=device)
+        sa = torch.empty((G * M,), dtype=torch.float32, device=device)
+        for r0 in range(0, G * M, chunk_rows):
+            r1 = min(G * M, r0 + chunk_rows)
+            x = torch.randn((r1 - r0, wl.K), generator=gen, device=device, dtype=torch.float32)
+            A[r0:r1], sa[r0:r1] = quantize_rows(x)
+        B = torch.empty((wl.N, wl.K), dtype=torch.uint8, device=device)
+        sb = torch.empty((wl.N,), dtype=torch.float32, device=device)
+        for n0 in range(0, wl.N, chunk_rows):
+            n1 = min(wl.N, n0 + chunk_rows)
+            x = torch.randn((n1 - n0, wl.K), generator=gen, device=device, dtype=torch.float32)
+            B[n0:n1], sb[n0:n1] = quantize_rows(x)
+    else:
+        A = torch.zeros((M, wl.K), dtype=torch.uint8, device=device)
+        B = torch.zeros((wl.N, wl.K), dtype=torch.uint8, device=device)
+        sa = torch.ones((G * M,), dtype=torch.float32, device=device)
+        sb = torch.ones((G * wl.N,), dtype=torch.float32, device=device)
+        for g, (k0, k1) in enumerate(wl.ranges()):
+            if k1 == k0:
+                continue
+            for (T, S, R) in ((A, sa, M), (B, sb, wl.N)):
+                for r0 in range(0, R, chunk_rows):
+                    r1 = min(R, r0 + chunk_rows)
+                    x = torch.randn((r1 - r0, k1 - k0), generator=gen, device=device,
+                                    dtype=torch.float32)
+                    T[r0:r1, k0:k1], S[g * R + r0:g * R + r1] = quantize_rows(x)
+    meta = torch.tensor(list(wl.meta), dtype=torch.int32, device=device)
     return {"A": A, "B": B, "scale_a": sa, "scale_b": sb, "meta": meta}
 
 

@@ -47,3 +47,52 @@ def test_full_size_sampled(orc, name):
     assert fx.device_status() == 0
     del inp, prob, out
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("name", ["n3_ragged_n_m1024", "n4_ragged_k_wgrad"])
+def test_full_size_ragged_sampled(orc, name):
+    # ragged layouts at full size through the C ABI, in the benchmark's plan; sampled output
+    # rows compared in full (every column / every group's slab row)
+    from parity_util import abs_codes
+    wl = workloads()[name]
+    inp = make_inputs(wl, "cuda")
+    G, M = wl.G, wl.rows
+    st = torch.cuda.current_stream().cuda_stream
+    if wl.layout == "ragged_n":
+        out = torch.full((M, wl.N), 0x7E7E, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+        s = fx.mslkb_f8f8bf16_rowwise_grouped_n_offsets(
+            inp["A"].data_ptr(), inp["B"].data_ptr(), inp["scale_a"].data_ptr(),
+            inp["scale_b"].data_ptr(), inp["meta"].data_ptr(), out.data_ptr(), G, M, wl.N,
+            wl.K, st)
+        rows = np.unique(np.concatenate([[0, M - 1], np.random.default_rng(wl.seed)
+                                         .integers(0, M, 14)])).astype(np.int64)
+    else:
+        out = torch.full((G * M, wl.N), 0x7E7E, dtype=torch.int16,
+                         device="cuda").view(torch.bfloat16)
+        s = fx.mslkb_f8f8bf16_rowwise_grouped_k_offsets(
+            inp["A"].data_ptr(), inp["B"].data_ptr(), inp["scale_a"].data_ptr(),
+            inp["scale_b"].data_ptr(), inp["meta"].data_ptr(), out.data_ptr(), G, M, wl.N,
+            wl.K, st)
+        rng = np.random.default_rng(wl.seed)
+        rows = np.unique(np.concatenate([[g * M, g * M + M - 1, g * M + rng.integers(0, M)]
+                                         for g in range(G)])).astype(np.int64)
+    assert s == fx.MSLKB_OK, fx.mslkb_status_string(s)
+    torch.cuda.synchronize()
+    got = bits_of(out[torch.from_numpy(rows).cuda()]).reshape(rows.size, wl.N)
+    h = {k: v.cpu().numpy() for k, v in inp.items()}
+    if wl.layout == "ragged_n":
+        A = h["A"].reshape(G, M, wl.K)
+        ref, _ = orc.n_offsets(A, h["B"], h["scale_a"].reshape(G, M), h["scale_b"], h["meta"],
+                               rows=rows)
+        ab, _ = orc.n_offsets(abs_codes(A), abs_codes(h["B"]), np.abs(h["scale_a"]).reshape(G, M),
+                              np.abs(h["scale_b"]), h["meta"], rows=rows)
+    else:
+        ref, _ = orc.k_offsets(h["A"], h["B"], h["scale_a"].reshape(G, M),
+                               h["scale_b"].reshape(G, wl.N), h["meta"], rows=rows)
+        ab, _ = orc.k_offsets(abs_codes(h["A"]), abs_codes(h["B"]),
+                              np.abs(h["scale_a"]).reshape(G, M),
+                              np.abs(h["scale_b"]).reshape(G, wl.N), h["meta"], rows=rows)
+    compare(got.ravel(), ref.ravel(), ab.ravel(), name)
+    assert fx.device_status() == 0
+    del inp, out
+    torch.cuda.empty_cache()
