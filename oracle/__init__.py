@@ -1,5 +1,5 @@
 """CPU oracle for the FP8 rowwise-scaled grouped GEMM (stacked, dynamic, offsets, batched,
-ragged-N and ragged-K layouts).
+ragged-N and ragged-K layouts) and its block-scaled (groupwise) stacked variant.
 
 TEST INFRASTRUCTURE ONLY: the tests, the smoke check and the benchmark's CPU-baseline
 leg are the only callers.  Nothing here imports the CUDA library or its package, and
@@ -48,6 +48,7 @@ MUTANTS = {
     10: "scale_b not applied",
     11: "ragged-N: the slab of group 0 used for every group",
     12: "ragged-K: every group's slice read from k = 0",
+    13: "block scaling: the scales of K block 0 used for every block",
 }
 
 
@@ -100,6 +101,9 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_n_offsets.restype = ctypes.c_int
     lib.oracle_k_offsets.argtypes = [p, p, p, p, p, i64, i64, i64, i64, p, i64, p, ctypes.c_int]
     lib.oracle_k_offsets.restype = ctypes.c_int
+    lib.oracle_blockwise_stacked.argtypes = [p, p, p, p, p, i64, i64, i64, i64, p, i64, p,
+                                             ctypes.c_int]
+    lib.oracle_blockwise_stacked.restype = ctypes.c_int
     lib.oracle_dot_int.argtypes = [p, p, i64]
     lib.oracle_dot_int.restype = ctypes.c_int64
     lib.oracle_dot.argtypes = [p, p, i64]
@@ -318,6 +322,34 @@ class Oracle:
         clamped = self.lib.oracle_k_offsets(_ptr(A), _ptr(B), _ptr(sa), _ptr(sb), _ptr(o), G, M,
                                             N, total_K, 0 if r is None else _ptr(r),
                                             0 if r is None else r.size, _ptr(out), int(threads))
+        return out, bool(clamped)
+
+    def blockwise_stacked(self, A, B, scale_a, scale_b, m_sizes, total_M=None, rows=None,
+                          out=None, threads: int = 0):
+        """Block-scaled stacked layout (blocks of 128 along K and N): A [total_M, K] u8,
+        B [G, N, K] u8, scale_a [total_M, K/128] f32, scale_b [G, N/128, K/128] f32,
+        m_sizes [G] i64.  Returns (out [total_M, N] u16 -- or the chosen ``rows`` of it,
+        0xFFFF for a row of no group --, clamped)."""
+        A = _c(A, np.uint8)
+        B = _c(B, np.uint8)
+        G, N, K = B.shape
+        if total_M is None:
+            total_M = A.shape[0]
+        sa = _c(scale_a, np.float32).ravel()
+        sb = _c(scale_b, np.float32).ravel()
+        m = _c(m_sizes, np.int64)
+        assert K % 128 == 0 and N % 128 == 0
+        assert sa.size == total_M * (K // 128) and sb.size == G * (N // 128) * (K // 128)
+        r = None if rows is None else _c(rows, np.int64)
+        n_out = total_M if r is None else r.size
+        if out is None:
+            out = np.zeros((n_out, N), dtype=np.uint16)
+        else:
+            out = _c(out, np.uint16).reshape(n_out, N).copy()
+        clamped = self.lib.oracle_blockwise_stacked(
+            _ptr(A), _ptr(B), _ptr(sa), _ptr(sb), _ptr(m), G, N, K, int(total_M),
+            0 if r is None else _ptr(r), 0 if r is None else r.size, _ptr(out), int(threads))
+        assert clamped != -2
         return out, bool(clamped)
 
 

@@ -171,3 +171,16 @@ def k_offsets(A, B, scale_a, scale_b, offsets_incl, total_K):
                 out[(g * M + m, n)] = element(list(A[m])[k0:k1], list(B[n])[k0:k1],
                                               scale_a[g][m], scale_b[g][n])
     return out
+
+
+def blockwise_element(arow, brow, sa_row, sb_blk, block=128) -> int:
+    """Block scaling: sum over K blocks of scale_a[kb] * scale_b[kb] * (exact block sum),
+    all in exact rationals, rounded once to bf16."""
+    total = Fraction(0)
+    for kb in range(len(arow) // block):
+        s = dot_exact(list(arow)[kb * block:(kb + 1) * block],
+                      list(brow)[kb * block:(kb + 1) * block])
+        if s is None:
+            return 0x7FC0
+        total += float_exact(float(sa_row[kb])) * float_exact(float(sb_blk[kb])) * s
+    return bf16_bits_exact(total)

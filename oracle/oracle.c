@@ -1,7 +1,7 @@
 /*
  * oracle.c -- plain, slow, obviously correct CPU oracle for the FP8 rowwise-scaled
  * grouped GEMM f8f8bf16_rowwise_grouped: stacked, dynamic, offsets, batched, ragged-N
- * and ragged-K layouts.
+ * and ragged-K layouts, and the block-scaled (groupwise) stacked variant.
  *
  * TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the CPU-baseline leg
  * of the benchmark may build, load or call this file.  It shares no code, header,
@@ -552,6 +552,97 @@ int oracle_k_offsets(const uint8_t *A, const uint8_t *B, const float *scale_a,
                                   scale_b[g * N + n], lut);
     }
     free(ks);
+    return clamped;
+}
+
+/* ------------------------------------------------------------------------------ */
+/* Block-scaled (groupwise) stacked layout (MSLK #471, commit introducing the rowwise */
+/* scheme beside the block scheme the kernel already had: a scale per scale block,    */
+/* applied to each block's partial sum inside the K loop).  Blocks of 128 along K and */
+/* 128 along N (the pages require K and N to cover whole blocks under block scaling): */
+/*   scale_a [total_M, K/128]     one scale per row and K block                        */
+/*   scale_b [G, N/128, K/128]    one scale per (128 columns x 128 K) block of B       */
+/*   out[r, n] = bf16( sum_kb scale_a[r, kb] * scale_b[g, n/128, kb] * S_kb(r, n) )    */
+/* with S_kb the exact sum over the block's 128 products.  Each term ab * S_kb is     */
+/* split exactly into p + e (fma) and the terms are summed in double-double (Knuth's   */
+/* TwoSum), so the bf16 rounding sees the exact value to ~106 bits.  Returns the       */
+/* stacked clamp flag, or -2 if K or N is not a multiple of 128.                       */
+/* ------------------------------------------------------------------------------ */
+#define ORACLE_SCALE_BLOCK 128
+
+static void two_sum(double a, double b, double *s, double *e)
+{
+    double x = a + b;
+    double bv = x - a;
+    double av = x - bv;
+    *s = x;
+    *e = (a - av) + (b - bv);
+}
+
+static uint16_t blockwise_element(const uint8_t *arow, const uint8_t *brow, int64_t K,
+                                  const float *sa_row, const float *sb_blk, const double *lut)
+{
+    int64_t nkb = K / ORACLE_SCALE_BLOCK;
+    if (nkb == 0) return 0x0000u;
+    double hi = 0.0, lo = 0.0;
+    for (int64_t kb = 0; kb < nkb; ++kb) {
+        double S = dot_lut(arow + kb * ORACLE_SCALE_BLOCK, brow + kb * ORACLE_SCALE_BLOCK,
+                           ORACLE_SCALE_BLOCK, lut);
+#if ORACLE_MUTANT == 13
+        double ab = (double)sa_row[0] * (double)sb_blk[0]; /* mutant: block 0's scales */
+#else
+        double ab = (double)sa_row[kb] * (double)sb_blk[kb]; /* exact */
+#endif
+        double p = ab * S;
+        double pe = fma(ab, S, -p);
+        double t;
+        two_sum(hi, p, &hi, &t);
+        lo += t + pe;
+    }
+    double e;
+    two_sum(hi, lo, &hi, &e);
+    return oracle_bf16_round(hi, e);
+}
+
+int oracle_blockwise_stacked(const uint8_t *A, const uint8_t *B, const float *scale_a,
+                             const float *scale_b, const int64_t *m_sizes, int64_t G,
+                             int64_t N, int64_t K, int64_t total_M, const int64_t *rows,
+                             int64_t nrows, uint16_t *out, int nthreads)
+{
+    /* rows == NULL: the whole output [total_M, N] (rows past the last group untouched);
+     * else out row i = output row rows[i] (0xFFFF for a row of no group) */
+    if (K % ORACLE_SCALE_BLOCK != 0 || N % ORACLE_SCALE_BLOCK != 0) return -2;
+    double lut[256];
+    fill_lut(lut);
+    int64_t *off = (int64_t *)malloc(sizeof(int64_t) * (size_t)(G + 1));
+    if (!off) return -1;
+    int clamped = oracle_stacked_offsets(m_sizes, G, total_M, off);
+    int64_t nkb = K / ORACLE_SCALE_BLOCK, nnb = N / ORACLE_SCALE_BLOCK;
+    int64_t n_out = rows ? nrows : off[G];
+#ifdef _OPENMP
+    if (nthreads <= 0) nthreads = omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads)
+#else
+    (void)nthreads;
+#endif
+    for (int64_t i = 0; i < n_out; ++i) {
+        int64_t r = rows ? rows[i] : i;
+        int64_t g = -1;
+        for (int64_t h = 0; h < G; ++h)
+            if (r >= off[h] && r < off[h + 1]) { g = h; break; }
+        uint16_t *o = out + (size_t)i * (size_t)N;
+        if (g < 0) {
+            if (rows) for (int64_t n = 0; n < N; ++n) o[n] = 0xFFFFu;
+            continue;
+        }
+        const uint8_t *arow = A + (size_t)r * (size_t)K;
+        const float *sa_row = scale_a + (size_t)r * (size_t)nkb;
+        for (int64_t n = 0; n < N; ++n) {
+            const float *sb_blk = scale_b + ((size_t)g * (size_t)nnb + (size_t)(n / ORACLE_SCALE_BLOCK)) * (size_t)nkb;
+            o[n] = blockwise_element(arow, b_row(B, g, n, N, K), K, sa_row, sb_blk, lut);
+        }
+    }
+    free(off);
     return clamped;
 }
 

@@ -554,6 +554,80 @@ def pin_ragged_sampled_rows(orc, seed=61):
     assert np.array_equal(part2, full2[rows2])
 
 
+def _blockwise_case(rng, G, rows_per, N, K, pow2=False):
+    m = [int(rows_per[g]) for g in range(G)]
+    total = sum(m)
+    A = _random_codes(rng, (total, K))
+    B = _random_codes(rng, (G, N, K))
+    nkb, nnb = K // 128, N // 128
+    if pow2:
+        sa = np.exp2(rng.integers(-3, 4, size=(total, nkb))).astype(np.float32)
+        sb = np.exp2(rng.integers(-3, 4, size=(G, nnb, nkb))).astype(np.float32)
+    else:
+        sa = _random_scales(rng, total * nkb).reshape(total, nkb)
+        sb = _random_scales(rng, G * nnb * nkb).reshape(G, nnb, nkb)
+    return A, B, sa, sb, m, total
+
+
+def pin_blockwise_bruteforce(orc, seed=67):
+    """Block scaling: sampled elements bit-equal to the exact-rational sum over K blocks of
+    scale_a[r, kb] * scale_b[g, n/128, kb] * (block sum), rounded once."""
+    rng = _rng(seed)
+    for i in range(3):
+        G = int(rng.integers(1, 3))
+        A, B, sa, sb, m, total = _blockwise_case(rng, G, rng.integers(0, 4, size=G) + (i == 0),
+                                                 int(rng.choice([128, 256])), int(rng.choice([128, 256])))
+        out, _ = orc.blockwise_stacked(A, B, sa, sb, m)
+        N, K = B.shape[1], B.shape[2]
+        start = 0
+        for g in range(G):
+            for r in range(start, start + m[g]):
+                for n in rng.integers(0, N, size=6):
+                    ref = bf.blockwise_element(A[r].tolist(), B[g, n].tolist(), sa[r].tolist(),
+                                               sb[g, n // 128].tolist())
+                    got = int(out[r, n])
+                    assert got == ref or (ref == 0 and got == 0x8000), f"case {i} ({r},{n})"
+            start += m[g]
+
+
+def pin_blockwise_reduces_to_rowwise(orc, seed=71):
+    """With scales constant over the K blocks (and over each 128-column block of B), block
+    scaling is rowwise scaling: bit-equal to the rowwise oracle for power-of-two scales."""
+    rng = _rng(seed)
+    G, N, K = 2, 256, 384
+    m = [3, 2]
+    total = sum(m)
+    A = _random_codes(rng, (total, K))
+    B = _random_codes(rng, (G, N, K))
+    sa_row = np.exp2(rng.integers(-4, 5, size=total)).astype(np.float32)
+    sb_blk = np.exp2(rng.integers(-4, 5, size=(G, N // 128))).astype(np.float32)
+    sa = np.repeat(sa_row[:, None], K // 128, axis=1)
+    sb = np.repeat(sb_blk[:, :, None], K // 128, axis=2)
+    out, _ = orc.blockwise_stacked(A, B, sa, sb, m)
+    st, _ = orc.stacked(A, B, sa_row, np.repeat(sb_blk, 128, axis=1), m)
+    assert np.array_equal(out, st)
+
+
+def pin_blockwise_block_isolation(orc, seed=73):
+    """A nonzero only in K block j: the result is that block's term alone, whatever the
+    other blocks' scales hold (a scale indexed by the wrong block shows at once)."""
+    rng = _rng(seed)
+    G, N, K = 1, 128, 384
+    A = np.zeros((3, K), np.uint8)
+    B = _random_codes(rng, (G, N, K))
+    for j in range(3):
+        A[:] = 0
+        A[:, j * 128:(j + 1) * 128] = _random_codes(rng, (3, 128))
+        sa = np.full((3, 3), 1e30, np.float32)
+        sb = np.full((G, 1, 3), 1e30, np.float32)
+        sa[:, j] = np.float32(0.5)
+        sb[:, :, j] = np.float32(2.0)
+        out, _ = orc.blockwise_stacked(A, B, sa, sb, [3])
+        ref, _ = orc.stacked(A[:, j * 128:(j + 1) * 128], B[:, :, j * 128:(j + 1) * 128],
+                             np.ones(3, np.float32), np.ones((G, N), np.float32), [3])
+        assert np.array_equal(out, ref), f"block {j}"
+
+
 PINS = [
     pin_decode_vs_torch, pin_decode_golden, pin_bf16_golden, pin_bf16_vs_torch,
     pin_dot_exact, pin_closed_form_k1, pin_closed_form_all_ones, pin_closed_form_identity,
@@ -561,4 +635,5 @@ PINS = [
     pin_scale_factoring, pin_stacked_ownership, pin_padding_zero, pin_layout_agreement,
     pin_k_zero, pin_sampled_rows, pin_offsets_layout, pin_batched_layout,
     pin_n_offsets_layout, pin_k_offsets_layout, pin_ragged_sampled_rows,
+    pin_blockwise_bruteforce, pin_blockwise_reduces_to_rowwise, pin_blockwise_block_isolation,
 ]
