@@ -75,7 +75,8 @@ def lib() -> ctypes.CDLL:
             p, i64 = ctypes.c_void_p, ctypes.c_int64
             for name in ("mslkb_f8f8bf16_rowwise_grouped_stacked",
                          "mslkb_f8f8bf16_rowwise_grouped_dynamic",
-                         "mslkb_f8f8bf16_rowwise_grouped_stacked_noalloc"):
+                         "mslkb_f8f8bf16_rowwise_grouped_stacked_noalloc",
+                         "mslkb_f8f8bf16_groupwise_grouped_stacked"):
                 fn = getattr(L, name)
                 fn.argtypes = [p, p, p, p, p, p, i64, i64, i64, i64, p]
                 fn.restype = ctypes.c_int
@@ -166,6 +167,13 @@ def mslkb_f8f8bf16_rowwise_grouped_k_offsets(A, B, scale_a, scale_b, offsets, ou
                                              total_K, stream=0) -> int:
     return lib().mslkb_f8f8bf16_rowwise_grouped_k_offsets(A, B, scale_a, scale_b, offsets, out,
                                                           G, M, N, total_K, stream)
+
+
+def mslkb_f8f8bf16_groupwise_grouped_stacked(A, B, scale_a, scale_b, m_sizes, out, total_M, G,
+                                             N, K, stream=0) -> int:
+    """Block-scaled stacked call: scale_a [total_M, K/128], scale_b [G, N/128, K/128]."""
+    return lib().mslkb_f8f8bf16_groupwise_grouped_stacked(A, B, scale_a, scale_b, m_sizes, out,
+                                                          total_M, G, N, K, stream)
 
 
 def mslkb_status_string(status: int) -> str:
@@ -445,6 +453,34 @@ def f8f8bf16_rowwise_grouped_k_offsets(XQ, WQ, x_scale, w_scale, offsets, out=No
         offsets.data_ptr(), out.data_ptr(), G, M, N, total_K, _stream_ptr(stream))
     if s != MSLKB_OK:
         raise MslkbError(s, "f8f8bf16_rowwise_grouped_k_offsets")
+    return out
+
+
+def f8f8bf16_groupwise_grouped_stacked(XQ, WQ, x_scale, w_scale, m_sizes, out=None,
+                                       stream=None):
+    """Block-scaled stacked: XQ [total_M, K] e4m3, WQ [G, N, K] e4m3, x_scale [total_M,
+    K/128] fp32, w_scale [G, N/128, K/128] fp32, m_sizes [G] int64 -> out [total_M, N] bf16
+    (K and N multiples of 128)."""
+    import torch
+    _check(XQ, "XQ", _fp8_types(), 2)
+    _check(WQ, "WQ", _fp8_types(), 3)
+    _check(x_scale, "x_scale", (torch.float32,))
+    _check(w_scale, "w_scale", (torch.float32,))
+    _check(m_sizes, "m_sizes", (torch.int64,), 1)
+    total_M, K = XQ.shape
+    G, N, K2 = WQ.shape
+    if K2 != K or K % 128 or N % 128 or x_scale.numel() != total_M * (K // 128) \
+            or w_scale.numel() != G * (N // 128) * (K // 128) or m_sizes.numel() != G:
+        raise ValueError("inconsistent shapes")
+    if out is None:
+        out = torch.zeros((total_M, N), dtype=torch.bfloat16, device=XQ.device)
+    else:
+        _check(out, "out", (torch.bfloat16,), 2)
+    s = mslkb_f8f8bf16_groupwise_grouped_stacked(
+        XQ.data_ptr(), WQ.data_ptr(), x_scale.data_ptr(), w_scale.data_ptr(),
+        m_sizes.data_ptr(), out.data_ptr(), total_M, G, N, K, _stream_ptr(stream))
+    if s != MSLKB_OK:
+        raise MslkbError(s, "f8f8bf16_groupwise_grouped_stacked")
     return out
 
 

@@ -78,7 +78,7 @@ struct GemmParams {
 };
 
 template <int kTileN_, int kStages_, bool kSwap_, bool kTma_, bool kDynamic_, int kEpiWarps_ = 4,
-          bool kPair_ = false, int kRagged_ = 0>
+          bool kPair_ = false, int kRagged_ = 0, bool kBlockScale_ = false>
 struct KernelCfg {
   static constexpr int kTileN = kTileN_;     // MMA N
   static constexpr int kStages = kStages_;
@@ -97,6 +97,12 @@ struct KernelCfg {
   static constexpr bool kRagN = kRagged_ == 1;
   static constexpr bool kRagK = kRagged_ == 2;
   static constexpr bool kRagged = kRagged_ != 0;
+  // Block scaling (groupwise; MSLK #471, commit introducing the rowwise scheme beside the
+  // block scheme): scale_a [rows, K/128], scale_b [G, N/128, K/128]; every K block's
+  // partial sum is scaled on its way from TMEM into the fp32 registers (one K block per
+  // TMEM chunk), and the epilogue applies no further scale.
+  static constexpr bool kBlockScale = kBlockScale_;
+  static constexpr int kScaleBlock = 128;
   static constexpr int kMmaM = 128;                           // accumulator rows per CTA
   static constexpr int kActRows = kSwap ? kTileN : kMmaM;     // activation rows per CTA
   static constexpr int kWRows = kSwap ? kMmaM : kTileN / kCtas;  // weight rows per CTA
@@ -160,6 +166,9 @@ struct KernelCfg {
   static_assert(kEpiWarps == 4 || (kEpiWarps == 8 && !kSwap), "epilogue warp split");
   static_assert(!kPair || (kTma && !kSwap && kTileN == 256), "CTA pairs: 256 x 256 tiles, TMA");
   static_assert(!kRagged || (kTma && !kPair && !kDynamic), "ragged layouts: TMA, single CTAs");
+  static_assert(!kBlockScale || (kTma && !kSwap && !kPair && !kRagged && !kDynamic &&
+                                 kBK == kScaleBlock),
+                "block scaling: stacked 128-row tiles, one K block per scale block");
   static_assert(kThreadCols % 16 == 0, "TMEM load granularity");
   static_assert(!kRegSplit || (kThreads == 384 && kEpiWarp0 == 4 &&
                                128 * kRegsLow + 256 * kRegsHigh == kThreads * kLaunchRegs),
@@ -412,6 +421,14 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
       }
     }
   }
+}
+
+// One TMEM value into an fp32 register accumulator: a round-to-nearest add, or (block
+// scaling) a fused multiply-add by the K block's scale.
+template <bool kScale>
+__device__ __forceinline__ float accum(float acc, uint32_t v, float scale) {
+  if constexpr (kScale) return fmaf(__uint_as_float(v), scale, acc);
+  else return acc + __uint_as_float(v);
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -893,8 +910,13 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
       // behind the MMA: scale_a of its row, and scale_b of column (col0 + lane) for each
       // 32-column piece, broadcast by shuffle when the piece is stored
       float sa_pre = 0.0f;
+      // block scaling: the scale of each K block (this thread's row x its columns' 128-block)
+      // is loaded one chunk ahead, so its latency hides behind the chunk wait
+      const float* bs_a = nullptr;
+      const float* bs_b = nullptr;
+      float bs_next = 0.0f;
       float sb_pre[Cfg::kSwap ? 1 : Cfg::kThreadCols / 32];
-      if constexpr (!Cfg::kSwap) {
+      if constexpr (!Cfg::kSwap && !Cfg::kBlockScale) {
         const int32_t R = c.m0 + row_off + static_cast<int32_t>(lane);
         if (active && R < c.valid_end) sa_pre = __ldg(p.scale_a + (R + c.srow_delta));
         const float* sb_g = p.scale_b + c.sb_off;
@@ -903,6 +925,20 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
           const int32_t col = c.n0 + ocol + pc * 32 + static_cast<int32_t>(lane);
           sb_pre[pc] = (active && col < c.n_end) ? __ldg(sb_g + col) : 0.0f;
         }
+      }
+      if constexpr (Cfg::kBlockScale) {
+        // the K-block scales are applied chunk by chunk: the epilogue multiplies by 1
+        const int32_t R = c.m0 + row_off + static_cast<int32_t>(lane);
+        const bool rv = active && R < c.valid_end;
+        const int32_t nblk = p.N / Cfg::kScaleBlock;
+        bs_a = p.scale_a + static_cast<size_t>(rv ? R : 0) * p.num_kb;
+        // (columns of a tile past N are never stored: clamp their block into range)
+        const int32_t blk = min((c.n0 + ocol) / Cfg::kScaleBlock, nblk - 1);
+        bs_b = p.scale_b + (static_cast<size_t>(c.g) * nblk + blk) * p.num_kb;
+        bs_next = (rv && it.kb0 < kb_end) ? __ldg(bs_a + it.kb0) * __ldg(bs_b + it.kb0) : 0.0f;
+        sa_pre = 1.0f;
+#pragma unroll
+        for (int pc = 0; pc < Cfg::kThreadCols / 32; ++pc) sb_pre[pc] = 1.0f;
       }
       // fp32 accumulator of this thread (round-to-nearest adds of the TMEM chunks)
       float acc[Cfg::kThreadCols];
@@ -919,6 +955,13 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         for (int32_t kb0 = it.kb0; kb0 < kb_end; kb0 += kpc) {
           const int buf = static_cast<int>(chunk & 1u);
           const uint32_t use = chunk >> 1;
+          // block scaling: this chunk (= K block kb0)'s scale, and the next one's load
+          float bs = 1.0f;
+          if constexpr (Cfg::kBlockScale) {
+            bs = bs_next;
+            if (kb0 + 1 < kb_end && bs_a != nullptr)
+              bs_next = __ldg(bs_a + kb0 + 1) * __ldg(bs_b + kb0 + 1);
+          }
           if (!wait_bar(tfull_bar(buf), use & 1u, abort_flag, p.status, p.timeout_ns)) {
             ok = false;
             break;
@@ -937,8 +980,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                 ptx::tmem_ld_wait();
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
-                  acc[pc * 64 + j] += __uint_as_float(v0[j]);
-                  acc[pc * 64 + 32 + j] += __uint_as_float(v1[j]);
+                  acc[pc * 64 + j] = accum<Cfg::kBlockScale>(acc[pc * 64 + j], v0[j], bs);
+                  acc[pc * 64 + 32 + j] = accum<Cfg::kBlockScale>(acc[pc * 64 + 32 + j], v1[j], bs);
                 }
               }
             } else if constexpr (Cfg::kThreadCols % 32 == 0 && Cfg::kThreadCols < 128) {
@@ -950,7 +993,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                 ptx::tmem_ld_x32(t_buf + static_cast<uint32_t>(pc * 32), v);
                 ptx::tmem_ld_wait();
 #pragma unroll
-                for (int j = 0; j < 32; ++j) acc[pc * 32 + j] += __uint_as_float(v[j]);
+                for (int j = 0; j < 32; ++j)
+                  acc[pc * 32 + j] = accum<Cfg::kBlockScale>(acc[pc * 32 + j], v[j], bs);
               }
             } else {
 #pragma unroll
@@ -959,7 +1003,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                 ptx::tmem_ld_x16(t_buf + static_cast<uint32_t>(pc * 16), v);
                 ptx::tmem_ld_wait();
 #pragma unroll
-                for (int j = 0; j < 16; ++j) acc[pc * 16 + j] += __uint_as_float(v[j]);
+                for (int j = 0; j < 16; ++j)
+                  acc[pc * 16 + j] = accum<Cfg::kBlockScale>(acc[pc * 16 + j], v[j], bs);
               }
             }
           }

@@ -38,6 +38,7 @@ struct VariantInfo {
   int box_w;      // weight rows one CTA loads per stage
   int cluster;    // CTAs per cluster: 2 for CTA pairs (cta_group::2), else 1
   int ragged;     // 0 grouped rows (stacked / dynamic), 1 ragged N, 2 ragged K
+  int block_scale;  // 1: block-scaled (groupwise) scales
   int partial_bytes;  // fp32 partial sums of one tile (a split tile's piece)
   int launch_regs;    // registers per thread the kernel must be built with (0: any)
   LaunchFn launch;
@@ -116,6 +117,7 @@ constexpr VariantInfo make_variant(const char* name) {
                      Cfg::kTma,      Cfg::kDynamic, Cfg::kThreads, Cfg::kSmemBytes,
                      Cfg::kTileAct,  Cfg::kTileW,   Cfg::kActRows, Cfg::kWRows,
                      Cfg::kCtas,     Cfg::kRagN ? 1 : (Cfg::kRagK ? 2 : 0),
+                     Cfg::kBlockScale ? 1 : 0,
                      Cfg::kEpiWarps * 32 * Cfg::kThreadCols * 4,
                      Cfg::kLaunchRegs, &launch_variant<Cfg>, &set_attr_variant<Cfg>,
                      &occupancy_variant<Cfg>};
@@ -144,5 +146,7 @@ extern const VariantInfo kVariantsRaggedN[];
 extern const int kNumVariantsRaggedN;
 extern const VariantInfo kVariantsRaggedK[];
 extern const int kNumVariantsRaggedK;
+extern const VariantInfo kVariantsBlockScale[];
+extern const int kNumVariantsBlockScale;
 
 }  // namespace mslkb

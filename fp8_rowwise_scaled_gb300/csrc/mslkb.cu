@@ -50,7 +50,8 @@ std::atomic<int> g_split_k{1};
 // ---------------------------------------------------------------------------------
 int num_variants() {
   return mslkb::kNumVariantsStackedTma + mslkb::kNumVariantsDynamicTma +
-         mslkb::kNumVariantsCpAsync + mslkb::kNumVariantsRaggedN + mslkb::kNumVariantsRaggedK;
+         mslkb::kNumVariantsCpAsync + mslkb::kNumVariantsRaggedN + mslkb::kNumVariantsRaggedK +
+         mslkb::kNumVariantsBlockScale;
 }
 
 const VariantInfo* variant(int i) {
@@ -64,14 +65,17 @@ const VariantInfo* variant(int i) {
   if (i < mslkb::kNumVariantsRaggedN) return &mslkb::kVariantsRaggedN[i];
   i -= mslkb::kNumVariantsRaggedN;
   if (i < mslkb::kNumVariantsRaggedK) return &mslkb::kVariantsRaggedK[i];
+  i -= mslkb::kNumVariantsRaggedK;
+  if (i < mslkb::kNumVariantsBlockScale) return &mslkb::kVariantsBlockScale[i];
   return nullptr;
 }
 
-int find_variant(bool dynamic, bool tma, bool swap, int tile_n, int cluster = 1, int ragged = 0) {
+int find_variant(bool dynamic, bool tma, bool swap, int tile_n, int cluster = 1, int ragged = 0,
+                 int block_scale = 0) {
   for (int i = 0; i < num_variants(); ++i) {
     const VariantInfo* v = variant(i);
     if (v->dynamic == dynamic && v->tma == tma && v->swap == swap && v->tile_n == tile_n &&
-        v->cluster == cluster && v->ragged == ragged)
+        v->cluster == cluster && v->ragged == ragged && v->block_scale == block_scale)
       return i;
   }
   return -1;
@@ -266,12 +270,17 @@ int64_t tiles_bound(const VariantInfo* v, int layout, int64_t rows, int64_t G, i
 
 mslkb_status plan(int layout, int64_t rows, int64_t G, int64_t N, int64_t K, int num_sms,
                   int64_t a_align, int64_t b_align, mslkb_plan_info* info) {
-  if (layout < 0 || layout > 3) return MSLKB_ERR_SHAPE;
+  if (layout < 0 || layout > 4) return MSLKB_ERR_SHAPE;
   if (num_sms <= 0 || rows < 0 || G < 0 || N < 0 || K < 0) return MSLKB_ERR_SHAPE;
   const bool dynamic = layout == 1;
-  const int ragged = layout >= 2 ? layout - 1 : 0;
+  const int ragged = (layout == 2 || layout == 3) ? layout - 1 : 0;
+  const int block_scale = layout == 4 ? 1 : 0;  // block-scaled stacked
+  if (block_scale) {  // whole scale blocks along K and N
+    if (K % 128 != 0 || N % 128 != 0) return MSLKB_ERR_SHAPE;
+    layout = 0;
+  }
   const bool tma = (K % 16 == 0) && (a_align % 16 == 0) && (b_align % 16 == 0);
-  if (ragged && !tma) return MSLKB_ERR_ALIGN;  // the ragged layouts are TMA-only
+  if ((ragged || block_scale) && !tma) return MSLKB_ERR_ALIGN;  // TMA-only kernels
   // rows of one group: the slab height (dynamic) or the mean over the groups that can
   // be non-empty (stacked; the counts themselves stay on the device)
   int64_t per_group = rows;
@@ -279,7 +288,12 @@ mslkb_status plan(int layout, int64_t rows, int64_t G, int64_t N, int64_t K, int
   bool swap;
   int tile_n;
   int cluster = 1;
-  if (ragged) {  // TMA variants: swap-AB 32, 128 x 256, 128 x 128
+  if (block_scale) {  // 128 x 256 when its tiles fill the SMs, else 128 x 128
+    swap = false;
+    tile_n = 128;
+    const int wide = find_variant(false, true, false, 256, 1, 0, 1);
+    if (wide >= 0 && tiles_bound(variant(wide), layout, rows, G, N) >= num_sms) tile_n = 256;
+  } else if (ragged) {  // TMA variants: swap-AB 32, 128 x 256, 128 x 128
     swap = per_group <= 32;
     tile_n = swap ? 32 : 128;
     if (!swap) {
@@ -310,11 +324,12 @@ mslkb_status plan(int layout, int64_t rows, int64_t G, int64_t N, int64_t K, int
   }
   int vi = g_forced_variant.load();
   if (vi < 0) {
-    vi = find_variant(dynamic, tma, swap, tile_n, cluster, ragged);
+    vi = find_variant(dynamic, tma, swap, tile_n, cluster, ragged, block_scale);
     if (vi < 0 && !tma) vi = find_variant(dynamic, false, false, 128);
   }
   const VariantInfo* v = variant(vi);
-  if (v == nullptr || v->dynamic != dynamic || v->ragged != ragged || (v->tma && !tma))
+  if (v == nullptr || v->dynamic != dynamic || v->ragged != ragged ||
+      v->block_scale != block_scale || (v->tma && !tma))
     return MSLKB_ERR_SHAPE;
   const int64_t bound = tiles_bound(v, layout, rows, G, N);
   if (bound > INT32_MAX) return MSLKB_ERR_SHAPE;
@@ -323,7 +338,8 @@ mslkb_status plan(int layout, int64_t rows, int64_t G, int64_t N, int64_t K, int
   // weights) but slows the 128-row-tile plans by 4-9% (128 KB of partial sums per piece).
   const int policy = g_split_k.load();
   // CTA pairs run whole tiles only (one pair per tile)
-  const bool split = nkb > 0 && v->cluster == 1 && !ragged && (policy == 2 || (policy == 1 && v->swap));
+  const bool split = nkb > 0 && v->cluster == 1 && !ragged && !block_scale &&
+                     (policy == 2 || (policy == 1 && v->swap));
   // with splitting every CTA gets K work as long as there are units to share
   const int64_t work = (split ? bound * nkb : bound) * v->cluster;
   const int64_t max_ctas = (num_sms / v->cluster) * v->cluster;
@@ -432,11 +448,14 @@ mslkb_status check_sizes(int64_t rows, int64_t G, int64_t N, int64_t K) {
 // zero_start_index_M) / 2 (no metadata: every slab full)
 mslkb_status run(int layout, const void* A, const void* B, const float* scale_a,
                  const float* scale_b, const void* meta, void* out, int64_t rows, int64_t G,
-                 int64_t E, int64_t N, int64_t K, void* stream, int meta_kind = 0) {
+                 int64_t E, int64_t N, int64_t K, void* stream, int meta_kind = 0,
+                 bool block_scale = false) {
   // rows: total_M (stacked) or G * E (dynamic)
   if (rows == 0 || N == 0 || G == 0) return MSLKB_OK;  // nothing is owned or written
-  if (out == nullptr || (meta == nullptr && meta_kind != 2) || scale_a == nullptr ||
-      scale_b == nullptr)
+  // (block scaling over K = 0 has empty scale arrays: nothing reads them)
+  const bool scales_needed = !(block_scale && K == 0);
+  if (out == nullptr || (meta == nullptr && meta_kind != 2) ||
+      (scales_needed && (scale_a == nullptr || scale_b == nullptr)))
     return MSLKB_ERR_NULL;
   if (K > 0 && (A == nullptr || B == nullptr)) return MSLKB_ERR_NULL;
   if (reinterpret_cast<uintptr_t>(out) % 16 != 0) return MSLKB_ERR_ALIGN;
@@ -447,8 +466,8 @@ mslkb_status run(int layout, const void* A, const void* B, const float* scale_a,
   if (s != MSLKB_OK) return s;
 
   mslkb_plan_info info;
-  s = plan(layout, layout == 0 ? rows : E, G, N, K, st->sm_count, addr_align(A), addr_align(B),
-           &info);
+  s = plan(block_scale ? 4 : layout, layout == 0 ? rows : E, G, N, K, st->sm_count,
+           addr_align(A), addr_align(B), &info);
   if (s != MSLKB_OK) return s;
   const VariantInfo* v = variant(info.variant);
   if ((s = ensure_attr(st, info.variant)) != MSLKB_OK) return s;
@@ -474,6 +493,7 @@ mslkb_status run(int layout, const void* A, const void* B, const float* scale_a,
   {
     const int kpc = g_kb_per_chunk.load();
     p.kb_per_chunk = (kpc <= 0 || kpc > p.num_kb) ? (p.num_kb > 0 ? p.num_kb : 1) : kpc;
+    if (block_scale) p.kb_per_chunk = 1;  // every K block scaled on its own
   }
   p.timeout_ns = kWaitTimeoutNs;
   p.split_k = 0;
@@ -698,6 +718,19 @@ mslkb_status mslkb_f8f8bf16_rowwise_grouped_batched(const void* A, const void* B
   if (s != MSLKB_OK) return s;
   if (M > 0 && G > MSLKB_MAX_DIM / M) return MSLKB_ERR_SHAPE;
   return run(1, A, B, scale_a, scale_b, nullptr, out, G * M, G, M, N, K, stream, 2);
+}
+
+mslkb_status mslkb_f8f8bf16_groupwise_grouped_stacked(const void* A, const void* B,
+                                                      const float* scale_a,
+                                                      const float* scale_b,
+                                                      const int64_t* m_sizes, void* out,
+                                                      int64_t total_M, int64_t G, int64_t N,
+                                                      int64_t K, void* stream) {
+  mslkb_status s = check_sizes(total_M, G, N, K);
+  if (s != MSLKB_OK) return s;
+  if (K % 128 != 0 || N % 128 != 0) return MSLKB_ERR_SHAPE;  // whole scale blocks
+  if (G * (N / 128) * (K / 128) > MSLKB_MAX_DIM) return MSLKB_ERR_SHAPE;
+  return run(0, A, B, scale_a, scale_b, m_sizes, out, total_M, G, 0, N, K, stream, 0, true);
 }
 
 mslkb_status mslkb_f8f8bf16_rowwise_grouped_n_offsets(const void* A, const void* B,

@@ -212,6 +212,28 @@ MSLKB_API mslkb_status mslkb_f8f8bf16_rowwise_grouped_k_offsets(
     void *stream);
 
 /*
+ * Block-scaled (groupwise) stacked layout (MSLK #471, commit introducing the rowwise
+ * scheme beside the block scheme the grouped kernel already had: a scale per scale block,
+ * applied to each block's partial sum inside the K loop; K and N must cover whole scale
+ * blocks).  Scale blocks of 128 along K and N:
+ *
+ *   out[r, n] = bf16_rne( sum_kb scale_a[r, kb] * scale_b[g, n / 128, kb] * S_kb ),
+ *   S_kb = sum over k in [128 kb, 128 kb + 128) of A[r, k] * B[g, n, k]
+ *
+ *   A, B, m_sizes, out  as for mslkb_f8f8bf16_rowwise_grouped_stacked
+ *   scale_a  device, fp32 [total_M, K / 128]
+ *   scale_b  device, fp32 [G, N / 128, K / 128]
+ *
+ * K and N must be multiples of 128 (MSLKB_ERR_SHAPE otherwise); A and B 16-byte aligned
+ * (MSLKB_ERR_ALIGN).  Each K block's partial sum is scaled in fp32 on its way from the
+ * tensor core into the fp32 accumulator.
+ */
+MSLKB_API mslkb_status mslkb_f8f8bf16_groupwise_grouped_stacked(
+    const void *A, const void *B, const float *scale_a, const float *scale_b,
+    const int64_t *m_sizes, void *out, int64_t total_M, int64_t G, int64_t N, int64_t K,
+    void *stream);
+
+/*
  * Allocation-free stacked call (no counterpart on the pages: an addition of this library).
  *
  * For callers that must not allocate device memory: code recording a CUDA graph (memory
@@ -255,7 +277,8 @@ MSLKB_API mslkb_status mslkb_get_device_status(void *stream, uint32_t *flags);
 /*
  * Kernel variants and the plan the host would choose.  Pure host code: no CUDA call.
  * layout: 0 = stacked (rows = total_M), 1 = dynamic (rows = expected_m per group),
- *         2 = ragged N (rows = M, N = total_N), 3 = ragged K (rows = M, K = total_K).
+ *         2 = ragged N (rows = M, N = total_N), 3 = ragged K (rows = M, K = total_K),
+ *         4 = block-scaled stacked (rows = total_M).
  * num_sms: streaming multiprocessors of the target device.
  * a_align / b_align: the byte alignment of the A and B base addresses (e.g. 256).
  */

@@ -149,7 +149,24 @@ def test_plan_ragged(L):
     with pytest.raises(fx.MslkbError):
         fx.mslkb_plan(3, 128, 2, 256, 1000, 152)   # K not a multiple of 16: TMA only
     with pytest.raises(fx.MslkbError):
-        fx.mslkb_plan(4, 128, 2, 256, 1024, 152)
+        fx.mslkb_plan(5, 128, 2, 256, 1024, 152)
+
+
+def test_groupwise_argument_errors_and_plan(L):
+    gw = lambda **kw: fx.mslkb_f8f8bf16_groupwise_grouped_stacked(
+        *[kw.get(k, d) for k, d in (("A", 256), ("B", 256), ("sa", 16), ("sb", 16), ("m", 16),
+                                     ("out", 256), ("M", 4), ("G", 2), ("N", 128), ("K", 256))], 0)
+    assert gw(K=192) == fx.MSLKB_ERR_SHAPE       # K not whole scale blocks
+    assert gw(N=136) == fx.MSLKB_ERR_SHAPE       # N not whole scale blocks
+    assert gw(m=0) == fx.MSLKB_ERR_NULL and gw(sb=0) == fx.MSLKB_ERR_NULL
+    assert gw(out=264) == fx.MSLKB_ERR_ALIGN
+    assert gw(M=0) == fx.MSLKB_OK and gw(G=0) == fx.MSLKB_OK
+    i = fx.mslkb_plan(4, 16384, 16, 16384, 16384, 152)
+    assert fx.variant_name(i.variant) == "blockscale_tile128x256_tma" and i.split_k == 0
+    i = fx.mslkb_plan(4, 64, 4, 256, 512, 152)
+    assert fx.variant_name(i.variant) == "blockscale_tile128x128_tma"
+    with pytest.raises(fx.MslkbError):
+        fx.mslkb_plan(4, 64, 4, 256, 520, 152)
 
 
 def test_accumulation_chunk_setting(L):
