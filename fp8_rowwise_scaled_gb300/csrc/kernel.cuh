@@ -423,12 +423,18 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
   }
 }
 
-// One TMEM value into an fp32 register accumulator: a round-to-nearest add, or (block
-// scaling) a fused multiply-add by the K block's scale.
+// Two TMEM values into two fp32 register accumulators with one packed (f32x2) operation:
+// round-to-nearest adds, or (block scaling) fused multiply-adds by the K block's scale.
+// Each lane of the pair rounds exactly as the scalar operation would.
 template <bool kScale>
-__device__ __forceinline__ float accum(float acc, uint32_t v, float scale) {
-  if constexpr (kScale) return fmaf(__uint_as_float(v), scale, acc);
-  else return acc + __uint_as_float(v);
+__device__ __forceinline__ void accum2(float& a0, float& a1, uint32_t v0, uint32_t v1,
+                                       float scale) {
+  const float2 v = make_float2(__uint_as_float(v0), __uint_as_float(v1));
+  float2 a = make_float2(a0, a1);
+  if constexpr (kScale) a = __ffma2_rn(v, make_float2(scale, scale), a);
+  else a = __fadd2_rn(a, v);
+  a0 = a.x;
+  a1 = a.y;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -979,9 +985,11 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                 ptx::tmem_ld_x32(t_buf + static_cast<uint32_t>(pc * 64 + 32), v1);
                 ptx::tmem_ld_wait();
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                  acc[pc * 64 + j] = accum<Cfg::kBlockScale>(acc[pc * 64 + j], v0[j], bs);
-                  acc[pc * 64 + 32 + j] = accum<Cfg::kBlockScale>(acc[pc * 64 + 32 + j], v1[j], bs);
+                for (int j = 0; j < 32; j += 2) {
+                  accum2<Cfg::kBlockScale>(acc[pc * 64 + j], acc[pc * 64 + j + 1], v0[j],
+                                           v0[j + 1], bs);
+                  accum2<Cfg::kBlockScale>(acc[pc * 64 + 32 + j], acc[pc * 64 + 33 + j], v1[j],
+                                           v1[j + 1], bs);
                 }
               }
             } else if constexpr (Cfg::kThreadCols % 32 == 0 && Cfg::kThreadCols < 128) {
@@ -993,8 +1001,9 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                 ptx::tmem_ld_x32(t_buf + static_cast<uint32_t>(pc * 32), v);
                 ptx::tmem_ld_wait();
 #pragma unroll
-                for (int j = 0; j < 32; ++j)
-                  acc[pc * 32 + j] = accum<Cfg::kBlockScale>(acc[pc * 32 + j], v[j], bs);
+                for (int j = 0; j < 32; j += 2)
+                  accum2<Cfg::kBlockScale>(acc[pc * 32 + j], acc[pc * 32 + j + 1], v[j], v[j + 1],
+                                           bs);
               }
             } else {
 #pragma unroll
@@ -1003,8 +1012,9 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                 ptx::tmem_ld_x16(t_buf + static_cast<uint32_t>(pc * 16), v);
                 ptx::tmem_ld_wait();
 #pragma unroll
-                for (int j = 0; j < 16; ++j)
-                  acc[pc * 16 + j] = accum<Cfg::kBlockScale>(acc[pc * 16 + j], v[j], bs);
+                for (int j = 0; j < 16; j += 2)
+                  accum2<Cfg::kBlockScale>(acc[pc * 16 + j], acc[pc * 16 + j + 1], v[j], v[j + 1],
+                                           bs);
               }
             }
           }

@@ -71,7 +71,8 @@ def multinomial_counts(seed: int, total: int, probs: list[float]) -> list[int]:
 class Workload:
     """One problem: layout, sizes and group metadata (m_sizes or zero_start_index_M)."""
     name: str
-    layout: str            # "stacked", "dynamic", "offsets", "batched", "ragged_n", "ragged_k"
+    layout: str            # "stacked", "dynamic", "offsets", "batched", "ragged_n", "ragged_k",
+                           # "groupwise" (stacked, block scales)
     G: int
     N: int                 # output columns (total_N for ragged_n)
     K: int                 # contraction length (total_K for ragged_k)
@@ -103,7 +104,7 @@ class Workload:
         """Rows of each group (ragged layouts: the M rows of every group)."""
         if self.layout in ("ragged_n", "ragged_k"):
             return [self.rows] * self.G
-        if self.layout == "stacked":
+        if self.layout in ("stacked", "groupwise"):
             return [max(0, m) for m in self.meta]
         if self.layout == "offsets":
             return [max(0, self.meta[g] - (self.meta[g - 1] if g else 0))
@@ -145,6 +146,10 @@ class Workload:
                     + 4 * self.G + 2 * self.G * self.rows * self.N)
         v = self.valid_rows()
         nz = self.nonempty_groups()
+        if self.layout == "groupwise":   # scales per (row, K block) and per 128 x 128 block
+            nkb = self.K // 128
+            return (v * (self.K + 4 * nkb) + nz * (self.N * self.K + 4 * (self.N // 128) * nkb)
+                    + 8 * self.G + 2 * v * self.N)
         b = v * self.K + 4 * v + nz * self.N * self.K + 4 * nz * self.N + 8 * self.G
         if self.slabs:
             b += 2 * self.G * self.expected_m * self.N
@@ -228,6 +233,13 @@ def workloads() -> dict[str, Workload]:
         name="n4_ragged_k_wgrad", layout="ragged_k", G=16, N=4096, K=32768, rows=4096,
         meta=tuple(_inclusive(ck)), seed=1000 * 7 + 0,
         note="ragged K: G=16 slices of 32768 (steps of 16), M=N=4096", tags=("perf",))
+    # NEXT-4: block scaling (128 x 128 weight blocks, 1 x 128 activation blocks) on the
+    # llama3-70b total_M = 8192 routing
+    w["n5_groupwise_llama70b_m8192"] = Workload(
+        name="n5_groupwise_llama70b_m8192", layout="groupwise", G=16, N=8192, K=8192,
+        rows=sum(m3), meta=tuple(m3), seed=1000 * 8 + 0,
+        note="block-scaled: llama3-70b total_M=8192 routing, N=K=8192, 128-blocks",
+        tags=("perf",))
     # 4: llama3-405b-shaped
     m4 = multinomial_counts(1000 * 4 + 0, 16384, [1.0 / 16] * 16)
     w["c4_llama405b"] = _stacked("c4_llama405b", 4, 0, 16, 16384, 16384, m4,
@@ -263,6 +275,8 @@ def make_inputs(wl: Workload, device="cpu", chunk_rows: int = 8192):
     gen.manual_seed(wl.seed)
     if wl.layout in ("ragged_n", "ragged_k"):
         return _make_ragged(wl, device, gen, chunk_rows)
+    if wl.layout == "groupwise":
+        return _make_groupwise(wl, device, gen, chunk_rows)
     G, N, K, R = wl.G, wl.N, wl.K, wl.rows
     A = torch.empty((R, K), dtype=torch.uint8, device=device)
     sa = torch.empty((R,), dtype=torch.float32, device=device)
@@ -316,6 +330,34 @@ def _make_ragged(wl: Workload, device, gen, chunk_rows: int):
                                     dtype=torch.float32)
                     T[r0:r1, k0:k1], S[g * R + r0:g * R + r1] = quantize_rows(x)
     meta = torch.tensor(list(wl.meta), dtype=torch.int32, device=device)
+    return {"A": A, "B": B, "scale_a": sa, "scale_b": sb, "meta": meta}
+
+
+def _make_groupwise(wl: Workload, device, gen, chunk_rows: int):
+    """Block-scaled stacked: A quantised per (row, 128-element K block) -> scale_a
+    [rows, K/128]; B per 128 x 128 block of each group -> scale_b [G, N/128, K/128]."""
+    G, N, K, R = wl.G, wl.N, wl.K, wl.rows
+    nkb, nnb = K // 128, N // 128
+    A = torch.empty((R, K), dtype=torch.uint8, device=device)
+    sa = torch.empty((R, nkb), dtype=torch.float32, device=device)
+    for r0 in range(0, R, chunk_rows):
+        r1 = min(R, r0 + chunk_rows)
+        x = torch.randn((r1 - r0, nkb, 128), generator=gen, device=device, dtype=torch.float32)
+        q, s = quantize_rows(x)
+        A[r0:r1], sa[r0:r1] = q.reshape(r1 - r0, K), s
+    B = torch.empty((G, N, K), dtype=torch.uint8, device=device)
+    sb = torch.empty((G, nnb, nkb), dtype=torch.float32, device=device)
+    for g in range(G):
+        for n0 in range(0, N, chunk_rows):
+            n1 = min(N, n0 + chunk_rows)
+            x = torch.randn((n1 - n0, K), generator=gen, device=device, dtype=torch.float32)
+            blk = x.reshape((n1 - n0) // 128, 128, nkb, 128).permute(0, 2, 1, 3)
+            blk = blk.reshape((n1 - n0) // 128, nkb, 128 * 128)
+            q, s = quantize_rows(blk)   # one scale per 128 x 128 block
+            B[g, n0:n1] = q.reshape((n1 - n0) // 128, nkb, 128, 128).permute(0, 2, 1, 3) \
+                .reshape(n1 - n0, K)
+            sb[g, n0 // 128:n1 // 128] = s
+    meta = torch.tensor(list(wl.meta), dtype=torch.int64, device=device)
     return {"A": A, "B": B, "scale_a": sa, "scale_b": sb, "meta": meta}
 
 

@@ -96,3 +96,31 @@ def test_full_size_ragged_sampled(orc, name):
     assert fx.device_status() == 0
     del inp, out
     torch.cuda.empty_cache()
+
+
+def test_full_size_groupwise_sampled(orc):
+    # the block-scaled workload at full size in the benchmark's plan; sampled rows in full
+    from parity_util import abs_codes
+    wl = workloads()["n5_groupwise_llama70b_m8192"]
+    inp = make_inputs(wl, "cuda")
+    out = torch.full((wl.rows, wl.N), 0x7E7E, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+    s = fx.mslkb_f8f8bf16_groupwise_grouped_stacked(
+        inp["A"].data_ptr(), inp["B"].data_ptr(), inp["scale_a"].data_ptr(),
+        inp["scale_b"].data_ptr(), inp["meta"].data_ptr(), out.data_ptr(), wl.rows, wl.G, wl.N,
+        wl.K, torch.cuda.current_stream().cuda_stream)
+    assert s == fx.MSLKB_OK, fx.mslkb_status_string(s)
+    torch.cuda.synchronize()
+    off = np.concatenate([[0], np.cumsum(wl.meta)])
+    rng = np.random.default_rng(wl.seed)
+    rows = np.unique(np.concatenate([[off[g], off[g + 1] - 1, rng.integers(off[g], off[g + 1])]
+                                     for g in range(wl.G) if off[g + 1] > off[g]])).astype(np.int64)
+    got = bits_of(out[torch.from_numpy(rows).cuda()]).reshape(rows.size, wl.N)
+    h = {k: v.cpu().numpy() for k, v in inp.items()}
+    ref, _ = orc.blockwise_stacked(h["A"], h["B"], h["scale_a"], h["scale_b"], h["meta"],
+                                   rows=rows)
+    ab, _ = orc.blockwise_stacked(abs_codes(h["A"]), abs_codes(h["B"]), np.abs(h["scale_a"]),
+                                  np.abs(h["scale_b"]), h["meta"], rows=rows)
+    compare(got.ravel(), ref.ravel(), ab.ravel(), wl.name)
+    assert fx.device_status() == 0
+    del inp, out
+    torch.cuda.empty_cache()
