@@ -313,11 +313,12 @@ mslkb_status plan(int layout, int64_t rows, int64_t G, int64_t N, int64_t K, int
       const int wide = find_variant(dynamic, true, false, 256);
       if (wide >= 0 && tiles_bound(variant(wide), layout, rows, G, N) >= num_sms) tile_n = 256;
       // CTA pairs (256 x 256 tiles, half the weight bytes per SM and K block): measured on
-      // GB300 ~5% ahead of 128 x 256 tiles on full 512-row slabs and level on 1024-row
-      // groups, behind on shorter or ragged groups and on HBM-bound shapes; taken for
-      // long groups with at least four waves of pairs
+      // GB300 4-5 % ahead of 128 x 256 tiles on full slabs of >= 512 rows.  Ragged groups
+      // end in half tiles that run at twice the pace of the full tiles sharing their weight
+      // tile, the sharers drift apart in K and the weights are read from DRAM again (c4:
+      // 9.4 GB against 5.6 GB per call, no faster): the stacked layouts keep 128-row tiles.
       const int pair = find_variant(dynamic, true, false, 256, 2);
-      if (tile_n == 256 && pair >= 0 && per_group >= (dynamic ? 512 : 1024) &&
+      if (tile_n == 256 && pair >= 0 && dynamic && per_group >= 512 &&
           tiles_bound(variant(pair), layout, rows, G, N) >= 4 * (num_sms / 2))
         cluster = 2;
     }

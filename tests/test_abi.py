@@ -207,7 +207,7 @@ GB300_SMS = 152
     ("c3_llama70b_m128", "stacked_swap_w128xa16_tma"),
     ("c3_llama70b_m1024", "stacked_tile128x256_tma"),
     ("c3_llama70b_m8192", "stacked_tile128x256_tma"),
-    ("c4_llama405b", "stacked_pair256x256_tma"),
+    ("c4_llama405b", "stacked_tile128x256_tma"),
     ("n1_batched_llama70b_m512", "dynamic_pair256x256_tma"),
     ("n2_offsets_llama70b_m8192", "stacked_tile128x256_tma"),
 ])
@@ -287,7 +287,7 @@ def test_plan_grid_bounds(L):
         assert i.split_k == 0
         fx.mslkb_set_split_k(2)  # every plan
         assert fx.mslkb_plan(0, 16384, 64, 16384, 16384, 152).split_k == 1
-        assert fx.mslkb_plan(0, 16384, 16, 16384, 16384, 152).split_k == 0  # pairs: whole
+        assert fx.mslkb_plan(1, 1024, 16, 16384, 16384, 152).split_k == 0  # pairs: whole
         assert fx.mslkb_plan(0, 512, 2, 4096, 64, 152).grid == 152
         with pytest.raises(fx.MslkbError):
             fx.mslkb_set_split_k(3)
