@@ -99,7 +99,7 @@ def test_config1_dynamic_with_poisoned_padding(orc):
 # ---------------------------------------------------------------------------------------
 def _variants(prefix):
     """Variant names from the library's own table (empty if it cannot be built here;
-    the tests that use it then fail on the GPU machine rather than at collection)."""
+    the tests that use it then fail on a GPU machine rather than at collection)."""
     try:
         fxbuild.build()
         return [fx.variant_name(i) for i in range(fx.mslkb_num_variants())
