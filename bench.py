@@ -266,6 +266,14 @@ def roofline_times(wl, pk, sustained=True):
     return wl.flops() / fp8, wl.bytes() / (pk["hbm_gbs"] * 1e9)
 
 
+def workload_config(wl, ws):
+    """The workload-defining part of the `config` object, the same in both arms."""
+    return {"workload": wl.name, "layout": wl.layout, "G": wl.G, "N": wl.N, "K": wl.K,
+            "total_M": wl.rows, "m_sizes": list(wl.meta), "seed": wl.seed,
+            "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
+            "l2": f"inputs larger than L2 ({wl.bytes() / 1e9:.2f} GB per call), no flush"}
+
+
 def plan_for(fx, wl, sms):
     if wl.layout in ("ragged_n", "ragged_k"):
         return fx.mslkb_plan(2 if wl.layout == "ragged_n" else 3, wl.rows, wl.G, wl.N, wl.K, sms)
@@ -449,11 +457,8 @@ def gpu_arm(args):
         "steps": steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "e4m3 x e4m3 -> fp32 accumulate -> bf16", "data": "synthetic",
-        "config": {"workload": wl.name, "layout": wl.layout, "G": wl.G, "N": wl.N, "K": wl.K,
-                   "total_M": wl.rows, "m_sizes": list(wl.meta), "seed": wl.seed,
+        "config": {**workload_config(wl, ws),
                    "us_per_call": round(ms_per_step * 1e3, 2),
-                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
-                   "l2": f"inputs larger than L2 ({wl.bytes() / 1e9:.2f} GB per call), no flush",
                    "variant": fx.variant_name(plan.variant), "grid": plan.grid,
                    "accumulation_chunk_kblocks": fx.mslkb_accumulation_chunk()},
         "roofline": roof,
@@ -514,8 +519,7 @@ def reference_arm(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64 (exact e4m3 products, correctly rounded bf16)", "data": "synthetic",
         "impl": "reference",
-        "config": {"workload": wl.name, "layout": wl.layout, "G": wl.G, "N": wl.N, "K": wl.K,
-                   "total_M": wl.rows},
+        "config": workload_config(wl, ws),
         "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": threads,
                          "kind": "oracle",
                          "sample": f"per step {rows} output rows x N={wl.N} x K={wl.K} of "
