@@ -115,6 +115,10 @@ def lib() -> ctypes.CDLL:
             L.mslkb_set_accumulation_chunk.restype = ctypes.c_int
             L.mslkb_accumulation_chunk.argtypes = []
             L.mslkb_accumulation_chunk.restype = ctypes.c_int32
+            L.mslkb_set_wait_timeout_us.argtypes = [i64]
+            L.mslkb_set_wait_timeout_us.restype = ctypes.c_int
+            L.mslkb_test_stall_next_launch.argtypes = []
+            L.mslkb_test_stall_next_launch.restype = ctypes.c_int
             L.mslkb_version.argtypes = []
             L.mslkb_version.restype = ctypes.c_int32
             _lib = L
@@ -242,6 +246,16 @@ def mslkb_set_accumulation_chunk(kblocks: int) -> None:
 
 def mslkb_accumulation_chunk() -> int:
     return lib().mslkb_accumulation_chunk()
+
+
+def mslkb_set_wait_timeout_us(us: int) -> None:
+    s = lib().mslkb_set_wait_timeout_us(us)
+    if s != MSLKB_OK:
+        raise MslkbError(s, "mslkb_set_wait_timeout_us")
+
+
+def mslkb_test_stall_next_launch() -> None:
+    lib().mslkb_test_stall_next_launch()
 
 
 def mslkb_version() -> int:

@@ -75,6 +75,8 @@ struct GemmParams {
   float* sk_ws;            // split tiles: fp32 partial sums, 2 slots per CTA
   uint32_t* sk_cnt;        // split tiles: arrival counters, one per (tile, epilogue warp)
   uint64_t timeout_ns;     // give-up time of one pipeline wait
+  int32_t test_stall;      // test hook: CTA 0 withholds its first stage (single-CTA TMA
+                           // kernels), so its MMA wait runs out and the timeout path runs
 };
 
 template <int kTileN_, int kStages_, bool kSwap_, bool kTma_, bool kDynamic_, int kEpiWarps_ = 4,
@@ -665,6 +667,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         // GB300: +2-4 % on the weight-streaming shapes, a loss on the 128-row tiles)
         const uint64_t pol_act = ptx::l2_policy_evict_last();
         const uint64_t pol_w = ptx::l2_policy_evict_first();
+        bool withhold = p.test_stall != 0 && blockIdx.x == 0;
         for (int32_t i = 0; ok && i < work.n_items; ++i) {
           const Item it = work_item(work, i, worker, workers);
           const TileCoord c = decode_tile<Cfg>(sched, it.tile, crank);
@@ -681,6 +684,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
               ptx::tma_load_2d_pair(s_act + stage * Cfg::kActBytes, &tmA, fb, kb * kBK, c.m0);
               ptx::tma_load_3d_pair(s_w + stage * Cfg::kWBytes, &tmB, fb, kb * kBK,
                                     c.n0 + static_cast<int32_t>(crank) * Cfg::kWRows, c.g);
+            } else if (withhold) {
+              withhold = false;  // this stage's full barrier never completes
             } else {
               ptx::mbar_arrive_expect_tx(full_bar(stage), Cfg::kStageBytes);
               // k0: a ragged-K slice starts on a multiple of 16 elements (16 bytes)

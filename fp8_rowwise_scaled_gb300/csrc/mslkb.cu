@@ -29,6 +29,8 @@ using mslkb::VariantInfo;
 constexpr int kVersion = 10000;  // 1.0.0
 constexpr int kMaxDevices = 64;
 constexpr uint64_t kWaitTimeoutNs = 1000000000ull;  // one pipeline wait gives up after ~1 s
+std::atomic<uint64_t> g_wait_timeout_ns{kWaitTimeoutNs};
+std::atomic<int> g_test_stall{0};  // one-shot: the next launch of run() withholds a stage
 
 __device__ uint32_t g_device_status;  // MSLKB_DEV_* bits, per device
 
@@ -496,7 +498,8 @@ mslkb_status run(int layout, const void* A, const void* B, const float* scale_a,
     p.kb_per_chunk = (kpc <= 0 || kpc > p.num_kb) ? (p.num_kb > 0 ? p.num_kb : 1) : kpc;
     if (block_scale) p.kb_per_chunk = 1;  // every K block scaled on its own
   }
-  p.timeout_ns = kWaitTimeoutNs;
+  p.timeout_ns = g_wait_timeout_ns.load();
+  p.test_stall = g_test_stall.exchange(0);
   p.split_k = 0;
   if (info.split_k) {
     Workspace ws;
@@ -572,7 +575,7 @@ mslkb_status run_ragged(int layout, const void* A, const void* B, const float* s
     const int kpc = g_kb_per_chunk.load();
     p.kb_per_chunk = (kpc <= 0 || kpc > p.num_kb) ? (p.num_kb > 0 ? p.num_kb : 1) : kpc;
   }
-  p.timeout_ns = kWaitTimeoutNs;
+  p.timeout_ns = g_wait_timeout_ns.load();
   p.split_k = 0;
   // A [a_rows, k_row]; B as a one-group [1, b_rows, k_row] map; out [out_rows, n_cols]
   if ((s = encode_maps(&la, v, A, B, a_rows, 1, b_rows, k_row)) != MSLKB_OK) return s;
@@ -653,7 +656,7 @@ mslkb_status run_stacked_with_scratch(const void* A, const void* B, const float*
     const int kpc = g_kb_per_chunk.load();
     p.kb_per_chunk = (kpc <= 0 || kpc > p.num_kb) ? (p.num_kb > 0 ? p.num_kb : 1) : kpc;
   }
-  p.timeout_ns = kWaitTimeoutNs;
+  p.timeout_ns = g_wait_timeout_ns.load();
   p.split_k = info.split_k;
   p.sk_ws = partials;
   p.sk_cnt = counters;
@@ -782,6 +785,20 @@ mslkb_status mslkb_get_device_status(void* stream, uint32_t* flags) {
   if (e == cudaSuccess) e = cudaMemsetAsync(st->status_ptr, 0, sizeof(uint32_t), cs);
   if (e == cudaSuccess) e = cudaStreamSynchronize(cs);
   if (e != cudaSuccess) return cuda_fail(e);
+  if (value & mslkb::kStatusTimeout) {
+    // a kernel that gave up may have left split-tile arrival counters short: clear the
+    // counters of every stream workspace of this device (on `stream`)
+    int dev = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return cuda_fail(e);
+    const size_t ncnt = 2 * static_cast<size_t>(st->sm_count) * 8;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    for (auto& kv : g_workspaces) {
+      if (kv.first.first != dev || kv.second.counters == nullptr) continue;
+      e = cudaMemsetAsync(kv.second.counters, 0, ncnt * sizeof(uint32_t), cs);
+      if (e != cudaSuccess) return cuda_fail(e);
+    }
+    if ((e = cudaStreamSynchronize(cs)) != cudaSuccess) return cuda_fail(e);
+  }
   *flags = value;
   return MSLKB_OK;
 }
@@ -839,6 +856,18 @@ mslkb_status mslkb_set_accumulation_chunk(int32_t kblocks) {
 }
 
 int32_t mslkb_accumulation_chunk(void) { return g_kb_per_chunk.load(); }
+
+mslkb_status mslkb_set_wait_timeout_us(int64_t us) {
+  if (us < 0) return MSLKB_ERR_SHAPE;
+  if (us > 0 && us < 1000) return MSLKB_ERR_SHAPE;  // at least 1 ms
+  g_wait_timeout_ns.store(us == 0 ? kWaitTimeoutNs : static_cast<uint64_t>(us) * 1000ull);
+  return MSLKB_OK;
+}
+
+mslkb_status mslkb_test_stall_next_launch(void) {
+  g_test_stall.store(1);
+  return MSLKB_OK;
+}
 
 int32_t mslkb_version(void) { return kVersion; }
 

@@ -270,7 +270,10 @@ MSLKB_API int mslkb_last_cuda_error(void);
 /*
  * Reads the device status word of the current device and clears it.  Enqueued on
  * `stream` and then waits for that stream, so it orders after earlier calls on it.
- * flags: host pointer receiving the MSLKB_DEV_* bits.
+ * flags: host pointer receiving the MSLKB_DEV_* bits.  When the word reports a timeout,
+ * the split-tile arrival counters of every stream workspace on the device are cleared as
+ * well (a kernel that gave up may have left them short), on `stream`: call it while no
+ * other stream runs this library's kernels on the device.
  */
 MSLKB_API mslkb_status mslkb_get_device_status(void *stream, uint32_t *flags);
 
@@ -349,6 +352,22 @@ MSLKB_API mslkb_status mslkb_set_split_k(int32_t enable);
  */
 MSLKB_API mslkb_status mslkb_set_accumulation_chunk(int32_t kblocks);
 MSLKB_API int32_t mslkb_accumulation_chunk(void);
+
+/*
+ * Failure detection (an addition of this library; the pages have no counterpart).  Every
+ * wait of the kernels' pipelines is bounded: a wait that runs past the limit (default
+ * ~1 s) makes the kernel give up, record MSLKB_DEV_TIMEOUT in the device status word, let
+ * its copies in flight land, free its tensor memory and return, so the context stays
+ * usable.  mslkb_set_wait_timeout_us sets the limit for the following launches (0: the
+ * default; otherwise at least 1000 us, else MSLKB_ERR_SHAPE).
+ *
+ * mslkb_test_stall_next_launch is a test hook: the next launch through the stacked,
+ * dynamic, offsets or batched entry points of a single-CTA TMA kernel has its CTA 0
+ * withhold one pipeline stage, so that CTA's MMA wait runs out and the timeout path runs
+ * (that launch's output is incomplete; the status word reports the timeout).
+ */
+MSLKB_API mslkb_status mslkb_set_wait_timeout_us(int64_t us);
+MSLKB_API mslkb_status mslkb_test_stall_next_launch(void);
 
 /* Library version, as major * 10000 + minor * 100 + patch. */
 MSLKB_API int32_t mslkb_version(void);

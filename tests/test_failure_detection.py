@@ -1,0 +1,67 @@
+"""Failure detection without a GPU fault: every pipeline wait in the kernels is bounded.
+A test hook makes CTA 0 of the next launch withhold one pipeline stage (a barrier that
+nothing completes); its MMA wait runs out after the configured limit, the kernel records
+MSLKB_DEV_TIMEOUT in the device status word, waits for its copies in flight, frees its
+tensor memory and returns.  The host reads the status, and the context stays usable: the
+same call then gives the oracle's result."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import fp8_rowwise_scaled_gb300 as fx
+from fp8_rowwise_scaled_gb300 import build as fxbuild
+from fp8_rowwise_scaled_gb300.synthetic import random_codes
+from parity_util import Problem, abs_codes, bits_of, compare
+
+
+@pytest.fixture(scope="module")
+def L():
+    fxbuild.build()
+    return fx.lib()
+
+
+def test_timeout_setting_arguments(L):
+    with pytest.raises(fx.MslkbError):
+        fx.mslkb_set_wait_timeout_us(-1)
+    with pytest.raises(fx.MslkbError):
+        fx.mslkb_set_wait_timeout_us(999)     # below 1 ms
+    fx.mslkb_set_wait_timeout_us(5000)
+    fx.mslkb_set_wait_timeout_us(0)           # back to the default
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("shape", ["tiles", "swap"])
+def test_wait_runs_out_and_the_context_survives(L, shape):
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    g = torch.Generator().manual_seed(77)
+    if shape == "tiles":    # 128-row tiles, whole (no split tiles)
+        G, N, K, m = 4, 1024, 1024, [300, 0, 257, 411]
+    else:                   # swap-AB tiles, split along K over every CTA
+        G, N, K, m = 8, 2048, 2048, [1, 0, 3, 2, 0, 1, 1, 2]
+    rows = sum(m)
+    A = random_codes((rows, K), g).numpy()
+    B = random_codes((G, N, K), g).numpy()
+    sa = (torch.rand(rows, generator=g) + 0.5).numpy().astype(np.float32)
+    sb = (torch.rand(G * N, generator=g) + 0.5).numpy().astype(np.float32).reshape(G, N)
+    prob = Problem.from_numpy("stacked", A, B, sa, sb, m)
+    fx.device_status()                        # start clean
+    fx.mslkb_set_wait_timeout_us(50_000)      # 50 ms
+    try:
+        fx.mslkb_test_stall_next_launch()
+        prob.run_gpu()
+        torch.cuda.synchronize()              # the launch returns: no hang, no fault
+        assert fx.device_status() & fx.MSLKB_DEV_TIMEOUT
+    finally:
+        fx.mslkb_set_wait_timeout_us(0)
+    # the context and the library keep working: the same call gives the oracle's result
+    out = bits_of(prob.run_gpu()).reshape(rows, N)
+    torch.cuda.synchronize()
+    assert fx.device_status() == 0
+    orc = oracle.load(0)
+    h = prob.host()
+    ref, _ = orc.stacked(h["A"], h["B"], h["sa"], h["sb"], h["meta"])
+    ab, _ = orc.stacked(abs_codes(h["A"]), abs_codes(h["B"]), np.abs(h["sa"]), np.abs(h["sb"]),
+                        h["meta"])
+    compare(out.ravel(), ref.ravel(), ab.ravel(), f"after a timeout ({shape})")
