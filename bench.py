@@ -44,7 +44,7 @@ HEADLINE = "c4_llama405b"
 SWEEP = ["c2a_dsv3_gate_up", "c2b_dsv3_down", "c3_llama70b_m1", "c3_llama70b_m16",
          "c3_llama70b_m128", "c3_llama70b_m1024", "c3_llama70b_m8192",
          "n1_batched_llama70b_m512", "n2_offsets_llama70b_m8192", "n3_ragged_n_m1024",
-         "n4_ragged_k_wgrad", "n5_groupwise_llama70b_m8192"]
+         "n4_ragged_k_wgrad", "n5_groupwise_llama70b_m8192", "n6_groupwise_llama70b_m16"]
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 FP8_OVER_BF16 = 2.0  # nominal dense ratio (4.5 / 2.25 PFLOP/s)

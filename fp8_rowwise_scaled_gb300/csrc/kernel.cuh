@@ -168,9 +168,10 @@ struct KernelCfg {
   static_assert(kEpiWarps == 4 || (kEpiWarps == 8 && !kSwap), "epilogue warp split");
   static_assert(!kPair || (kTma && !kSwap && kTileN == 256), "CTA pairs: 256 x 256 tiles, TMA");
   static_assert(!kRagged || (kTma && !kPair && !kDynamic), "ragged layouts: TMA, single CTAs");
-  static_assert(!kBlockScale || (kTma && !kSwap && !kPair && !kRagged && !kDynamic &&
-                                 kBK == kScaleBlock),
-                "block scaling: stacked 128-row tiles, one K block per scale block");
+  static_assert(!kBlockScale || (kTma && !kPair && !kRagged && !kDynamic &&
+                                 kBK == kScaleBlock && (!kSwap || kTileN <= 32)),
+                "block scaling: stacked TMA tiles (swap-AB up to 32 rows), one K block per "
+                "scale block");
   static_assert(kThreadCols % 16 == 0, "TMEM load granularity");
   static_assert(!kRegSplit || (kThreads == 384 && kEpiWarp0 == 4 &&
                                128 * kRegsLow + 256 * kRegsHigh == kThreads * kLaunchRegs),
@@ -430,10 +431,10 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
 // Each lane of the pair rounds exactly as the scalar operation would.
 template <bool kScale>
 __device__ __forceinline__ void accum2(float& a0, float& a1, uint32_t v0, uint32_t v1,
-                                       float scale) {
+                                       float s0, float s1) {
   const float2 v = make_float2(__uint_as_float(v0), __uint_as_float(v1));
   float2 a = make_float2(a0, a1);
-  if constexpr (kScale) a = __ffma2_rn(v, make_float2(scale, scale), a);
+  if constexpr (kScale) a = __ffma2_rn(v, make_float2(s0, s1), a);
   else a = __fadd2_rn(a, v);
   a0 = a.x;
   a1 = a.y;
@@ -949,7 +950,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
           sb_pre[pc] = (active && col < c.n_end) ? __ldg(sb_g + col) : 0.0f;
         }
       }
-      if constexpr (Cfg::kBlockScale) {
+      if constexpr (Cfg::kBlockScale && !Cfg::kSwap) {
         // the K-block scales are applied chunk by chunk: the epilogue multiplies by 1
         const int32_t R = c.m0 + row_off + static_cast<int32_t>(lane);
         const bool rv = active && R < c.valid_end;
@@ -962,6 +963,22 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         sa_pre = 1.0f;
 #pragma unroll
         for (int pc = 0; pc < Cfg::kThreadCols / 32; ++pc) sb_pre[pc] = 1.0f;
+      }
+      // swap-AB with block scaling: this thread's weight row owns one 128-column block of
+      // scale_b; lane j holds scale_a of activation row m0 + j (broadcast by shuffle)
+      float bs_row_next = 0.0f;
+      if constexpr (Cfg::kBlockScale && Cfg::kSwap) {
+        const int32_t nw = c.n0 + static_cast<int32_t>(32u * q + lane);
+        const int32_t nblk = p.N / Cfg::kScaleBlock;
+        const int32_t blk = min(nw / Cfg::kScaleBlock, nblk - 1);
+        bs_b = p.scale_b + (static_cast<size_t>(c.g) * nblk + blk) * p.num_kb;
+        const int32_t Rl = c.m0 + static_cast<int32_t>(lane);
+        const bool rv = lane < static_cast<uint32_t>(Cfg::kTileN) && Rl < c.valid_end;
+        bs_a = p.scale_a + static_cast<size_t>(rv ? Rl : 0) * p.num_kb;
+        if (it.kb0 < kb_end) {
+          bs_next = __ldg(bs_b + it.kb0);
+          bs_row_next = rv ? __ldg(bs_a + it.kb0) : 0.0f;
+        }
       }
       // fp32 accumulator of this thread (round-to-nearest adds of the TMEM chunks)
       float acc[Cfg::kThreadCols];
@@ -979,12 +996,27 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
           const int buf = static_cast<int>(chunk & 1u);
           const uint32_t use = chunk >> 1;
           // block scaling: this chunk (= K block kb0)'s scale, and the next one's load
-          float bs = 1.0f;
-          if constexpr (Cfg::kBlockScale) {
+          float bs = 1.0f;      // this thread's scale of the chunk (swap-AB: its column's)
+          float bs_row = 0.0f;  // swap-AB: lane j's activation-row scale
+          if constexpr (Cfg::kBlockScale && Cfg::kSwap) {
+            bs = bs_next;
+            bs_row = bs_row_next;
+            if (kb0 + 1 < kb_end) {
+              bs_next = __ldg(bs_b + kb0 + 1);
+              bs_row_next = __ldg(bs_a + kb0 + 1);
+            }
+          } else if constexpr (Cfg::kBlockScale) {
             bs = bs_next;
             if (kb0 + 1 < kb_end && bs_a != nullptr)
               bs_next = __ldg(bs_a + kb0 + 1) * __ldg(bs_b + kb0 + 1);
           }
+          // scale of accumulator column j (block scaling; swap-AB: row j's times column's)
+          auto cs = [&](int j) -> float {
+            if constexpr (Cfg::kBlockScale && Cfg::kSwap)
+              return __shfl_sync(0xffffffffu, bs_row, j) * bs;
+            else
+              return bs;
+          };
           if (!wait_bar(tfull_bar(buf), use & 1u, abort_flag, p.status, p.timeout_ns)) {
             ok = false;
             break;
@@ -1004,9 +1036,9 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
 #pragma unroll
                 for (int j = 0; j < 32; j += 2) {
                   accum2<Cfg::kBlockScale>(acc[pc * 64 + j], acc[pc * 64 + j + 1], v0[j],
-                                           v0[j + 1], bs);
+                                           v0[j + 1], bs, bs);
                   accum2<Cfg::kBlockScale>(acc[pc * 64 + 32 + j], acc[pc * 64 + 33 + j], v1[j],
-                                           v1[j + 1], bs);
+                                           v1[j + 1], bs, bs);
                 }
               }
             } else if constexpr (Cfg::kThreadCols % 32 == 0 && Cfg::kThreadCols < 128) {
@@ -1020,7 +1052,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
 #pragma unroll
                 for (int j = 0; j < 32; j += 2)
                   accum2<Cfg::kBlockScale>(acc[pc * 32 + j], acc[pc * 32 + j + 1], v[j], v[j + 1],
-                                           bs);
+                                           cs(pc * 32 + j), cs(pc * 32 + j + 1));
               }
             } else {
 #pragma unroll
@@ -1031,7 +1063,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
 #pragma unroll
                 for (int j = 0; j < 16; j += 2)
                   accum2<Cfg::kBlockScale>(acc[pc * 16 + j], acc[pc * 16 + j + 1], v[j], v[j + 1],
-                                           bs);
+                                           cs(pc * 16 + j), cs(pc * 16 + j + 1));
               }
             }
           }
@@ -1172,7 +1204,9 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         // thread = one weight row (output column n); accumulator columns are activation rows
         const int32_t n = c.n0 + static_cast<int32_t>(32u * q + lane);
         const bool col_ok = n >= c.n_begin && n < c.n_end;
-        const float sb = col_ok ? __ldg(p.scale_b + c.sb_off + n) : 0.0f;
+        // block scaling: the scales were applied chunk by chunk
+        const float sb = Cfg::kBlockScale ? 1.0f
+                                          : (col_ok ? __ldg(p.scale_b + c.sb_off + n) : 0.0f);
 #pragma unroll
         for (int pc = 0; pc < (Cfg::kTileN + 31) / 32; ++pc) {
           constexpr int kCols = Cfg::kTileN < 32 ? Cfg::kTileN : 32;
@@ -1180,8 +1214,9 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
           if (m_first >= c.zero_end) break;
           // lane j holds scale_a of row m_first + j
           const int32_t Rl = m_first + static_cast<int32_t>(lane);
-          const float sa_l = (lane < static_cast<uint32_t>(kCols) && Rl < c.valid_end)
-                                 ? __ldg(p.scale_a + (Rl + c.srow_delta)) : 0.0f;
+          const float sa_l = Cfg::kBlockScale ? 1.0f
+                             : ((lane < static_cast<uint32_t>(kCols) && Rl < c.valid_end)
+                                    ? __ldg(p.scale_a + (Rl + c.srow_delta)) : 0.0f);
 #pragma unroll
           for (int j = 0; j < kCols; ++j) {
             const float sa = __shfl_sync(0xffffffffu, sa_l, j);

@@ -290,11 +290,13 @@ mslkb_status plan(int layout, int64_t rows, int64_t G, int64_t N, int64_t K, int
   bool swap;
   int tile_n;
   int cluster = 1;
-  if (block_scale) {  // 128 x 256 when its tiles fill the SMs, else 128 x 128
-    swap = false;
-    tile_n = 128;
-    const int wide = find_variant(false, true, false, 256, 1, 0, 1);
-    if (wide >= 0 && tiles_bound(variant(wide), layout, rows, G, N) >= num_sms) tile_n = 256;
+  if (block_scale) {  // swap-AB up to 32 rows per group; else 128 x 256 / 128 x 128
+    swap = per_group <= 32;
+    tile_n = per_group <= 16 ? 16 : (swap ? 32 : 128);
+    if (!swap) {
+      const int wide = find_variant(false, true, false, 256, 1, 0, 1);
+      if (wide >= 0 && tiles_bound(variant(wide), layout, rows, G, N) >= num_sms) tile_n = 256;
+    }
   } else if (ragged) {  // TMA variants: swap-AB 32, 128 x 256, 128 x 128
     swap = per_group <= 32;
     tile_n = swap ? 32 : 128;
@@ -341,7 +343,7 @@ mslkb_status plan(int layout, int64_t rows, int64_t G, int64_t N, int64_t K, int
   // weights) but slows the 128-row-tile plans by 4-9% (128 KB of partial sums per piece).
   const int policy = g_split_k.load();
   // CTA pairs run whole tiles only (one pair per tile)
-  const bool split = nkb > 0 && v->cluster == 1 && !ragged && !block_scale &&
+  const bool split = nkb > 0 && v->cluster == 1 && !ragged &&
                      (policy == 2 || (policy == 1 && v->swap));
   // with splitting every CTA gets K work as long as there are units to share
   const int64_t work = (split ? bound * nkb : bound) * v->cluster;

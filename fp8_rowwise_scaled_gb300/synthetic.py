@@ -240,6 +240,12 @@ def workloads() -> dict[str, Workload]:
         rows=sum(m3), meta=tuple(m3), seed=1000 * 8 + 0,
         note="block-scaled: llama3-70b total_M=8192 routing, N=K=8192, 128-blocks",
         tags=("perf",))
+    m16 = w["c3_llama70b_m16"].meta
+    w["n6_groupwise_llama70b_m16"] = Workload(
+        name="n6_groupwise_llama70b_m16", layout="groupwise", G=16, N=8192, K=8192,
+        rows=sum(m16), meta=tuple(m16), seed=1000 * 8 + 1,
+        note="block-scaled decode: llama3-70b total_M=16 routing, N=K=8192, 128-blocks",
+        tags=("perf",))
     # 4: llama3-405b-shaped
     m4 = multinomial_counts(1000 * 4 + 0, 16384, [1.0 / 16] * 16)
     w["c4_llama405b"] = _stacked("c4_llama405b", 4, 0, 16, 16384, 16384, m4,

@@ -163,8 +163,12 @@ def test_groupwise_argument_errors_and_plan(L):
     assert gw(M=0) == fx.MSLKB_OK and gw(G=0) == fx.MSLKB_OK
     i = fx.mslkb_plan(4, 16384, 16, 16384, 16384, 152)
     assert fx.variant_name(i.variant) == "blockscale_tile128x256_tma" and i.split_k == 0
-    i = fx.mslkb_plan(4, 64, 4, 256, 512, 152)
+    i = fx.mslkb_plan(4, 512, 4, 256, 512, 152)
     assert fx.variant_name(i.variant) == "blockscale_tile128x128_tma"
+    i = fx.mslkb_plan(4, 64, 4, 256, 512, 152)     # 16 rows per group: swap-AB, split along K
+    assert fx.variant_name(i.variant) == "blockscale_swap_w128xa16_tma" and i.split_k == 1
+    i = fx.mslkb_plan(4, 100, 4, 256, 512, 152)
+    assert fx.variant_name(i.variant) == "blockscale_swap_w128xa32_tma"
     with pytest.raises(fx.MslkbError):
         fx.mslkb_plan(4, 64, 4, 256, 520, 152)
 

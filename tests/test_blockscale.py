@@ -117,6 +117,15 @@ def test_blockscale_equals_rowwise_for_constant_scales(orc):
     assert np.array_equal(ref, orc.blockwise_stacked(A, B, sa, sb, m)[0])
 
 
+@pytest.mark.parametrize("m", [[1, 0, 3, 2], [9, 16, 0, 30]])
+def test_blockscale_decode_shapes(orc, m):
+    # few rows per group: the planner's swap-AB tiles, split along K over every CTA
+    A, B, sa, sb, m, rows = _case(14, 4, m, 1024, 2048, wide=True)
+    got = _run(A, B, sa, sb, m, rows, 1024)
+    _check(orc, A, B, sa, sb, m, rows, got, f"decode {m.tolist()}")
+    assert fx.device_status() == 0
+
+
 def test_blockscale_k_zero():
     out = fx.f8f8bf16_groupwise_grouped_stacked(
         torch.zeros((8, 0), dtype=torch.uint8, device="cuda"),

@@ -124,3 +124,26 @@ def test_full_size_groupwise_sampled(orc):
     assert fx.device_status() == 0
     del inp, out
     torch.cuda.empty_cache()
+
+
+def test_full_size_groupwise_decode_sampled(orc):
+    # the block-scaled decode workload (swap-AB tiles split along K) at full size, all rows
+    from parity_util import abs_codes
+    wl = workloads()["n6_groupwise_llama70b_m16"]
+    inp = make_inputs(wl, "cuda")
+    out = torch.full((wl.rows, wl.N), 0x7E7E, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+    s = fx.mslkb_f8f8bf16_groupwise_grouped_stacked(
+        inp["A"].data_ptr(), inp["B"].data_ptr(), inp["scale_a"].data_ptr(),
+        inp["scale_b"].data_ptr(), inp["meta"].data_ptr(), out.data_ptr(), wl.rows, wl.G, wl.N,
+        wl.K, torch.cuda.current_stream().cuda_stream)
+    assert s == fx.MSLKB_OK, fx.mslkb_status_string(s)
+    torch.cuda.synchronize()
+    got = bits_of(out).reshape(wl.rows, wl.N)
+    h = {k: v.cpu().numpy() for k, v in inp.items()}
+    ref, _ = orc.blockwise_stacked(h["A"], h["B"], h["scale_a"], h["scale_b"], h["meta"])
+    ab, _ = orc.blockwise_stacked(abs_codes(h["A"]), abs_codes(h["B"]), np.abs(h["scale_a"]),
+                                  np.abs(h["scale_b"]), h["meta"])
+    compare(got.ravel(), ref.ravel(), ab.ravel(), wl.name)
+    assert fx.device_status() == 0
+    del inp, out
+    torch.cuda.empty_cache()
