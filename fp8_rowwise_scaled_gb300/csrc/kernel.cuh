@@ -133,11 +133,15 @@ struct KernelCfg {
   // accumulator columns one epilogue thread owns (and keeps in fp32 registers)
   static constexpr int kThreadCols = kSwap ? kTileN : kTileN / (kEpiWarps / 4);
   static constexpr int kAccCols = kTileN;  // fp32 TMEM columns of one accumulator
-  static constexpr int kTmemCols = (2 * kAccCols <= 32)    ? 32
-                                   : (2 * kAccCols <= 64)  ? 64
-                                   : (2 * kAccCols <= 128) ? 128
-                                   : (2 * kAccCols <= 256) ? 256
-                                                           : 512;
+  // TMEM accumulator buffers the MMA can run ahead of the epilogue by: two for 256-column
+  // accumulators (all 512 columns), more for narrower ones (up to 8: swap-AB tiles drain
+  // every K block under block scaling and need the slack)
+  static constexpr int kNumAcc = (kAccCols >= 256) ? 2 : (kAccCols >= 128) ? 4 : 8;
+  static constexpr int kTmemCols = (kNumAcc * kAccCols <= 32)    ? 32
+                                   : (kNumAcc * kAccCols <= 64)  ? 64
+                                   : (kNumAcc * kAccCols <= 128) ? 128
+                                   : (kNumAcc * kAccCols <= 256) ? 256
+                                                                 : 512;
   static constexpr int kCpLag = kStages - 2;  // cp.async groups kept in flight per thread
   static constexpr uint32_t kIdesc = ptx::idesc_e4m3_f32(kMmaM * kCtas, kTileN);
   // CTA pairs, a group's last <= 128 rows: one M = 128 MMA over both CTAs (64 rows each)
@@ -153,7 +157,7 @@ struct KernelCfg {
   static constexpr int kOffW = kStages * kActBytes;
   static constexpr int kOffOut = kOffW + kStages * kWBytes;
   static constexpr int kOffBar = kOffOut + (kTmaStore ? kEpiWarps * kStageOutBytes : 0);
-  static constexpr int kNumBars = 2 * kStages + 4;
+  static constexpr int kNumBars = 2 * kStages + 2 * kNumAcc;
   static constexpr int kOffMisc = kOffBar + 8 * kNumBars;  // tmem address, abort flag
   static constexpr int kOffWork = kOffMisc + 16;           // the CTA's Work (below)
   static constexpr int kOffSched = kOffWork + 64;
@@ -164,7 +168,7 @@ struct KernelCfg {
   static_assert(kActBytes % 1024 == 0 && kWBytes % 1024 == 0, "swizzle atoms");
   static_assert(kStages >= 3, "pipeline depth");
   static_assert(kSmemBytes <= 232448, "shared memory per CTA");
-  static_assert(2 * kAccCols <= 512, "two accumulators must fit TMEM");
+  static_assert(kNumAcc * kAccCols <= 512, "the accumulators must fit TMEM");
   static_assert(kEpiWarps == 4 || (kEpiWarps == 8 && !kSwap), "epilogue warp split");
   static_assert(!kPair || (kTma && !kSwap && kTileN == 256), "CTA pairs: 256 x 256 tiles, TMA");
   static_assert(!kRagged || (kTma && !kPair && !kDynamic), "ragged layouts: TMA, single CTAs");
@@ -574,7 +578,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
   auto full_bar = [&](int s) { return s_bar + 8u * s; };
   auto empty_bar = [&](int s) { return s_bar + 8u * (Cfg::kStages + s); };
   auto tfull_bar = [&](int b) { return s_bar + 8u * (2 * Cfg::kStages + b); };
-  auto tempty_bar = [&](int b) { return s_bar + 8u * (2 * Cfg::kStages + 2 + b); };
+  auto tempty_bar = [&](int b) { return s_bar + 8u * (2 * Cfg::kStages + Cfg::kNumAcc + b); };
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + Cfg::kOffMisc);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + Cfg::kOffMisc + 4);
   int32_t* rowinfo = reinterpret_cast<int32_t*>(smem + Cfg::kOffSched);
@@ -592,7 +596,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
       ptx::mbar_init(full_bar(s), Cfg::kTma ? 1u : static_cast<uint32_t>(Cfg::kLoaderThreads));
       ptx::mbar_init(empty_bar(s), 1u);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < Cfg::kNumAcc; ++b) {
       ptx::mbar_init(tfull_bar(b), 1u);
       // pairs: the leader's MMA waits for the epilogue warps of both CTAs
       ptx::mbar_init(tempty_bar(b), static_cast<uint32_t>(Cfg::kEpiWarps * Cfg::kCtas));
@@ -812,8 +816,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
           k_len = c.k_len;
         }
         for (int32_t kb0 = it.kb0; ok && kb0 < kb_end; kb0 += kpc) {
-          const int buf = static_cast<int>(chunk & 1u);
-          const uint32_t use = chunk >> 1;  // how often this buffer was used before
+          const int buf = static_cast<int>(chunk % Cfg::kNumAcc);
+          const uint32_t use = chunk / Cfg::kNumAcc;  // how often this buffer was used before
           if (!wait_bar<Cfg::kPair>(tempty_bar(buf), (use & 1u) ^ 1u, abort_flag, p.status,
                                     p.timeout_ns)) {
             ok = false;
@@ -993,8 +997,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
       }
       if (has_k) {
         for (int32_t kb0 = it.kb0; kb0 < kb_end; kb0 += kpc) {
-          const int buf = static_cast<int>(chunk & 1u);
-          const uint32_t use = chunk >> 1;
+          const int buf = static_cast<int>(chunk % Cfg::kNumAcc);
+          const uint32_t use = chunk / Cfg::kNumAcc;
           // block scaling: this chunk (= K block kb0)'s scale, and the next one's load
           float bs = 1.0f;      // this thread's scale of the chunk (swap-AB: its column's)
           float bs_row = 0.0f;  // swap-AB: lane j's activation-row scale
