@@ -487,20 +487,24 @@ __device__ void build_sched(const GemmParams& p, int32_t* rowinfo, int32_t* tile
         return static_cast<int64_t>(offs[g]) - (g > 0 ? static_cast<int64_t>(offs[g - 1]) : 0);
       return p.meta[g];
     };
-    // clamped exclusive prefix: off_g = min(sum_{h<g} max(m_h, 0), total_M)
+    // ragged layouts partition the columns (N) or the contraction (K) instead of the rows
+    const int64_t total = Cfg::kRagN ? p.N : (Cfg::kRagK ? p.K : p.rows);
+    // clamped exclusive prefix: off_g = min(sum_{h<g} max(m_h, 0), total_M).  Each count
+    // is read from global memory once, kept in the table as min(max(m, 0), total) (a count
+    // above the total clamps everything after it anyway), and replaced by its prefix.
     int64_t my_sum = 0;
     for (int32_t g = g0; g < g1; ++g) {
       const int64_t m = count(g);
-      if (m < 0) clamped = true;
-      my_sum += m < 0 ? 0 : m;
+      if (m < 0 || m > total) clamped = true;
+      const int64_t mc = m < 0 ? 0 : (m > total ? total : m);
+      rowinfo[g] = static_cast<int32_t>(mc);
+      my_sum += mc;
     }
-    // ragged layouts partition the columns (N) or the contraction (K) instead of the rows
-    const int64_t total = Cfg::kRagN ? p.N : (Cfg::kRagK ? p.K : p.rows);
     int64_t run = warp_incl_scan(my_sum, lane) - my_sum;
     for (int32_t g = g0; g < g1; ++g) {
-      const int64_t m = count(g);
+      const int64_t mc = rowinfo[g];
       rowinfo[g] = static_cast<int32_t>(run < total ? run : total);
-      run += m < 0 ? 0 : m;
+      run += mc;
     }
     if (lane == 31) {  // the last chunk ends at G, so run is the sum over all groups
       if (run > total) clamped = true;
@@ -1098,29 +1102,48 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         float* mine = piece(blockIdx.x) + lane;
 #pragma unroll
         for (int j = 0; j < Cfg::kThreadCols; ++j) __stcg(mine + j * 32, acc[j]);
-        __threadfence();
+        // the warp barrier orders every lane's stores before lane 0's count, which releases
+        // them at GPU scope; the last piece's count acquires the others' releases, and the
+        // warp barrier after it hands them on to every lane
         __syncwarp();
         uint32_t* cnt = p.sk_cnt + static_cast<size_t>(it.sk_tile) * Cfg::kEpiWarps + ew;
         uint32_t prev = 0;
-        if (lane == 0) {
-          prev = atomicAdd(cnt, 1u);
-          __threadfence();
-        }
+        if (lane == 0) prev = ptx::atom_add_acq_rel_gpu(cnt, 1u);
         prev = __shfl_sync(0xffffffffu, prev, 0);
-        __syncwarp();
         if (prev != static_cast<uint32_t>(c_last - c_first)) continue;  // not the last piece
-        __threadfence();
+        __syncwarp();
         // every piece, this CTA's own included, is read back from the workspace so that
-        // the sum runs in CTA order: ((p_first + p_next) + ...) + p_last
-        {
-          const float* src = piece(c_first) + lane;
+        // the sum runs in CTA order: ((p_first + p_next) + ...) + p_last.  The loads of up
+        // to kBatch pieces are in flight together before their adds.
+        constexpr int kBatch = Cfg::kThreadCols >= 64 ? 1 : 64 / Cfg::kThreadCols;
+        if constexpr (kBatch == 1) {
+          // wide accumulators: no registers to spare, one piece at a time
+          for (int32_t cta = c_first; cta <= c_last; ++cta) {
+            const float* src = piece(cta) + lane;
 #pragma unroll
-          for (int j = 0; j < Cfg::kThreadCols; ++j) acc[j] = __ldcg(src + j * 32);
-        }
-        for (int32_t cta = c_first + 1; cta <= c_last; ++cta) {
-          const float* src = piece(cta) + lane;
+            for (int j = 0; j < Cfg::kThreadCols; ++j)
+              acc[j] = (cta == c_first) ? __ldcg(src + j * 32) : acc[j] + __ldcg(src + j * 32);
+          }
+        } else {
+          for (int32_t c0 = c_first; c0 <= c_last; c0 += kBatch) {
+            float v[kBatch][Cfg::kThreadCols];
 #pragma unroll
-          for (int j = 0; j < Cfg::kThreadCols; ++j) acc[j] += __ldcg(src + j * 32);
+            for (int b = 0; b < kBatch; ++b) {
+              if (c0 + b <= c_last) {
+                const float* src = piece(c0 + b) + lane;
+#pragma unroll
+                for (int j = 0; j < Cfg::kThreadCols; ++j) v[b][j] = __ldcg(src + j * 32);
+              }
+            }
+#pragma unroll
+            for (int b = 0; b < kBatch; ++b) {
+              if (c0 + b <= c_last) {
+#pragma unroll
+                for (int j = 0; j < Cfg::kThreadCols; ++j)
+                  acc[j] = (c0 + b == c_first) ? v[b][j] : acc[j] + v[b][j];
+              }
+            }
+          }
         }
         if (lane == 0) *cnt = 0u;  // ready for the next call
       }

@@ -371,6 +371,16 @@ __device__ __forceinline__ void tmem_ld_x32(uint32_t taddr, uint32_t (&r)[32]) {
 
 // Programmatic dependent launch: let the next kernel on the stream start launching, and
 // wait until the kernels this one depends on have completed and their writes are visible.
+// atomic add with acquire-release semantics at GPU scope; returns the old value
+__device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t* ptr, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;"
+               : "=r"(old)
+               : "l"(ptr), "r"(v)
+               : "memory");
+  return old;
+}
+
 __device__ __forceinline__ void griddep_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
