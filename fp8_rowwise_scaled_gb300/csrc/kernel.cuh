@@ -948,6 +948,21 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
       const float* bs_b = nullptr;
       float bs_next = 0.0f;
       float sb_pre[Cfg::kSwap ? 1 : Cfg::kThreadCols / 32];
+      // swap-AB: scale_b of this thread's weight row, and scale_a of row m0 + 32 pc + lane
+      float sw_sb = 0.0f;
+      float sw_sa[(Cfg::kTileN + 31) / 32];
+      if constexpr (Cfg::kSwap && !Cfg::kBlockScale) {
+        const int32_t n = c.n0 + static_cast<int32_t>(32u * q + lane);
+        sw_sb = (n >= c.n_begin && n < c.n_end) ? __ldg(p.scale_b + c.sb_off + n) : 0.0f;
+#pragma unroll
+        for (int pc = 0; pc < (Cfg::kTileN + 31) / 32; ++pc) {
+          constexpr int kCols = Cfg::kTileN < 32 ? Cfg::kTileN : 32;
+          const int32_t Rl = c.m0 + pc * 32 + static_cast<int32_t>(lane);
+          sw_sa[pc] = (lane < static_cast<uint32_t>(kCols) && Rl < c.valid_end)
+                          ? __ldg(p.scale_a + (Rl + c.srow_delta))
+                          : 0.0f;
+        }
+      }
       if constexpr (!Cfg::kSwap && !Cfg::kBlockScale) {
         const int32_t R = c.m0 + row_off + static_cast<int32_t>(lane);
         if (active && R < c.valid_end) sa_pre = __ldg(p.scale_a + (R + c.srow_delta));
@@ -1093,10 +1108,12 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         const int32_t c_first = unit_owner(work, u_first);
         const int32_t c_last = unit_owner(work, u_first + work.nkb - 1);
         constexpr size_t kPerWarp = 32 * Cfg::kThreadCols;
+        // slot 0: the first tile of that CTA's range; slot 1: its last tile.  Every CTA after
+        // c_first starts its range inside this tile; c_first does when its range starts on
+        // the tile's first unit.
+        const int slot_first = work.units * c_first / work.sk_ctas < u_first ? 1 : 0;
         auto piece = [&](int32_t cta) -> float* {
-          // slot 0: the first tile of that CTA's range; slot 1: its last tile
-          const int64_t first_tile = (work.units * cta / work.sk_ctas) / work.nkb;
-          const int slot = (first_tile == it.sk_tile) ? 0 : 1;
+          const int slot = cta == c_first ? slot_first : 0;
           return p.sk_ws + (static_cast<size_t>(cta * 2 + slot) * Cfg::kEpiWarps + ew) * kPerWarp;
         };
         float* mine = piece(blockIdx.x) + lane;
@@ -1232,18 +1249,14 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         const int32_t n = c.n0 + static_cast<int32_t>(32u * q + lane);
         const bool col_ok = n >= c.n_begin && n < c.n_end;
         // block scaling: the scales were applied chunk by chunk
-        const float sb = Cfg::kBlockScale ? 1.0f
-                                          : (col_ok ? __ldg(p.scale_b + c.sb_off + n) : 0.0f);
+        const float sb = Cfg::kBlockScale ? 1.0f : sw_sb;
 #pragma unroll
         for (int pc = 0; pc < (Cfg::kTileN + 31) / 32; ++pc) {
           constexpr int kCols = Cfg::kTileN < 32 ? Cfg::kTileN : 32;
           const int32_t m_first = c.m0 + pc * 32;
           if (m_first >= c.zero_end) break;
           // lane j holds scale_a of row m_first + j
-          const int32_t Rl = m_first + static_cast<int32_t>(lane);
-          const float sa_l = Cfg::kBlockScale ? 1.0f
-                             : ((lane < static_cast<uint32_t>(kCols) && Rl < c.valid_end)
-                                    ? __ldg(p.scale_a + (Rl + c.srow_delta)) : 0.0f);
+          const float sa_l = Cfg::kBlockScale ? 1.0f : sw_sa[pc];
 #pragma unroll
           for (int j = 0; j < kCols; ++j) {
             const float sa = __shfl_sync(0xffffffffu, sa_l, j);
