@@ -115,6 +115,8 @@ def lib() -> ctypes.CDLL:
             L.mslkb_set_accumulation_chunk.restype = ctypes.c_int
             L.mslkb_accumulation_chunk.argtypes = []
             L.mslkb_accumulation_chunk.restype = ctypes.c_int32
+            L.mslkb_set_weight_prefetch.argtypes = [ctypes.c_int32]
+            L.mslkb_set_weight_prefetch.restype = ctypes.c_int
             L.mslkb_set_wait_timeout_us.argtypes = [i64]
             L.mslkb_set_wait_timeout_us.restype = ctypes.c_int
             L.mslkb_test_stall_next_launch.argtypes = []
@@ -246,6 +248,12 @@ def mslkb_set_accumulation_chunk(kblocks: int) -> None:
 
 def mslkb_accumulation_chunk() -> int:
     return lib().mslkb_accumulation_chunk()
+
+
+def mslkb_set_weight_prefetch(kblocks: int) -> None:
+    s = lib().mslkb_set_weight_prefetch(kblocks)
+    if s != MSLKB_OK:
+        raise MslkbError(s, "mslkb_set_weight_prefetch")
 
 
 def mslkb_set_wait_timeout_us(us: int) -> None:

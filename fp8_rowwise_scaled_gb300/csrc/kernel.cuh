@@ -77,6 +77,8 @@ struct GemmParams {
   uint64_t timeout_ns;     // give-up time of one pipeline wait
   int32_t test_stall;      // test hook: CTA 0 withholds its first stage (single-CTA TMA
                            // kernels), so its MMA wait runs out and the timeout path runs
+  int32_t prefetch_kb;     // swap-AB: K blocks of weights each CTA asks L2 to prefetch
+                           // before the dependency wait (0: none)
 };
 
 template <int kTileN_, int kStages_, bool kSwap_, bool kTma_, bool kDynamic_, int kEpiWarps_ = 4,
@@ -461,8 +463,10 @@ __device__ __forceinline__ int64_t warp_incl_scan(int64_t v, uint32_t lane) {
 }
 
 // One warp builds the scheduler tables from the [G] metadata (lane l takes a
-// contiguous chunk of groups; chunks are combined with warp scans).
-template <class Cfg>
+// contiguous chunk of groups; chunks are combined with warp scans).  kSpec: a speculative
+// build ahead of the dependency wait, whose metadata may still change -- its reads skip
+// L1 (so no stale line is left there) and it reports nothing in the status word.
+template <class Cfg, bool kSpec = false>
 __device__ void build_sched(const GemmParams& p, int32_t* rowinfo, int32_t* tile_pre,
                             uint32_t lane) {
   const int32_t G = p.G;
@@ -474,7 +478,8 @@ __device__ void build_sched(const GemmParams& p, int32_t* rowinfo, int32_t* tile
   if constexpr (Cfg::kDynamic) {
     for (int32_t g = g0; g < g1; ++g) {
       // full slabs (batched layout) read no metadata
-      int64_t v = p.meta_kind == 2 ? p.E : p.meta[g];
+      int64_t v = p.meta_kind == 2 ? p.E
+                  : (kSpec ? __ldcg(reinterpret_cast<const long long*>(p.meta) + g) : p.meta[g]);
       v = v < 0 ? 0 : (v > p.E ? p.E : v);
       rowinfo[g] = static_cast<int32_t>(v);
     }
@@ -482,10 +487,10 @@ __device__ void build_sched(const GemmParams& p, int32_t* rowinfo, int32_t* tile
     // rows of group g: m_sizes[g], or the step between successive int32 inclusive
     // offsets (offsets[-1] = 0)
     const int32_t* offs = reinterpret_cast<const int32_t*>(p.meta);
+    auto ld32 = [&](int32_t g) -> int64_t { return kSpec ? __ldcg(offs + g) : offs[g]; };
     auto count = [&](int32_t g) -> int64_t {
-      if (p.meta_kind == 1)
-        return static_cast<int64_t>(offs[g]) - (g > 0 ? static_cast<int64_t>(offs[g - 1]) : 0);
-      return p.meta[g];
+      if (p.meta_kind == 1) return ld32(g) - (g > 0 ? ld32(g - 1) : 0);
+      return kSpec ? __ldcg(reinterpret_cast<const long long*>(p.meta) + g) : p.meta[g];
     };
     // ragged layouts partition the columns (N) or the contraction (K) instead of the rows
     const int64_t total = Cfg::kRagN ? p.N : (Cfg::kRagK ? p.K : p.rows);
@@ -526,9 +531,11 @@ __device__ void build_sched(const GemmParams& p, int32_t* rowinfo, int32_t* tile
   }
   if (lane == 31) tile_pre[G] = static_cast<int32_t>(incl);
   const bool any_clamped = __any_sync(0xffffffffu, clamped);
-  if (any_clamped && lane == 0 && blockIdx.x == 0) atomicOr(p.status, kStatusClamped);
   const bool any_bad = __any_sync(0xffffffffu, bad_slice);
-  if (any_bad && lane == 0 && blockIdx.x == 0) atomicOr(p.status, kStatusBadSlice);
+  if constexpr (!kSpec) {
+    if (any_clamped && lane == 0 && blockIdx.x == 0) atomicOr(p.status, kStatusClamped);
+    if (any_bad && lane == 0 && blockIdx.x == 0) atomicOr(p.status, kStatusBadSlice);
+  }
 }
 
 // cp.async loader: one 16-byte chunk of a swizzled tile row.
@@ -631,10 +638,48 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     ptx::tc_fence_after_sync();
   }
   // Everything above is CTA-local.  With programmatic dependent launch the next kernel on
-  // the stream may begin launching now; this kernel's first global-memory access (the
-  // metadata, operands, scales, output, split workspace, status word) waits below until
-  // the kernels it depends on have completed.
+  // the stream may begin launching now; every global-memory access whose result matters
+  // (the metadata, operands, scales, output, split workspace, status word) waits for the
+  // kernels this one depends on to complete, below.
   if (threadIdx.x == 0) ptx::griddep_launch_dependents();
+  // Swap-AB plans stream weights, and with programmatic dependent launch this CTA may be
+  // resident while the kernel before it finishes.  Meanwhile the loader warp works out its
+  // first K blocks from a speculative read of the group metadata and asks L2 to prefetch
+  // their weight tiles.  Only a hint: the real schedule below reads the metadata again
+  // after the dependency wait, every load goes through L2 (coherent with whatever the
+  // earlier kernel writes), and the speculative tables live in stage memory that no load
+  // has touched yet.
+  if constexpr (Cfg::kSwap && Cfg::kTma && !Cfg::kRagged) {
+    if (warp == 0 && p.num_kb > 0 && p.prefetch_kb > 0) {
+      int32_t* s_rows = reinterpret_cast<int32_t*>(smem + Cfg::kOffW);
+      int32_t* s_tpre = s_rows + (kMaxGroups + 1);
+      build_sched<Cfg, true>(p, s_rows, s_tpre, lane);
+      __syncwarp();
+      if (lane == 0) {
+        Sched ss;
+        ss.rowinfo = s_rows;
+        ss.tile_pre = s_tpre;
+        ss.G = p.G;
+        ss.E = p.E;
+        ss.n_tiles_n = (p.N + Cfg::kWRows - 1) / Cfg::kWRows;
+        ss.total = s_tpre[p.G];
+        ss.N = p.N;
+        ss.K = p.K;
+        ss.num_kb = p.num_kb;
+        const Work w = make_work(ss.total, p.num_kb, p.split_k != 0, worker, workers);
+        int32_t budget = p.prefetch_kb;
+        for (int32_t i = 0; i < w.n_items && budget > 0; ++i) {
+          const Item it = work_item(w, i, worker, workers);
+          const TileCoord c = decode_tile<Cfg>(ss, it.tile, 0u);
+          for (int32_t kb = it.kb0; kb < it.kb1 && budget > 0; ++kb, --budget)
+            ptx::tma_prefetch_3d(&tmB, kb * kBK, c.n0, c.g);
+        }
+        // the tables' generic-proxy writes come before the first TMA write to this memory
+        ptx::fence_proxy_async_smem();
+      }
+      __syncwarp();
+    }
+  }
   ptx::griddep_wait();
   if (warp == Cfg::kEpiWarp0) build_sched<Cfg>(p, rowinfo, tile_pre, lane);
   ptx::tc_fence_before_sync();

@@ -43,6 +43,14 @@ std::atomic<int> g_forced_variant{-1};
 // K-blocks; the llama405b shape runs 2777 / 2938 / 3060 (whole K) TFLOPS at full clock.
 constexpr int kDefaultKbPerChunk = 8;
 std::atomic<int> g_kb_per_chunk{kDefaultKbPerChunk};
+// swap-AB weight prefetch ahead of the dependency wait: -1 = two rings of stages
+std::atomic<int> g_prefetch_kb{-1};
+
+int prefetch_kb_for(const VariantInfo* v) {
+  const int pf = g_prefetch_kb.load();
+  if (!v->swap || !v->tma || v->ragged) return 0;
+  return pf < 0 ? 2 * v->stages : pf;
+}
 // Split policy: 0 whole tiles only; 1 split the last waves' tiles along K over all CTAs
 // (stream-K) for swap-AB plans, where a piece's partial sums are small; 2 split every plan
 std::atomic<int> g_split_k{1};
@@ -502,6 +510,7 @@ mslkb_status run(int layout, const void* A, const void* B, const float* scale_a,
   }
   p.timeout_ns = g_wait_timeout_ns.load();
   p.test_stall = g_test_stall.exchange(0);
+  p.prefetch_kb = prefetch_kb_for(v);
   p.split_k = 0;
   if (info.split_k) {
     Workspace ws;
@@ -659,6 +668,7 @@ mslkb_status run_stacked_with_scratch(const void* A, const void* B, const float*
     p.kb_per_chunk = (kpc <= 0 || kpc > p.num_kb) ? (p.num_kb > 0 ? p.num_kb : 1) : kpc;
   }
   p.timeout_ns = g_wait_timeout_ns.load();
+  p.prefetch_kb = prefetch_kb_for(v);
   p.split_k = info.split_k;
   p.sk_ws = partials;
   p.sk_cnt = counters;
@@ -858,6 +868,12 @@ mslkb_status mslkb_set_accumulation_chunk(int32_t kblocks) {
 }
 
 int32_t mslkb_accumulation_chunk(void) { return g_kb_per_chunk.load(); }
+
+mslkb_status mslkb_set_weight_prefetch(int32_t kblocks) {
+  if (kblocks < -1) return MSLKB_ERR_SHAPE;
+  g_prefetch_kb.store(kblocks);
+  return MSLKB_OK;
+}
 
 mslkb_status mslkb_set_wait_timeout_us(int64_t us) {
   if (us < 0) return MSLKB_ERR_SHAPE;

@@ -141,6 +141,16 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// Asks L2 to fetch one tile of a 3D tensor map (a hint: nothing lands in shared memory
+// and no barrier is signalled).
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int32_t x, int32_t y,
+                                                int32_t z) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+
 // Paired-CTA loads: the tile lands in this CTA's shared memory and its bytes complete
 // on `bar`, a shared::cluster address that may be the peer CTA's barrier (the pair's
 // leader counts both CTAs' bytes on its own barrier).

@@ -354,6 +354,18 @@ MSLKB_API mslkb_status mslkb_set_accumulation_chunk(int32_t kblocks);
 MSLKB_API int32_t mslkb_accumulation_chunk(void);
 
 /*
+ * Weight prefetch of the swap-AB (few rows per group) plans.  With programmatic dependent
+ * launch a CTA can be resident while the kernel before it on the stream finishes; in that
+ * time it reads the group metadata speculatively, works out its first `kblocks` K blocks
+ * of weights and asks L2 to prefetch them.  A hint only: the schedule is rebuilt from the
+ * metadata after the dependency wait, and every load reads L2, which is coherent with
+ * what the earlier kernel writes.  -1 (default): twice the kernel's stage count; 0: off.
+ * Applies to every following call from any thread; a tuning and test hook.  Values
+ * below -1 give MSLKB_ERR_SHAPE.
+ */
+MSLKB_API mslkb_status mslkb_set_weight_prefetch(int32_t kblocks);
+
+/*
  * Failure detection (an addition of this library; the pages have no counterpart).  Every
  * wait of the kernels' pipelines is bounded: a wait that runs past the limit (default
  * ~1 s) makes the kernel give up, record MSLKB_DEV_TIMEOUT in the device status word, let
