@@ -126,7 +126,11 @@ struct KernelCfg {
   // Budget: launched with 384 x 168 registers = 128 x 40 + 256 x 232; per SM sub-partition
   // one warpgroup-0 warp and two epilogue warps: (40 + 232 + 232) x 32 <= 16384.
   static constexpr bool kRegSplit = kTma && !kSwap && kEpiWarps == 8 && kTileN == 256;
-  static constexpr int kIdleWarps = kRegSplit ? 2 : 0;
+  // Swap-AB plans (weight streaming) carry one more warp, which prefetches the CTA's first
+  // weight tiles into L2 while the kernel before it on the stream finishes (below)
+  static constexpr bool kSpecWarp = kSwap && kTma && !kRagged;
+  static constexpr int kIdleWarps = kRegSplit ? 2 : (kSpecWarp ? 1 : 0);
+  static constexpr int kSpecWarpIdx = kLoaderWarps + 1;
   static constexpr int kEpiWarp0 = kLoaderWarps + 1 + kIdleWarps;
   static constexpr int kThreads = 32 * (kLoaderWarps + 1 + kIdleWarps + kEpiWarps);
   static constexpr int kLaunchRegs = kRegSplit ? 168 : 0;  // required at launch (0: any)
@@ -164,7 +168,9 @@ struct KernelCfg {
   static constexpr int kOffWork = kOffMisc + 16;           // the CTA's Work (below)
   static constexpr int kOffSched = kOffWork + 64;
   static constexpr int kSchedBytes = 2 * 4 * (kMaxGroups + 1);
-  static constexpr int kSmemBytes = kOffSched + kSchedBytes + 1024;  // + alignment slack
+  static constexpr int kOffSpec = kOffSched + kSchedBytes;  // the prefetch warp's tables
+  static constexpr int kSmemBytes =
+      kOffSpec + (kSpecWarp ? kSchedBytes : 0) + 1024;  // + alignment slack
 
   static_assert(kTileN % 16 == 0 && kTileN >= 16 && kTileN <= 256, "MMA N for M = 128");
   static_assert(kActBytes % 1024 == 0 && kWBytes % 1024 == 0, "swizzle atoms");
@@ -643,15 +649,17 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
   // kernels this one depends on to complete, below.
   if (threadIdx.x == 0) ptx::griddep_launch_dependents();
   // Swap-AB plans stream weights, and with programmatic dependent launch this CTA may be
-  // resident while the kernel before it finishes.  Meanwhile the loader warp works out its
-  // first K blocks from a speculative read of the group metadata and asks L2 to prefetch
-  // their weight tiles.  Only a hint: the real schedule below reads the metadata again
-  // after the dependency wait, every load goes through L2 (coherent with whatever the
-  // earlier kernel writes), and the speculative tables live in stage memory that no load
-  // has touched yet.
-  if constexpr (Cfg::kSwap && Cfg::kTma && !Cfg::kRagged) {
-    if (warp == 0 && p.num_kb > 0 && p.prefetch_kb > 0) {
-      int32_t* s_rows = reinterpret_cast<int32_t*>(smem + Cfg::kOffW);
+  // resident while the kernel before it finishes.  Meanwhile the prefetch warp works out
+  // the CTA's first K blocks from a speculative read of the group metadata and asks L2 to
+  // prefetch their weight tiles.  Only a hint: the real schedule below reads the metadata
+  // again after the dependency wait, and every load goes through L2 (coherent with
+  // whatever the earlier kernel writes).  The warp keeps its own tables and takes no part
+  // in the setup barriers, so a CTA that starts late is not held up by it; its next and
+  // last barrier is the teardown's.
+  const bool spec_warp = Cfg::kSpecWarp && warp == static_cast<uint32_t>(Cfg::kSpecWarpIdx);
+  if constexpr (Cfg::kSpecWarp) {
+    if (spec_warp && p.num_kb > 0 && p.prefetch_kb > 0) {
+      int32_t* s_rows = reinterpret_cast<int32_t*>(smem + Cfg::kOffSpec);
       int32_t* s_tpre = s_rows + (kMaxGroups + 1);
       build_sched<Cfg, true>(p, s_rows, s_tpre, lane);
       __syncwarp();
@@ -674,18 +682,24 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
           for (int32_t kb = it.kb0; kb < it.kb1 && budget > 0; ++kb, --budget)
             ptx::tma_prefetch_3d(&tmB, kb * kBK, c.n0, c.g);
         }
-        // the tables' generic-proxy writes come before the first TMA write to this memory
-        ptx::fence_proxy_async_smem();
       }
       __syncwarp();
     }
   }
-  ptx::griddep_wait();
+  // setup barriers: every warp but the prefetch warp
+  auto setup_sync = [&]() {
+    if constexpr (Cfg::kSpecWarp) {
+      if (!spec_warp) ptx::named_bar_sync(1, Cfg::kThreads - 32);
+    } else {
+      __syncthreads();
+    }
+  };
+  if (!spec_warp) ptx::griddep_wait();
   if (warp == Cfg::kEpiWarp0) build_sched<Cfg>(p, rowinfo, tile_pre, lane);
   ptx::tc_fence_before_sync();
-  __syncthreads();
+  setup_sync();
   ptx::tc_fence_after_sync();
-  const uint32_t tmem_base = *tmem_holder;
+  const uint32_t tmem_base = spec_warp ? 0u : *tmem_holder;
 
   Sched sched;
   sched.rowinfo = rowinfo;
@@ -693,7 +707,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
   sched.G = p.G;
   sched.E = p.E;
   sched.n_tiles_n = (p.N + Cfg::kWRows - 1) / Cfg::kWRows;
-  sched.total = tile_pre[p.G];
+  sched.total = spec_warp ? 0 : tile_pre[p.G];
   sched.N = p.N;
   sched.K = p.K;
   sched.num_kb = p.num_kb;
@@ -703,11 +717,12 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
   if (threadIdx.x == 0)
     *work_smem = make_work(sched.total, p.num_kb, p.split_k != 0 && !Cfg::kPair && !Cfg::kRagged,
                            worker, workers);
-  __syncthreads();
+  setup_sync();
   const Work& work = *work_smem;
 
   if (warp < static_cast<uint32_t>(Cfg::kEpiWarp0)) {
-  // producer side: loader warp(s), MMA warp and (register split) two idle warps
+  // producer side: loader warp(s), MMA warp, and idle warps (register split: two; the
+  // prefetch warp, whose work is done)
   if constexpr (Cfg::kRegSplit) ptx::setmaxnreg_dec<Cfg::kRegsLow>();
   if (warp < static_cast<uint32_t>(Cfg::kLoaderWarps)) {
     // ------------------------------------------------------------------ loader

@@ -223,7 +223,7 @@ def test_plan_per_workload(L, name, expect):
     assert fx.variant_name(info.variant) == expect
     assert 1 <= info.grid <= GB300_SMS
     assert info.smem_bytes <= 232448
-    assert info.threads in (192, 320, 384, 416)
+    assert info.threads in (192, 224, 320, 384, 416)
 
 
 def test_plan_copy_width(L):
