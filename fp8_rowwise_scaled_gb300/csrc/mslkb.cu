@@ -43,13 +43,17 @@ std::atomic<int> g_forced_variant{-1};
 // K-blocks; the llama405b shape runs 2777 / 2938 / 3060 (whole K) TFLOPS at full clock.
 constexpr int kDefaultKbPerChunk = 8;
 std::atomic<int> g_kb_per_chunk{kDefaultKbPerChunk};
-// swap-AB weight prefetch ahead of the dependency wait: -1 = two rings of stages
+// swap-AB weight prefetch ahead of the dependency wait, in K blocks (16 KB of weights each)
+// per CTA; -1 = the default.  Measured on GB300 (back-to-back calls, llama3-70b shapes):
+// 14 blocks (224 KB per CTA, 34 MB over 152 SMs: about what HBM delivers while a CTA
+// waits) beat 4-11 and 17-22 at total_M = 1 and tie the best at 16 and 128 rows.
+constexpr int kDefaultPrefetchKb = 14;
 std::atomic<int> g_prefetch_kb{-1};
 
 int prefetch_kb_for(const VariantInfo* v) {
   const int pf = g_prefetch_kb.load();
   if (!v->swap || !v->tma || v->ragged) return 0;
-  return pf < 0 ? 2 * v->stages : pf;
+  return pf < 0 ? kDefaultPrefetchKb : pf;
 }
 // Split policy: 0 whole tiles only; 1 split the last waves' tiles along K over all CTAs
 // (stream-K) for swap-AB plans, where a piece's partial sums are small; 2 split every plan

@@ -359,7 +359,8 @@ MSLKB_API int32_t mslkb_accumulation_chunk(void);
  * time it reads the group metadata speculatively, works out its first `kblocks` K blocks
  * of weights and asks L2 to prefetch them.  A hint only: the schedule is rebuilt from the
  * metadata after the dependency wait, and every load reads L2, which is coherent with
- * what the earlier kernel writes.  -1 (default): twice the kernel's stage count; 0: off.
+ * what the earlier kernel writes.  -1: the default, 14 K blocks (224 KB of weights per
+ * CTA); 0: off.
  * Applies to every following call from any thread; a tuning and test hook.  Values
  * below -1 give MSLKB_ERR_SHAPE.
  */
