@@ -117,6 +117,8 @@ def lib() -> ctypes.CDLL:
             L.mslkb_accumulation_chunk.restype = ctypes.c_int32
             L.mslkb_set_weight_prefetch.argtypes = [ctypes.c_int32]
             L.mslkb_set_weight_prefetch.restype = ctypes.c_int
+            L.mslkb_test_speculate_from_next_launch.argtypes = [ctypes.c_void_p]
+            L.mslkb_test_speculate_from_next_launch.restype = ctypes.c_int
             L.mslkb_set_wait_timeout_us.argtypes = [i64]
             L.mslkb_set_wait_timeout_us.restype = ctypes.c_int
             L.mslkb_test_stall_next_launch.argtypes = []
@@ -260,6 +262,12 @@ def mslkb_set_wait_timeout_us(us: int) -> None:
     s = lib().mslkb_set_wait_timeout_us(us)
     if s != MSLKB_OK:
         raise MslkbError(s, "mslkb_set_wait_timeout_us")
+
+
+def mslkb_test_speculate_from_next_launch(meta) -> None:
+    """Test hook: the next launch's speculative weight prefetch reads `meta` (a device
+    tensor laid out like that call's metadata) instead of the call's own metadata."""
+    lib().mslkb_test_speculate_from_next_launch(ctypes.c_void_p(meta.data_ptr()))
 
 
 def mslkb_test_stall_next_launch() -> None:

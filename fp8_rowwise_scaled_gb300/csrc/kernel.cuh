@@ -79,6 +79,8 @@ struct GemmParams {
                            // kernels), so its MMA wait runs out and the timeout path runs
   int32_t prefetch_kb;     // swap-AB: K blocks of weights each CTA asks L2 to prefetch
                            // before the dependency wait (0: none)
+  const int64_t* spec_meta;  // metadata the speculative schedule reads (= meta, unless a
+                             // test points it elsewhere)
 };
 
 template <int kTileN_, int kStages_, bool kSwap_, bool kTma_, bool kDynamic_, int kEpiWarps_ = 4,
@@ -475,6 +477,7 @@ __device__ __forceinline__ int64_t warp_incl_scan(int64_t v, uint32_t lane) {
 template <class Cfg, bool kSpec = false>
 __device__ void build_sched(const GemmParams& p, int32_t* rowinfo, int32_t* tile_pre,
                             uint32_t lane) {
+  const int64_t* meta = kSpec ? p.spec_meta : p.meta;
   const int32_t G = p.G;
   const int32_t per = (G + 31) / 32;
   const int32_t g0 = min(G, static_cast<int32_t>(lane) * per);
@@ -485,18 +488,18 @@ __device__ void build_sched(const GemmParams& p, int32_t* rowinfo, int32_t* tile
     for (int32_t g = g0; g < g1; ++g) {
       // full slabs (batched layout) read no metadata
       int64_t v = p.meta_kind == 2 ? p.E
-                  : (kSpec ? __ldcg(reinterpret_cast<const long long*>(p.meta) + g) : p.meta[g]);
+                  : (kSpec ? __ldcg(reinterpret_cast<const long long*>(meta) + g) : meta[g]);
       v = v < 0 ? 0 : (v > p.E ? p.E : v);
       rowinfo[g] = static_cast<int32_t>(v);
     }
   } else {
     // rows of group g: m_sizes[g], or the step between successive int32 inclusive
     // offsets (offsets[-1] = 0)
-    const int32_t* offs = reinterpret_cast<const int32_t*>(p.meta);
+    const int32_t* offs = reinterpret_cast<const int32_t*>(meta);
     auto ld32 = [&](int32_t g) -> int64_t { return kSpec ? __ldcg(offs + g) : offs[g]; };
     auto count = [&](int32_t g) -> int64_t {
       if (p.meta_kind == 1) return ld32(g) - (g > 0 ? ld32(g - 1) : 0);
-      return kSpec ? __ldcg(reinterpret_cast<const long long*>(p.meta) + g) : p.meta[g];
+      return kSpec ? __ldcg(reinterpret_cast<const long long*>(meta) + g) : meta[g];
     };
     // ragged layouts partition the columns (N) or the contraction (K) instead of the rows
     const int64_t total = Cfg::kRagN ? p.N : (Cfg::kRagK ? p.K : p.rows);

@@ -31,6 +31,8 @@ constexpr int kMaxDevices = 64;
 constexpr uint64_t kWaitTimeoutNs = 1000000000ull;  // one pipeline wait gives up after ~1 s
 std::atomic<uint64_t> g_wait_timeout_ns{kWaitTimeoutNs};
 std::atomic<int> g_test_stall{0};  // one-shot: the next launch of run() withholds a stage
+// one-shot: the next launch's speculative schedule reads this metadata instead
+std::atomic<const void*> g_test_spec_meta{nullptr};
 
 __device__ uint32_t g_device_status;  // MSLKB_DEV_* bits, per device
 
@@ -515,6 +517,10 @@ mslkb_status run(int layout, const void* A, const void* B, const float* scale_a,
   p.timeout_ns = g_wait_timeout_ns.load();
   p.test_stall = g_test_stall.exchange(0);
   p.prefetch_kb = prefetch_kb_for(v);
+  {
+    const void* spec = g_test_spec_meta.exchange(nullptr);
+    p.spec_meta = static_cast<const int64_t*>(spec != nullptr ? spec : p.meta);
+  }
   p.split_k = 0;
   if (info.split_k) {
     Workspace ws;
@@ -673,6 +679,7 @@ mslkb_status run_stacked_with_scratch(const void* A, const void* B, const float*
   }
   p.timeout_ns = g_wait_timeout_ns.load();
   p.prefetch_kb = prefetch_kb_for(v);
+  p.spec_meta = p.meta;
   p.split_k = info.split_k;
   p.sk_ws = partials;
   p.sk_cnt = counters;
@@ -883,6 +890,11 @@ mslkb_status mslkb_set_wait_timeout_us(int64_t us) {
   if (us < 0) return MSLKB_ERR_SHAPE;
   if (us > 0 && us < 1000) return MSLKB_ERR_SHAPE;  // at least 1 ms
   g_wait_timeout_ns.store(us == 0 ? kWaitTimeoutNs : static_cast<uint64_t>(us) * 1000ull);
+  return MSLKB_OK;
+}
+
+mslkb_status mslkb_test_speculate_from_next_launch(const void* meta) {
+  g_test_spec_meta.store(meta);
   return MSLKB_OK;
 }
 

@@ -367,6 +367,14 @@ MSLKB_API int32_t mslkb_accumulation_chunk(void);
 MSLKB_API mslkb_status mslkb_set_weight_prefetch(int32_t kblocks);
 
 /*
+ * Test hook for the weight prefetch: the next launch through the stacked, dynamic or
+ * offsets entry points builds its speculative schedule from `meta` (a device buffer laid
+ * out like that call's own metadata, G entries) instead of the call's metadata, so that
+ * the prefetch goes to other tiles than the call computes.  The results must not change.
+ */
+MSLKB_API mslkb_status mslkb_test_speculate_from_next_launch(const void* meta);
+
+/*
  * Failure detection (an addition of this library; the pages have no counterpart).  Every
  * wait of the kernels' pipelines is bounded: a wait that runs past the limit (default
  * ~1 s) makes the kernel give up, record MSLKB_DEV_TIMEOUT in the device status word, let

@@ -437,6 +437,36 @@ def test_dynamic_split_tiles(orc):
         fx.mslkb_set_split_k(1)
 
 
+@pytest.mark.parametrize("layout", ["stacked", "dynamic"])
+def test_weight_prefetch_is_only_a_hint(orc, layout):
+    """Swap-AB plans prefetch weights from a speculative schedule ahead of the dependency
+    wait.  The results are bit-identical with the prefetch off, and with the speculation
+    reading other metadata -- rows moved to other groups, or counts out of every range --
+    so that it prefetches tiles the call never computes."""
+    G, N, K = 8, 1024, 4096
+    if layout == "stacked":
+        prob = _rand_problem("stacked", G, N, K, [0, 3, 0, 9, 1, 0, 16, 2], seed=41)
+        fakes = [[31, 0, 0, 0, 0, 0, 0, 0], [2**40, -7, 2**62, 0, -1, 5, 0, 2**33]]
+    else:
+        prob = _rand_problem("dynamic", G, N, K, [0, 5, 16, 1, 0, 7, 3, 12], E=16, seed=42)
+        fakes = [[16, 0, 0, 0, 16, 16, 0, 0], [-3, 2**40, 99, -2**50, 0, 17, 2**31, 1]]
+    v = f"{layout}_swap_w128xa16_tma"
+    base, _ = _check_full(prob, orc, variant=v, what=f"{layout} prefetch on")
+    fx.mslkb_set_weight_prefetch(0)
+    try:
+        off = bits_of(prob.run_gpu(variant=v)).reshape(base.shape)
+    finally:
+        fx.mslkb_set_weight_prefetch(-1)
+    assert np.array_equal(base, off), f"{layout}: prefetch changed the result"
+    for fake in fakes:
+        f = torch.tensor(fake, dtype=torch.int64, device="cuda")
+        fx.mslkb_test_speculate_from_next_launch(f)
+        got = bits_of(prob.run_gpu(variant=v)).reshape(base.shape)
+        torch.cuda.synchronize()
+        assert np.array_equal(base, got), f"{layout}: speculation from {fake} leaked"
+    assert fx.device_status() == 0
+
+
 def test_empty_problems_are_noops():
     dev = torch.empty(16, dtype=torch.uint8, device="cuda")
     p = dev.data_ptr()
