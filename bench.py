@@ -26,6 +26,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import math
 import os
@@ -58,12 +59,20 @@ def peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+# string and character literals (kept), // and /* */ comments (dropped)
+_CODE_TOKENS = re.compile(r'"(?:\\.|[^"\\])*"|\'(?:\\.|[^\'\\])*\'|//[^\n]*|/\*.*?\*/', re.S)
+
+
 def kernel_source_hash() -> str:
+    """Hash of the kernel sources' code: comments and whitespace do not count, so a
+    committed traffic capture stays valid across documentation edits."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "fp8_rowwise_scaled_gb300", "csrc")
     for name in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(name.encode() + f.read())
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
+            text = f.read()
+        code = _CODE_TOKENS.sub(lambda m: m.group(0) if m.group(0)[0] in "\"'" else " ", text)
+        h.update(name.encode() + " ".join(code.split()).encode())
     return h.hexdigest()[:16]
 
 

@@ -11,10 +11,13 @@
 //   loader warp(s)   TMA (one elected thread) or cp.async (4 warps) fill an S-stage
 //                    ring of 128-byte-swizzled shared-memory tiles (full/empty mbarriers)
 //   MMA warp         allocates TMEM; one thread issues tcgen05.mma (K = 32 per
-//                    instruction, 4 per 128-byte stage) into one of two TMEM
-//                    accumulators, and tcgen05.commit releases stages / accumulators
-//   4 epilogue warps tcgen05.ld the accumulator, scale, convert to bf16, store with
-//                    row / column predicates; padding rows get +0.0
+//                    instruction, 4 per 128-byte stage) into a ring of 2-8 TMEM
+//                    accumulator buffers (kNumAcc), and tcgen05.commit releases stages
+//                    and buffers
+//   prefetch warp    (swap-AB plans) asks L2 for the CTA's first weight tiles while the
+//                    kernel before it on the stream finishes
+//   4/8 epilogue     tcgen05.ld the accumulator, scale, convert to bf16, store with
+//   warps            row / column predicates; padding rows get +0.0
 //
 // Group/tile scheduler (MSLK #471, commits on the packed and padded layouts and on the
 // group resolution step): each CTA reads the [G] metadata once, prefix-sums it in shared
@@ -866,7 +869,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     if (lane == 0 && has_k && crank == 0) {
       int stage = 0;
       uint32_t phase = 0;
-      uint32_t chunk = 0;  // chunks issued by this CTA: buffer = chunk & 1
+      uint32_t chunk = 0;  // chunks issued by this CTA: buffer = chunk % kNumAcc
       bool ok = true;
       const int32_t kpc = p.kb_per_chunk;
       for (int32_t i = 0; ok && i < work.n_items; ++i) {
