@@ -210,6 +210,7 @@ struct TileCoord {
   int32_t sb_off;     // scale_b index of column 0 of the group
   int32_t k0;         // first K element of the contraction
   int32_t k_len;      // K elements of the contraction
+  int32_t k_skip;     // ragged K: elements of the first K block before the slice starts
   int32_t nkb;        // K blocks of the contraction
 };
 
@@ -302,6 +303,7 @@ __device__ __forceinline__ TileCoord decode_tile(const Sched& s, int32_t t, uint
       c.sb_off = 0;
       c.k0 = 0;
       c.k_len = s.K;
+      c.k_skip = 0;
       c.nkb = s.num_kb;
     } else {
       // A rows shared by the groups; output slab g and scales of group g; the K slice
@@ -313,10 +315,15 @@ __device__ __forceinline__ TileCoord decode_tile(const Sched& s, int32_t t, uint
       c.n_begin = 0;
       c.n_end = s.N;
       c.sb_off = g * s.N;
-      c.k0 = lo_g;
-      // a slice whose bounds are off the 16-element TMA grid is not computed (+0.0)
+      // a slice whose bounds are off the 16-element TMA grid is not computed (+0.0).  The
+      // K blocks are loaded from the 128-element boundary at or below the slice start
+      // (TMA boxes that start inside a 128-byte line fetch two lines per row: measured 26 %
+      // slower on the weight-gradient shape); the MMA skips what lies before the slice in
+      // the first block and past it in the last.
       c.k_len = ((lo_g | hi_g) & 15) ? 0 : hi_g - lo_g;
-      c.nkb = (c.k_len + kBK - 1) / kBK;
+      c.k0 = lo_g & ~(kBK - 1);
+      c.k_skip = c.k_len > 0 ? lo_g - c.k0 : 0;
+      c.nkb = c.k_len > 0 ? (c.k_skip + c.k_len + kBK - 1) / kBK : 0;
     }
     c.bz = 0;
     return c;
@@ -334,6 +341,7 @@ __device__ __forceinline__ TileCoord decode_tile(const Sched& s, int32_t t, uint
   c.sb_off = g * s.N;
   c.k0 = 0;
   c.k_len = s.K;
+  c.k_skip = 0;
   c.nkb = s.num_kb;
   const int32_t base = Cfg::kDynamic ? g * s.E : s.rowinfo[g];
   if constexpr (Cfg::kPair) {
@@ -548,6 +556,34 @@ __device__ void build_sched(const GemmParams& p, int32_t* rowinfo, int32_t* tile
     if (any_clamped && lane == 0 && blockIdx.x == 0) atomicOr(p.status, kStatusClamped);
     if (any_bad && lane == 0 && blockIdx.x == 0) atomicOr(p.status, kStatusBadSlice);
   }
+}
+
+// Ragged K, the first K block of a slice that starts `lo` bytes into it and ends at `hi`
+// (<= 128): the block was loaded from the 128-byte boundary below the slice start, and
+// before lo and past hi lie other groups' K (or TMA zero fill).  Whole 32-byte steps
+// outside [lo, hi) are not issued; in a half-used step the unused 16 bytes of every row of
+// both operands are zeroed first (slices start and end on a 16-element boundary; both
+// operands, since 0 x NaN is NaN; 128-byte swizzle: chunk c of row r sits at c ^ (r & 7)).
+// The first issued step overwrites the accumulator.  Out of line: once per tile, off the
+// MMA thread's per-block path.
+template <class Cfg>
+__device__ __noinline__ void mma_ragk_first_block(uint32_t d_tmem, uint64_t a_desc,
+                                                  uint64_t b_desc, uint32_t sa_base,
+                                                  uint32_t sw_base, int32_t lo, int32_t hi) {
+  auto zero_chunk = [&](uint32_t chunk) {
+    for (int row = 0; row < Cfg::kActRows; ++row)
+      ptx::st_shared_v4(sa_base + row * 128u + ((chunk ^ (row & 7u)) << 4), 0u, 0u, 0u, 0u);
+    for (int row = 0; row < Cfg::kWRows; ++row)
+      ptx::st_shared_v4(sw_base + row * 128u + ((chunk ^ (row & 7u)) << 4), 0u, 0u, 0u, 0u);
+  };
+  if (lo & 16) zero_chunk(static_cast<uint32_t>(lo >> 4) - 1u);
+  if (hi & 16) zero_chunk(static_cast<uint32_t>(hi >> 4));
+  if ((lo | hi) & 16) ptx::fence_proxy_async_smem();
+  const int k_first = lo / 32;
+  const int k_end = (hi + 31) / 32;
+  for (int k = k_first; k < k_end; ++k)
+    ptx::mma_f8f6f4(d_tmem, a_desc + 2u * k, b_desc + 2u * k, Cfg::kIdesc,
+                    k > k_first ? 1u : 0u);
 }
 
 // cp.async loader: one 16-byte chunk of a swizzled tile row.
@@ -879,11 +915,13 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
           if (decode_tile<Cfg>(sched, it.tile, 0u).half) idesc = Cfg::kIdescHalf;
         }
         int32_t kb_end = it.kb1;
-        int32_t k_len = 0;
+        int32_t k_len = 0;  // ragged K: the slice, counted from the first block's start
+        int32_t k_skip = 0;
         if constexpr (Cfg::kRagK) {
           const TileCoord c = decode_tile<Cfg>(sched, it.tile, 0u);
           kb_end = c.nkb;
-          k_len = c.k_len;
+          k_skip = c.k_skip;
+          k_len = c.k_skip + c.k_len;
         }
         for (int32_t kb0 = it.kb0; ok && kb0 < kb_end; kb0 += kpc) {
           const int buf = static_cast<int>(chunk % Cfg::kNumAcc);
@@ -907,6 +945,19 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
             const uint64_t a_desc = Cfg::kSwap ? w_desc : act_desc;
             const uint64_t b_desc = Cfg::kSwap ? act_desc : w_desc;
             int nmma = kBK / 32;
+            if (Cfg::kRagK && kb == 0 && k_skip != 0) {
+              // a slice that starts inside its first block: that block's MMAs come from
+              // the out-of-line edge path
+              mma_ragk_first_block<Cfg>(d_tmem, a_desc, b_desc, s_act + stage * Cfg::kActBytes,
+                                        s_w + stage * Cfg::kWBytes, k_skip,
+                                        min(kBK, k_len));
+              ptx::mma_commit(empty_bar(stage));
+              if (++stage == Cfg::kStages) {
+                stage = 0;
+                phase ^= 1u;
+              }
+              continue;
+            }
             if constexpr (Cfg::kRagK) {
               // the last block of a K slice: the bytes past the slice belong to the next
               // group (or are TMA zero fill past total_K).  Whole 32-byte steps past it are

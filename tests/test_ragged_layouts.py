@@ -147,6 +147,29 @@ def test_ragged_k_next_group_data_never_leaks(orc):
     compare(got.ravel(), ref.ravel(), ab.ravel(), "ragged K with poisoned neighbours")
 
 
+def test_ragged_k_previous_group_data_never_leaks(orc):
+    # group 0's slice [0, 48) ends in NaN codes over [32, 48); group 1's slice [48, 96)
+    # starts half-way through the 32-byte MMA step over [32, 64) of the block that is
+    # loaded from K = 0, so any use of the bytes before its start would turn group 1's
+    # results into NaN (group 0's own results are NaN, as the oracle's are)
+    G, M, N, total_K = 3, 130, 264, 512
+    ks = [48, 48, 416]
+    A, B, sa, sb = _data(5, (M, total_K), (N, total_K), G * M, G * N)
+    A[:, 32:48] = 0x7F
+    B[:, 40:48] = 0xFF
+    off = np.cumsum(ks).astype(np.int32)
+    tA, tB, tsa, tsb, toff = _cuda(A, B, sa, sb, off)
+    out = fx.f8f8bf16_rowwise_grouped_k_offsets(tA, tB, tsa, tsb, toff)
+    torch.cuda.synchronize()
+    got = bits_of(out).reshape(G * M, N)
+    ref, _ = orc.k_offsets(A, B, sa.reshape(G, M), sb.reshape(G, N), off)
+    ab, _ = orc.k_offsets(abs_codes(A), abs_codes(B), np.abs(sa).reshape(G, M),
+                          np.abs(sb).reshape(G, N), off)
+    assert np.isnan(oracle.bf16_bits_to_float(ref[:M])).all()
+    assert not np.isnan(oracle.bf16_bits_to_float(ref[M:])).any()
+    compare(got.ravel(), ref.ravel(), ab.ravel(), "ragged K after poisoned neighbours")
+
+
 def test_ragged_k_bad_slice_is_zero_and_flagged(orc):
     # a slice ending off the 16-element grid: that group is not computed (+0.0) and the
     # status bit is set; the other groups are unaffected
