@@ -991,9 +991,11 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                 ptx::mma_f8f6f4(d_tmem, a_desc + 2u * k, b_desc + 2u * k, Cfg::kIdesc,
                                 (kb > kb0 || k > 0) ? 1u : 0u);
             }
-            // pairs: the stage is free in both CTAs once the MMAs reading it complete
+            // pairs: the stage is free in both CTAs once the MMAs reading it complete.
+            // Block scaling (one K block = one stage per chunk) has one commit per block:
+            // the epilogue frees the stage once it sees the chunk's accumulator commit.
             if constexpr (Cfg::kPair) ptx::mma_commit_pair(empty_bar(stage), 0x3);
-            else ptx::mma_commit(empty_bar(stage));
+            else if constexpr (!Cfg::kBlockScale) ptx::mma_commit(empty_bar(stage));
             if (++stage == Cfg::kStages) {
               stage = 0;
               phase ^= 1u;
@@ -1160,6 +1162,12 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
           if (!wait_bar(tfull_bar(buf), use & 1u, abort_flag, p.status, p.timeout_ns)) {
             ok = false;
             break;
+          }
+          // block scaling: chunk c is K block c of this CTA and lives in stage c % kStages,
+          // whose MMAs have completed -- one lane frees the stage for the loader
+          if constexpr (Cfg::kBlockScale) {
+            if (ew == 0 && lane == 0)
+              ptx::mbar_arrive(empty_bar(static_cast<int>(chunk % Cfg::kStages)));
           }
           ptx::tc_fence_after_sync();
           if (warp_any) {
