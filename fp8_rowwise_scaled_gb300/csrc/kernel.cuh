@@ -144,14 +144,21 @@ struct KernelCfg {
   // accumulator columns one epilogue thread owns (and keeps in fp32 registers)
   static constexpr int kThreadCols = kSwap ? kTileN : kTileN / (kEpiWarps / 4);
   static constexpr int kAccCols = kTileN;  // fp32 TMEM columns of one accumulator
-  // TMEM accumulator buffers the MMA can run ahead of the epilogue by: two for 256-column
-  // accumulators (all 512 columns), more for narrower ones (up to 8: swap-AB tiles drain
-  // every K block under block scaling and need the slack)
-  static constexpr int kNumAcc = (kAccCols >= 256) ? 2 : (kAccCols >= 128) ? 4 : 8;
-  static constexpr int kTmemCols = (kNumAcc * kAccCols <= 32)    ? 32
-                                   : (kNumAcc * kAccCols <= 64)  ? 64
-                                   : (kNumAcc * kAccCols <= 128) ? 128
-                                   : (kNumAcc * kAccCols <= 256) ? 256
+  // K blocks per chunk under block scaling, each summed into an accumulator of its own (so
+  // that each gets its own scales): the swap-AB tiles put two side by side in a chunk
+  // buffer and so commit and hand over once per two blocks; 128-row tiles fill TMEM with
+  // one.  Without block scaling a chunk buffer is one accumulator summing
+  // GemmParams::kb_per_chunk blocks.
+  static constexpr int kBSSub = (kBlockScale && kSwap) ? 2 : 1;
+  static constexpr int kBufCols = kAccCols * kBSSub;  // fp32 TMEM columns of a chunk buffer
+  // TMEM chunk buffers the MMA can run ahead of the epilogue by: two for 256-column
+  // buffers (all 512 columns), more for narrower ones (up to 8: the swap-AB tiles, which
+  // under block scaling hand over a buffer every one or two K blocks and need the slack)
+  static constexpr int kNumAcc = (kBufCols >= 256) ? 2 : (kBufCols >= 128) ? 4 : 8;
+  static constexpr int kTmemCols = (kNumAcc * kBufCols <= 32)    ? 32
+                                   : (kNumAcc * kBufCols <= 64)  ? 64
+                                   : (kNumAcc * kBufCols <= 128) ? 128
+                                   : (kNumAcc * kBufCols <= 256) ? 256
                                                                  : 512;
   static constexpr int kCpLag = kStages - 2;  // cp.async groups kept in flight per thread
   static constexpr uint32_t kIdesc = ptx::idesc_e4m3_f32(kMmaM * kCtas, kTileN);
@@ -181,7 +188,7 @@ struct KernelCfg {
   static_assert(kActBytes % 1024 == 0 && kWBytes % 1024 == 0, "swizzle atoms");
   static_assert(kStages >= 3, "pipeline depth");
   static_assert(kSmemBytes <= 232448, "shared memory per CTA");
-  static_assert(kNumAcc * kAccCols <= 512, "the accumulators must fit TMEM");
+  static_assert(kNumAcc * kBufCols <= 512, "the accumulators must fit TMEM");
   static_assert(kEpiWarps == 4 || (kEpiWarps == 8 && !kSwap), "epilogue warp split");
   static_assert(!kPair || (kTma && !kSwap && kTileN == 256), "CTA pairs: 256 x 256 tiles, TMA");
   static_assert(!kRagged || (kTma && !kPair && !kDynamic), "ragged layouts: TMA, single CTAs");
@@ -907,7 +914,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
       uint32_t phase = 0;
       uint32_t chunk = 0;  // chunks issued by this CTA: buffer = chunk % kNumAcc
       bool ok = true;
-      const int32_t kpc = p.kb_per_chunk;
+      const int32_t kpc = Cfg::kBlockScale ? Cfg::kBSSub : p.kb_per_chunk;
       for (int32_t i = 0; ok && i < work.n_items; ++i) {
         const Item it = work_item(work, i, worker, workers);
         uint32_t idesc = Cfg::kIdesc;
@@ -932,13 +939,18 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
             break;
           }
           ptx::tc_fence_after_sync();
-          const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * Cfg::kAccCols);
+          const uint32_t d_buf = tmem_base + static_cast<uint32_t>(buf * Cfg::kBufCols);
           const int32_t kb1 = min(kb_end, kb0 + kpc);
           for (int32_t kb = kb0; kb < kb1; ++kb) {
             if (!wait_bar(full_bar(stage), phase, abort_flag, p.status, p.timeout_ns)) {
               ok = false;
               break;
             }
+            // block scaling: K block kb0 + j sums into sub-accumulator j of the buffer, from
+            // zero; otherwise the chunk's blocks all add into the one accumulator
+            const uint32_t d_tmem =
+                d_buf + (Cfg::kBlockScale ? static_cast<uint32_t>((kb - kb0) * Cfg::kAccCols) : 0u);
+            const bool first_of_acc = Cfg::kBlockScale || kb == kb0;
             ptx::tc_fence_after_sync();
             const uint64_t act_desc = ptx::sw128_kmajor_desc(s_act + stage * Cfg::kActBytes);
             const uint64_t w_desc = ptx::sw128_kmajor_desc(s_w + stage * Cfg::kWBytes);
@@ -986,10 +998,10 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
               // advance 32 bytes of K inside the 128-byte swizzled row: +2 in 16-byte units
               if constexpr (Cfg::kPair)
                 ptx::mma_f8f6f4_pair(d_tmem, a_desc + 2u * k, b_desc + 2u * k, idesc,
-                                     (kb > kb0 || k > 0) ? 1u : 0u);
+                                     (!first_of_acc || k > 0) ? 1u : 0u);
               else
                 ptx::mma_f8f6f4(d_tmem, a_desc + 2u * k, b_desc + 2u * k, Cfg::kIdesc,
-                                (kb > kb0 || k > 0) ? 1u : 0u);
+                                (!first_of_acc || k > 0) ? 1u : 0u);
             }
             // pairs: the stage is free in both CTAs once the MMAs reading it complete.
             // Block scaling (one K block = one stage per chunk) has one commit per block:
@@ -1033,8 +1045,9 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
       }
     }
     uint32_t chunk = 0;
+    uint32_t kbs_done = 0;  // block scaling: K blocks taken over (their stages freed)
     bool ok = true;
-    const int32_t kpc = p.kb_per_chunk;
+    const int32_t kpc = Cfg::kBlockScale ? Cfg::kBSSub : p.kb_per_chunk;
     for (int32_t i = 0; ok && i < work.n_items; ++i) {
       const Item it = work_item(work, i, worker, workers);
       TileCoord c = decode_tile<Cfg>(sched, it.tile, crank);
@@ -1108,7 +1121,6 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
       }
       // swap-AB with block scaling: this thread's weight row owns one 128-column block of
       // scale_b; lane j holds scale_a of activation row m0 + j (broadcast by shuffle)
-      float bs_row_next = 0.0f;
       if constexpr (Cfg::kBlockScale && Cfg::kSwap) {
         const int32_t nw = c.n0 + static_cast<int32_t>(32u * q + lane);
         const int32_t nblk = p.N / Cfg::kScaleBlock;
@@ -1117,10 +1129,6 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         const int32_t Rl = c.m0 + static_cast<int32_t>(lane);
         const bool rv = lane < static_cast<uint32_t>(Cfg::kTileN) && Rl < c.valid_end;
         bs_a = p.scale_a + static_cast<size_t>(rv ? Rl : 0) * p.num_kb;
-        if (it.kb0 < kb_end) {
-          bs_next = __ldg(bs_b + it.kb0);
-          bs_row_next = rv ? __ldg(bs_a + it.kb0) : 0.0f;
-        }
       }
       // fp32 accumulator of this thread (round-to-nearest adds of the TMEM chunks)
       float acc[Cfg::kThreadCols];
@@ -1137,15 +1145,19 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         for (int32_t kb0 = it.kb0; kb0 < kb_end; kb0 += kpc) {
           const int buf = static_cast<int>(chunk % Cfg::kNumAcc);
           const uint32_t use = chunk / Cfg::kNumAcc;
-          // block scaling: this chunk (= K block kb0)'s scale, and the next one's load
-          float bs = 1.0f;      // this thread's scale of the chunk (swap-AB: its column's)
+          const int32_t nsub = min(kpc, kb_end - kb0);  // K blocks in this chunk
+          // block scaling: the scale of K block kb0 (128-row tiles: loaded one chunk
+          // ahead), or of each of the chunk's blocks (swap-AB: loaded before the wait)
+          float bs = 1.0f;      // this thread's scale of the block (swap-AB: its column's)
           float bs_row = 0.0f;  // swap-AB: lane j's activation-row scale
+          float sub_bs[Cfg::kBSSub];
+          float sub_row[Cfg::kBSSub];
           if constexpr (Cfg::kBlockScale && Cfg::kSwap) {
-            bs = bs_next;
-            bs_row = bs_row_next;
-            if (kb0 + 1 < kb_end) {
-              bs_next = __ldg(bs_b + kb0 + 1);
-              bs_row_next = __ldg(bs_a + kb0 + 1);
+#pragma unroll
+            for (int j = 0; j < Cfg::kBSSub; ++j) {
+              const int32_t kbj = min(kb0 + j, kb_end - 1);
+              sub_bs[j] = __ldg(bs_b + kbj);
+              sub_row[j] = __ldg(bs_a + kbj);
             }
           } else if constexpr (Cfg::kBlockScale) {
             bs = bs_next;
@@ -1163,56 +1175,74 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
             ok = false;
             break;
           }
-          // block scaling: chunk c is K block c of this CTA and lives in stage c % kStages,
-          // whose MMAs have completed -- one lane frees the stage for the loader
+          // block scaling: the chunk's K blocks are this CTA's blocks kbs_done.. and lived in
+          // the stages of those numbers mod kStages, whose MMAs have completed -- one lane
+          // frees them for the loader
           if constexpr (Cfg::kBlockScale) {
             if (ew == 0 && lane == 0)
-              ptx::mbar_arrive(empty_bar(static_cast<int>(chunk % Cfg::kStages)));
+              for (int32_t j = 0; j < nsub; ++j)
+                ptx::mbar_arrive(empty_bar(static_cast<int>((kbs_done + j) % Cfg::kStages)));
+            kbs_done += static_cast<uint32_t>(nsub);
           }
           ptx::tc_fence_after_sync();
           if (warp_any) {
             const uint32_t t_buf = tmem_base + ((32u * q) << 16) +
-                                   static_cast<uint32_t>(buf * Cfg::kAccCols + col_base);
-            if constexpr (Cfg::kRegSplit && Cfg::kThreadCols % 64 == 0) {
-              // two 32-column loads in flight per wait
+                                   static_cast<uint32_t>(buf * Cfg::kBufCols + col_base);
+            // one accumulator at t_acc into the fp32 registers (with the scale in bs / cs)
+            auto drain = [&](uint32_t t_acc) {
+              if constexpr (Cfg::kRegSplit && Cfg::kThreadCols % 64 == 0) {
+                // two 32-column loads in flight per wait
 #pragma unroll
-              for (int pc = 0; pc < Cfg::kThreadCols / 64; ++pc) {
-                uint32_t v0[32], v1[32];
-                ptx::tmem_ld_x32(t_buf + static_cast<uint32_t>(pc * 64), v0);
-                ptx::tmem_ld_x32(t_buf + static_cast<uint32_t>(pc * 64 + 32), v1);
-                ptx::tmem_ld_wait();
+                for (int pc = 0; pc < Cfg::kThreadCols / 64; ++pc) {
+                  uint32_t v0[32], v1[32];
+                  ptx::tmem_ld_x32(t_acc + static_cast<uint32_t>(pc * 64), v0);
+                  ptx::tmem_ld_x32(t_acc + static_cast<uint32_t>(pc * 64 + 32), v1);
+                  ptx::tmem_ld_wait();
 #pragma unroll
-                for (int j = 0; j < 32; j += 2) {
-                  accum2<Cfg::kBlockScale>(acc[pc * 64 + j], acc[pc * 64 + j + 1], v0[j],
-                                           v0[j + 1], bs, bs);
-                  accum2<Cfg::kBlockScale>(acc[pc * 64 + 32 + j], acc[pc * 64 + 33 + j], v1[j],
-                                           v1[j + 1], bs, bs);
+                  for (int j = 0; j < 32; j += 2) {
+                    accum2<Cfg::kBlockScale>(acc[pc * 64 + j], acc[pc * 64 + j + 1], v0[j],
+                                             v0[j + 1], bs, bs);
+                    accum2<Cfg::kBlockScale>(acc[pc * 64 + 32 + j], acc[pc * 64 + 33 + j], v1[j],
+                                             v1[j + 1], bs, bs);
+                  }
+                }
+              } else if constexpr (Cfg::kThreadCols % 32 == 0 && Cfg::kThreadCols < 128) {
+                // 128 accumulators per thread leave no room for 32 more load registers at
+                // the 168-register limit of 10+ warps: those drain 16 columns at a time
+#pragma unroll
+                for (int pc = 0; pc < Cfg::kThreadCols / 32; ++pc) {
+                  uint32_t v[32];
+                  ptx::tmem_ld_x32(t_acc + static_cast<uint32_t>(pc * 32), v);
+                  ptx::tmem_ld_wait();
+#pragma unroll
+                  for (int j = 0; j < 32; j += 2)
+                    accum2<Cfg::kBlockScale>(acc[pc * 32 + j], acc[pc * 32 + j + 1], v[j], v[j + 1],
+                                             cs(pc * 32 + j), cs(pc * 32 + j + 1));
+                }
+              } else {
+#pragma unroll
+                for (int pc = 0; pc < Cfg::kThreadCols / 16; ++pc) {
+                  uint32_t v[16];
+                  ptx::tmem_ld_x16(t_acc + static_cast<uint32_t>(pc * 16), v);
+                  ptx::tmem_ld_wait();
+#pragma unroll
+                  for (int j = 0; j < 16; j += 2)
+                    accum2<Cfg::kBlockScale>(acc[pc * 16 + j], acc[pc * 16 + j + 1], v[j], v[j + 1],
+                                             cs(pc * 16 + j), cs(pc * 16 + j + 1));
                 }
               }
-            } else if constexpr (Cfg::kThreadCols % 32 == 0 && Cfg::kThreadCols < 128) {
-              // 128 accumulators per thread leave no room for 32 more load registers at
-              // the 168-register limit of 10+ warps: those drain 16 columns at a time
+            };
+            if constexpr (Cfg::kBlockScale && Cfg::kSwap) {
 #pragma unroll
-              for (int pc = 0; pc < Cfg::kThreadCols / 32; ++pc) {
-                uint32_t v[32];
-                ptx::tmem_ld_x32(t_buf + static_cast<uint32_t>(pc * 32), v);
-                ptx::tmem_ld_wait();
-#pragma unroll
-                for (int j = 0; j < 32; j += 2)
-                  accum2<Cfg::kBlockScale>(acc[pc * 32 + j], acc[pc * 32 + j + 1], v[j], v[j + 1],
-                                           cs(pc * 32 + j), cs(pc * 32 + j + 1));
+              for (int j = 0; j < Cfg::kBSSub; ++j) {
+                if (j < nsub) {
+                  bs = sub_bs[j];
+                  bs_row = sub_row[j];
+                  drain(t_buf + static_cast<uint32_t>(j * Cfg::kAccCols));
+                }
               }
             } else {
-#pragma unroll
-              for (int pc = 0; pc < Cfg::kThreadCols / 16; ++pc) {
-                uint32_t v[16];
-                ptx::tmem_ld_x16(t_buf + static_cast<uint32_t>(pc * 16), v);
-                ptx::tmem_ld_wait();
-#pragma unroll
-                for (int j = 0; j < 16; j += 2)
-                  accum2<Cfg::kBlockScale>(acc[pc * 16 + j], acc[pc * 16 + j + 1], v[j], v[j + 1],
-                                           cs(pc * 16 + j), cs(pc * 16 + j + 1));
-              }
+              drain(t_buf);
             }
           }
           ptx::tc_fence_before_sync();
