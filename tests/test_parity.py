@@ -467,6 +467,23 @@ def test_weight_prefetch_is_only_a_hint(orc, layout):
     assert fx.device_status() == 0
 
 
+@pytest.mark.parametrize("layout", ["stacked", "dynamic"])
+def test_many_groups_swap_plan(orc, layout):
+    """100 groups of a few rows each (swap-AB plan, split along K): the scheduler's warp
+    takes several groups per lane, both in the speculative schedule of the weight prefetch
+    and in the real one; empty groups and groups of one row throughout."""
+    G, N, K = 100, 256, 1024
+    rng = np.random.default_rng(57)
+    meta = rng.integers(0, 4, size=G)
+    meta[::9] = 0
+    if layout == "stacked":
+        prob = _rand_problem("stacked", G, N, K, meta.tolist(), seed=58)
+    else:
+        prob = _rand_problem("dynamic", G, N, K, meta.tolist(), E=4, seed=59)
+    _check_full(prob, orc, poison_value=0x5A5A, what=f"{layout}, 100 groups")
+    assert fx.device_status() == 0
+
+
 def test_empty_problems_are_noops():
     dev = torch.empty(16, dtype=torch.uint8, device="cuda")
     p = dev.data_ptr()
