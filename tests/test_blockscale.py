@@ -126,6 +126,22 @@ def test_blockscale_decode_shapes(orc, m):
     assert fx.device_status() == 0
 
 
+@pytest.mark.parametrize("K", [128, 384, 640])
+@pytest.mark.parametrize("split", [0, 2])
+def test_blockscale_swap_odd_block_counts(orc, K, split):
+    # swap-AB tiles take two K blocks per chunk: 1, 3 and 5 blocks leave a chunk of one,
+    # and split pieces may start on an odd block; both swap-AB widths, split or not
+    A, B, sa, sb, m, rows = _case(16, 3, [5, 0, 19], 512, K, wide=True)
+    fx.mslkb_set_split_k(split)
+    try:
+        for v in ("blockscale_swap_w128xa16_tma", "blockscale_swap_w128xa32_tma"):
+            got = _run(A, B, sa, sb, m, rows, 512, v)
+            _check(orc, A, B, sa, sb, m, rows, got, f"K={K} split={split} {v}")
+    finally:
+        fx.mslkb_set_split_k(1)
+    assert fx.device_status() == 0
+
+
 def test_blockscale_k_zero():
     out = fx.f8f8bf16_groupwise_grouped_stacked(
         torch.zeros((8, 0), dtype=torch.uint8, device="cuda"),
