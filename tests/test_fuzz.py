@@ -1,0 +1,80 @@
+"""Seeded random problems through the planner's own choice of variant, compared with the
+oracle element by element: random group counts and sizes (empty groups, single rows,
+groups larger than a tile), N any multiple of 8, K any size (K % 16 != 0 takes the
+cp.async loader), dynamic valid-row counts outside [0, E], scales over 16 binades.  Rows a
+layout does not own must keep their contents."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import fp8_rowwise_scaled_gb300 as fx
+from fp8_rowwise_scaled_gb300 import build as fxbuild
+from fp8_rowwise_scaled_gb300.synthetic import random_codes
+from parity_util import Problem, bits_of, compare
+
+pytestmark = pytest.mark.gpu
+
+LAYOUTS = ("stacked", "dynamic", "offsets", "batched")
+CASES_PER_LAYOUT = 16
+POISON = 0x5A5A
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    fxbuild.build()
+    fx.lib()
+    fx.device_status()
+
+
+@pytest.fixture(scope="module")
+def orc():
+    return oracle.load(0)
+
+
+def _problem(layout: str, i: int) -> Problem:
+    rng = np.random.default_rng(4000 + 97 * LAYOUTS.index(layout) + i)
+    G = int(rng.integers(1, 17))
+    N = 8 * int(rng.integers(1, 65))
+    K = int(rng.integers(1, 41)) * 16 if rng.random() < 0.6 else int(rng.integers(1, 641))
+    per = int(rng.choice([1, 3, 16, 40, 140]))
+    g = torch.Generator().manual_seed(int(rng.integers(1 << 30)))
+    if layout in ("stacked", "offsets"):
+        counts = rng.integers(0, 2 * per + 1, size=G)
+        counts[rng.random(G) < 0.25] = 0
+        rows = int(counts.sum())
+        meta = np.cumsum(counts).astype(np.int32) if layout == "offsets" else counts
+        E = 0
+    else:
+        E = max(1, per)
+        rows = G * E
+        meta = rng.integers(-2, E + 3, size=G) if layout == "dynamic" else np.zeros(G, np.int64)
+    A = random_codes((max(rows, 0), K), g).numpy()
+    B = random_codes((G, N, K), g).numpy()
+    sa = (np.exp2(rng.integers(-8, 8, size=rows)) * rng.uniform(0.5, 1.5, size=rows))
+    sb = (np.exp2(rng.integers(-8, 8, size=(G, N))) * rng.uniform(0.5, 1.5, size=(G, N)))
+    return Problem.from_numpy(layout, A, B, sa.astype(np.float32), sb.astype(np.float32),
+                              meta, expected_m=E)
+
+
+@pytest.mark.parametrize("layout", LAYOUTS)
+@pytest.mark.parametrize("i", range(CASES_PER_LAYOUT))
+def test_fuzz(orc, layout, i):
+    prob = _problem(layout, i)
+    if prob.rows == 0:
+        pytest.skip("no rows drawn")
+    out = torch.full((prob.rows, prob.N), POISON, dtype=torch.int16, device="cuda")
+    out = out.view(torch.bfloat16)
+    res = prob.run_gpu(out=out)
+    torch.cuda.synchronize()
+    got = bits_of(res).reshape(prob.rows, prob.N)
+    ref, ab = prob.oracle_full(orc, poison=np.full((prob.rows, prob.N), POISON, np.uint16))
+    owned = prob.owned_rows_mask()
+    what = f"{layout} #{i}: G={prob.G} N={prob.N} K={prob.K} rows={prob.rows}"
+    compare(got[owned].ravel(), ref[owned].ravel(), ab[owned].ravel(), what)
+    assert np.all(got[~owned] == POISON), f"{what}: rows it does not own were written"
+    assert fx.device_status() == 0
