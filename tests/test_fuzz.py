@@ -78,3 +78,55 @@ def test_fuzz(orc, layout, i):
     compare(got[owned].ravel(), ref[owned].ravel(), ab[owned].ravel(), what)
     assert np.all(got[~owned] == POISON), f"{what}: rows it does not own were written"
     assert fx.device_status() == 0
+
+
+# -- the ragged and block-scaled entry points, through their own parity helpers ---------
+
+@pytest.mark.parametrize("i", range(10))
+def test_fuzz_ragged_n(orc, i):
+    from test_ragged_layouts import _n_offsets_case
+    rng = np.random.default_rng(5000 + i)
+    G = int(rng.integers(1, 13))
+    M = int(rng.choice([int(rng.integers(1, 33)), int(rng.integers(33, 300))]))
+    K = 16 * int(rng.integers(1, 41))
+    cols = rng.integers(0, 600, size=G)
+    cols[rng.random(G) < 0.2] = 0
+    total_N = 8 * (-(-int(cols.sum()) // 8)) + 8 * int(rng.integers(0, 4))
+    if total_N == 0:
+        pytest.skip("no columns drawn")
+    _n_offsets_case(orc, G, M, total_N, K, cols.tolist(), seed=5100 + i)
+    assert fx.device_status() == 0
+
+
+@pytest.mark.parametrize("i", range(10))
+def test_fuzz_ragged_k(orc, i):
+    from test_ragged_layouts import _k_offsets_case
+    rng = np.random.default_rng(6000 + i)
+    G = int(rng.integers(1, 13))
+    M = int(rng.choice([int(rng.integers(1, 33)), int(rng.integers(33, 260))]))
+    N = 8 * int(rng.integers(1, 49))
+    ks = 16 * rng.integers(0, 60, size=G)
+    ks[rng.random(G) < 0.2] = 0
+    total_K = int(ks.sum()) + 16 * int(rng.integers(0, 8))
+    if total_K == 0:
+        pytest.skip("no K drawn")
+    _k_offsets_case(orc, G, M, N, total_K, ks.tolist(), seed=6100 + i)
+    assert fx.device_status() == 0
+
+
+@pytest.mark.parametrize("i", range(10))
+def test_fuzz_groupwise(orc, i):
+    from test_blockscale import _case, _check, _run
+    rng = np.random.default_rng(7000 + i)
+    G = int(rng.integers(1, 9))
+    per = int(rng.choice([2, 16, 30, 150]))
+    m = rng.integers(0, 2 * per + 1, size=G)
+    m[rng.random(G) < 0.2] = 0
+    if int(m.sum()) == 0:
+        pytest.skip("no rows drawn")
+    N = 128 * int(rng.integers(1, 5))
+    K = 128 * int(rng.integers(1, 9))
+    A, B, sa, sb, mm, rows = _case(7100 + i, G, m.tolist(), N, K, wide=bool(rng.random() < 0.5))
+    got = _run(A, B, sa, sb, mm, rows, N)
+    _check(orc, A, B, sa, sb, mm, rows, got, f"groupwise #{i}: G={G} N={N} K={K} m={m.tolist()}")
+    assert fx.device_status() == 0
