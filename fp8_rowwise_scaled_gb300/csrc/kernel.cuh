@@ -458,6 +458,28 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
   }
 }
 
+// Bounded wait (one thread) for a global counter to reach `want`, with acquire semantics:
+// false if the CTA is aborting or the wait gave up (the abort flag and the device status
+// word are then set).
+__device__ __forceinline__ bool wait_count(const uint32_t* cnt, uint32_t want,
+                                           volatile uint32_t* abort, uint32_t* status,
+                                           uint64_t timeout_ns) {
+  if (ptx::ld_acquire_gpu_u32(cnt) >= want) return true;
+  const uint64_t t0 = ptx::globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    ptx::nanosleep(32);
+    if (ptx::ld_acquire_gpu_u32(cnt) >= want) return true;
+    if ((it & 63u) == 0) {
+      if (*abort) return false;
+      if (ptx::globaltimer_ns() - t0 > timeout_ns) {
+        *abort = 1u;
+        atomicOr(status, kStatusTimeout);
+        return false;
+      }
+    }
+  }
+}
+
 // Two TMEM values into two fp32 register accumulators with one packed (f32x2) operation:
 // round-to-nearest adds, or (block scaling) fused multiply-adds by the K block's scale.
 // Each lane of the pair rounds exactly as the scalar operation would.
@@ -1256,48 +1278,56 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         if (!ok) break;
       }
       if (it.sk_tile >= 0) {
-        // One piece of a split tile.  Each epilogue warp publishes its partial sums and
-        // counts itself in; the warp that arrives last (same warp index, any CTA) adds the
-        // pieces in CTA order -- the same order whoever is last -- and stores the tile.
+        // One piece of a split tile.  The tile's owner is the CTA whose piece holds its first
+        // K block (c_first); every other piece is the first split item of its CTA, whose
+        // epilogue warps publish their partial sums and count themselves in.  The owner's
+        // warps keep theirs in registers, wait (bounded) for the others' counts and add the
+        // pieces in CTA order -- ((p_first + p_next) + ...) + p_last -- and store the tile.
+        // (No cycle: a non-owner piece is processed before any wait of its CTA.)
         const int64_t u_first = static_cast<int64_t>(it.sk_tile) * work.nkb;
         const int32_t c_first = unit_owner(work, u_first);
         const int32_t c_last = unit_owner(work, u_first + work.nkb - 1);
         constexpr size_t kPerWarp = 32 * Cfg::kThreadCols;
         // slot 0: the first tile of that CTA's range; slot 1: its last tile.  Every CTA after
-        // c_first starts its range inside this tile; c_first does when its range starts on
-        // the tile's first unit.
-        const int slot_first = work.units * c_first / work.sk_ctas < u_first ? 1 : 0;
+        // c_first starts its range inside this tile.
         auto piece = [&](int32_t cta) -> float* {
-          const int slot = cta == c_first ? slot_first : 0;
-          return p.sk_ws + (static_cast<size_t>(cta * 2 + slot) * Cfg::kEpiWarps + ew) * kPerWarp;
+          return p.sk_ws + (static_cast<size_t>(cta * 2) * Cfg::kEpiWarps + ew) * kPerWarp;
         };
-        float* mine = piece(blockIdx.x) + lane;
-#pragma unroll
-        for (int j = 0; j < Cfg::kThreadCols; ++j) __stcg(mine + j * 32, acc[j]);
-        // the warp barrier orders every lane's stores before lane 0's count, which releases
-        // them at GPU scope; the last piece's count acquires the others' releases, and the
-        // warp barrier after it hands them on to every lane
-        __syncwarp();
         uint32_t* cnt = p.sk_cnt + static_cast<size_t>(it.sk_tile) * Cfg::kEpiWarps + ew;
-        uint32_t prev = 0;
-        if (lane == 0) prev = ptx::atom_add_acq_rel_gpu(cnt, 1u);
-        prev = __shfl_sync(0xffffffffu, prev, 0);
-        if (prev != static_cast<uint32_t>(c_last - c_first)) continue;  // not the last piece
+        if (static_cast<int32_t>(blockIdx.x) != c_first) {
+          float* mine = piece(blockIdx.x) + lane;
+#pragma unroll
+          for (int j = 0; j < Cfg::kThreadCols; ++j) __stcg(mine + j * 32, acc[j]);
+          // the warp barrier orders every lane's stores before lane 0's count, which
+          // releases them at GPU scope
+          __syncwarp();
+          if (lane == 0) ptx::red_add_release_gpu(cnt, 1u);
+          continue;
+        }
+        // the owner: its count acquires the others' releases; the warp barrier after it
+        // hands them on to every lane
+        uint32_t got_all = 1u;
+        if (lane == 0)
+          got_all = wait_count(cnt, static_cast<uint32_t>(c_last - c_first), abort_flag,
+                               p.status, p.timeout_ns) ? 1u : 0u;
+        got_all = __shfl_sync(0xffffffffu, got_all, 0);
+        if (!got_all) {
+          ok = false;
+          break;
+        }
         __syncwarp();
-        // every piece, this CTA's own included, is read back from the workspace so that
-        // the sum runs in CTA order: ((p_first + p_next) + ...) + p_last.  The loads of up
-        // to kBatch pieces are in flight together before their adds.
+        // the other pieces added to the owner's in CTA order; the loads of up to kBatch
+        // pieces are in flight together before their adds
         constexpr int kBatch = Cfg::kThreadCols >= 64 ? 1 : 64 / Cfg::kThreadCols;
         if constexpr (kBatch == 1) {
           // wide accumulators: no registers to spare, one piece at a time
-          for (int32_t cta = c_first; cta <= c_last; ++cta) {
+          for (int32_t cta = c_first + 1; cta <= c_last; ++cta) {
             const float* src = piece(cta) + lane;
 #pragma unroll
-            for (int j = 0; j < Cfg::kThreadCols; ++j)
-              acc[j] = (cta == c_first) ? __ldcg(src + j * 32) : acc[j] + __ldcg(src + j * 32);
+            for (int j = 0; j < Cfg::kThreadCols; ++j) acc[j] += __ldcg(src + j * 32);
           }
         } else {
-          for (int32_t c0 = c_first; c0 <= c_last; c0 += kBatch) {
+          for (int32_t c0 = c_first + 1; c0 <= c_last; c0 += kBatch) {
             float v[kBatch][Cfg::kThreadCols];
 #pragma unroll
             for (int b = 0; b < kBatch; ++b) {
@@ -1311,8 +1341,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
             for (int b = 0; b < kBatch; ++b) {
               if (c0 + b <= c_last) {
 #pragma unroll
-                for (int j = 0; j < Cfg::kThreadCols; ++j)
-                  acc[j] = (c0 + b == c_first) ? v[b][j] : acc[j] + v[b][j];
+                for (int j = 0; j < Cfg::kThreadCols; ++j) acc[j] += v[b][j];
               }
             }
           }

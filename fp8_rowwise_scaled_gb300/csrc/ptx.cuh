@@ -381,6 +381,18 @@ __device__ __forceinline__ void tmem_ld_x32(uint32_t taddr, uint32_t (&r)[32]) {
 
 // Programmatic dependent launch: let the next kernel on the stream start launching, and
 // wait until the kernels this one depends on have completed and their writes are visible.
+// add to a global counter with release semantics at GPU scope (no result)
+__device__ __forceinline__ void red_add_release_gpu(uint32_t* ptr, uint32_t v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(ptr), "r"(v) : "memory");
+}
+
+// load of a global word with acquire semantics at GPU scope
+__device__ __forceinline__ uint32_t ld_acquire_gpu_u32(const uint32_t* ptr) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
+  return v;
+}
+
 // atomic add with acquire-release semantics at GPU scope; returns the old value
 __device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t* ptr, uint32_t v) {
   uint32_t old;
