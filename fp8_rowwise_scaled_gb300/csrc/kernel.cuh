@@ -1156,6 +1156,51 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
       float acc[Cfg::kThreadCols];
 #pragma unroll
       for (int j = 0; j < Cfg::kThreadCols; ++j) acc[j] = 0.0f;
+      // A split tile: the CTAs holding its K blocks (the owner, c_first, holds the first),
+      // each piece's partial sums in the workspace (slot 0 of its CTA: the first tile of
+      // that CTA's range, which every CTA after c_first starts inside this tile), and the
+      // count the non-owners add themselves to.
+      int32_t sk_first = 0, sk_last = 0;
+      if (it.sk_tile >= 0) {
+        const int64_t u_first = static_cast<int64_t>(it.sk_tile) * work.nkb;
+        sk_first = unit_owner(work, u_first);
+        sk_last = unit_owner(work, u_first + work.nkb - 1);
+      }
+      constexpr size_t kPerWarp = 32 * Cfg::kThreadCols;
+      auto piece = [&](int32_t cta) -> float* {
+        return p.sk_ws + (static_cast<size_t>(cta * 2) * Cfg::kEpiWarps + ew) * kPerWarp;
+      };
+      uint32_t* const cnt =
+          it.sk_tile >= 0 ? p.sk_cnt + static_cast<size_t>(it.sk_tile) * Cfg::kEpiWarps + ew
+                          : nullptr;
+      // The owner of a split tile whose other pieces are already counted in -- they are
+      // their CTAs' first items and normally finished long before the owner's own piece --
+      // loads them now (narrow TMA swap-AB accumulators: up to kPre pieces in registers), so
+      // that after its own drain only the adds remain.
+      constexpr int kPre = (Cfg::kTma && Cfg::kThreadCols <= 32) ? 64 / Cfg::kThreadCols : 0;
+      float pre[kPre > 0 ? kPre : 1][Cfg::kThreadCols];
+      int32_t n_pre = 0;  // pieces loaded early
+      if constexpr (kPre > 0) {
+        if (it.sk_tile >= 0 && static_cast<int32_t>(blockIdx.x) == sk_first &&
+            sk_last - sk_first <= kPre) {
+          uint32_t ready = 0;
+          if (lane == 0)
+            ready = ptx::ld_acquire_gpu_u32(cnt) >= static_cast<uint32_t>(sk_last - sk_first);
+          ready = __shfl_sync(0xffffffffu, ready, 0);
+          __syncwarp();
+          if (ready) {
+#pragma unroll
+            for (int b = 0; b < kPre; ++b) {
+              if (b < sk_last - sk_first) {
+                const float* src = piece(sk_first + 1 + b) + lane;
+#pragma unroll
+                for (int j = 0; j < Cfg::kThreadCols; ++j) pre[b][j] = __ldcg(src + j * 32);
+              }
+            }
+            n_pre = sk_last - sk_first;
+          }
+        }
+      }
       // TMEM data is needed only when this warp's lanes hold rows with computed values
       bool warp_any;
       if constexpr (!Cfg::kSwap) {
@@ -1284,16 +1329,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         // warps keep theirs in registers, wait (bounded) for the others' counts and add the
         // pieces in CTA order -- ((p_first + p_next) + ...) + p_last -- and store the tile.
         // (No cycle: a non-owner piece is processed before any wait of its CTA.)
-        const int64_t u_first = static_cast<int64_t>(it.sk_tile) * work.nkb;
-        const int32_t c_first = unit_owner(work, u_first);
-        const int32_t c_last = unit_owner(work, u_first + work.nkb - 1);
-        constexpr size_t kPerWarp = 32 * Cfg::kThreadCols;
-        // slot 0: the first tile of that CTA's range; slot 1: its last tile.  Every CTA after
-        // c_first starts its range inside this tile.
-        auto piece = [&](int32_t cta) -> float* {
-          return p.sk_ws + (static_cast<size_t>(cta * 2) * Cfg::kEpiWarps + ew) * kPerWarp;
-        };
-        uint32_t* cnt = p.sk_cnt + static_cast<size_t>(it.sk_tile) * Cfg::kEpiWarps + ew;
+        const int32_t c_first = sk_first;
+        const int32_t c_last = sk_last;
         if (static_cast<int32_t>(blockIdx.x) != c_first) {
           float* mine = piece(blockIdx.x) + lane;
 #pragma unroll
@@ -1304,44 +1341,57 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
           if (lane == 0) ptx::red_add_release_gpu(cnt, 1u);
           continue;
         }
-        // the owner: its count acquires the others' releases; the warp barrier after it
-        // hands them on to every lane
-        uint32_t got_all = 1u;
-        if (lane == 0)
-          got_all = wait_count(cnt, static_cast<uint32_t>(c_last - c_first), abort_flag,
-                               p.status, p.timeout_ns) ? 1u : 0u;
-        got_all = __shfl_sync(0xffffffffu, got_all, 0);
-        if (!got_all) {
-          ok = false;
-          break;
-        }
-        __syncwarp();
-        // the other pieces added to the owner's in CTA order; the loads of up to kBatch
-        // pieces are in flight together before their adds
-        constexpr int kBatch = Cfg::kThreadCols >= 64 ? 1 : 64 / Cfg::kThreadCols;
-        if constexpr (kBatch == 1) {
-          // wide accumulators: no registers to spare, one piece at a time
-          for (int32_t cta = c_first + 1; cta <= c_last; ++cta) {
-            const float* src = piece(cta) + lane;
+        if constexpr (kPre > 0) {
+          if (n_pre > 0) {
 #pragma unroll
-            for (int j = 0; j < Cfg::kThreadCols; ++j) acc[j] += __ldcg(src + j * 32);
-          }
-        } else {
-          for (int32_t c0 = c_first + 1; c0 <= c_last; c0 += kBatch) {
-            float v[kBatch][Cfg::kThreadCols];
+            for (int b = 0; b < kPre; ++b) {
+              if (b < n_pre) {
 #pragma unroll
-            for (int b = 0; b < kBatch; ++b) {
-              if (c0 + b <= c_last) {
-                const float* src = piece(c0 + b) + lane;
-#pragma unroll
-                for (int j = 0; j < Cfg::kThreadCols; ++j) v[b][j] = __ldcg(src + j * 32);
+                for (int j = 0; j < Cfg::kThreadCols; ++j) acc[j] += pre[b][j];
               }
             }
+          }
+        }
+        if (n_pre == 0) {
+          // the owner: its count acquires the others' releases; the warp barrier after it
+          // hands them on to every lane
+          uint32_t got_all = 1u;
+          if (lane == 0)
+            got_all = wait_count(cnt, static_cast<uint32_t>(c_last - c_first), abort_flag,
+                                 p.status, p.timeout_ns) ? 1u : 0u;
+          got_all = __shfl_sync(0xffffffffu, got_all, 0);
+          if (!got_all) {
+            ok = false;
+            break;
+          }
+          __syncwarp();
+          // the other pieces added to the owner's in CTA order; the loads of up to kBatch
+          // pieces are in flight together before their adds
+          constexpr int kBatch = Cfg::kThreadCols >= 64 ? 1 : 64 / Cfg::kThreadCols;
+          if constexpr (kBatch == 1) {
+            // wide accumulators: no registers to spare, one piece at a time
+            for (int32_t cta = c_first + 1; cta <= c_last; ++cta) {
+              const float* src = piece(cta) + lane;
 #pragma unroll
-            for (int b = 0; b < kBatch; ++b) {
-              if (c0 + b <= c_last) {
+              for (int j = 0; j < Cfg::kThreadCols; ++j) acc[j] += __ldcg(src + j * 32);
+            }
+          } else {
+            for (int32_t c0 = c_first + 1; c0 <= c_last; c0 += kBatch) {
+              float v[kBatch][Cfg::kThreadCols];
 #pragma unroll
-                for (int j = 0; j < Cfg::kThreadCols; ++j) acc[j] += v[b][j];
+              for (int b = 0; b < kBatch; ++b) {
+                if (c0 + b <= c_last) {
+                  const float* src = piece(c0 + b) + lane;
+#pragma unroll
+                  for (int j = 0; j < Cfg::kThreadCols; ++j) v[b][j] = __ldcg(src + j * 32);
+                }
+              }
+#pragma unroll
+              for (int b = 0; b < kBatch; ++b) {
+                if (c0 + b <= c_last) {
+#pragma unroll
+                  for (int j = 0; j < Cfg::kThreadCols; ++j) acc[j] += v[b][j];
+                }
               }
             }
           }
