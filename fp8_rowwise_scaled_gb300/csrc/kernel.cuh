@@ -615,6 +615,75 @@ __device__ __noinline__ void mma_ragk_first_block(uint32_t d_tmem, uint64_t a_de
                     k > k_first ? 1u : 0u);
 }
 
+// K blocks per accumulation chunk that the unrolled MMA path below serves (the default
+// chunk; other chunk lengths take the general loop).
+constexpr int kUnrolledChunkKb = 8;
+
+// One whole accumulation chunk of kUnrolledChunkKb K blocks whose first block sits in
+// stage kS0 of the ring, the ring's phase for that pass being `phase`.  Stage numbers,
+// barrier addresses, descriptor offsets and accumulate flags are all compile-time here, so
+// per K block the MMA thread only waits, fences, issues its four MMAs and commits.  The
+// tensor core's queue hides little of what this thread does between two blocks' MMAs
+// (measured on GB300: back-to-back 128 x 256 x 32 MMAs take the nominal 128 cycles each,
+// but a wait, a commit and a few dozen instructions of loop bookkeeping per block leave
+// the tensor core idle); with the loads replaced by bare barrier arrivals, a 128 x 256
+// tile's MMA stream takes ~669 cycles per K block of four MMAs in the general loop below
+// and ~565 in this form, a CTA pair's ~696 and ~562 (512 at the nominal rate).  The
+// chunk's commit to its TMEM buffer's barrier goes before the last stage's commit.
+template <class Cfg, int kS0, int kJ = 0>
+__device__ __forceinline__ bool mma_chunk_unrolled(const GemmParams& p, uint32_t s_bar,
+                                                   uint32_t tfull, uint32_t d_buf,
+                                                   uint32_t idesc, uint32_t a_lo0,
+                                                   uint32_t b_lo0, uint32_t phase,
+                                                   volatile uint32_t* abort) {
+  if constexpr (kJ == kUnrolledChunkKb) {
+    return true;
+  } else {
+    // block kJ of the chunk: its stage, and whether the ring wrapped since the chunk's start
+    constexpr int kSt = (kS0 + kJ) % Cfg::kStages;
+    constexpr uint32_t kFlip = static_cast<uint32_t>(((kS0 + kJ) / Cfg::kStages) & 1);
+    if (!wait_bar(s_bar + 8u * kSt, phase ^ kFlip, abort, p.status, p.timeout_ns)) return false;
+    ptx::tc_fence_after_sync();
+    // the stage's operand tiles, then K steps of 32 bytes inside the 128-byte swizzled row
+    // (+2 in 16-byte descriptor units each)
+    static_assert(kBK / 32 == 4, "four MMAs per stage");
+    constexpr uint32_t kAOff =
+        static_cast<uint32_t>(((Cfg::kSwap ? Cfg::kWBytes : Cfg::kActBytes) * kSt) >> 4);
+    constexpr uint32_t kBOff =
+        static_cast<uint32_t>(((Cfg::kSwap ? Cfg::kActBytes : Cfg::kWBytes) * kSt) >> 4);
+    ptx::mma_f8f6f4_lo<Cfg::kPair, kAOff + 0, kBOff + 0>(d_buf, a_lo0, b_lo0, idesc,
+                                                        kJ > 0 ? 1u : 0u);
+    ptx::mma_f8f6f4_lo<Cfg::kPair, kAOff + 2, kBOff + 2>(d_buf, a_lo0, b_lo0, idesc, 1u);
+    ptx::mma_f8f6f4_lo<Cfg::kPair, kAOff + 4, kBOff + 4>(d_buf, a_lo0, b_lo0, idesc, 1u);
+    ptx::mma_f8f6f4_lo<Cfg::kPair, kAOff + 6, kBOff + 6>(d_buf, a_lo0, b_lo0, idesc, 1u);
+    const uint32_t empty = s_bar + 8u * (Cfg::kStages + kSt);
+    if constexpr (Cfg::kPair) {
+      if constexpr (kJ == kUnrolledChunkKb - 1) ptx::mma_commit_pair(tfull, 0x3);
+      ptx::mma_commit_pair(empty, 0x3);
+    } else {
+      if constexpr (kJ == kUnrolledChunkKb - 1) ptx::mma_commit(tfull);
+      ptx::mma_commit(empty);
+    }
+    return mma_chunk_unrolled<Cfg, kS0, kJ + 1>(p, s_bar, tfull, d_buf, idesc, a_lo0, b_lo0,
+                                                phase, abort);
+  }
+}
+
+// mma_chunk_unrolled for the runtime stage `stage` (one instance per ring position).
+template <class Cfg, int kS = 0>
+__device__ __forceinline__ bool mma_chunk_at(int stage, const GemmParams& p, uint32_t s_bar,
+                                             uint32_t tfull, uint32_t d_buf, uint32_t idesc,
+                                             uint32_t a_lo0, uint32_t b_lo0, uint32_t phase,
+                                             volatile uint32_t* abort) {
+  if constexpr (kS + 1 < Cfg::kStages) {
+    if (stage != kS)
+      return mma_chunk_at<Cfg, kS + 1>(stage, p, s_bar, tfull, d_buf, idesc, a_lo0, b_lo0,
+                                       phase, abort);
+  }
+  return mma_chunk_unrolled<Cfg, kS>(p, s_bar, tfull, d_buf, idesc, a_lo0, b_lo0, phase,
+                                     abort);
+}
+
 // cp.async loader: one 16-byte chunk of a swizzled tile row.
 __device__ __forceinline__ void load_chunk(uint32_t dst, const uint8_t* row_ptr, bool row_ok,
                                            int32_t k, int32_t K, int32_t width,
@@ -937,6 +1006,11 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
       uint32_t chunk = 0;  // chunks issued by this CTA: buffer = chunk % kNumAcc
       bool ok = true;
       const int32_t kpc = Cfg::kBlockScale ? Cfg::kBSSub : p.kb_per_chunk;
+      // the unrolled chunk path (128-row and pair tiles; ragged K, block scaling and the
+      // swap-AB tiles keep the general loop)
+      constexpr bool kUnrolledMma = !Cfg::kSwap && !Cfg::kRagK && !Cfg::kBlockScale;
+      const uint32_t a_lo0 = ptx::sw128_kmajor_desc_lo(Cfg::kSwap ? s_w : s_act);
+      const uint32_t b_lo0 = ptx::sw128_kmajor_desc_lo(Cfg::kSwap ? s_act : s_w);
       for (int32_t i = 0; ok && i < work.n_items; ++i) {
         const Item it = work_item(work, i, worker, workers);
         uint32_t idesc = Cfg::kIdesc;
@@ -963,6 +1037,21 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
           ptx::tc_fence_after_sync();
           const uint32_t d_buf = tmem_base + static_cast<uint32_t>(buf * Cfg::kBufCols);
           const int32_t kb1 = min(kb_end, kb0 + kpc);
+          if constexpr (kUnrolledMma) {
+            if (kb1 - kb0 == kUnrolledChunkKb) {
+              // a whole default-length chunk: the compile-time unrolled path
+              if (!mma_chunk_at<Cfg>(stage, p, s_bar, tfull_bar(buf), d_buf, idesc, a_lo0,
+                                     b_lo0, phase, abort_flag)) {
+                ok = false;
+                break;
+              }
+              const int adv = stage + kUnrolledChunkKb;
+              stage = adv % Cfg::kStages;
+              phase ^= static_cast<uint32_t>((adv / Cfg::kStages) & 1);
+              ++chunk;
+              continue;
+            }
+          }
           for (int32_t kb = kb0; kb < kb1; ++kb) {
             if (!wait_bar(full_bar(stage), phase, abort_flag, p.status, p.timeout_ns)) {
               ok = false;

@@ -437,14 +437,20 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
 //   bits 49-51  base offset (0: atoms are 1024-byte aligned)
 //   bit  52     leading-dimension mode (0: byte offset)
 //   bits 61-63  swizzle mode (2: 128-byte swizzle)
+// The high word (bits 32-63) is the same for every address; the low word holds the start
+// address, so offsets within shared memory (< 256 KB) add to the low word alone.
+constexpr uint32_t kSw128DescHi = (1024u >> 4) | (1u << (46 - 32)) | (2u << (61 - 32));
+
+__device__ __forceinline__ uint32_t sw128_kmajor_desc_lo(uint32_t saddr) {
+  return ((saddr & 0x3FFFFu) >> 4) | (1u << 16);
+}
+
+__device__ __forceinline__ uint64_t sw128_desc_join(uint32_t lo) {
+  return (static_cast<uint64_t>(kSw128DescHi) << 32) | lo;
+}
+
 __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr) {
-  uint64_t d = 0;
-  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
-  d |= static_cast<uint64_t>(1u) << 16;
-  d |= static_cast<uint64_t>(1024u >> 4) << 32;
-  d |= static_cast<uint64_t>(1u) << 46;
-  d |= static_cast<uint64_t>(2u) << 61;
-  return d;
+  return sw128_desc_join(sw128_kmajor_desc_lo(saddr));
 }
 
 // Instruction descriptor of tcgen05.mma .kind::f8f6f4, dense, both operands K-major:
@@ -455,6 +461,36 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr) {
 __host__ __device__ constexpr uint32_t idesc_e4m3_f32(int m, int n) {
   return (1u << 4) | (0u << 7) | (0u << 10) | (0u << 15) | (0u << 16) |
          (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
+}
+
+// mma_f8f6f4 / mma_f8f6f4_pair with both shared-memory descriptors given as the low word of
+// a 128-byte-swizzle K-major descriptor (sw128_kmajor_desc_lo) plus a compile-time offset in
+// 16-byte units; the descriptors are put together inside the instruction sequence, so a
+// caller that unrolls many MMAs keeps two base registers live rather than every descriptor.
+template <bool kPair, uint32_t kAOff, uint32_t kBOff>
+__device__ __forceinline__ void mma_f8f6f4_lo(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo,
+                                              uint32_t idesc, uint32_t accumulate) {
+  if constexpr (kPair) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b32 al, bl;\n\t.reg .b64 ad, bd;\n\t"
+        "add.u32 al, %1, %5;\n\tadd.u32 bl, %2, %6;\n\t"
+        "mov.b64 ad, {al, %7};\n\tmov.b64 bd, {bl, %7};\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], ad, bd, %3, p;\n\t}\n" ::"r"(d_tmem),
+        "r"(a_lo), "r"(b_lo), "r"(idesc), "r"(accumulate), "n"(kAOff), "n"(kBOff),
+        "n"(kSw128DescHi)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b32 al, bl;\n\t.reg .b64 ad, bd;\n\t"
+        "add.u32 al, %1, %5;\n\tadd.u32 bl, %2, %6;\n\t"
+        "mov.b64 ad, {al, %7};\n\tmov.b64 bd, {bl, %7};\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], ad, bd, %3, p;\n\t}\n" ::"r"(d_tmem),
+        "r"(a_lo), "r"(b_lo), "r"(idesc), "r"(accumulate), "n"(kAOff), "n"(kBOff),
+        "n"(kSw128DescHi)
+        : "memory");
+  }
 }
 
 }  // namespace ptx
