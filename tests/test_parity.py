@@ -365,6 +365,27 @@ def test_accumulation_chunk_lengths(orc, kpc):
         fx.mslkb_set_accumulation_chunk(old)
 
 
+@pytest.mark.parametrize("variant,K,G,N,meta,E", [
+    # 128x256 tiles, 4 stages: 9 K blocks per tile (a whole 8-block chunk, then one block),
+    # so a CTA's k-th tile starts its whole chunk at ring position k mod 4; 31 row tiles x
+    # 16 column tiles = 496 tiles give some of the 152 CTAs four tiles
+    ("stacked_tile128x256_tma", 128 * 9, 3, 4096, [1280, 1290, 1237], 0),
+    # 128x128 tiles, 6 stages: 13 K blocks (13 = 1 mod 6), 49 x 16 = 784 tiles (six per CTA)
+    ("stacked_tile128x128_tma", 128 * 13, 3, 2048, [2048, 2100, 1990], 0),
+    # CTA pairs, 6 stages, slabs ending in full and half pair tiles: 13 K blocks, 26 x 16 =
+    # 416 tiles over 76 pairs (six for some)
+    ("dynamic_pair256x256_tma", 128 * 13, 4, 4096, [1600, 1500, 1600, 1345], 1600),
+])
+def test_unrolled_chunks_at_every_ring_position(orc, variant, K, G, N, meta, E):
+    """Whole accumulation chunks are issued from a compile-time unrolled path, one instance
+    per ring position; these shapes start whole chunks at every position of the ring."""
+    layout = variant.split("_")[0]
+    prob = _rand_problem(layout, G, N, K, meta, E=E, seed=31)
+    assert fx.mslkb_accumulation_chunk() == 8
+    _check_full(prob, orc, variant=variant, what=variant)
+    assert fx.device_status() == 0
+
+
 def test_cuda_graph_replay(orc):
     prob = _rand_problem("stacked", 4, 256, 512, [64, 0, 100, 3], seed=19)
     out = torch.empty((prob.rows, prob.N), dtype=torch.bfloat16, device="cuda")
