@@ -629,7 +629,9 @@ constexpr int kUnrolledChunkKb = 8;
 // the tensor core idle); with the loads replaced by bare barrier arrivals, a 128 x 256
 // tile's MMA stream takes ~669 cycles per K block of four MMAs in the general loop below
 // and ~565 in this form, a CTA pair's ~696 and ~562 (512 at the nominal rate).  The
-// chunk's commit to its TMEM buffer's barrier goes before the last stage's commit.
+// chunk's commit to its TMEM buffer's barrier goes before the last stage's commit.  The
+// barrier addresses follow the kernel's layout: stage s's full barrier at s_bar + 8 s, its
+// empty barrier at s_bar + 8 (kStages + s).
 template <class Cfg, int kS0, int kJ = 0>
 __device__ __forceinline__ bool mma_chunk_unrolled(const GemmParams& p, uint32_t s_bar,
                                                    uint32_t tfull, uint32_t d_buf,
