@@ -84,6 +84,9 @@ struct GemmParams {
                            // before the dependency wait (0: none)
   const int64_t* spec_meta;  // metadata the speculative schedule reads (= meta, unless a
                              // test points it elsewhere)
+  uint32_t* tile_ctr;      // CTA pairs: {tiles claimed, leaders finished}, zero between
+                           // calls (the last leader to finish resets both); null: every
+                           // pair takes its tiles in a fixed stride
 };
 
 template <int kTileN_, int kStages_, bool kSwap_, bool kTma_, bool kDynamic_, int kEpiWarps_ = 4,
@@ -175,10 +178,15 @@ struct KernelCfg {
   static constexpr int kOffW = kStages * kActBytes;
   static constexpr int kOffOut = kOffW + kStages * kWBytes;
   static constexpr int kOffBar = kOffOut + (kTmaStore ? kEpiWarps * kStageOutBytes : 0);
-  static constexpr int kNumBars = 2 * kStages + 2 * kNumAcc;
+  // CTA pairs: a ring of tile numbers that the leader's loader claims from a global
+  // counter and hands to the pair's other roles (slots, then a full and an empty barrier
+  // per slot)
+  static constexpr int kTQ = kPair ? 4 : 0;
+  static constexpr int kNumBars = 2 * kStages + 2 * kNumAcc + 2 * kTQ;
   static constexpr int kOffMisc = kOffBar + 8 * kNumBars;  // tmem address, abort flag
   static constexpr int kOffWork = kOffMisc + 16;           // the CTA's Work (below)
-  static constexpr int kOffSched = kOffWork + 64;
+  static constexpr int kOffTQ = kOffWork + 64;             // the tile ring (pairs)
+  static constexpr int kOffSched = kOffTQ + 16;
   static constexpr int kSchedBytes = 2 * 4 * (kMaxGroups + 1);
   static constexpr int kOffSpec = kOffSched + kSchedBytes;  // the prefetch warp's tables
   static constexpr int kSmemBytes =
@@ -738,6 +746,13 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
   auto empty_bar = [&](int s) { return s_bar + 8u * (Cfg::kStages + s); };
   auto tfull_bar = [&](int b) { return s_bar + 8u * (2 * Cfg::kStages + b); };
   auto tempty_bar = [&](int b) { return s_bar + 8u * (2 * Cfg::kStages + Cfg::kNumAcc + b); };
+  auto tq_full_bar = [&](int i) {
+    return s_bar + 8u * (2 * Cfg::kStages + 2 * Cfg::kNumAcc + i);
+  };
+  auto tq_empty_bar = [&](int i) {
+    return s_bar + 8u * (2 * Cfg::kStages + 2 * Cfg::kNumAcc + Cfg::kTQ + i);
+  };
+  volatile int32_t* tq = reinterpret_cast<volatile int32_t*>(smem + Cfg::kOffTQ);
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + Cfg::kOffMisc);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + Cfg::kOffMisc + 4);
   int32_t* rowinfo = reinterpret_cast<int32_t*>(smem + Cfg::kOffSched);
@@ -759,6 +774,12 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
       ptx::mbar_init(tfull_bar(b), 1u);
       // pairs: the leader's MMA waits for the epilogue warps of both CTAs
       ptx::mbar_init(tempty_bar(b), static_cast<uint32_t>(Cfg::kEpiWarps * Cfg::kCtas));
+    }
+    for (int i = 0; i < Cfg::kTQ; ++i) {
+      ptx::mbar_init(tq_full_bar(i), 1u);
+      // on the leader: its MMA thread and epilogue warps, the peer's loader and epilogue
+      // warps (the peer's empty barriers go unused)
+      ptx::mbar_init(tq_empty_bar(i), static_cast<uint32_t>(2 + 2 * Cfg::kEpiWarps));
     }
     *abort_flag = 0u;
     ptx::fence_mbar_init();
@@ -854,6 +875,67 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
   sched.K = p.K;
   sched.num_kb = p.num_kb;
   const bool has_k = p.num_kb > 0;
+  // CTA pairs with a claim counter take their tiles in claim order: a pair that finishes a
+  // tile early (a group's half-used last tile) takes the next unclaimed one, so the tiles in
+  // flight stay a window of consecutive tiles and the pairs that share a weight tile stay in
+  // step on it (with tiles in a fixed stride they drift apart and re-read weights from DRAM).
+  // Item i of every role is slot i % kTQ of the tile ring: the leader's loader claims and
+  // writes it into both CTAs; the leader's MMA thread and epilogue warps and the peer's
+  // loader and epilogue warps take it.  Every wait is bounded.  The results do not depend
+  // on which pair runs which tile.
+  const bool dyn = Cfg::kPair && p.tile_ctr != nullptr && has_k;
+  auto whole_tile = [&](int32_t t) {
+    Item it;
+    it.tile = t;
+    it.kb0 = 0;
+    it.kb1 = p.num_kb;
+    it.sk_tile = -1;
+    return it;
+  };
+  // the leader's loader: claim item i (a tile number, or -1 past the last tile).  The
+  // claim for item i + 1 is issued while item i's last loads go out (claim_early), so its
+  // round trip to the counter does not hold up the next tile's first load.
+  uint32_t claim_u = 0;
+  bool claimed = false;
+  auto claim_early = [&]() {
+    claim_u = atomicAdd(p.tile_ctr, 1u);
+    claimed = true;
+  };
+  auto tq_claim = [&](int32_t i, bool& ok) -> int32_t {
+    const int slot = i % (Cfg::kTQ > 0 ? Cfg::kTQ : 1);
+    const uint32_t par = static_cast<uint32_t>(((i / (Cfg::kTQ > 0 ? Cfg::kTQ : 1)) & 1) ^ 1);
+    if (!claimed) claim_early();
+    claimed = false;
+    if (!wait_bar<true>(tq_empty_bar(slot), par, abort_flag, p.status, p.timeout_ns)) {
+      ok = false;
+      return -1;
+    }
+    const uint32_t u = claim_u;
+    const int32_t t = u < static_cast<uint32_t>(sched.total) ? static_cast<int32_t>(u) : -1;
+    tq[slot] = t;
+    ptx::st_shared_cluster_u32(ptx::mapa_shared(ptx::smem_addr(const_cast<int32_t*>(tq + slot)), 1u),
+                               static_cast<uint32_t>(t));
+    ptx::mbar_arrive(tq_full_bar(slot));
+    ptx::mbar_arrive_cluster(ptx::mapa_shared(tq_full_bar(slot), 1u));
+    return t;
+  };
+  // any other role (one thread): take item i
+  auto tq_take = [&](int32_t i, bool& ok) -> int32_t {
+    const int slot = i % (Cfg::kTQ > 0 ? Cfg::kTQ : 1);
+    const uint32_t par = static_cast<uint32_t>((i / (Cfg::kTQ > 0 ? Cfg::kTQ : 1)) & 1);
+    const bool got = crank == 0
+                         ? wait_bar(tq_full_bar(slot), par, abort_flag, p.status, p.timeout_ns)
+                         : wait_bar<true>(tq_full_bar(slot), par, abort_flag, p.status,
+                                          p.timeout_ns);
+    if (!got) {
+      ok = false;
+      return -1;
+    }
+    const int32_t t = tq[slot];
+    if (crank == 0) ptx::mbar_arrive(tq_empty_bar(slot));
+    else ptx::mbar_arrive_cluster(ptx::mapa_shared(tq_empty_bar(slot), 0u));
+    return t;
+  };
   // the work split lives in shared memory: every role reads it, none keeps it in registers
   Work* work_smem = reinterpret_cast<Work*>(smem + Cfg::kOffWork);
   if (threadIdx.x == 0)
@@ -879,11 +961,20 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         const uint64_t pol_act = ptx::l2_policy_evict_last();
         const uint64_t pol_w = ptx::l2_policy_evict_first();
         bool withhold = p.test_stall != 0 && blockIdx.x == 0;
-        for (int32_t i = 0; ok && i < work.n_items; ++i) {
-          const Item it = work_item(work, i, worker, workers);
+        for (int32_t i = 0; ok && (dyn || i < work.n_items); ++i) {
+          Item it;
+          if (dyn) {
+            const int32_t t = crank == 0 ? tq_claim(i, ok) : tq_take(i, ok);
+            if (t < 0) break;
+            it = whole_tile(t);
+          } else {
+            it = work_item(work, i, worker, workers);
+          }
           const TileCoord c = decode_tile<Cfg>(sched, it.tile, crank);
           const int32_t kb_end = Cfg::kRagK ? c.nkb : it.kb1;  // a ragged-K tile's own K
+          const int32_t kb_claim = max(it.kb0, kb_end - 4);    // pairs: next tile's claim
           for (int32_t kb = it.kb0; kb < kb_end; ++kb) {
+            if (dyn && crank == 0 && kb == kb_claim) claim_early();
             if (!wait_bar(empty_bar(stage), phase ^ 1u, abort_flag, p.status, p.timeout_ns)) {
               ok = false;
               break;
@@ -1013,8 +1104,15 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
       constexpr bool kUnrolledMma = !Cfg::kSwap && !Cfg::kRagK && !Cfg::kBlockScale;
       const uint32_t a_lo0 = ptx::sw128_kmajor_desc_lo(Cfg::kSwap ? s_w : s_act);
       const uint32_t b_lo0 = ptx::sw128_kmajor_desc_lo(Cfg::kSwap ? s_act : s_w);
-      for (int32_t i = 0; ok && i < work.n_items; ++i) {
-        const Item it = work_item(work, i, worker, workers);
+      for (int32_t i = 0; ok && (dyn || i < work.n_items); ++i) {
+        Item it;
+        if (dyn) {
+          const int32_t t = tq_take(i, ok);
+          if (t < 0) break;
+          it = whole_tile(t);
+        } else {
+          it = work_item(work, i, worker, workers);
+        }
         uint32_t idesc = Cfg::kIdesc;
         if constexpr (Cfg::kPair) {
           if (decode_tile<Cfg>(sched, it.tile, 0u).half) idesc = Cfg::kIdescHalf;
@@ -1161,8 +1259,24 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     uint32_t kbs_done = 0;  // block scaling: K blocks taken over (their stages freed)
     bool ok = true;
     const int32_t kpc = Cfg::kBlockScale ? Cfg::kBSSub : p.kb_per_chunk;
-    for (int32_t i = 0; ok && i < work.n_items; ++i) {
-      const Item it = work_item(work, i, worker, workers);
+    for (int32_t i = 0; ok && (dyn || i < work.n_items); ++i) {
+      Item it;
+      if (dyn) {
+        // lane 0 takes the item for the warp
+        int32_t t = -1;
+        bool took = true;
+        if (lane == 0) t = tq_take(i, took);
+        t = __shfl_sync(0xffffffffu, t, 0);
+        took = __shfl_sync(0xffffffffu, took ? 1 : 0, 0) != 0;
+        if (!took) {
+          ok = false;
+          break;
+        }
+        if (t < 0) break;
+        it = whole_tile(t);
+      } else {
+        it = work_item(work, i, worker, workers);
+      }
       TileCoord c = decode_tile<Cfg>(sched, it.tile, crank);
       // an empty reduction (K = 0) writes +0.0 to every owned row, whatever the scales
       if (!has_k) c.valid_end = c.m0;
@@ -1616,6 +1730,17 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         ptx::mapa_shared(ptx::smem_addr(smem + Cfg::kOffMisc + 4), crank ^ 1u));
     aborting = aborting || peer_abort != 0u;
     ptx::cluster_sync();
+    // the last leader to get here (every claim is made by then) resets the claim counter
+    // for the next call; teardown runs on the abort path too
+    if (dyn && crank == 0 && threadIdx.x == 0) {
+      __threadfence();
+      if (atomicAdd(p.tile_ctr + 1, 1u) == static_cast<uint32_t>(workers - 1)) {
+        volatile uint32_t* ctr = p.tile_ctr;
+        ctr[0] = 0u;
+        ctr[1] = 0u;
+        __threadfence();
+      }
+    }
   }
   if (aborting) {
     // let any copy or MMA still in flight land before the memory is released

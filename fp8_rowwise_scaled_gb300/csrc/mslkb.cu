@@ -160,14 +160,20 @@ mslkb_status device_state(DeviceState** out) {
 
 // ---------------------------------------------------------------------------------
 // split-tile workspace, one per (device, stream): 2 partial-sum slots per CTA and one
-// arrival counter per (split tile, epilogue warp).  Calls on one stream run in order,
-// so they can share it; calls on different streams get different workspaces.
+// arrival counter per (split tile, epilogue warp), then the two words of the CTA pairs'
+// tile claim counter.  Calls on one stream run in order, so they can share it; calls on
+// different streams get different workspaces.
 // ---------------------------------------------------------------------------------
 struct Workspace {
   float* partials = nullptr;
   uint32_t* counters = nullptr;
 };
 std::map<std::pair<int, uintptr_t>, Workspace> g_workspaces;
+
+// Where the CTA pairs' tile claim counter sits in a workspace's counters.
+size_t pair_counter_offset(const DeviceState* st) {
+  return 2 * static_cast<size_t>(st->sm_count) * 8;
+}
 
 size_t max_partial_bytes() {
   size_t m = 0;
@@ -201,7 +207,8 @@ mslkb_status stream_workspace(const DeviceState* st, cudaStream_t stream, Worksp
   const size_t slots = 2 * static_cast<size_t>(st->sm_count);
   if ((e = cudaMalloc(&w.partials, slots * max_partial_bytes())) != cudaSuccess)
     return cuda_fail(e);
-  const size_t ncnt = slots * 8;  // split tiles < 2 x CTAs, 8 epilogue warps at most
+  // split tiles < 2 x CTAs, 8 epilogue warps at most; then the pairs' claim counter
+  const size_t ncnt = pair_counter_offset(st) + 2;
   if ((e = cudaMalloc(&w.counters, ncnt * sizeof(uint32_t))) != cudaSuccess) {
     cudaFree(w.partials);
     return cuda_fail(e);
@@ -531,6 +538,18 @@ mslkb_status run(int layout, const void* A, const void* B, const float* scale_a,
       p.sk_ws = ws.partials;
       p.sk_cnt = ws.counters;
     }
+  }
+  // Stacked CTA-pair plans claim their tiles from the stream's counter: groups end at any
+  // row, and a group's half-used last tile would otherwise put the pairs that share a
+  // weight tile out of step (measured on the llama3-405b shape: 5.3 GB of DRAM reads per
+  // call instead of up to 9.6, same time in the back-to-back loop).  Slab layouts keep the
+  // fixed stride (full slabs have no half tiles; the claims cost ~2 % there).  In a stream
+  // capture that has no workspace yet, tiles go in the fixed stride too: same results.
+  p.tile_ctr = nullptr;
+  if (v->cluster > 1 && !v->dynamic && p.num_kb > 0) {
+    Workspace ws;
+    if ((s = stream_workspace(st, static_cast<cudaStream_t>(stream), &ws)) != MSLKB_OK) return s;
+    if (ws.counters != nullptr) p.tile_ctr = ws.counters + pair_counter_offset(st);
   }
   if ((s = encode_maps(&la, v, A, B, rows, G, N, K)) != MSLKB_OK) return s;
   if ((s = encode_out_map(&la, v, out, rows, N)) != MSLKB_OK) return s;

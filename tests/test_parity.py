@@ -405,6 +405,53 @@ def test_cuda_graph_replay(orc):
     assert np.array_equal(bits_of(out), eager)
 
 
+@pytest.mark.parametrize("layout", ["stacked", "dynamic"])
+def test_pair_tile_claims_across_calls_and_graphs(orc, layout):
+    """Stacked CTA-pair plans claim their tiles from a per-stream counter that the last pair
+    of each call resets (slab layouts take them in a fixed stride): back-to-back calls, graph
+    replays and a capture made before the stream had a counter (fixed stride) all give the
+    oracle's result, bit-identical to each other."""
+    if layout == "stacked":
+        meta = [520, 3, 0, 700, 256, 129, 511, 520]
+        prob = _rand_problem("stacked", 8, 4096, 1024 + 128, meta, seed=41, total_extra=5)
+    else:
+        meta = [520, 3, 0, 600, 256, 129, 511, 520]
+        prob = _rand_problem("dynamic", 8, 4096, 1024 + 128, meta, E=600, seed=42)
+    # 9 K blocks per tile (an unrolled chunk, then one block); ~220 pair tiles over the pairs
+    v = f"{layout}_pair256x256_tma"
+    # zeros where the stacked layout owns no rows, so whole outputs compare
+    out = torch.zeros((prob.rows, prob.N), dtype=torch.bfloat16, device="cuda")
+    fresh = torch.cuda.Stream()
+    fresh.wait_stream(torch.cuda.current_stream())
+    graph0 = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph0, stream=fresh):   # no workspace on this stream yet
+        prob.run_gpu(out=out, variant=v)
+    with torch.cuda.stream(fresh):
+        graph0.replay()
+    fresh.synchronize()
+    ref_bits, _ = _check_full(prob, orc, out=out.clone(), variant=v, what=f"{v} first call")
+    assert np.array_equal(bits_of(out).reshape(prob.rows, prob.N), ref_bits)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            out.zero_()
+            prob.run_gpu(out=out, variant=v)
+    s.synchronize()
+    assert np.array_equal(bits_of(out).reshape(prob.rows, prob.N), ref_bits)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        for _ in range(2):
+            prob.run_gpu(out=out, variant=v)
+    for _ in range(2):
+        out.zero_()
+        with torch.cuda.stream(s):
+            graph.replay()
+        s.synchronize()
+        assert np.array_equal(bits_of(out).reshape(prob.rows, prob.N), ref_bits)
+    assert fx.device_status() == 0
+
+
 def test_cuda_graph_on_fresh_stream(orc):
     """Captured on a stream never used before: no workspace can be allocated during
     capture, so the call runs with whole tiles; still within tolerance."""
