@@ -830,10 +830,11 @@ mslkb_status mslkb_get_device_status(void* stream, uint32_t* flags) {
   if (e != cudaSuccess) return cuda_fail(e);
   if (value & mslkb::kStatusTimeout) {
     // a kernel that gave up may have left split-tile arrival counters short: clear the
-    // counters of every stream workspace of this device (on `stream`)
+    // counters of every stream workspace of this device (on `stream`), the CTA pairs' tile
+    // claim counter with them (its own reset at teardown also runs on the abort path)
     int dev = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return cuda_fail(e);
-    const size_t ncnt = 2 * static_cast<size_t>(st->sm_count) * 8;
+    const size_t ncnt = pair_counter_offset(st) + 2;
     std::lock_guard<std::mutex> lock(g_mutex);
     for (auto& kv : g_workspaces) {
       if (kv.first.first != dev || kv.second.counters == nullptr) continue;
