@@ -24,10 +24,12 @@
  *   Calls are asynchronous: they enqueue work and return without synchronising.
  *   The first call on a device performs one-time set-up (device query, kernel attributes,
  *   driver entry point).  The first call on each stream (outside stream capture) also
- *   allocates that stream's split-tile workspace (2 x #SMs x 128 KB of fp32 partial sums
- *   plus counters, about 40 MB on GB300); later calls allocate nothing and may be
- *   captured in a CUDA graph.  A call captured on a stream that has no workspace yet
- *   runs without splitting tiles (same results within tolerance, possibly slower).
+ *   allocates that stream's workspace (2 x #SMs x 128 KB of fp32 partial sums for split
+ *   tiles, plus counters, among them the tile claim counter of the CTA-pair plans; about
+ *   40 MB on GB300); later calls allocate nothing and may be captured in a CUDA graph.  A
+ *   call captured on a stream that has no workspace yet runs without splitting tiles and,
+ *   on CTA pairs, takes its tiles in a fixed stride (same results within tolerance,
+ *   possibly slower).
  *   Calls on one stream share its workspace in stream order; a captured graph keeps the
  *   workspace of the stream it was captured on, so two launches of such graphs, or one
  *   and a call on that stream, must not run at the same time.
