@@ -1,7 +1,7 @@
 """Benchmark of the FP8 rowwise-scaled grouped GEMM on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gemm|reference]
-                    [--workload NAME] [--no-sweep] [--no-cpu]
+                    [--workload NAME] [--variant NAME] [--no-sweep] [--no-cpu]
 
 One step = one call of the whole hot path (host checks and planning, the device group
 scheduler, the TMA/tcgen05 pipeline and the fused epilogue) on one batch of seeded
@@ -368,6 +368,8 @@ def gpu_arm(args):
     fx.lib()
     if args.chunk is not None:
         fx.mslkb_set_accumulation_chunk(args.chunk)
+    if args.variant is not None:
+        fx.mslkb_force_variant(fx.variant_index(args.variant))
     pk, pk_kind = peaks()
     wl = workloads()[args.workload]
     inp = make_inputs(wl, device)
@@ -476,6 +478,8 @@ def gpu_arm(args):
         "clocks": clk.summary(),
         "device_status": status,
     }
+    if args.variant is not None:
+        fx.mslkb_force_variant(-1)  # the sweep runs the planner's choices
     if args.sweep and rank == 0:
         shapes = []
         for name in SWEEP:
@@ -549,6 +553,9 @@ def main():
     ap.add_argument("--workload", default=HEADLINE)
     ap.add_argument("--chunk", type=int, default=None,
                     help="tensor-core accumulation chunk in K blocks (default: library's)")
+    ap.add_argument("--variant", default=None,
+                    help="run the headline workload on this kernel variant instead of the "
+                         "planner's choice (for profiling; the per-shape sweep keeps the planner's)")
     ap.add_argument("--no-sweep", dest="sweep", action="store_false")
     ap.add_argument("--no-cpu", dest="cpu", action="store_false")
     ap.add_argument("--cpu-rows", type=int, default=256,
