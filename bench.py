@@ -10,10 +10,17 @@ synthetic input resident in HBM.  Prints ONE JSON line (rank 0).
 Headline workload: the largest single-GPU configuration, llama3-405b-shaped stacked
 G=16, N=K=total_M=16384 (inputs 5.1 GB, larger than L2, so no flush is needed).  The
 metric is FP8 grouped GEMM TFLOPS (2 * sum_g m_g * N * K per call); the line also carries
-us/call, the roofline fraction, the end-to-end figure through host buffers, the CPU
-oracle baseline, the SM clocks seen, and a per-shape sweep of the other shapes
-(DS-V3 gate_up/down, llama3-70b total_M in {1, 16, 128, 1024, 8192}) timed by CUDA-graph
-replay with rotating input sets sized past twice the L2.
+us/call, the roofline of the kernel, the end-to-end figure through host buffers (with the
+host link's measured copy bandwidth), the CPU oracle baseline, the SM clocks seen, and,
+last on the line, one compact row per shape of the sweep (DS-V3 gate_up/down, llama3-70b
+total_M in {1, 16, 128, 1024, 8192}, the other layouts) timed by CUDA-graph replay with
+rotating input sets sized past twice the L2.
+
+Roofline fractions use the measured peaks: the copy bandwidth, and the FP8 peak = 2 x the
+measured bf16 GEMM rate, burst or sustained according to the SM clock seen during each
+timed window (burst unless the median clock under load was at or below the clock of the
+sustained measurement).  The fraction against the nominal dense FP8 peak (4.5 PFLOP/s) and
+HBM bandwidth (8 TB/s) is reported beside it.
 
 --impl reference times the CPU oracle (the plain fp64 C reference) on the same workload,
 one bounded row sample per step, on the host cores.
@@ -49,6 +56,11 @@ SWEEP = ["c2a_dsv3_gate_up", "c2b_dsv3_down", "c3_llama70b_m1", "c3_llama70b_m16
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 FP8_OVER_BF16 = 2.0  # nominal dense ratio (4.5 / 2.25 PFLOP/s)
+FP8_NOMINAL_TFLOPS = 4500.0  # GB300 dense FP8, nominal
+HBM_NOMINAL_GBS = 8000.0     # GB300 HBM3e, nominal
+# columns of the compact per-shape rows
+PER_SHAPE_COLS = ["workload", "us_per_call", "tflops", "bound", "frac", "frac_nominal",
+                  "sm_mhz", "variant"]
 
 
 def peaks():
@@ -91,23 +103,28 @@ def dram_traffic(workload: str):
 
 
 class ClockSampler:
-    """nvidia-smi sampling of SM clocks and throttle reasons while the timed region runs."""
+    """nvidia-smi sampling of SM clocks, power and throttle reasons, every sample stamped
+    with the host clock, so that each timed window (the headline's timed steps, every
+    sweep shape's replays) gets the clocks seen inside it."""
 
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    Q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    PERIOD_MS = 25
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
         self.file = None
+        self.rows = None
 
     def __enter__(self):
         self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
-                 "--format=csv,noheader,nounits", "-lms", "50"],
+                 "--format=csv,noheader,nounits", "-lms", str(self.PERIOD_MS)],
                 stdout=self.file, stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
@@ -123,32 +140,66 @@ class ClockSampler:
                 self.proc.kill()
         self.file.flush()
 
-    def summary(self):
+    def _load(self):
+        if self.rows is not None:
+            return self.rows
+        self.rows = []
         try:
             with open(self.file.name) as f:
-                rows = [ln.strip().split(", ") for ln in f if ln.strip()]
+                lines = [ln.strip() for ln in f if ln.strip()]
             os.unlink(self.file.name)
         except OSError:
+            return self.rows
+        for ln in lines:
+            self.rows.extend(parse_smi_rows([ln]))
+        return self.rows
+
+    def window(self, t0: float | None = None, t1: float | None = None):
+        """Clocks of the samples taken in [t0, t1] (host time.time()); the nearest sample
+        when none falls inside a window shorter than the sampling period."""
+        rows = self._load()
+        if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"]}
-        sm, mx, pw, reasons = [], [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for r in rows:
-            if len(r) < 9:
-                continue
-            try:
-                sm.append(float(r[1]))
-                mx.append(float(r[2]))
-                pw.append(float(r[3]))
-            except ValueError:
-                continue
-            for n, v in zip(names, r[5:9]):
-                if v.strip().lower() == "active":
-                    reasons.add(n)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"]}
-        loaded = [s for s, p in zip(sm, pw) if p > 0.3 * max(pw)] or sm
-        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(mx),
-                "reasons": sorted(reasons), "samples": len(sm), "power_w_max": max(pw)}
+        sel = rows
+        if t0 is not None and t1 is not None:
+            sel = [r for r in rows if t0 <= r["t"] <= t1]
+            if not sel:
+                mid = 0.5 * (t0 + t1)
+                sel = [min(rows, key=lambda r: abs(r["t"] - mid))]
+        return summarize_clocks(sel)
+
+
+def parse_smi_rows(lines):
+    """Rows of `nvidia-smi --query-gpu=<ClockSampler.Q> --format=csv,noheader,nounits`."""
+    import datetime
+    out = []
+    for ln in lines:
+        r = [x.strip() for x in ln.split(",")]
+        if len(r) < 10:
+            continue
+        try:
+            t = datetime.datetime.strptime(r[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            sm, mx, pw = float(r[2]), float(r[3]), float(r[4])
+        except ValueError:
+            continue
+        active = {n for n, v in zip(ClockSampler.REASONS, r[6:10]) if v.lower() == "active"}
+        out.append({"t": t, "sm": sm, "max": mx, "power": pw, "reasons": active})
+    return out
+
+
+def summarize_clocks(rows):
+    """Median SM clock under load (samples above 30 % of the highest power seen), the
+    maximum clock, and every throttle reason that was active."""
+    if not rows:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"]}
+    pmax = max(r["power"] for r in rows)
+    loaded = [r for r in rows if r["power"] > 0.3 * pmax] or rows
+    reasons = set()
+    for r in rows:
+        reasons |= r["reasons"]
+    return {"sm_mhz": statistics.median(r["sm"] for r in loaded),
+            "sm_max_mhz": max(r["max"] for r in rows), "reasons": sorted(reasons),
+            "samples": len(rows), "power_w_max": pmax}
 
 
 # ---------------------------------------------------------------------------------------
@@ -260,19 +311,49 @@ def run_call(fx, inp, out, wl, stream_ptr):
         raise fx.MslkbError(s, wl.name)
 
 
-def fp8_peak(pk, sustained=True):
-    """FP8 dense peak in TFLOP/s: the measured bf16 GEMM rate times the nominal fp8/bf16
-    ratio.  Every timed region here runs the kernel back to back (after a 0.5 s clock
-    ramp), where the GPU settles at its power cap, so the sustained (back-to-back) bf16
-    figure is the matching denominator; the burst figure is reported beside it."""
-    key = "bf16_tflops_sustained" if sustained and "bf16_tflops_sustained" in pk else "bf16_tflops"
-    return pk[key] * FP8_OVER_BF16
+def fp8_peaks(pk):
+    """(burst, sustained) FP8 dense peaks in TFLOP/s -- the measured bf16 GEMM rates times
+    the nominal fp8/bf16 dense ratio -- and the SM clock (MHz) the sustained figure was
+    measured at (None if not recorded)."""
+    burst = pk["bf16_tflops"] * FP8_OVER_BF16
+    sust = pk.get("bf16_tflops_sustained", pk["bf16_tflops"]) * FP8_OVER_BF16
+    f_sust = (pk.get("clocks_under_load") or {}).get("sm_mhz_median")
+    return burst, sust, f_sust
 
 
-def roofline_times(wl, pk, sustained=True):
-    """(t_fp8, t_hbm) in seconds for one call at the measured peaks."""
-    fp8 = fp8_peak(pk, sustained) * 1e12
-    return wl.flops() / fp8, wl.bytes() / (pk["hbm_gbs"] * 1e9)
+def fp8_peak_for_clock(pk, sm_mhz):
+    """The FP8 peak that matches the clocks of a timed window: the burst figure, unless the
+    window's median SM clock under load was at or below the clock at which the sustained
+    (seconds-long, power-capped) figure was measured.  Returns (TFLOP/s, reason)."""
+    burst, sust, f_sust = fp8_peaks(pk)
+    if sm_mhz is None or f_sust is None:
+        return burst, "burst (no clock record to match)"
+    if sm_mhz > f_sust:
+        return burst, (f"burst: median SM clock {sm_mhz:.0f} MHz above the {f_sust:.0f} MHz "
+                       f"of the sustained measurement")
+    return sust, (f"sustained: median SM clock {sm_mhz:.0f} MHz at or below the "
+                  f"{f_sust:.0f} MHz of the sustained measurement")
+
+
+def roofline(wl, pk, t_call, sm_mhz):
+    """Roofline figures of one call that took t_call seconds in a window whose median SM
+    clock was sm_mhz: t_roof = max(F / P_fp8, bytes / BW) with P_fp8 matched to the clock
+    and BW the measured copy bandwidth; also the fractions against the burst and the
+    sustained peaks, against the sustained figure scaled to the window's clock
+    (flops per SM cycle), and against the nominal dense FP8 peak and HBM bandwidth."""
+    p_fp8, why = fp8_peak_for_clock(pk, sm_mhz)
+    burst, sust, f_sust = fp8_peaks(pk)
+    t_fp8 = wl.flops() / (p_fp8 * 1e12)
+    t_hbm = wl.bytes() / (pk["hbm_gbs"] * 1e9)
+    t_nom = max(wl.flops() / (FP8_NOMINAL_TFLOPS * 1e12), wl.bytes() / (HBM_NOMINAL_GBS * 1e9))
+    r = {"bound": "tensor" if t_fp8 >= t_hbm else "hbm",
+         "frac": max(t_fp8, t_hbm) / t_call, "p_fp8": p_fp8, "peak_choice": why,
+         "frac_of_burst": wl.flops() / (burst * 1e12) / t_call,
+         "frac_of_sustained": wl.flops() / (sust * 1e12) / t_call,
+         "frac_of_hbm": t_hbm / t_call, "frac_nominal": t_nom / t_call}
+    if sm_mhz and f_sust:
+        r["frac_at_clock"] = wl.flops() / (sust * 1e12 * sm_mhz / f_sust) / t_call
+    return r
 
 
 def workload_config(wl, ws):
@@ -298,8 +379,9 @@ def out_shape(wl):
 
 
 def sweep_shape(fx, wl, pk, device):
-    """us/call of one shape by CUDA-graph replay (median of 7), rotating input sets so
-    the data touched by one replay cycle exceeds twice the L2."""
+    """us/call of one shape by CUDA-graph replay (median of 7 timed replays of ~25 ms),
+    rotating input sets so that the data touched by one replay cycle exceeds twice the L2.
+    Returns the time and the host-clock window of the timed replays (for their clocks)."""
     import torch
     from fp8_rowwise_scaled_gb300.synthetic import make_inputs
     ws_bytes = max(1, wl.bytes())
@@ -315,9 +397,10 @@ def sweep_shape(fx, wl, pk, device):
             for i in range(n_sets):
                 run_call(fx, sets[i], outs[i], wl, sp)
             stream.synchronize()
-    # calls per replay: ~10 ms of work and at least 16 calls, a multiple of the set count
-    t_est = max(roofline_times(wl, pk)) * 1.5 + 3e-6
-    reps = max(16 // n_sets + 1, min(400, int(1e-2 / t_est) // n_sets)) * n_sets
+    # calls per replay: ~25 ms of work and at least 16 calls, a multiple of the set count
+    t_fp8 = wl.flops() / (fp8_peaks(pk)[0] * 1e12)
+    t_est = max(t_fp8, wl.bytes() / (pk["hbm_gbs"] * 1e9)) * 1.5 + 3e-6
+    reps = max(16 // n_sets + 1, min(1600, int(2.5e-2 / t_est) // n_sets)) * n_sets
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=stream):
         for r in range(reps):
@@ -325,7 +408,10 @@ def sweep_shape(fx, wl, pk, device):
             run_call(fx, sets[i], outs[i], wl, sp)
     times = []
     with torch.cuda.stream(stream):  # replay() launches on the current stream
-        for _ in range(8):
+        graph.replay()  # untimed
+        stream.synchronize()
+        t0 = time.time()
+        for _ in range(7):
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
             e0.record(stream)
@@ -333,27 +419,63 @@ def sweep_shape(fx, wl, pk, device):
             e1.record(stream)
             e1.synchronize()
             times.append(e0.elapsed_time(e1) * 1e3 / reps)  # us per call
-    us = statistics.median(times[1:])
-    t_fp8, t_hbm = roofline_times(wl, pk)
-    t_fp8_burst, _ = roofline_times(wl, pk, sustained=False)
-    t_roof = max(t_fp8, t_hbm)
+        t1 = time.time()
+    us = statistics.median(times)
     plan = plan_for(fx, wl, torch.cuda.get_device_properties(device).multi_processor_count)
-    res = {
-        "workload": wl.name, "us_per_call": round(us, 3),
-        "tflops": round(wl.flops() / (us * 1e-6) / 1e12, 2),
-        "gbs": round(wl.bytes() / (us * 1e-6) / 1e9, 1),
-        "bound": "tensor" if t_fp8 >= t_hbm else "hbm",
-        "roofline_frac": round(t_roof / (us * 1e-6), 4),
-        "frac_of_fp8_peak": round(t_fp8 / (us * 1e-6), 4),
-        "frac_of_fp8_burst": round(t_fp8_burst / (us * 1e-6), 4),
-        "frac_of_hbm": round(t_hbm / (us * 1e-6), 4),
-        "variant": fx.variant_name(plan.variant), "grid": plan.grid,
-        "input_sets": n_sets, "calls_per_replay": reps,
-        "nonempty_groups": wl.nonempty_groups(),
-    }
     del graph, sets, outs, base
     torch.cuda.empty_cache()
-    return res
+    return {"wl": wl, "us": us, "window": (t0, t1), "variant": fx.variant_name(plan.variant)}
+
+
+def shape_row(res, pk, clk):
+    """Compact per-shape row (PER_SHAPE_COLS) with the clocks of the shape's own window."""
+    if "error" in res:
+        return [res["workload"], None, None, None, None, None, None, res["error"][:80]]
+    wl, us = res["wl"], res["us"]
+    sm = clk.window(*res["window"])["sm_mhz"]
+    r = roofline(wl, pk, us * 1e-6, sm)
+    return [wl.name, round(us, 2), round(wl.flops() / (us * 1e-6) / 1e12, 1), r["bound"],
+            round(r["frac"], 3), round(r["frac_nominal"], 3), sm, res["variant"]]
+
+
+def link_bandwidth(device, nbytes=1 << 30, reps=3):
+    """Pinned host <-> device copy bandwidth in GB/s: host to device, device to host, and
+    both directions at once (best of `reps`, CUDA events on the copying streams)."""
+    import torch
+    host = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    host2 = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    dev = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    dev2 = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    s1 = torch.cuda.Stream(device=device)
+    s2 = torch.cuda.Stream(device=device)
+
+    def best(fn):
+        ts = []
+        for _ in range(reps):
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            fn()
+            torch.cuda.synchronize()
+            ts.append(time.perf_counter() - t0)
+        return min(ts)
+
+    def h2d():
+        with torch.cuda.stream(s1):
+            dev.copy_(host, non_blocking=True)
+
+    def d2h():
+        with torch.cuda.stream(s2):
+            host2.copy_(dev2, non_blocking=True)
+
+    def both():
+        h2d()
+        d2h()
+
+    r = {"h2d_gbs": round(nbytes / best(h2d) / 1e9, 1),
+         "d2h_gbs": round(nbytes / best(d2h) / 1e9, 1),
+         "both_gbs": round(2 * nbytes / best(both) / 1e9, 1)}
+    del host, host2, dev, dev2
+    return r
 
 
 def gpu_arm(args):
@@ -380,63 +502,133 @@ def gpu_arm(args):
     plan = plan_for(fx, wl, sms)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        # clock ramp (0.5 s), then the untimed warm-up steps
-        t_end = time.perf_counter() + 0.5
-        while time.perf_counter() < t_end:
-            run_call(fx, inp, out, wl, sp)
+    # one clock sampler over the whole arm; each timed window reads its own samples
+    clk = ClockSampler(local).__enter__()
+    try:
+        with torch.cuda.stream(stream):
+            # clock ramp (0.5 s), then the untimed warm-up steps
+            t_end = time.perf_counter() + 0.5
+            while time.perf_counter() < t_end:
+                run_call(fx, inp, out, wl, sp)
+                stream.synchronize()
+            e0.record(stream)
+            for _ in range(args.warmup):
+                run_call(fx, inp, out, wl, sp)
+            e1.record(stream)
+            e1.synchronize()
+            t_call = e0.elapsed_time(e1) / 1e3 / max(1, args.warmup)
+            steps = (args.steps if args.steps is not None
+                     else max(20, math.ceil(1.5 / max(t_call, 1e-6))))
             stream.synchronize()
-        e0.record(stream)
-        for _ in range(args.warmup):
-            run_call(fx, inp, out, wl, sp)
-        e1.record(stream)
-        e1.synchronize()
-        t_call = e0.elapsed_time(e1) / 1e3 / max(1, args.warmup)
-        steps = args.steps if args.steps is not None else max(20, math.ceil(1.5 / max(t_call, 1e-6)))
-        stream.synchronize()
-        dist_barrier(ws)
-        torch.cuda.synchronize()
-        with ClockSampler(local) as clk:
+            dist_barrier(ws)
+            torch.cuda.synchronize()
+            w0 = time.time()
             e0.record(stream)
             for _ in range(steps):
                 run_call(fx, inp, out, wl, sp)
             e1.record(stream)
             e1.synchronize()
-        torch.cuda.synchronize()
-        dist_barrier(ws)
-    t_total = e0.elapsed_time(e1) / 1e3
-    t_max = dist_max(t_total, ws, device)
-    ms_per_step = t_max / steps * 1e3
-    value = ws * wl.flops() * steps / t_max / 1e12
-    status = fx.device_status(stream)
+            w1 = time.time()
+            torch.cuda.synchronize()
+            dist_barrier(ws)
+        t_total = e0.elapsed_time(e1) / 1e3
+        t_max = dist_max(t_total, ws, device)
+        ms_per_step = t_max / steps * 1e3
+        value = ws * wl.flops() * steps / t_max / 1e12
+        status = fx.device_status(stream)
+        e2e = e2e_leg(fx, wl, inp, out, stream, sp, steps, ws, device)
+        link = link_bandwidth(device)
+        t_link = max(e2e["h2d_bytes_per_step"] / (link["h2d_gbs"] * 1e9),
+                     e2e["d2h_bytes_per_step"] / (link["d2h_gbs"] * 1e9),
+                     (e2e["h2d_bytes_per_step"] + e2e["d2h_bytes_per_step"])
+                     / (link["both_gbs"] * 1e9))
+        e2e["host_link"] = link
+        e2e["frac_of_link"] = round(t_link / (e2e["ms_per_step"] * 1e-3), 4)
+        if args.variant is not None:
+            fx.mslkb_force_variant(-1)  # the sweep runs the planner's choices
+        sweep = []
+        if args.sweep and rank == 0:
+            for name in SWEEP:
+                try:
+                    sweep.append(sweep_shape(fx, workloads()[name], pk, device))
+                except Exception as e:  # noqa: BLE001 - report and continue
+                    sweep.append({"workload": name, "error": repr(e)})
+    finally:
+        clk.__exit__(None, None, None)
+    clocks = clk.window(w0, w1)
 
-    # roofline of the one kernel launched per step (per-launch time = per-step time)
+    # roofline of the one kernel launched per step (per-launch time = per-step time),
+    # against the peak that matches the timed region's clocks
     t_launch = t_total / steps
-    t_fp8, t_hbm = roofline_times(wl, pk)
-    if t_fp8 >= t_hbm:
-        peak = fp8_peak(pk)
-        achieved = wl.flops() / t_launch / 1e12
-        roof = {"bound": "tensor", "achieved": round(achieved, 2),
-                "peak": round(peak, 1), "unit": "TFLOP/s",
-                "peak_source": f"{pk_kind} bf16 sustained (back to back, at the power cap) "
-                               f"{pk.get('bf16_tflops_sustained', pk['bf16_tflops'])} TFLOP/s x "
-                               f"{FP8_OVER_BF16:g} (nominal fp8/bf16 dense ratio); the timed "
-                               f"region runs the kernel back to back",
-                "frac_of_burst": round(achieved / fp8_peak(pk, sustained=False), 4)}
+    rf = roofline(wl, pk, t_launch, clocks["sm_mhz"])
+    burst, sust, f_sust = fp8_peaks(pk)
+    if rf["bound"] == "tensor":
+        roof = {"bound": "tensor", "achieved": round(wl.flops() / t_launch / 1e12, 2),
+                "peak": round(rf["p_fp8"], 1), "unit": "TFLOP/s",
+                "peak_source": f"{pk_kind}: bf16 GEMM {pk['bf16_tflops']} TFLOP/s burst / "
+                               f"{pk.get('bf16_tflops_sustained')} sustained (at "
+                               f"{f_sust} MHz) x {FP8_OVER_BF16:g}, the nominal fp8/bf16 "
+                               f"dense ratio"}
     else:
         roof = {"bound": "hbm", "achieved": round(wl.bytes() / t_launch / 1e9, 1),
                 "peak": pk["hbm_gbs"], "unit": "GB/s",
                 "peak_source": f"{pk_kind} copy bandwidth"}
     roof["frac"] = round(roof["achieved"] / roof["peak"], 4)
     roof["traffic"] = dram_traffic(wl.name)
+    roof["peak_choice"] = rf["peak_choice"]
+    roof["sm_mhz"] = clocks["sm_mhz"]
+    for k in ("frac_of_burst", "frac_of_sustained", "frac_at_clock", "frac_nominal"):
+        if k in rf:
+            roof[k] = round(rf[k], 4)
     roof["algorithmic"] = {"flops": wl.flops(), "bytes": wl.bytes()}
     roof["kernel"] = fx.variant_name(plan.variant)
 
-    # end to end through the C ABI with host buffers: every step copies its inputs in from
-    # pinned host memory, makes the call, and copies its result out.  Two device buffer sets
-    # let step j + 1's inputs cross the host link while step j computes and its result comes
-    # back (host-to-device copies, calls and device-to-host copies on three streams, ordered
-    # by events so that no buffer is overwritten before the step that reads it is done).
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": ws,
+        "steps": steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3 x e4m3 -> fp32 accumulate -> bf16", "data": "synthetic",
+        "config": {**workload_config(wl, ws),
+                   "us_per_call": round(ms_per_step * 1e3, 2),
+                   "variant": fx.variant_name(plan.variant), "grid": plan.grid,
+                   "accumulation_chunk_kblocks": fx.mslkb_accumulation_chunk()},
+        "roofline": roof,
+        "e2e": e2e,
+        "gpu_launches": steps,
+        "clocks": clocks,
+        "device_status": status,
+    }
+    if args.cpu and rank == 0 and ws == 1:
+        rows = args.cpu_rows
+        flops, times, threads = time_oracle(wl, rows)
+        result["cpu_baseline"] = {
+            "value": round(flops / times[0] / 1e12, 6), "unit": UNIT, "cores": threads,
+            "kind": "oracle", "seconds": round(times[0], 2),
+            "sample": f"{rows} output rows x N={wl.N} x K={wl.K} of {wl.name} (one group's "
+                      f"weights), plain fp64 C oracle, OpenMP over rows"}
+    if sweep:
+        # compact rows, last on the line: each shape's roofline fraction against the peak
+        # that matches the clocks of its own timed replays
+        rows = [shape_row(r, pk, clk) for r in sweep]
+        rows.append([wl.name, round(ms_per_step * 1e3, 2), round(value / ws, 1), rf["bound"],
+                     round(rf["frac"], 3), round(rf["frac_nominal"], 3), clocks["sm_mhz"],
+                     fx.variant_name(plan.variant)])
+        result["per_shape_cols"] = PER_SHAPE_COLS
+        result["per_shape"] = rows
+    if rank == 0:
+        print(json.dumps(result, separators=(",", ":")), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def e2e_leg(fx, wl, inp, out, stream, sp, steps, ws, device):
+    """End to end through the C ABI with host buffers: every step copies its inputs in from
+    pinned host memory, makes the call, and copies its result out.  Two device buffer sets
+    let step j + 1's inputs cross the host link while step j computes and its result comes
+    back (host-to-device copies, calls and device-to-host copies on three streams, ordered
+    by events so that no buffer is overwritten before the step that reads it is done)."""
+    import torch
     host = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in inp.items()}
     for k in inp:
         host[k].copy_(inp[k])
@@ -448,11 +640,13 @@ def gpu_arm(args):
     ev_in = [torch.cuda.Event() for _ in range(2)]
     ev_k = [torch.cuda.Event() for _ in range(2)]
     ev_o = [torch.cuda.Event() for _ in range(2)]
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
     e2e_steps = max(3, min(steps, 10))
     h2d = sum(v.numel() * v.element_size() for v in host.values())
     d2h = host_out.numel() * host_out.element_size()
 
-    def e2e_steps_run(n):
+    def run(n):
         for j in range(n):
             b = j % 2
             if j >= 2:
@@ -472,62 +666,21 @@ def gpu_arm(args):
                 host_out.copy_(outs[b], non_blocking=True)
             ev_o[b].record(s_out)
 
-    e2e_steps_run(2)  # untimed round
+    run(2)  # untimed round
     torch.cuda.synchronize()
     dist_barrier(ws)
     e0.record(s_in)
-    e2e_steps_run(e2e_steps)
+    run(e2e_steps)
     e1.record(s_out)  # after the last result's copy, which follows every earlier step
     e1.synchronize()
     torch.cuda.synchronize()
     dist_barrier(ws)
     t_e2e = dist_max(e0.elapsed_time(e1) / 1e3, ws, device)
-    e2e = {"value": round(ws * wl.flops() * e2e_steps / t_e2e / 1e12, 3), "unit": UNIT,
-           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-           "ms_per_step": round(t_e2e / e2e_steps * 1e3, 3), "steps": e2e_steps}
     del host, dev, outs, host_out
-
-    result = {
-        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": ws,
-        "steps": steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "e4m3 x e4m3 -> fp32 accumulate -> bf16", "data": "synthetic",
-        "config": {**workload_config(wl, ws),
-                   "us_per_call": round(ms_per_step * 1e3, 2),
-                   "variant": fx.variant_name(plan.variant), "grid": plan.grid,
-                   "accumulation_chunk_kblocks": fx.mslkb_accumulation_chunk()},
-        "roofline": roof,
-        "e2e": e2e,
-        "gpu_launches": steps,
-        "clocks": clk.summary(),
-        "device_status": status,
-    }
-    if args.variant is not None:
-        fx.mslkb_force_variant(-1)  # the sweep runs the planner's choices
-    if args.sweep and rank == 0:
-        shapes = []
-        for name in SWEEP:
-            try:
-                shapes.append(sweep_shape(fx, workloads()[name], pk, device))
-            except Exception as e:  # noqa: BLE001 - report and continue
-                shapes.append({"workload": name, "error": repr(e)})
-        shapes.append({"workload": wl.name, "us_per_call": round(ms_per_step * 1e3, 2),
-                       "tflops": round(value / ws, 2), "roofline_frac": roof["frac"],
-                       "bound": roof["bound"], "variant": fx.variant_name(plan.variant)})
-        result["per_shape"] = shapes
-    if args.cpu and rank == 0 and ws == 1:
-        rows = args.cpu_rows
-        flops, times, threads = time_oracle(wl, rows)
-        result["cpu_baseline"] = {
-            "value": round(flops / times[0] / 1e12, 6), "unit": UNIT, "cores": threads,
-            "kind": "oracle", "seconds": round(times[0], 2),
-            "sample": f"{rows} output rows x N={wl.N} x K={wl.K} of {wl.name} (one group's "
-                      f"weights), plain fp64 C oracle, OpenMP over rows"}
-    if rank == 0:
-        print(json.dumps(result), flush=True)
-    if ws > 1:
-        import torch.distributed as dist
-        dist.destroy_process_group()
+    torch.cuda.empty_cache()
+    return {"value": round(ws * wl.flops() * e2e_steps / t_e2e / 1e12, 3), "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": round(t_e2e / e2e_steps * 1e3, 3), "steps": e2e_steps}
 
 
 def reference_arm(args):

@@ -123,6 +123,10 @@ def lib() -> ctypes.CDLL:
             L.mslkb_set_wait_timeout_us.restype = ctypes.c_int
             L.mslkb_test_stall_next_launch.argtypes = []
             L.mslkb_test_stall_next_launch.restype = ctypes.c_int
+            L.mslkb_release_workspace.argtypes = [p]
+            L.mslkb_release_workspace.restype = ctypes.c_int
+            L.mslkb_workspace_count.argtypes = []
+            L.mslkb_workspace_count.restype = ctypes.c_int32
             L.mslkb_version.argtypes = []
             L.mslkb_version.restype = ctypes.c_int32
             _lib = L
@@ -268,6 +272,21 @@ def mslkb_test_speculate_from_next_launch(meta) -> None:
     """Test hook: the next launch's speculative weight prefetch reads `meta` (a device
     tensor laid out like that call's metadata) instead of the call's own metadata."""
     lib().mslkb_test_speculate_from_next_launch(ctypes.c_void_p(meta.data_ptr()))
+
+
+def mslkb_release_workspace(stream=None) -> None:
+    """Free the split-tile workspace of `stream` (default: the current torch stream) on
+    the current device; the next call on that stream allocates a new one."""
+    if stream is None:
+        import torch
+        stream = torch.cuda.current_stream().cuda_stream
+    s = lib().mslkb_release_workspace(ctypes.c_void_p(stream))
+    if s != MSLKB_OK:
+        raise MslkbError(s, "mslkb_release_workspace")
+
+
+def mslkb_workspace_count() -> int:
+    return lib().mslkb_workspace_count()
 
 
 def mslkb_test_stall_next_launch() -> None:

@@ -78,8 +78,9 @@ struct GemmParams {
   float* sk_ws;            // split tiles: fp32 partial sums, 2 slots per CTA
   uint32_t* sk_cnt;        // split tiles: arrival counters, one per (tile, epilogue warp)
   uint64_t timeout_ns;     // give-up time of one pipeline wait
-  int32_t test_stall;      // test hook: CTA 0 withholds its first stage (single-CTA TMA
-                           // kernels), so its MMA wait runs out and the timeout path runs
+  int32_t test_stall;      // test hook: CTA 0 (CTA pairs: the first pair) withholds its
+                           // first stage (TMA kernels), so the MMA wait runs out and the
+                           // timeout path runs
   int32_t prefetch_kb;     // swap-AB: K blocks of weights each CTA asks L2 to prefetch
                            // before the dependency wait (0: none)
   const int64_t* spec_meta;  // metadata the speculative schedule reads (= meta, unless a
@@ -960,7 +961,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         // GB300: +2-4 % on the weight-streaming shapes, a loss on the 128-row tiles)
         const uint64_t pol_act = ptx::l2_policy_evict_last();
         const uint64_t pol_w = ptx::l2_policy_evict_first();
-        bool withhold = p.test_stall != 0 && blockIdx.x == 0;
+        // test hook: the first CTA (CTA pairs: both CTAs of the first pair) skips one stage
+        bool withhold = p.test_stall != 0 && worker == 0;
         for (int32_t i = 0; ok && (dyn || i < work.n_items); ++i) {
           Item it;
           if (dyn) {
@@ -980,12 +982,18 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
               break;
             }
             if constexpr (Cfg::kPair) {
-              // both CTAs' bytes complete on the leader's full barrier, which expects them all
-              const uint32_t fb = ptx::mapa_shared(full_bar(stage), 0u);
-              if (crank == 0) ptx::mbar_arrive_expect_tx(full_bar(stage), 2 * Cfg::kStageBytes);
-              ptx::tma_load_2d_pair(s_act + stage * Cfg::kActBytes, &tmA, fb, kb * kBK, c.m0);
-              ptx::tma_load_3d_pair(s_w + stage * Cfg::kWBytes, &tmB, fb, kb * kBK,
-                                    c.n0 + static_cast<int32_t>(crank) * Cfg::kWRows, c.g);
+              if (withhold) {
+                // neither CTA of the pair arrives or loads: the leader's full barrier for this
+                // stage never completes, so the leader's MMA wait runs out
+                withhold = false;
+              } else {
+                // both CTAs' bytes complete on the leader's full barrier, which expects them all
+                const uint32_t fb = ptx::mapa_shared(full_bar(stage), 0u);
+                if (crank == 0) ptx::mbar_arrive_expect_tx(full_bar(stage), 2 * Cfg::kStageBytes);
+                ptx::tma_load_2d_pair(s_act + stage * Cfg::kActBytes, &tmA, fb, kb * kBK, c.m0);
+                ptx::tma_load_3d_pair(s_w + stage * Cfg::kWBytes, &tmB, fb, kb * kBK,
+                                      c.n0 + static_cast<int32_t>(crank) * Cfg::kWRows, c.g);
+              }
             } else if (withhold) {
               withhold = false;  // this stage's full barrier never completes
             } else {

@@ -19,6 +19,7 @@
 
 #include "launch.h"
 #include "mslkb.h"
+#include "mslkb_tuning.h"
 
 namespace {
 
@@ -44,6 +45,7 @@ std::atomic<int> g_forced_variant{-1};
 // at 0.24 / 0.50 / 1.04 of the 1e-6 * sum|terms| tolerance for chunks of 4 / 8 / 16
 // K-blocks; the llama405b shape runs 2777 / 2938 / 3060 (whole K) TFLOPS at full clock.
 constexpr int kDefaultKbPerChunk = 8;
+constexpr int kMaxKbPerChunk = 8;
 std::atomic<int> g_kb_per_chunk{kDefaultKbPerChunk};
 // swap-AB weight prefetch ahead of the dependency wait, in K blocks (16 KB of weights each)
 // per CTA; -1 = the default.  Measured on GB300 (back-to-back calls, llama3-70b shapes):
@@ -847,6 +849,37 @@ mslkb_status mslkb_get_device_status(void* stream, uint32_t* flags) {
   return MSLKB_OK;
 }
 
+mslkb_status mslkb_release_workspace(void* stream) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  const auto key = std::make_pair(dev, reinterpret_cast<uintptr_t>(stream));
+  Workspace w;
+  {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    auto it = g_workspaces.find(key);
+    if (it == g_workspaces.end()) return MSLKB_OK;
+    w = it->second;
+    g_workspaces.erase(it);
+  }
+  // the stream's enqueued calls may still use it
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  if ((e = cudaStreamSynchronize(cs)) != cudaSuccess) return cuda_fail(e);
+  if ((e = cudaFree(w.partials)) != cudaSuccess) return cuda_fail(e);
+  if ((e = cudaFree(w.counters)) != cudaSuccess) return cuda_fail(e);
+  return MSLKB_OK;
+}
+
+int32_t mslkb_workspace_count(void) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  int32_t n = 0;
+  for (const auto& kv : g_workspaces)
+    if (kv.first.first == dev) ++n;
+  return n;
+}
+
 mslkb_status mslkb_plan(int32_t layout, int64_t rows, int64_t G, int64_t N, int64_t K,
                         int32_t num_sms, int64_t a_align, int64_t b_align,
                         mslkb_plan_info* info) {
@@ -894,7 +927,9 @@ mslkb_status mslkb_set_split_k(int32_t enable) {
 }
 
 mslkb_status mslkb_set_accumulation_chunk(int32_t kblocks) {
-  if (kblocks < 0) return MSLKB_ERR_SHAPE;
+  // longer chunks (or the whole K) let the tensor core's round-toward-zero adds run past
+  // the tolerance on cancelling sums
+  if (kblocks < 1 || kblocks > kMaxKbPerChunk) return MSLKB_ERR_SHAPE;
   g_kb_per_chunk.store(kblocks);
   return MSLKB_OK;
 }

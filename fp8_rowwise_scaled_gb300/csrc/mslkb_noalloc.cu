@@ -1,11 +1,10 @@
 // mslkb_noalloc.cu -- the allocation-free stacked entry point.
 //
-// Some callers cannot allocate device memory at call time: code recording a CUDA graph
-// (allocation is not allowed during stream capture), plug-ins whose host framework owns
-// all device memory, and serving loops that cannot take the device-wide synchronisation a
-// cudaMalloc can bring.  This entry point runs the same stacked kernel with tiles split
-// along K, but the split tiles' scratch lives in one static device array instead of a
-// workspace the library allocates per stream.
+// Some callers cannot allocate device memory when they call this library: plug-ins whose
+// host framework owns all device memory, and serving loops that cannot take the
+// device-wide synchronisation a cudaMalloc can bring.  This entry point runs the same
+// stacked kernels, but the split tiles' scratch lives in one static device array instead
+// of a workspace the library allocates per stream; nothing here allocates.
 #include <cuda_runtime.h>
 
 #include <cstdint>

@@ -26,7 +26,8 @@
  *   driver entry point).  The first call on each stream (outside stream capture) also
  *   allocates that stream's workspace (2 x #SMs x 128 KB of fp32 partial sums for split
  *   tiles, plus counters, among them the tile claim counter of the CTA-pair plans; about
- *   40 MB on GB300); later calls allocate nothing and may be captured in a CUDA graph.  A
+ *   40 MB on GB300), which lasts until mslkb_release_workspace or the end of the process;
+ *   later calls on the stream allocate nothing and may be captured in a CUDA graph.  A
  *   call captured on a stream that has no workspace yet runs without splitting tiles and,
  *   on CTA pairs, takes its tiles in a fixed stride (same results within tolerance,
  *   possibly slower).
@@ -238,23 +239,25 @@ MSLKB_API mslkb_status mslkb_f8f8bf16_groupwise_grouped_stacked(
 /*
  * Allocation-free stacked call (no counterpart on the pages: an addition of this library).
  *
- * For callers that must not allocate device memory: code recording a CUDA graph (memory
- * allocation is not allowed during stream capture), plug-ins whose host framework owns
- * every device allocation, and serving loops that cannot afford the device-wide
- * synchronisation a cudaMalloc can cause.  Same arguments, layout, results and errors as
- * mslkb_f8f8bf16_rowwise_grouped_stacked; the caller still provides inputs and output.
+ * For callers that cannot allocate device memory when they call: plug-ins whose host
+ * framework owns every device allocation (and gives a library none of its own), and
+ * serving loops that cannot take the device-wide synchronisation a cudaMalloc can cause.
+ * Same arguments, layout, results and errors as mslkb_f8f8bf16_rowwise_grouped_stacked;
+ * the caller still provides inputs and output.  It calls no cudaMalloc, cudaFree or other
+ * allocating routine.
  *
  * Its split-tile scratch (fp32 partial sums and arrival counters) is a static device
  * array of MSLKB_NOALLOC_SCRATCH_BYTES (8 MiB) that every GPU loading the library holds
  * until the process exits.  The plans that split tiles by default (swap-AB tiles, up to
  * 32 rows per group on average, e.g. MoE decode) need at most 2 x #SMs x 16 KB of it; a
  * plan that needs more -- 128-row activation tiles split under mslkb_set_split_k(2), or a
- * device with very many SMs -- returns MSLKB_ERR_TOO_LARGE and launches nothing.
- * The first call on a device looks up the array's device address (a CUDA call);
- * make that first call before any stream capture.  Each call clears the counters it
- * uses on `stream` (cudaMemsetAsync) before its kernel.  All calls share the one array:
- * calls that overlap on the GPU (different streams, or graphs replayed concurrently) race
- * and must be serialised by the caller.
+ * device with very many SMs -- returns MSLKB_ERR_TOO_LARGE and launches nothing.  CTA-pair
+ * plans take their tiles in a fixed stride here (no claim counter).
+ * The first call on a device looks up the array's device address (cudaGetSymbolAddress,
+ * once per device, with that device current).  Each call clears the counters it uses on
+ * `stream` (cudaMemsetAsync) before its kernel.  All calls share the one array, which
+ * keeps the last call's contents: calls that overlap on the GPU (different streams, say)
+ * race and must be serialised by the caller.
  */
 #define MSLKB_NOALLOC_SCRATCH_BYTES (8u << 20)
 MSLKB_API mslkb_status mslkb_f8f8bf16_rowwise_grouped_stacked_noalloc(
@@ -320,77 +323,26 @@ MSLKB_API mslkb_status mslkb_variant_resources(int32_t variant, int32_t *blocks_
                                                int32_t *regs_per_thread);
 
 /*
- * Test hook: force every following call on any thread to use one variant (index from
- * mslkb_variant_name; -1 restores the heuristic).  A variant that cannot serve a call
- * (a TMA variant with K % 16 != 0, say) makes that call return MSLKB_ERR_SHAPE.
- * Used to check that different variants give bit-identical results.
- */
-MSLKB_API mslkb_status mslkb_force_variant(int32_t variant);
-
-/*
- * Split policy (stream-K).  With T output tiles and P CTAs, tiles of all full waves but
- * the last run whole; the remaining tiles are cut into K blocks and every CTA takes an
- * equal contiguous share, so no SM idles in the last wave.  A split tile is finished by
- * the CTA that completes its last piece, which adds the fp32 partial sums of all pieces
- * in a fixed order (results do not depend on timing).  0 runs whole tiles only; 1 (the
- * default) splits plans with swap-AB tiles (few rows per group: each piece's partial sums
- * are small, and more SMs stream the weights); 2 splits every plan.  Applies to every
- * following call from any thread; a tuning and test hook.  Other values give
- * MSLKB_ERR_SHAPE.
- */
-MSLKB_API mslkb_status mslkb_set_split_k(int32_t enable);
-
-/*
- * Accumulation chunk.  The tensor core's own fp32 accumulation adds with round-toward-
- * zero; over a long K with cancelling partial sums that bias exceeds the tolerance of
- * 1e-6 * sum|terms|.  So the kernel lets the tensor core sum at most `kblocks` blocks of
- * 128 K elements into one TMEM buffer, and its epilogue adds each such partial sum into
- * fp32 registers with round-to-nearest (the accumulator is still fp32 and is never
- * rounded to a narrower type before the scales are applied).  Default 8 (1024 K
- * elements): partial sums built to cancel inside every chunk then stay within half the
- * tolerance on GB300 (4 K-blocks: a quarter; 16: just over it); 0 lets the tensor core
- * accumulate the whole K.  Applies to every following call from
- * any thread; a tuning and test hook.  Negative values give MSLKB_ERR_SHAPE.
- */
-MSLKB_API mslkb_status mslkb_set_accumulation_chunk(int32_t kblocks);
-MSLKB_API int32_t mslkb_accumulation_chunk(void);
-
-/*
- * Weight prefetch of the swap-AB (few rows per group) plans.  With programmatic dependent
- * launch a CTA can be resident while the kernel before it on the stream finishes; in that
- * time it reads the group metadata speculatively, works out its first `kblocks` K blocks
- * of weights and asks L2 to prefetch them.  A hint only: the schedule is rebuilt from the
- * metadata after the dependency wait, and every load reads L2, which is coherent with
- * what the earlier kernel writes.  -1: the default, 14 K blocks (224 KB of weights per
- * CTA); 0: off.
- * Applies to every following call from any thread; a tuning and test hook.  Values
- * below -1 give MSLKB_ERR_SHAPE.
- */
-MSLKB_API mslkb_status mslkb_set_weight_prefetch(int32_t kblocks);
-
-/*
- * Test hook for the weight prefetch: the next launch through the stacked, dynamic or
- * offsets entry points builds its speculative schedule from `meta` (a device buffer laid
- * out like that call's own metadata, G entries) instead of the call's metadata, so that
- * the prefetch goes to other tiles than the call computes.  The results must not change.
- */
-MSLKB_API mslkb_status mslkb_test_speculate_from_next_launch(const void* meta);
-
-/*
  * Failure detection (an addition of this library; the pages have no counterpart).  Every
  * wait of the kernels' pipelines is bounded: a wait that runs past the limit (default
  * ~1 s) makes the kernel give up, record MSLKB_DEV_TIMEOUT in the device status word, let
  * its copies in flight land, free its tensor memory and return, so the context stays
  * usable.  mslkb_set_wait_timeout_us sets the limit for the following launches (0: the
  * default; otherwise at least 1000 us, else MSLKB_ERR_SHAPE).
- *
- * mslkb_test_stall_next_launch is a test hook: the next launch through the stacked,
- * dynamic, offsets or batched entry points of a single-CTA TMA kernel has its CTA 0
- * withhold one pipeline stage, so that CTA's MMA wait runs out and the timeout path runs
- * (that launch's output is incomplete; the status word reports the timeout).
  */
 MSLKB_API mslkb_status mslkb_set_wait_timeout_us(int64_t us);
-MSLKB_API mslkb_status mslkb_test_stall_next_launch(void);
+
+/*
+ * Frees the split-tile workspace of `stream` on the current device (see the conventions
+ * above), after waiting for the work already enqueued on `stream`.  The next call on that
+ * stream allocates a new one.  A CUDA graph captured on the stream keeps the address of
+ * the workspace it was captured with: destroy such graphs first.  A stream with no
+ * workspace: nothing to do.  Other streams' workspaces are not touched.
+ */
+MSLKB_API mslkb_status mslkb_release_workspace(void *stream);
+
+/* Number of stream workspaces the library holds on the current device. */
+MSLKB_API int32_t mslkb_workspace_count(void);
 
 /* Library version, as major * 10000 + minor * 100 + patch. */
 MSLKB_API int32_t mslkb_version(void);

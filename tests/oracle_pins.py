@@ -79,8 +79,9 @@ def pin_bf16_golden(orc):
         assert got == bits, f"bf16({hi!r} + {lo!r}) = {got:#06x}, expected {bits:#06x}"
 
 
-def pin_bf16_vs_torch(orc, n=200_000, seed=11):
-    """Every binary32 value: the oracle's rounding equals torch's fp32 -> bf16 RNE."""
+def pin_bf16_vs_torch(orc, n=10_000_000, seed=11):
+    """A 10^7-value sweep of binary32 (a quarter on exact bf16 midpoints, a quarter next to
+    them, an eighth subnormal): the oracle's rounding equals torch's fp32 -> bf16 RNE."""
     rng = _rng(seed)
     bits = rng.integers(0, 2 ** 32, size=n, dtype=np.uint64).astype(np.uint32)
     # force a quarter of the sample onto exact bf16 midpoints, a quarter near them

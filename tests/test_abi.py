@@ -1,5 +1,5 @@
 """C-ABI checks that need no GPU: the library builds, loads and exports every symbol
-include/mslkb.h declares; argument errors are reported before any CUDA call; the host
+include/*.h declare; argument errors are reported before any CUDA call; the host
 planner picks the intended kernel variant for each workload shape."""
 import ctypes
 import os
@@ -12,7 +12,7 @@ from fp8_rowwise_scaled_gb300 import build as fxbuild
 from fp8_rowwise_scaled_gb300.synthetic import workloads
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "mslkb.h")
+HEADERS = [os.path.join(ROOT, "include", h) for h in ("mslkb.h", "mslkb_tuning.h")]
 
 
 @pytest.fixture(scope="module")
@@ -22,7 +22,7 @@ def L():
 
 
 def declared_functions():
-    text = open(HEADER).read()
+    text = "".join(open(h).read() for h in HEADERS)
     return sorted(set(re.findall(r"MSLKB_API\s+[\w\s\*]*?\b(mslkb_\w+)\s*\(", text)))
 
 
@@ -174,15 +174,32 @@ def test_groupwise_argument_errors_and_plan(L):
 
 
 def test_accumulation_chunk_setting(L):
+    """Only chunk lengths that keep the tolerance (1-8 K blocks) are accepted; a rejected
+    value leaves the setting as it was."""
     old = fx.mslkb_accumulation_chunk()
     assert old == 8
     try:
-        fx.mslkb_set_accumulation_chunk(0)
-        assert fx.mslkb_accumulation_chunk() == 0
-        with pytest.raises(fx.MslkbError):
-            fx.mslkb_set_accumulation_chunk(-1)
+        fx.mslkb_set_accumulation_chunk(1)
+        assert fx.mslkb_accumulation_chunk() == 1
+        for bad in (0, -1, 9, 16, 1 << 20):
+            with pytest.raises(fx.MslkbError):
+                fx.mslkb_set_accumulation_chunk(bad)
+            assert fx.mslkb_accumulation_chunk() == 1
     finally:
         fx.mslkb_set_accumulation_chunk(old)
+    assert fx.mslkb_accumulation_chunk() == 8
+
+
+def test_hooks_live_in_their_own_header():
+    """The process-global tuning and test hooks are declared apart from the entry points."""
+    def declared(path):
+        return set(re.findall(r"MSLKB_API\s+[\w\s\*]*?\b(mslkb_\w+)\s*\(", open(path).read()))
+    main, tuning = declared(HEADERS[0]), declared(HEADERS[1])
+    assert not main & tuning
+    for name in ("mslkb_force_variant", "mslkb_set_split_k", "mslkb_set_accumulation_chunk",
+                 "mslkb_set_weight_prefetch", "mslkb_test_stall_next_launch",
+                 "mslkb_test_speculate_from_next_launch"):
+        assert name in tuning and name not in main
 
 
 def test_variant_table(L):

@@ -65,3 +65,58 @@ def test_wait_runs_out_and_the_context_survives(L, shape):
     ab, _ = orc.stacked(abs_codes(h["A"]), abs_codes(h["B"]), np.abs(h["sa"]), np.abs(h["sb"]),
                         h["meta"])
     compare(out.ravel(), ref.ravel(), ab.ravel(), f"after a timeout ({shape})")
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("layout", ["stacked", "dynamic"])
+def test_cta_pair_wait_runs_out_and_the_next_calls_are_right(L, layout):
+    """The same on the CTA-pair kernels: both CTAs of the first pair skip one stage, so the
+    leader's MMA wait runs out, the peer's waits run out after it, and both meet at the
+    pair's teardown barriers, free their tensor memory and return.  The stacked plan takes
+    its tiles from the stream's claim counter, which the last leader through teardown resets
+    on the abort path too: the next call, enqueued right behind the stalled one (before the
+    host reads the status word, which would also clear the counter), and one more after it
+    must both match the oracle.  The dynamic plan takes its tiles in a fixed stride."""
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    g = torch.Generator().manual_seed(78)
+    if layout == "stacked":
+        G, N, K, meta, E = 2, 8192, 1024, [1100, 1000], 0
+        rows = sum(meta)
+    else:
+        G, N, K, meta, E = 4, 8192, 512, [600, 300, 0, 599], 600
+        rows = G * E
+    A = random_codes((rows, K), g).numpy()
+    B = random_codes((G, N, K), g).numpy()
+    sa = (torch.rand(rows, generator=g) + 0.5).numpy().astype(np.float32)
+    sb = (torch.rand(G * N, generator=g) + 0.5).numpy().astype(np.float32).reshape(G, N)
+    prob = Problem.from_numpy(layout, A, B, sa, sb, meta, expected_m=E)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    plan = fx.mslkb_plan(0 if layout == "stacked" else 1, rows if layout == "stacked" else E,
+                         G, N, K, sms)
+    assert fx.variant_name(plan.variant) == f"{layout}_pair256x256_tma"
+    orc = oracle.load(0)
+    ref, ab = prob.oracle_full(orc)
+
+    def poisoned():
+        return torch.full((rows, N), 0x7E7E, dtype=torch.int16,
+                          device="cuda").view(torch.bfloat16)
+
+    fx.device_status()                        # start clean
+    outs = [poisoned() for _ in range(3)]
+    fx.mslkb_set_wait_timeout_us(50_000)      # 50 ms
+    try:
+        fx.mslkb_test_stall_next_launch()
+        prob.run_gpu(out=outs[0])
+    finally:
+        fx.mslkb_set_wait_timeout_us(0)
+    prob.run_gpu(out=outs[1])                 # right behind the stalled launch
+    torch.cuda.synchronize()                  # both return: no hang, no fault
+    assert fx.device_status() & fx.MSLKB_DEV_TIMEOUT
+    compare(bits_of(outs[1]).ravel(), ref.ravel(), ab.ravel(),
+            f"{layout} pairs, the call after a timeout")
+    prob.run_gpu(out=outs[2])
+    torch.cuda.synchronize()
+    assert fx.device_status() == 0
+    compare(bits_of(outs[2]).ravel(), ref.ravel(), ab.ravel(),
+            f"{layout} pairs, the second call after a timeout")

@@ -351,10 +351,10 @@ def test_accumulator_cancellation_inside_chunks(orc):
         _check_full(prob, orc, variant=v, what=f"chunk-scale cancellation {v}")
 
 
-@pytest.mark.parametrize("kpc", [0, 1, 3, 4, 32])
+@pytest.mark.parametrize("kpc", [1, 3, 4, 7])
 def test_accumulation_chunk_lengths(orc, kpc):
-    """Every chunk length (0 = the whole K in the tensor core) stays within tolerance on
-    random data, including a K whose last chunk is partial."""
+    """Every accepted chunk length stays within tolerance on random data, including a K
+    whose last chunk is partial."""
     prob = _rand_problem("stacked", 3, 264, 128 * 13 + 64, [150, 0, 77], seed=21)
     old = fx.mslkb_accumulation_chunk()
     try:

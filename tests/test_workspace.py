@@ -1,0 +1,60 @@
+"""Per-stream split-tile workspaces: the first call on a stream allocates one, and
+mslkb_release_workspace frees it; the next call on that stream allocates a new one and
+still matches the oracle (split swap-AB tiles, which use its partial sums and counters, and
+CTA pairs, which take their tiles from its claim counter)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import fp8_rowwise_scaled_gb300 as fx
+from fp8_rowwise_scaled_gb300 import build as fxbuild
+from fp8_rowwise_scaled_gb300.synthetic import random_codes
+from parity_util import Problem, bits_of, compare
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    fxbuild.build()
+    fx.lib()
+
+
+def _problem(G, N, K, m_sizes, seed):
+    g = torch.Generator().manual_seed(seed)
+    rows = int(sum(m_sizes))
+    A = random_codes((rows, K), g).numpy()
+    B = random_codes((G, N, K), g).numpy()
+    sa = (torch.rand(rows, generator=g) + 0.5).numpy().astype(np.float32)
+    sb = (torch.rand(G * N, generator=g) + 0.5).numpy().astype(np.float32).reshape(G, N)
+    return Problem.from_numpy("stacked", A, B, sa, sb, m_sizes)
+
+
+@pytest.mark.parametrize("case", ["split_swap", "cta_pairs"])
+def test_release_then_call_again(case):
+    if case == "split_swap":
+        prob = _problem(8, 2048, 2048, [1, 0, 3, 2, 0, 1, 1, 2], 61)
+        want = "stacked_swap_w128xa16_tma"
+    else:
+        prob = _problem(2, 8192, 256, [1100, 1000], 62)
+        want = "stacked_pair256x256_tma"
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    plan = fx.mslkb_plan(0, prob.rows, prob.G, prob.N, prob.K, sms)
+    assert fx.variant_name(plan.variant) == want
+    orc = oracle.load(0)
+    ref, ab = prob.oracle_full(orc)
+    s = torch.cuda.Stream()
+    base = fx.mslkb_workspace_count()
+    for rnd in range(2):
+        with torch.cuda.stream(s):
+            out = prob.run_gpu()
+        s.synchronize()
+        assert fx.mslkb_workspace_count() == base + 1
+        compare(bits_of(out).ravel(), ref.ravel(), ab.ravel(), f"{case}, round {rnd + 1}")
+        fx.mslkb_release_workspace(s.cuda_stream)
+        assert fx.mslkb_workspace_count() == base
+    fx.mslkb_release_workspace(s.cuda_stream)  # nothing left to release: fine
+    assert fx.device_status() == 0

@@ -1,12 +1,16 @@
-"""The allocation-free stacked entry point, through the C ABI.
+"""The allocation-free stacked entry point, through the C ABI, against the oracle.
 
-Callers that cannot allocate device memory -- code recording a CUDA graph, plug-ins whose
-framework owns all device memory, serving loops that cannot take a cudaMalloc's device
-synchronisation -- use mslkb_f8f8bf16_rowwise_grouped_stacked_noalloc, whose split-tile
-scratch is a static device array.  Its output must match the regular stacked entry
-point's within the parity tolerance, on two calls in a row (the second call finds the
-array holding the first call's leftovers).  This file runs last so that a failure here
-cannot hide any other test; it passes alone in a fresh process as well.
+Some callers cannot allocate device memory when they call this library: plug-ins whose
+host framework owns every device allocation, and serving loops that cannot take the
+device-wide synchronisation a cudaMalloc can cause.  They use
+mslkb_f8f8bf16_rowwise_grouped_stacked_noalloc, whose split-tile scratch is a static
+device array instead of a workspace the library allocates.  Its output must match the
+oracle within the parity tolerance on two calls in a row (the second call finds the array
+holding the first call's leftovers), on every kind of plan it can take: split swap-AB
+tiles (some or all tiles split), the cp.async loader for a K that is not a multiple of
+16, K = 0, and CTA pairs (which take their tiles in a fixed stride here).  This file runs
+last so that a failure here cannot hide any other test; it passes alone in a fresh
+process as well.
 """
 import numpy as np
 import pytest
@@ -16,7 +20,7 @@ import oracle
 import fp8_rowwise_scaled_gb300 as fx
 from fp8_rowwise_scaled_gb300 import build as fxbuild
 from fp8_rowwise_scaled_gb300.synthetic import random_codes
-from parity_util import Problem, abs_codes, bits_of, compare
+from parity_util import Problem, bits_of, compare
 
 pytestmark = pytest.mark.gpu
 
@@ -27,6 +31,11 @@ def _gpu():
         pytest.skip("needs a CUDA GPU")
     fxbuild.build()
     fx.lib()
+
+
+@pytest.fixture(scope="module")
+def orc():
+    return oracle.load(0)
 
 
 def _problem(G, N, K, m_sizes, seed):
@@ -45,32 +54,41 @@ def _call(fn, prob, out):
               prob.meta.data_ptr(), out.data_ptr(), prob.rows, prob.G, prob.N, prob.K, st)
 
 
-@pytest.mark.parametrize("shape", ["split_remainder", "every_tile_split"])
-def test_noalloc_matches_stacked_twice(shape):
-    if shape == "split_remainder":   # whole waves, then a split remainder
-        prob = _problem(16, 4096, 4096, [3, 0, 1, 2, 0, 4, 1, 1, 0, 2, 1, 1, 0, 1, 2, 1], 41)
-    else:                            # fewer tiles than SMs: every tile is split
-        prob = _problem(4, 1024, 4096, [1, 0, 2, 0], 42)
-    sms = torch.cuda.get_device_properties(0).multi_processor_count
-    plan = fx.mslkb_plan(0, prob.rows, prob.G, prob.N, prob.K, sms)
-    assert plan.split_k == 1, "the shape must exercise the split-tile scratch"
+CASES = {
+    # whole waves of swap-AB tiles, then a split remainder
+    "split_remainder": (16, 4096, 4096, [3, 0, 1, 2, 0, 4, 1, 1, 0, 2, 1, 1, 0, 1, 2, 1], 41,
+                        "stacked_swap_w128xa16_tma", True),
+    # fewer tiles than SMs: every tile is split
+    "every_tile_split": (4, 1024, 4096, [1, 0, 2, 0], 42, "stacked_swap_w128xa16_tma", True),
+    # K = 1000 (8 mod 16): the cp.async loader, split too
+    "cpasync_k_tail": (8, 2048, 1000, [2, 0, 1, 3, 0, 1, 4, 1], 44,
+                       "stacked_swap_w128xa16_cpasync", True),
+    # an empty reduction: every owned row +0.0
+    "k_zero": (4, 512, 0, [5, 0, 9, 2], 45, None, False),
+    # groups of ~1000 rows: CTA pairs, tiles in a fixed stride (no claim counter here)
+    "cta_pairs": (2, 8192, 256, [1100, 1000], 46, "stacked_pair256x256_tma", False),
+}
 
-    ref = torch.zeros((prob.rows, prob.N), dtype=torch.bfloat16, device="cuda")
-    assert _call(fx.mslkb_f8f8bf16_rowwise_grouped_stacked, prob, ref) == fx.MSLKB_OK
-    torch.cuda.synchronize()
-    ref_bits = bits_of(ref).ravel()
-    # tolerance term 1e-6 * |sa * sb| * sum_k |a_k b_k| from the oracle on |codes|, |scales|
-    h = prob.host()
-    orc = oracle.load(0)
-    ab, _ = orc.stacked(abs_codes(h["A"]), abs_codes(h["B"]), np.abs(h["sa"]), np.abs(h["sb"]),
-                        h["meta"])
+
+@pytest.mark.parametrize("case", list(CASES))
+def test_noalloc_matches_oracle_twice(orc, case):
+    G, N, K, m_sizes, seed, variant, split = CASES[case]
+    prob = _problem(G, N, K, m_sizes, seed)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    plan = fx.mslkb_plan(0, prob.rows, prob.G, prob.N, prob.K, sms,
+                         a_align=256, b_align=256)
+    if variant is not None:
+        assert fx.variant_name(plan.variant) == variant, "the case must take its plan"
+    assert plan.split_k == int(split), "the case must (not) use the split-tile scratch"
+    ref, ab = prob.oracle_full(orc)
+    fx.device_status()
     for call in range(2):
         out = torch.full((prob.rows, prob.N), 0x7E7E, dtype=torch.int16,
                          device="cuda").view(torch.bfloat16)
         s = _call(fx.mslkb_f8f8bf16_rowwise_grouped_stacked_noalloc, prob, out)
         assert s == fx.MSLKB_OK, fx.mslkb_status_string(s)
         torch.cuda.synchronize()
-        compare(bits_of(out).ravel(), ref_bits, ab.ravel(), f"{shape}, call {call + 1}")
+        compare(bits_of(out).ravel(), ref.ravel(), ab.ravel(), f"{case}, call {call + 1}")
     assert fx.device_status() == 0
 
 
