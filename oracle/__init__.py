@@ -1,5 +1,6 @@
 """CPU oracle for the FP8 rowwise-scaled grouped GEMM (stacked, dynamic, offsets, batched,
-ragged-N and ragged-K layouts) and its block-scaled (groupwise) stacked variant.
+ragged-N and ragged-K layouts) and its block-scaled (groupwise) stacked, dynamic and
+batched variants.
 
 TEST INFRASTRUCTURE ONLY: the tests, the smoke check and the benchmark's CPU-baseline
 leg are the only callers.  Nothing here imports the CUDA library or its package, and
@@ -49,6 +50,7 @@ MUTANTS = {
     11: "ragged-N: the slab of group 0 used for every group",
     12: "ragged-K: every group's slice read from k = 0",
     13: "block scaling: the scales of K block 0 used for every block",
+    14: "block-scaled dynamic: scale_a of the slab-local row",
 }
 
 
@@ -104,6 +106,9 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_blockwise_stacked.argtypes = [p, p, p, p, p, i64, i64, i64, i64, p, i64, p,
                                              ctypes.c_int]
     lib.oracle_blockwise_stacked.restype = ctypes.c_int
+    lib.oracle_blockwise_dynamic.argtypes = [p, p, p, p, p, i64, i64, i64, i64, p, i64, p,
+                                             ctypes.c_int]
+    lib.oracle_blockwise_dynamic.restype = ctypes.c_int
     lib.oracle_dot_int.argtypes = [p, p, i64]
     lib.oracle_dot_int.restype = ctypes.c_int64
     lib.oracle_dot.argtypes = [p, p, i64]
@@ -351,6 +356,37 @@ class Oracle:
             0 if r is None else _ptr(r), 0 if r is None else r.size, _ptr(out), int(threads))
         assert clamped != -2
         return out, bool(clamped)
+
+
+    def blockwise_dynamic(self, A, B, scale_a, scale_b, zsi, expected_m: int, rows=None,
+                          threads: int = 0):
+        """Block-scaled dynamic layout (blocks of 128 along K and N): A [G*E, K] u8,
+        B [G, N, K] u8, scale_a [G*E, K/128] f32, scale_b [G, N/128, K/128] f32, zsi [G]
+        i64 (None: every slab row valid -- the batched layout).  Returns out [G*E, N] u16,
+        or the chosen slab ``rows`` of it; padding rows are +0.0."""
+        A = _c(A, np.uint8)
+        B = _c(B, np.uint8)
+        G, N, K = B.shape
+        E = int(expected_m)
+        sa = _c(scale_a, np.float32).ravel()
+        sb = _c(scale_b, np.float32).ravel()
+        assert K % 128 == 0 and N % 128 == 0
+        assert sa.size == G * E * (K // 128) and sb.size == G * (N // 128) * (K // 128)
+        z = None if zsi is None else _c(zsi, np.int64)
+        r = None if rows is None else _c(rows, np.int64)
+        n_out = G * E if r is None else r.size
+        out = np.zeros((n_out, N), dtype=np.uint16)
+        rc = self.lib.oracle_blockwise_dynamic(
+            _ptr(A), _ptr(B), _ptr(sa), _ptr(sb), 0 if z is None else _ptr(z), G, E, N, K,
+            0 if r is None else _ptr(r), 0 if r is None else r.size, _ptr(out), int(threads))
+        assert rc == 0
+        return out
+
+    def blockwise_batched(self, A, B, scale_a, scale_b, rows=None, threads: int = 0):
+        """Block-scaled batched layout: every group owns a full slab of A.shape[0] / G rows."""
+        G = B.shape[0]
+        return self.blockwise_dynamic(A, B, scale_a, scale_b, None, A.shape[0] // G, rows,
+                                      threads)
 
 
 def bf16_bits_to_float(bits: np.ndarray) -> np.ndarray:

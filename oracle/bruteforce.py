@@ -184,3 +184,23 @@ def blockwise_element(arow, brow, sa_row, sb_blk, block=128) -> int:
             return 0x7FC0
         total += float_exact(float(sa_row[kb])) * float_exact(float(sb_blk[kb])) * s
     return bf16_bits_exact(total)
+
+
+def blockwise_dynamic(A, B, scale_a, scale_b, zsi, expected_m, cols=None, block=128):
+    """Block-scaled dynamic layout (zsi None: batched, every slab row valid): dict
+    (row, n) -> bf16 bits, padding rows +0.0.  ``cols``: the columns to compute (all by
+    default)."""
+    G = len(B)
+    N = len(B[0]) if G else 0
+    out = {}
+    for g in range(G):
+        v = expected_m if zsi is None else max(0, min(int(zsi[g]), expected_m))
+        for r in range(expected_m):
+            row = g * expected_m + r
+            for n in (range(N) if cols is None else cols):
+                if r < v:
+                    out[(row, n)] = blockwise_element(A[row], B[g][n], scale_a[row],
+                                                      scale_b[g][n // block], block)
+                else:
+                    out[(row, n)] = 0x0000
+    return out

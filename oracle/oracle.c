@@ -1,7 +1,8 @@
 /*
  * oracle.c -- plain, slow, obviously correct CPU oracle for the FP8 rowwise-scaled
  * grouped GEMM f8f8bf16_rowwise_grouped: stacked, dynamic, offsets, batched, ragged-N
- * and ragged-K layouts, and the block-scaled (groupwise) stacked variant.
+ * and ragged-K layouts, and the block-scaled (groupwise) stacked, dynamic and batched
+ * variants.
  *
  * TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the CPU-baseline leg
  * of the benchmark may build, load or call this file.  It shares no code, header,
@@ -644,6 +645,58 @@ int oracle_blockwise_stacked(const uint8_t *A, const uint8_t *B, const float *sc
     }
     free(off);
     return clamped;
+}
+
+/* ------------------------------------------------------------------------------ */
+/* Block-scaled (groupwise) dynamic and batched layouts: the slabs of the dynamic    */
+/* layout (group g owns rows [g*E, (g+1)*E); the first min(max(zsi[g], 0), E) are    */
+/* valid and every other slab row is +0.0) with the block scaling above:             */
+/*   scale_a [G*E, K/128]         one scale per slab row and K block                 */
+/*   scale_b [G, N/128, K/128]    one scale per (128 columns x 128 K) block of B     */
+/* zsi == NULL: every slab row is valid (the batched layout, no metadata).            */
+/* rows == NULL: the whole output [G*E, N]; else out row i = slab row rows[i].        */
+/* Returns -2 if K or N is not a multiple of 128, else 0.                             */
+/* ------------------------------------------------------------------------------ */
+int oracle_blockwise_dynamic(const uint8_t *A, const uint8_t *B, const float *scale_a,
+                             const float *scale_b, const int64_t *zsi, int64_t G, int64_t E,
+                             int64_t N, int64_t K, const int64_t *rows, int64_t nrows,
+                             uint16_t *out, int nthreads)
+{
+    if (K % ORACLE_SCALE_BLOCK != 0 || N % ORACLE_SCALE_BLOCK != 0) return -2;
+    double lut[256];
+    fill_lut(lut);
+    int64_t nkb = K / ORACLE_SCALE_BLOCK, nnb = N / ORACLE_SCALE_BLOCK;
+    int64_t n_out = rows ? nrows : G * E;
+#ifdef _OPENMP
+    if (nthreads <= 0) nthreads = omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads)
+#else
+    (void)nthreads;
+#endif
+    for (int64_t i = 0; i < n_out; ++i) {
+        int64_t row = rows ? rows[i] : i;
+        int64_t g = row / E;
+        int64_t r = row - g * E;
+        int64_t v = zsi ? zsi[g] : E;
+        if (v < 0) v = 0;
+        if (v > E) v = E;
+        uint16_t *o = out + (size_t)i * (size_t)N;
+        if (r >= v) {
+            for (int64_t n = 0; n < N; ++n) o[n] = 0x0000u;
+            continue;
+        }
+        const uint8_t *arow = A + (size_t)row * (size_t)K;
+#if ORACLE_MUTANT == 14
+        const float *sa_row = scale_a + (size_t)r * (size_t)nkb; /* mutant: slab-local row */
+#else
+        const float *sa_row = scale_a + (size_t)row * (size_t)nkb;
+#endif
+        for (int64_t n = 0; n < N; ++n) {
+            const float *sb_blk = scale_b + ((size_t)g * (size_t)nnb + (size_t)(n / ORACLE_SCALE_BLOCK)) * (size_t)nkb;
+            o[n] = blockwise_element(arow, b_row(B, g, n, N, K), K, sa_row, sb_blk, lut);
+        }
+    }
+    return 0;
 }
 
 /* Exact unscaled dot products as integers: S * 2^18 for one (row, n) pair, using   */

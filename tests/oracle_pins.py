@@ -629,6 +629,65 @@ def pin_blockwise_block_isolation(orc, seed=73):
         assert np.array_equal(out, ref), f"block {j}"
 
 
+def _blockwise_dynamic_case(rng, G, E, N, K):
+    A = _random_codes(rng, (G * E, K))
+    B = _random_codes(rng, (G, N, K))
+    sa = _random_scales(rng, G * E * (K // 128)).reshape(G * E, K // 128)
+    sb = _random_scales(rng, G * (N // 128) * (K // 128)).reshape(G, N // 128, K // 128)
+    return A, B, sa, sb
+
+
+def pin_blockwise_dynamic_bruteforce(orc, seed=79):
+    """Block-scaled dynamic and batched layouts: sampled columns of every slab row bit-equal
+    to the exact-rational definition (padding rows +0.0; zsi clamped into [0, E])."""
+    rng = _rng(seed)
+    for i in range(4):
+        G = int(rng.integers(2, 4))
+        E = int(rng.integers(1, 4))
+        N, K = int(rng.choice([128, 256])), int(rng.choice([128, 256]))
+        A, B, sa, sb = _blockwise_dynamic_case(rng, G, E, N, K)
+        zsi = None if i == 3 else rng.integers(-1, E + 2, size=G).astype(np.int64)
+        if zsi is not None:
+            zsi[0] = E  # one full slab at least
+        out = (orc.blockwise_batched(A, B, sa, sb) if zsi is None
+               else orc.blockwise_dynamic(A, B, sa, sb, zsi, E))
+        cols = sorted(set(int(c) for c in rng.integers(0, N, size=5)) | {0, N - 1})
+        ref = bf.blockwise_dynamic(A.tolist(), B.tolist(), sa.tolist(), sb.tolist(),
+                                   None if zsi is None else zsi.tolist(), E, cols)
+        for (r, n), bits in ref.items():
+            got = int(out[r, n])
+            valid = zsi is None or (r % E) < max(0, min(int(zsi[r // E]), E))
+            if bits == 0x0000 and valid:
+                assert got in (0x0000, 0x8000), f"case {i} ({r},{n}): {got:#06x} != 0"
+            else:
+                assert got == bits, f"case {i} ({r},{n}): {got:#06x} != {bits:#06x}"
+
+
+def pin_blockwise_dynamic_layouts(orc, seed=83):
+    """The valid rows of the block-scaled dynamic layout are the block-scaled stacked
+    layout's rows bit for bit (rows scattered into slabs), padding rows are +0.0 whatever
+    A and scale_a hold there, and the batched layout is the dynamic one with every slab
+    full."""
+    rng = _rng(seed)
+    G, E, N, K = 3, 5, 256, 384
+    zsi = np.array([2, 0, 5], np.int64)
+    A, B, sa, sb = _blockwise_dynamic_case(rng, G, E, N, K)
+    valid = np.concatenate([np.arange(g * E, g * E + zsi[g]) for g in range(G)])
+    st, _ = orc.blockwise_stacked(A[valid], B, sa[valid], sb, zsi)
+    dyn = orc.blockwise_dynamic(A, B, sa, sb, zsi, E)
+    assert np.array_equal(dyn[valid], st)
+    pad = np.setdiff1d(np.arange(G * E), valid)
+    assert np.all(dyn[pad] == 0x0000)
+    A2, sa2 = A.copy(), sa.copy()
+    A2[pad] = 0x7F      # NaN codes
+    sa2[pad] = np.nan
+    assert np.array_equal(orc.blockwise_dynamic(A2, B, sa2, sb, zsi, E), dyn)
+    full = orc.blockwise_dynamic(A, B, sa, sb, np.full(G, E, np.int64), E)
+    assert np.array_equal(orc.blockwise_batched(A, B, sa, sb), full)
+    rows = np.array([0, 4, 7, 11, 14], np.int64)
+    assert np.array_equal(orc.blockwise_dynamic(A, B, sa, sb, zsi, E, rows=rows), dyn[rows])
+
+
 PINS = [
     pin_decode_vs_torch, pin_decode_golden, pin_bf16_golden, pin_bf16_vs_torch,
     pin_dot_exact, pin_closed_form_k1, pin_closed_form_all_ones, pin_closed_form_identity,
@@ -637,4 +696,5 @@ PINS = [
     pin_k_zero, pin_sampled_rows, pin_offsets_layout, pin_batched_layout,
     pin_n_offsets_layout, pin_k_offsets_layout, pin_ragged_sampled_rows,
     pin_blockwise_bruteforce, pin_blockwise_reduces_to_rowwise, pin_blockwise_block_isolation,
+    pin_blockwise_dynamic_bruteforce, pin_blockwise_dynamic_layouts,
 ]
