@@ -52,7 +52,8 @@ HEADLINE = "c4_llama405b"
 SWEEP = ["c2a_dsv3_gate_up", "c2b_dsv3_down", "c3_llama70b_m1", "c3_llama70b_m16",
          "c3_llama70b_m128", "c3_llama70b_m1024", "c3_llama70b_m8192",
          "n1_batched_llama70b_m512", "n2_offsets_llama70b_m8192", "n3_ragged_n_m1024",
-         "n4_ragged_k_wgrad", "n5_groupwise_llama70b_m8192", "n6_groupwise_llama70b_m16"]
+         "n4_ragged_k_wgrad", "n5_groupwise_llama70b_m8192", "n6_groupwise_llama70b_m16",
+         "n7_groupwise_batched_llama70b_m512", "n8_groupwise_dynamic_dsv3_m256"]
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 FP8_OVER_BF16 = 2.0  # nominal dense ratio (4.5 / 2.25 PFLOP/s)
@@ -287,6 +288,16 @@ def run_call(fx, inp, out, wl, stream_ptr):
             inp["A"].data_ptr(), inp["B"].data_ptr(), inp["scale_a"].data_ptr(),
             inp["scale_b"].data_ptr(), inp["meta"].data_ptr(), out.data_ptr(), wl.rows, wl.G,
             wl.N, wl.K, stream_ptr)
+    elif wl.layout == "groupwise_dynamic":
+        s = fx.mslkb_f8f8bf16_groupwise_grouped_dynamic(
+            inp["A"].data_ptr(), inp["B"].data_ptr(), inp["scale_a"].data_ptr(),
+            inp["scale_b"].data_ptr(), inp["meta"].data_ptr(), out.data_ptr(), wl.G,
+            wl.expected_m, wl.N, wl.K, stream_ptr)
+    elif wl.layout == "groupwise_batched":
+        s = fx.mslkb_f8f8bf16_groupwise_grouped_batched(
+            inp["A"].data_ptr(), inp["B"].data_ptr(), inp["scale_a"].data_ptr(),
+            inp["scale_b"].data_ptr(), out.data_ptr(), wl.G, wl.expected_m, wl.N, wl.K,
+            stream_ptr)
     elif wl.layout == "ragged_n":
         s = fx.mslkb_f8f8bf16_rowwise_grouped_n_offsets(
             inp["A"].data_ptr(), inp["B"].data_ptr(), inp["scale_a"].data_ptr(),
@@ -369,6 +380,8 @@ def plan_for(fx, wl, sms):
         return fx.mslkb_plan(2 if wl.layout == "ragged_n" else 3, wl.rows, wl.G, wl.N, wl.K, sms)
     if wl.layout == "groupwise":
         return fx.mslkb_plan(4, wl.rows, wl.G, wl.N, wl.K, sms)
+    if wl.block_scaled:
+        return fx.mslkb_plan(5, wl.expected_m, wl.G, wl.N, wl.K, sms)
     return fx.mslkb_plan(1 if wl.slabs else 0, wl.expected_m if wl.slabs else wl.rows, wl.G,
                          wl.N, wl.K, sms)
 

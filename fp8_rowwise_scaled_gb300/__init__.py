@@ -86,6 +86,12 @@ def lib() -> ctypes.CDLL:
             L.mslkb_f8f8bf16_rowwise_grouped_batched.argtypes = [p, p, p, p, p, i64, i64, i64,
                                                                  i64, p]
             L.mslkb_f8f8bf16_rowwise_grouped_batched.restype = ctypes.c_int
+            L.mslkb_f8f8bf16_groupwise_grouped_dynamic.argtypes = [p, p, p, p, p, p, i64, i64,
+                                                                   i64, i64, p]
+            L.mslkb_f8f8bf16_groupwise_grouped_dynamic.restype = ctypes.c_int
+            L.mslkb_f8f8bf16_groupwise_grouped_batched.argtypes = [p, p, p, p, p, i64, i64, i64,
+                                                                   i64, p]
+            L.mslkb_f8f8bf16_groupwise_grouped_batched.restype = ctypes.c_int
             for name in ("mslkb_f8f8bf16_rowwise_grouped_n_offsets",
                          "mslkb_f8f8bf16_rowwise_grouped_k_offsets"):
                 fn = getattr(L, name)
@@ -186,6 +192,21 @@ def mslkb_f8f8bf16_groupwise_grouped_stacked(A, B, scale_a, scale_b, m_sizes, ou
     """Block-scaled stacked call: scale_a [total_M, K/128], scale_b [G, N/128, K/128]."""
     return lib().mslkb_f8f8bf16_groupwise_grouped_stacked(A, B, scale_a, scale_b, m_sizes, out,
                                                           total_M, G, N, K, stream)
+
+
+def mslkb_f8f8bf16_groupwise_grouped_dynamic(A, B, scale_a, scale_b, zero_start_index_M, out,
+                                             G, expected_m, N, K, stream=0) -> int:
+    """Block-scaled dynamic call: scale_a [G*E, K/128], scale_b [G, N/128, K/128]."""
+    return lib().mslkb_f8f8bf16_groupwise_grouped_dynamic(A, B, scale_a, scale_b,
+                                                          zero_start_index_M, out, G,
+                                                          expected_m, N, K, stream)
+
+
+def mslkb_f8f8bf16_groupwise_grouped_batched(A, B, scale_a, scale_b, out, G, M, N, K,
+                                             stream=0) -> int:
+    """Block-scaled batched call: scale_a [G*M, K/128], scale_b [G, N/128, K/128]."""
+    return lib().mslkb_f8f8bf16_groupwise_grouped_batched(A, B, scale_a, scale_b, out, G, M, N,
+                                                          K, stream)
 
 
 def mslkb_status_string(status: int) -> str:
@@ -530,6 +551,74 @@ def f8f8bf16_groupwise_grouped_stacked(XQ, WQ, x_scale, w_scale, m_sizes, out=No
         m_sizes.data_ptr(), out.data_ptr(), total_M, G, N, K, _stream_ptr(stream))
     if s != MSLKB_OK:
         raise MslkbError(s, "f8f8bf16_groupwise_grouped_stacked")
+    return out
+
+
+def f8f8bf16_groupwise_grouped_dynamic(XQ, WQ, x_scale, w_scale, zero_start_index_M, out=None,
+                                       stream=None):
+    """Block-scaled dynamic: XQ [G, E, K] (or [G*E, K]) e4m3, WQ [G, N, K] e4m3, x_scale
+    [G*E, K/128] fp32, w_scale [G, N/128, K/128] fp32, zero_start_index_M [G] int64
+    -> out [G, E, N] (or [G*E, N]) bf16 with every padding row +0.0 (K, N multiples of
+    128)."""
+    import torch
+    _check(XQ, "XQ", _fp8_types(), (2, 3))
+    _check(WQ, "WQ", _fp8_types(), 3)
+    _check(x_scale, "x_scale", (torch.float32,))
+    _check(w_scale, "w_scale", (torch.float32,))
+    _check(zero_start_index_M, "zero_start_index_M", (torch.int64,), 1)
+    G, N, K = WQ.shape
+    if XQ.dim() == 3:
+        if XQ.shape[0] != G:
+            raise ValueError("XQ and WQ disagree on G")
+        E = XQ.shape[1]
+        out_shape = (G, E, N)
+    else:
+        if G == 0 or XQ.shape[0] % G:
+            raise ValueError("XQ rows must be G * expected_m")
+        E = XQ.shape[0] // G
+        out_shape = (G * E, N)
+    if XQ.shape[-1] != K or K % 128 or N % 128 or x_scale.numel() != G * E * (K // 128) \
+            or w_scale.numel() != G * (N // 128) * (K // 128) \
+            or zero_start_index_M.numel() != G:
+        raise ValueError("inconsistent shapes")
+    if out is None:
+        out = torch.empty(out_shape, dtype=torch.bfloat16, device=XQ.device)
+    else:
+        _check(out, "out", (torch.bfloat16,))
+        if out.numel() != G * E * N:
+            raise ValueError("out has the wrong size")
+    s = mslkb_f8f8bf16_groupwise_grouped_dynamic(
+        XQ.data_ptr(), WQ.data_ptr(), x_scale.data_ptr(), w_scale.data_ptr(),
+        zero_start_index_M.data_ptr(), out.data_ptr(), G, E, N, K, _stream_ptr(stream))
+    if s != MSLKB_OK:
+        raise MslkbError(s, "f8f8bf16_groupwise_grouped_dynamic")
+    return out
+
+
+def f8f8bf16_groupwise_grouped_batched(XQ, WQ, x_scale, w_scale, out=None, stream=None):
+    """Block-scaled batched: XQ [G, M, K] e4m3, WQ [G, N, K] e4m3, x_scale [G, M, K/128],
+    w_scale [G, N/128, K/128] fp32 -> out [G, M, N] bf16; every slab row computed."""
+    import torch
+    _check(XQ, "XQ", _fp8_types(), 3)
+    _check(WQ, "WQ", _fp8_types(), 3)
+    _check(x_scale, "x_scale", (torch.float32,))
+    _check(w_scale, "w_scale", (torch.float32,))
+    G, M, K = XQ.shape
+    G2, N, K2 = WQ.shape
+    if G2 != G or K2 != K or K % 128 or N % 128 or x_scale.numel() != G * M * (K // 128) \
+            or w_scale.numel() != G * (N // 128) * (K // 128):
+        raise ValueError("inconsistent shapes")
+    if out is None:
+        out = torch.empty((G, M, N), dtype=torch.bfloat16, device=XQ.device)
+    else:
+        _check(out, "out", (torch.bfloat16,))
+        if out.numel() != G * M * N:
+            raise ValueError("out has the wrong size")
+    s = mslkb_f8f8bf16_groupwise_grouped_batched(
+        XQ.data_ptr(), WQ.data_ptr(), x_scale.data_ptr(), w_scale.data_ptr(), out.data_ptr(),
+        G, M, N, K, _stream_ptr(stream))
+    if s != MSLKB_OK:
+        raise MslkbError(s, "f8f8bf16_groupwise_grouped_batched")
     return out
 
 

@@ -25,7 +25,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmslkb.so")
 SOURCES = ["mslkb.cu", "mslkb_noalloc.cu", "variants_stacked_tma.cu",
            "variants_dynamic_tma.cu", "variants_cpasync.cu", "variants_ragged_n.cu",
-           "variants_ragged_k.cu", "variants_blockscale.cu"]
+           "variants_ragged_k.cu", "variants_blockscale.cu", "variants_blockscale_dynamic.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

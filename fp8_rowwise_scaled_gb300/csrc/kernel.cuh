@@ -111,7 +111,8 @@ struct KernelCfg {
   static constexpr bool kRagK = kRagged_ == 2;
   static constexpr bool kRagged = kRagged_ != 0;
   // Block scaling (groupwise; MSLK #471, commit introducing the rowwise scheme beside the
-  // block scheme): scale_a [rows, K/128], scale_b [G, N/128, K/128]; every K block's
+  // block scheme), stacked or slab (dynamic, batched) layouts: scale_a [rows of A, K/128],
+  // scale_b [G, N/128, K/128]; every K block's
   // partial sum is scaled on its way from TMEM into the fp32 registers (one K block per
   // TMEM chunk), and the epilogue applies no further scale.
   static constexpr bool kBlockScale = kBlockScale_;
@@ -201,10 +202,10 @@ struct KernelCfg {
   static_assert(kEpiWarps == 4 || (kEpiWarps == 8 && !kSwap), "epilogue warp split");
   static_assert(!kPair || (kTma && !kSwap && kTileN == 256), "CTA pairs: 256 x 256 tiles, TMA");
   static_assert(!kRagged || (kTma && !kPair && !kDynamic), "ragged layouts: TMA, single CTAs");
-  static_assert(!kBlockScale || (kTma && !kPair && !kRagged && !kDynamic &&
-                                 kBK == kScaleBlock && (!kSwap || kTileN <= 32)),
-                "block scaling: stacked TMA tiles (swap-AB up to 32 rows), one K block per "
-                "scale block");
+  static_assert(!kBlockScale || (kTma && !kPair && !kRagged && kBK == kScaleBlock &&
+                                 (!kSwap || kTileN <= 32)),
+                "block scaling: stacked or slab TMA tiles (swap-AB up to 32 rows), one K block "
+                "per scale block");
   static_assert(kThreadCols % 16 == 0, "TMEM load granularity");
   static_assert(!kRegSplit || (kThreads == 384 && kEpiWarp0 == 4 &&
                                128 * kRegsLow + 256 * kRegsHigh == kThreads * kLaunchRegs),

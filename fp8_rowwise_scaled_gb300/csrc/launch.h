@@ -148,5 +148,7 @@ extern const VariantInfo kVariantsRaggedK[];
 extern const int kNumVariantsRaggedK;
 extern const VariantInfo kVariantsBlockScale[];
 extern const int kNumVariantsBlockScale;
+extern const VariantInfo kVariantsBlockScaleDynamic[];
+extern const int kNumVariantsBlockScaleDynamic;
 
 }  // namespace mslkb

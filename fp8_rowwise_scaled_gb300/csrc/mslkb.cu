@@ -69,7 +69,7 @@ std::atomic<int> g_split_k{1};
 int num_variants() {
   return mslkb::kNumVariantsStackedTma + mslkb::kNumVariantsDynamicTma +
          mslkb::kNumVariantsCpAsync + mslkb::kNumVariantsRaggedN + mslkb::kNumVariantsRaggedK +
-         mslkb::kNumVariantsBlockScale;
+         mslkb::kNumVariantsBlockScale + mslkb::kNumVariantsBlockScaleDynamic;
 }
 
 const VariantInfo* variant(int i) {
@@ -85,6 +85,8 @@ const VariantInfo* variant(int i) {
   if (i < mslkb::kNumVariantsRaggedK) return &mslkb::kVariantsRaggedK[i];
   i -= mslkb::kNumVariantsRaggedK;
   if (i < mslkb::kNumVariantsBlockScale) return &mslkb::kVariantsBlockScale[i];
+  i -= mslkb::kNumVariantsBlockScale;
+  if (i < mslkb::kNumVariantsBlockScaleDynamic) return &mslkb::kVariantsBlockScaleDynamic[i];
   return nullptr;
 }
 
@@ -295,14 +297,15 @@ int64_t tiles_bound(const VariantInfo* v, int layout, int64_t rows, int64_t G, i
 
 mslkb_status plan(int layout, int64_t rows, int64_t G, int64_t N, int64_t K, int num_sms,
                   int64_t a_align, int64_t b_align, mslkb_plan_info* info) {
-  if (layout < 0 || layout > 4) return MSLKB_ERR_SHAPE;
+  if (layout < 0 || layout > 5) return MSLKB_ERR_SHAPE;
   if (num_sms <= 0 || rows < 0 || G < 0 || N < 0 || K < 0) return MSLKB_ERR_SHAPE;
-  const bool dynamic = layout == 1;
+  const bool dynamic = layout == 1 || layout == 5;
   const int ragged = (layout == 2 || layout == 3) ? layout - 1 : 0;
-  const int block_scale = layout == 4 ? 1 : 0;  // block-scaled stacked
+  // block-scaled stacked (4) or slab (5) layouts
+  const int block_scale = (layout == 4 || layout == 5) ? 1 : 0;
   if (block_scale) {  // whole scale blocks along K and N
     if (K % 128 != 0 || N % 128 != 0) return MSLKB_ERR_SHAPE;
-    layout = 0;
+    layout = dynamic ? 1 : 0;
   }
   const bool tma = (K % 16 == 0) && (a_align % 16 == 0) && (b_align % 16 == 0);
   if ((ragged || block_scale) && !tma) return MSLKB_ERR_ALIGN;  // TMA-only kernels
@@ -317,7 +320,7 @@ mslkb_status plan(int layout, int64_t rows, int64_t G, int64_t N, int64_t K, int
     swap = per_group <= 32;
     tile_n = per_group <= 16 ? 16 : (swap ? 32 : 128);
     if (!swap) {
-      const int wide = find_variant(false, true, false, 256, 1, 0, 1);
+      const int wide = find_variant(dynamic, true, false, 256, 1, 0, 1);
       if (wide >= 0 && tiles_bound(variant(wide), layout, rows, G, N) >= num_sms) tile_n = 256;
     }
   } else if (ragged) {  // TMA variants: swap-AB 32, 128 x 256, 128 x 128
@@ -495,7 +498,8 @@ mslkb_status run(int layout, const void* A, const void* B, const float* scale_a,
   if (s != MSLKB_OK) return s;
 
   mslkb_plan_info info;
-  s = plan(block_scale ? 4 : layout, layout == 0 ? rows : E, G, N, K, st->sm_count,
+  s = plan(block_scale ? (layout == 0 ? 4 : 5) : layout, layout == 0 ? rows : E, G, N, K,
+           st->sm_count,
            addr_align(A), addr_align(B), &info);
   if (s != MSLKB_OK) return s;
   const VariantInfo* v = variant(info.variant);
@@ -780,6 +784,38 @@ mslkb_status mslkb_f8f8bf16_groupwise_grouped_stacked(const void* A, const void*
   if (K % 128 != 0 || N % 128 != 0) return MSLKB_ERR_SHAPE;  // whole scale blocks
   if (G * (N / 128) * (K / 128) > MSLKB_MAX_DIM) return MSLKB_ERR_SHAPE;
   return run(0, A, B, scale_a, scale_b, m_sizes, out, total_M, G, 0, N, K, stream, 0, true);
+}
+
+mslkb_status mslkb_f8f8bf16_groupwise_grouped_dynamic(const void* A, const void* B,
+                                                      const float* scale_a,
+                                                      const float* scale_b,
+                                                      const int64_t* zero_start_index_M,
+                                                      void* out, int64_t G, int64_t expected_m,
+                                                      int64_t N, int64_t K, void* stream) {
+  if (expected_m < 0) return MSLKB_ERR_SHAPE;
+  mslkb_status s = check_sizes(0, G, N, K);
+  if (s != MSLKB_OK) return s;
+  if (expected_m > 0 && G > MSLKB_MAX_DIM / expected_m) return MSLKB_ERR_SHAPE;
+  if (K % 128 != 0 || N % 128 != 0) return MSLKB_ERR_SHAPE;  // whole scale blocks
+  if (G * (N / 128) * (K / 128) > MSLKB_MAX_DIM || G * expected_m * (K / 128) > MSLKB_MAX_DIM)
+    return MSLKB_ERR_SHAPE;
+  return run(1, A, B, scale_a, scale_b, zero_start_index_M, out, G * expected_m, G, expected_m,
+             N, K, stream, 0, true);
+}
+
+mslkb_status mslkb_f8f8bf16_groupwise_grouped_batched(const void* A, const void* B,
+                                                      const float* scale_a,
+                                                      const float* scale_b, void* out,
+                                                      int64_t G, int64_t M, int64_t N,
+                                                      int64_t K, void* stream) {
+  if (M < 0) return MSLKB_ERR_SHAPE;
+  mslkb_status s = check_sizes(0, G, N, K);
+  if (s != MSLKB_OK) return s;
+  if (M > 0 && G > MSLKB_MAX_DIM / M) return MSLKB_ERR_SHAPE;
+  if (K % 128 != 0 || N % 128 != 0) return MSLKB_ERR_SHAPE;  // whole scale blocks
+  if (G * (N / 128) * (K / 128) > MSLKB_MAX_DIM || G * M * (K / 128) > MSLKB_MAX_DIM)
+    return MSLKB_ERR_SHAPE;
+  return run(1, A, B, scale_a, scale_b, nullptr, out, G * M, G, M, N, K, stream, 2, true);
 }
 
 mslkb_status mslkb_f8f8bf16_rowwise_grouped_n_offsets(const void* A, const void* B,

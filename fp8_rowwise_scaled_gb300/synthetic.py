@@ -72,7 +72,8 @@ class Workload:
     """One problem: layout, sizes and group metadata (m_sizes or zero_start_index_M)."""
     name: str
     layout: str            # "stacked", "dynamic", "offsets", "batched", "ragged_n", "ragged_k",
-                           # "groupwise" (stacked, block scales)
+                           # "groupwise" (stacked, block scales), "groupwise_dynamic",
+                           # "groupwise_batched" (slabs, block scales)
     G: int
     N: int                 # output columns (total_N for ragged_n)
     K: int                 # contraction length (total_K for ragged_k)
@@ -109,14 +110,19 @@ class Workload:
         if self.layout == "offsets":
             return [max(0, self.meta[g] - (self.meta[g - 1] if g else 0))
                     for g in range(self.G)]
-        if self.layout == "batched":
+        if self.layout in ("batched", "groupwise_batched"):
             return [self.expected_m] * self.G
         return [max(0, min(v, self.expected_m)) for v in self.meta]
 
     @property
     def slabs(self) -> bool:
         """True for the layouts whose groups own fixed slabs of expected_m rows."""
-        return self.layout in ("dynamic", "batched")
+        return self.layout in ("dynamic", "batched", "groupwise_dynamic", "groupwise_batched")
+
+    @property
+    def block_scaled(self) -> bool:
+        """True for the block-scaled (groupwise) layouts."""
+        return self.layout.startswith("groupwise")
 
     def valid_rows(self) -> int:
         return sum(self.counts())
@@ -146,10 +152,11 @@ class Workload:
                     + 4 * self.G + 2 * self.G * self.rows * self.N)
         v = self.valid_rows()
         nz = self.nonempty_groups()
-        if self.layout == "groupwise":   # scales per (row, K block) and per 128 x 128 block
+        if self.block_scaled:   # scales per (row, K block) and per 128 x 128 block
             nkb = self.K // 128
-            return (v * (self.K + 4 * nkb) + nz * (self.N * self.K + 4 * (self.N // 128) * nkb)
-                    + 8 * self.G + 2 * v * self.N)
+            b = (v * (self.K + 4 * nkb) + nz * (self.N * self.K + 4 * (self.N // 128) * nkb)
+                 + (8 * self.G if self.layout != "groupwise_batched" else 0))
+            return b + 2 * (self.G * self.expected_m if self.slabs else v) * self.N
         b = v * self.K + 4 * v + nz * self.N * self.K + 4 * nz * self.N + 8 * self.G
         if self.slabs:
             b += 2 * self.G * self.expected_m * self.N
@@ -246,6 +253,20 @@ def workloads() -> dict[str, Workload]:
         rows=sum(m16), meta=tuple(m16), seed=1000 * 8 + 1,
         note="block-scaled decode: llama3-70b total_M=16 routing, N=K=8192, 128-blocks",
         tags=("perf",))
+    # NEXT-4 on the slab layouts: a batched problem of the n1 size, and a DS-V3 decode step
+    # (256 routed token-rows, Zipf(1.1) over 32 experts, slabs of capacity 32 -- counts
+    # above the capacity are clamped, as zero_start_index_M entries are)
+    w["n7_groupwise_batched_llama70b_m512"] = Workload(
+        name="n7_groupwise_batched_llama70b_m512", layout="groupwise_batched", G=16, N=8192,
+        K=8192, rows=16 * 512, meta=(), seed=1000 * 8 + 2, expected_m=512,
+        note="block-scaled batched: G=16 full slabs of 512 rows, N=K=8192, 128-blocks",
+        tags=("perf",))
+    z8 = multinomial_counts(1000 * 8 + 3, 256, zipf_probs(32, 1.1))
+    w["n8_groupwise_dynamic_dsv3_m256"] = Workload(
+        name="n8_groupwise_dynamic_dsv3_m256", layout="groupwise_dynamic", G=32, N=4096,
+        K=7168, rows=32 * 32, meta=tuple(z8), seed=1000 * 8 + 3, expected_m=32,
+        note="block-scaled dynamic: DS-V3 gate_up decode, 256 token-rows Zipf(1.1) over 32 "
+             "slabs of 32 rows, N=4096, K=7168, 128-blocks", tags=("perf",))
     # 4: llama3-405b-shaped
     m4 = multinomial_counts(1000 * 4 + 0, 16384, [1.0 / 16] * 16)
     w["c4_llama405b"] = _stacked("c4_llama405b", 4, 0, 16, 16384, 16384, m4,
@@ -281,7 +302,7 @@ def make_inputs(wl: Workload, device="cpu", chunk_rows: int = 8192):
     gen.manual_seed(wl.seed)
     if wl.layout in ("ragged_n", "ragged_k"):
         return _make_ragged(wl, device, gen, chunk_rows)
-    if wl.layout == "groupwise":
+    if wl.block_scaled:
         return _make_groupwise(wl, device, gen, chunk_rows)
     G, N, K, R = wl.G, wl.N, wl.K, wl.rows
     A = torch.empty((R, K), dtype=torch.uint8, device=device)
@@ -340,8 +361,10 @@ def _make_ragged(wl: Workload, device, gen, chunk_rows: int):
 
 
 def _make_groupwise(wl: Workload, device, gen, chunk_rows: int):
-    """Block-scaled stacked: A quantised per (row, 128-element K block) -> scale_a
-    [rows, K/128]; B per 128 x 128 block of each group -> scale_b [G, N/128, K/128]."""
+    """Block-scaled layouts: A quantised per (row, 128-element K block) -> scale_a
+    [rows, K/128] (rows = total_M, or G * expected_m for the slab layouts); B per 128 x 128
+    block of each group -> scale_b [G, N/128, K/128]; meta: m_sizes or zero_start_index_M
+    (int64; empty for the batched layout)."""
     G, N, K, R = wl.G, wl.N, wl.K, wl.rows
     nkb, nnb = K // 128, N // 128
     A = torch.empty((R, K), dtype=torch.uint8, device=device)

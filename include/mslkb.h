@@ -237,6 +237,46 @@ MSLKB_API mslkb_status mslkb_f8f8bf16_groupwise_grouped_stacked(
     void *stream);
 
 /*
+ * Block-scaled (groupwise) dynamic layout (MSLK #471: the block scheme of the commit
+ * introducing the rowwise scheme -- "a compile-time blockscale flag" over the grouped
+ * kernel's layouts -- on the padded layout of the PR Summary table and its commit; the
+ * padded layout's per-group slab addressing is what a [G, scale_k, M] scale tensor needs).
+ * Scale blocks of 128 along K and N:
+ *
+ *   A                   device, e4m3 codes [G * expected_m, K]   one slab per group
+ *   B                   device, e4m3 codes [G, N, K]
+ *   scale_a             device, fp32 [G * expected_m, K / 128]   per slab row and K block
+ *   scale_b             device, fp32 [G, N / 128, K / 128]
+ *   zero_start_index_M  device, int64 [G]      valid rows at the top of each slab
+ *   out                 device, bf16 [G * expected_m, N], 16-byte aligned
+ *
+ *   out[r, n] = bf16_rne( sum_kb scale_a[r, kb] * scale_b[g, n / 128, kb] * S_kb )
+ *
+ * for the first v_g = min(max(zero_start_index_M[g], 0), E) rows of slab g, +0.0 for the
+ * rest of the slab whatever A and scale_a hold there.  K and N must be multiples of 128
+ * (MSLKB_ERR_SHAPE otherwise); A and B 16-byte aligned (MSLKB_ERR_ALIGN).
+ */
+MSLKB_API mslkb_status mslkb_f8f8bf16_groupwise_grouped_dynamic(
+    const void *A, const void *B, const float *scale_a, const float *scale_b,
+    const int64_t *zero_start_index_M, void *out, int64_t G, int64_t expected_m,
+    int64_t N, int64_t K, void *stream);
+
+/*
+ * Block-scaled (groupwise) batched layout: the block scaling above on the batched layout
+ * (MSLK #471, commit adding the layout whose groups all carry their full complement of
+ * rows): every group owns a full slab of M rows and no metadata is read.
+ *
+ *   A        device, e4m3 codes [G, M, K]
+ *   B        device, e4m3 codes [G, N, K]
+ *   scale_a  device, fp32 [G, M, K / 128]
+ *   scale_b  device, fp32 [G, N / 128, K / 128]
+ *   out      device, bf16 [G, M, N], 16-byte aligned
+ */
+MSLKB_API mslkb_status mslkb_f8f8bf16_groupwise_grouped_batched(
+    const void *A, const void *B, const float *scale_a, const float *scale_b, void *out,
+    int64_t G, int64_t M, int64_t N, int64_t K, void *stream);
+
+/*
  * Allocation-free stacked call (no counterpart on the pages: an addition of this library).
  *
  * For callers that cannot allocate device memory when they call: plug-ins whose host
@@ -286,7 +326,8 @@ MSLKB_API mslkb_status mslkb_get_device_status(void *stream, uint32_t *flags);
  * Kernel variants and the plan the host would choose.  Pure host code: no CUDA call.
  * layout: 0 = stacked (rows = total_M), 1 = dynamic (rows = expected_m per group),
  *         2 = ragged N (rows = M, N = total_N), 3 = ragged K (rows = M, K = total_K),
- *         4 = block-scaled stacked (rows = total_M).
+ *         4 = block-scaled stacked (rows = total_M), 5 = block-scaled dynamic or batched
+ *         (rows = expected_m per group).
  * num_sms: streaming multiprocessors of the target device.
  * a_align / b_align: the byte alignment of the A and B base addresses (e.g. 256).
  */

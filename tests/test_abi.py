@@ -149,7 +149,56 @@ def test_plan_ragged(L):
     with pytest.raises(fx.MslkbError):
         fx.mslkb_plan(3, 128, 2, 256, 1000, 152)   # K not a multiple of 16: TMA only
     with pytest.raises(fx.MslkbError):
-        fx.mslkb_plan(5, 128, 2, 256, 1024, 152)
+        fx.mslkb_plan(6, 128, 2, 256, 1024, 152)
+
+
+def test_plan_blockscale_slabs(L):
+    """Block-scaled dynamic / batched slabs (layout 5, rows = slab height): swap-AB up to 32
+    rows per slab, 128 x 256 tiles when they fill the SMs, else 128 x 128; whole scale
+    blocks along K and N, TMA only."""
+    i = fx.mslkb_plan(5, 512, 16, 8192, 8192, 152)
+    assert fx.variant_name(i.variant) == "dynamic_blockscale_tile128x256_tma"
+    i = fx.mslkb_plan(5, 200, 2, 256, 1024, 152)
+    assert fx.variant_name(i.variant) == "dynamic_blockscale_tile128x128_tma"
+    i = fx.mslkb_plan(5, 16, 8, 4096, 2048, 152)
+    assert fx.variant_name(i.variant) == "dynamic_blockscale_swap_w128xa16_tma"
+    assert i.split_k == 1
+    i = fx.mslkb_plan(5, 32, 8, 4096, 2048, 152)
+    assert fx.variant_name(i.variant) == "dynamic_blockscale_swap_w128xa32_tma"
+    for bad in ((5, 64, 2, 256, 1000), (5, 64, 2, 200, 1024)):
+        with pytest.raises(fx.MslkbError):
+            fx.mslkb_plan(*bad, 152)
+    with pytest.raises(fx.MslkbError):  # unaligned bases: no cp.async block-scaled kernel
+        fx.mslkb_plan(5, 64, 2, 256, 1024, 152, a_align=8)
+
+
+def _groupwise_dynamic(**kw):
+    a = dict(A=16, B=16, scale_a=16, scale_b=16, zsi=16, out=256, G=2, E=4, N=128, K=128)
+    a.update(kw)
+    return fx.mslkb_f8f8bf16_groupwise_grouped_dynamic(a["A"], a["B"], a["scale_a"],
+                                                       a["scale_b"], a["zsi"], a["out"], a["G"],
+                                                       a["E"], a["N"], a["K"], 0)
+
+
+def _groupwise_batched(**kw):
+    a = dict(A=16, B=16, scale_a=16, scale_b=16, out=256, G=2, E=4, N=128, K=128)
+    a.update(kw)
+    return fx.mslkb_f8f8bf16_groupwise_grouped_batched(a["A"], a["B"], a["scale_a"],
+                                                       a["scale_b"], a["out"], a["G"], a["E"],
+                                                       a["N"], a["K"], 0)
+
+
+@pytest.mark.parametrize("call", [_groupwise_dynamic, _groupwise_batched],
+                         ids=["dynamic", "batched"])
+def test_groupwise_slab_argument_errors_before_cuda(L, call):
+    assert call(K=192) == fx.MSLKB_ERR_SHAPE          # K not whole scale blocks
+    assert call(N=136) == fx.MSLKB_ERR_SHAPE          # N not whole scale blocks
+    assert call(E=-1) == fx.MSLKB_ERR_SHAPE
+    assert call(G=fx.MAX_GROUPS + 1) == fx.MSLKB_ERR_SHAPE
+    assert call(out=0) == fx.MSLKB_ERR_NULL
+    assert call(scale_a=0) == fx.MSLKB_ERR_NULL
+    assert call(out=264) == fx.MSLKB_ERR_ALIGN        # out not 16-byte aligned
+    assert call(G=0) == fx.MSLKB_OK and call(E=0) == fx.MSLKB_OK   # nothing owned
 
 
 def test_groupwise_argument_errors_and_plan(L):

@@ -103,7 +103,8 @@ def _variants(prefix):
     try:
         fxbuild.build()
         return [fx.variant_name(i) for i in range(fx.mslkb_num_variants())
-                if fx.variant_name(i).startswith(prefix)]
+                if fx.variant_name(i).startswith(prefix)
+                and "blockscale" not in fx.variant_name(i)]   # rowwise variants only
     except Exception:  # noqa: BLE001 - collection must not depend on a toolchain
         return []
 
