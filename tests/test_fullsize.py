@@ -32,6 +32,18 @@ def orc():
     return oracle.load(0)
 
 
+def _no_tile_skipped(out, owned, what):
+    """Beyond the sampled rows, on the GPU: no owned row still holds the 0x7E7E fill (a tile
+    skipped by the scheduler, the claim counter or a split), and nothing is NaN or Inf (the
+    inputs hold neither, so a tile written twice with garbage or a lost partial sum would
+    show)."""
+    owned_t = torch.from_numpy(np.asarray(owned)).cuda()
+    o = out[owned_t]
+    left = int((o.view(torch.int16) == 0x7E7E).sum().item())
+    assert left == 0, f"{what}: {left} owned elements still hold the fill pattern"
+    assert bool(torch.isfinite(o).all().item()), f"{what}: NaN or Inf in the output"
+
+
 @pytest.mark.parametrize("name", FULL)
 def test_full_size_sampled(orc, name):
     wl = workloads()[name]
@@ -44,6 +56,7 @@ def test_full_size_sampled(orc, name):
     got = bits_of(out[torch.from_numpy(rows).cuda()]).reshape(rows.size, wl.N)
     ref, ab = prob.oracle_rows(orc, rows)
     compare(got.ravel(), ref.ravel(), ab.ravel(), name)
+    _no_tile_skipped(out, prob.owned_rows_mask(), name)
     assert fx.device_status() == 0
     del inp, prob, out
     torch.cuda.empty_cache()
@@ -121,6 +134,7 @@ def test_full_size_groupwise_sampled(orc):
     ab, _ = orc.blockwise_stacked(abs_codes(h["A"]), abs_codes(h["B"]), np.abs(h["scale_a"]),
                                   np.abs(h["scale_b"]), h["meta"], rows=rows)
     compare(got.ravel(), ref.ravel(), ab.ravel(), wl.name)
+    _no_tile_skipped(out, np.ones(wl.rows, bool), wl.name)
     assert fx.device_status() == 0
     del inp, out
     torch.cuda.empty_cache()
