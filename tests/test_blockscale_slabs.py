@@ -219,3 +219,42 @@ def test_fuzz_block_scaled_slabs(orc, i):
     _check(orc, A, B, sa, sb, zsi, E, got,
            f"block-scaled slabs #{i}: G={G} E={E} N={N} K={K} zsi={zsi}")
     assert fx.device_status() == 0
+
+
+@pytest.mark.parametrize("layout", ["dynamic", "batched"])
+def test_cuda_graph_replay(orc, layout):
+    """The block-scaled slab calls captured in a CUDA graph (after one eager call on the
+    stream, which sets up its workspace) and replayed twice, with new inputs copied into
+    the captured buffers between the replays."""
+    G, E, N, K = 4, 16, 1024, 1024   # decode-sized slabs: swap-AB tiles split along K
+    zsi = [3, 16, 0, 9] if layout == "dynamic" else None
+    cases = [_case(90 + i, G, E, N, K, zsi) for i in range(2)]
+    dev = [torch.from_numpy(np.ascontiguousarray(x)).cuda() for x in cases[0]]
+    tz = None if zsi is None else torch.tensor(zsi, dtype=torch.int64, device="cuda")
+    out = torch.empty((G * E, N), dtype=torch.bfloat16, device="cuda")
+
+    def call():
+        tA, tB, tsa, tsb = dev
+        if tz is None:
+            fx.f8f8bf16_groupwise_grouped_batched(tA.view(G, E, K), tB, tsa, tsb,
+                                                  out=out.view(G, E, N))
+        else:
+            fx.f8f8bf16_groupwise_grouped_dynamic(tA, tB, tsa, tsb, tz, out=out)
+
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        call()
+    s.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        call()
+    for i, (A, B, sa, sb) in enumerate(cases):
+        for d, h in zip(dev, (A, B, sa, sb)):
+            d.copy_(torch.from_numpy(np.ascontiguousarray(h)))
+        with torch.cuda.stream(s):
+            graph.replay()
+        s.synchronize()
+        _check(orc, A, B, sa, sb, zsi, E, bits_of(out).reshape(G * E, N),
+               f"{layout} graph replay {i + 1}")
+    del graph
+    assert fx.device_status() == 0

@@ -58,3 +58,25 @@ def test_release_then_call_again(case):
         assert fx.mslkb_workspace_count() == base
     fx.mslkb_release_workspace(s.cuda_stream)  # nothing left to release: fine
     assert fx.device_status() == 0
+
+
+def test_two_streams_at_once():
+    """Two streams run split-tile problems at the same time, each on its own workspace
+    (partial sums and arrival counters): interleaved launches on both streams, no
+    synchronisation between them, and both results still match the oracle."""
+    p1 = _problem(8, 2048, 2048, [1, 0, 3, 2, 0, 1, 1, 2], 63)
+    p2 = _problem(4, 4096, 1024, [2, 1, 0, 3], 64)
+    orc = oracle.load(0)
+    refs = [p.oracle_full(orc) for p in (p1, p2)]
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    outs = [None, None]
+    for _ in range(12):
+        for i, (p, s) in enumerate(((p1, s1), (p2, s2))):
+            with torch.cuda.stream(s):
+                outs[i] = p.run_gpu()
+    torch.cuda.synchronize()
+    for i, (out, (ref, ab)) in enumerate(zip(outs, refs)):
+        compare(bits_of(out).ravel(), ref.ravel(), ab.ravel(), f"stream {i + 1}")
+    for s in (s1, s2):
+        fx.mslkb_release_workspace(s.cuda_stream)
+    assert fx.device_status() == 0
