@@ -696,6 +696,66 @@ __device__ __forceinline__ bool mma_chunk_at(int stage, const GemmParams& p, uin
                                      abort);
 }
 
+// Block scaling on 128-row tiles: every K block sums into an accumulator of its own (a TMEM
+// buffer, kNumAcc of them in a ring), so each block is a chunk of one: wait for the buffer to
+// be drained, wait for the stage, four MMAs that start the accumulator afresh, commit the
+// buffer to the epilogue (which frees the stage once it sees the commit).  The general loop
+// does that with runtime stage, phase, buffer and descriptor bookkeeping per block; this
+// issues kUnrolledChunkKb blocks in a row with all of it fixed at compile time, one instance
+// per ring position kS0 and buffer kB0 of the first block.  use_par: parity of the number of
+// times the first block's buffer was used before (the epilogue's hand-backs).
+template <class Cfg, int kS0, int kB0, int kJ = 0>
+__device__ __forceinline__ bool mma_bs_run_unrolled(const GemmParams& p, uint32_t s_bar,
+                                                    uint32_t tmem_base, uint32_t a_lo0,
+                                                    uint32_t b_lo0, uint32_t phase,
+                                                    uint32_t use_par, volatile uint32_t* abort) {
+  if constexpr (kJ == kUnrolledChunkKb) {
+    return true;
+  } else {
+    constexpr int kSt = (kS0 + kJ) % Cfg::kStages;
+    constexpr uint32_t kFlip = static_cast<uint32_t>(((kS0 + kJ) / Cfg::kStages) & 1);
+    constexpr int kBuf = (kB0 + kJ) % Cfg::kNumAcc;
+    constexpr uint32_t kUseFlip = static_cast<uint32_t>(((kB0 + kJ) / Cfg::kNumAcc) & 1);
+    const uint32_t tempty = s_bar + 8u * (2 * Cfg::kStages + Cfg::kNumAcc + kBuf);
+    const uint32_t tfull = s_bar + 8u * (2 * Cfg::kStages + kBuf);
+    if (!wait_bar(tempty, (use_par ^ kUseFlip) ^ 1u, abort, p.status, p.timeout_ns))
+      return false;
+    ptx::tc_fence_after_sync();
+    if (!wait_bar(s_bar + 8u * kSt, phase ^ kFlip, abort, p.status, p.timeout_ns)) return false;
+    ptx::tc_fence_after_sync();
+    constexpr uint32_t kAOff = static_cast<uint32_t>((Cfg::kActBytes * kSt) >> 4);
+    constexpr uint32_t kBOff = static_cast<uint32_t>((Cfg::kWBytes * kSt) >> 4);
+    const uint32_t d_buf = tmem_base + static_cast<uint32_t>(kBuf * Cfg::kBufCols);
+    ptx::mma_f8f6f4_lo<false, kAOff + 0, kBOff + 0>(d_buf, a_lo0, b_lo0, Cfg::kIdesc, 0u);
+    ptx::mma_f8f6f4_lo<false, kAOff + 2, kBOff + 2>(d_buf, a_lo0, b_lo0, Cfg::kIdesc, 1u);
+    ptx::mma_f8f6f4_lo<false, kAOff + 4, kBOff + 4>(d_buf, a_lo0, b_lo0, Cfg::kIdesc, 1u);
+    ptx::mma_f8f6f4_lo<false, kAOff + 6, kBOff + 6>(d_buf, a_lo0, b_lo0, Cfg::kIdesc, 1u);
+    ptx::mma_commit(tfull);
+    return mma_bs_run_unrolled<Cfg, kS0, kB0, kJ + 1>(p, s_bar, tmem_base, a_lo0, b_lo0, phase,
+                                                      use_par, abort);
+  }
+}
+
+// mma_bs_run_unrolled for the runtime ring position `stage` and first buffer `buf`.
+template <class Cfg, int kS = 0, int kB = 0>
+__device__ __forceinline__ bool mma_bs_run_at(int stage, int buf, const GemmParams& p,
+                                              uint32_t s_bar, uint32_t tmem_base,
+                                              uint32_t a_lo0, uint32_t b_lo0, uint32_t phase,
+                                              uint32_t use_par, volatile uint32_t* abort) {
+  if constexpr (kB + 1 < Cfg::kNumAcc) {
+    if (buf != kB)
+      return mma_bs_run_at<Cfg, kS, kB + 1>(stage, buf, p, s_bar, tmem_base, a_lo0, b_lo0,
+                                            phase, use_par, abort);
+  }
+  if constexpr (kS + 1 < Cfg::kStages) {
+    if (stage != kS)
+      return mma_bs_run_at<Cfg, kS + 1, kB>(stage, buf, p, s_bar, tmem_base, a_lo0, b_lo0,
+                                            phase, use_par, abort);
+  }
+  return mma_bs_run_unrolled<Cfg, kS, kB>(p, s_bar, tmem_base, a_lo0, b_lo0, phase, use_par,
+                                          abort);
+}
+
 // cp.async loader: one 16-byte chunk of a swizzled tile row.
 __device__ __forceinline__ void load_chunk(uint32_t dst, const uint8_t* row_ptr, bool row_ok,
                                            int32_t k, int32_t K, int32_t width,
@@ -1136,6 +1196,23 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
           k_len = c.k_skip + c.k_len;
         }
         for (int32_t kb0 = it.kb0; ok && kb0 < kb_end; kb0 += kpc) {
+          if constexpr (Cfg::kBlockScale && !Cfg::kSwap) {
+            if (kb_end - kb0 >= kUnrolledChunkKb) {
+              // the next kUnrolledChunkKb blocks, one accumulator each, from the unrolled path
+              if (!mma_bs_run_at<Cfg>(stage, static_cast<int>(chunk % Cfg::kNumAcc), p, s_bar,
+                                      tmem_base, a_lo0, b_lo0, phase,
+                                      (chunk / Cfg::kNumAcc) & 1u, abort_flag)) {
+                ok = false;
+                break;
+              }
+              const int adv = stage + kUnrolledChunkKb;
+              stage = adv % Cfg::kStages;
+              phase ^= static_cast<uint32_t>((adv / Cfg::kStages) & 1);
+              chunk += kUnrolledChunkKb;
+              kb0 += kUnrolledChunkKb - kpc;  // the loop adds kpc (= 1) back
+              continue;
+            }
+          }
           const int buf = static_cast<int>(chunk % Cfg::kNumAcc);
           const uint32_t use = chunk / Cfg::kNumAcc;  // how often this buffer was used before
           if (!wait_bar<Cfg::kPair>(tempty_bar(buf), (use & 1u) ^ 1u, abort_flag, p.status,
