@@ -23,6 +23,7 @@ import threading
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libmslkb.so")
+CHECKED_LIB_PATH = os.path.join(_PKG, "libmslkb_checked.so")
 
 MSLKB_OK, MSLKB_ERR_NULL, MSLKB_ERR_SHAPE, MSLKB_ERR_ALIGN, MSLKB_ERR_DEVICE, MSLKB_ERR_CUDA = range(6)
 MSLKB_ERR_TOO_LARGE = 6
@@ -30,6 +31,7 @@ NOALLOC_SCRATCH_BYTES = 8 << 20
 MSLKB_DEV_TIMEOUT = 0x1
 MSLKB_DEV_MSIZES_CLAMPED = 0x2
 MSLKB_DEV_BAD_SLICE = 0x4
+MSLKB_DEV_BOUNDS = 0x8
 MAX_GROUPS = 1024
 
 _lib = None
@@ -60,6 +62,75 @@ class PlanInfo(ctypes.Structure):
         return d
 
 
+def declare(L: ctypes.CDLL) -> ctypes.CDLL:
+    """Declare the argument and result types of the C entry points on a loaded copy of
+    the library (libmslkb.so, or the checked build libmslkb_checked.so)."""
+    p, i64 = ctypes.c_void_p, ctypes.c_int64
+    for name in ("mslkb_f8f8bf16_rowwise_grouped_stacked",
+                 "mslkb_f8f8bf16_rowwise_grouped_dynamic",
+                 "mslkb_f8f8bf16_rowwise_grouped_stacked_noalloc",
+                 "mslkb_f8f8bf16_groupwise_grouped_stacked"):
+        fn = getattr(L, name)
+        fn.argtypes = [p, p, p, p, p, p, i64, i64, i64, i64, p]
+        fn.restype = ctypes.c_int
+    L.mslkb_f8f8bf16_rowwise_grouped_offsets.argtypes = [p, p, p, p, p, p, i64, i64,
+                                                         i64, i64, p]
+    L.mslkb_f8f8bf16_rowwise_grouped_offsets.restype = ctypes.c_int
+    L.mslkb_f8f8bf16_rowwise_grouped_batched.argtypes = [p, p, p, p, p, i64, i64, i64,
+                                                         i64, p]
+    L.mslkb_f8f8bf16_rowwise_grouped_batched.restype = ctypes.c_int
+    L.mslkb_f8f8bf16_groupwise_grouped_dynamic.argtypes = [p, p, p, p, p, p, i64, i64,
+                                                           i64, i64, p]
+    L.mslkb_f8f8bf16_groupwise_grouped_dynamic.restype = ctypes.c_int
+    L.mslkb_f8f8bf16_groupwise_grouped_batched.argtypes = [p, p, p, p, p, i64, i64, i64,
+                                                           i64, p]
+    L.mslkb_f8f8bf16_groupwise_grouped_batched.restype = ctypes.c_int
+    for name in ("mslkb_f8f8bf16_rowwise_grouped_n_offsets",
+                 "mslkb_f8f8bf16_rowwise_grouped_k_offsets"):
+        fn = getattr(L, name)
+        fn.argtypes = [p, p, p, p, p, p, i64, i64, i64, i64, p]
+        fn.restype = ctypes.c_int
+    L.mslkb_status_string.argtypes = [ctypes.c_int]
+    L.mslkb_status_string.restype = ctypes.c_char_p
+    L.mslkb_last_cuda_error.argtypes = []
+    L.mslkb_last_cuda_error.restype = ctypes.c_int
+    L.mslkb_get_device_status.argtypes = [p, ctypes.POINTER(ctypes.c_uint32)]
+    L.mslkb_get_device_status.restype = ctypes.c_int
+    L.mslkb_plan.argtypes = [ctypes.c_int32, i64, i64, i64, i64, ctypes.c_int32, i64,
+                             i64, ctypes.POINTER(PlanInfo)]
+    L.mslkb_plan.restype = ctypes.c_int
+    L.mslkb_num_variants.argtypes = []
+    L.mslkb_num_variants.restype = ctypes.c_int32
+    L.mslkb_variant_name.argtypes = [ctypes.c_int32]
+    L.mslkb_variant_name.restype = ctypes.c_char_p
+    L.mslkb_force_variant.argtypes = [ctypes.c_int32]
+    L.mslkb_force_variant.restype = ctypes.c_int
+    L.mslkb_variant_resources.argtypes = [ctypes.c_int32, ctypes.POINTER(ctypes.c_int32),
+                                          ctypes.POINTER(ctypes.c_int32)]
+    L.mslkb_variant_resources.restype = ctypes.c_int
+    L.mslkb_set_split_k.argtypes = [ctypes.c_int32]
+    L.mslkb_set_split_k.restype = ctypes.c_int
+    L.mslkb_set_accumulation_chunk.argtypes = [ctypes.c_int32]
+    L.mslkb_set_accumulation_chunk.restype = ctypes.c_int
+    L.mslkb_accumulation_chunk.argtypes = []
+    L.mslkb_accumulation_chunk.restype = ctypes.c_int32
+    L.mslkb_set_weight_prefetch.argtypes = [ctypes.c_int32]
+    L.mslkb_set_weight_prefetch.restype = ctypes.c_int
+    L.mslkb_test_speculate_from_next_launch.argtypes = [ctypes.c_void_p]
+    L.mslkb_test_speculate_from_next_launch.restype = ctypes.c_int
+    L.mslkb_set_wait_timeout_us.argtypes = [i64]
+    L.mslkb_set_wait_timeout_us.restype = ctypes.c_int
+    L.mslkb_test_stall_next_launch.argtypes = []
+    L.mslkb_test_stall_next_launch.restype = ctypes.c_int
+    L.mslkb_release_workspace.argtypes = [p]
+    L.mslkb_release_workspace.restype = ctypes.c_int
+    L.mslkb_workspace_count.argtypes = []
+    L.mslkb_workspace_count.restype = ctypes.c_int32
+    L.mslkb_version.argtypes = []
+    L.mslkb_version.restype = ctypes.c_int32
+    return L
+
+
 def lib() -> ctypes.CDLL:
     """The loaded libmslkb.so (raises if it has not been built)."""
     global _lib
@@ -71,71 +142,7 @@ def lib() -> ctypes.CDLL:
                 raise RuntimeError(
                     f"{LIB_PATH} is missing: build it with "
                     "`python -m fp8_rowwise_scaled_gb300.build` (there is no fallback path)")
-            L = ctypes.CDLL(LIB_PATH)
-            p, i64 = ctypes.c_void_p, ctypes.c_int64
-            for name in ("mslkb_f8f8bf16_rowwise_grouped_stacked",
-                         "mslkb_f8f8bf16_rowwise_grouped_dynamic",
-                         "mslkb_f8f8bf16_rowwise_grouped_stacked_noalloc",
-                         "mslkb_f8f8bf16_groupwise_grouped_stacked"):
-                fn = getattr(L, name)
-                fn.argtypes = [p, p, p, p, p, p, i64, i64, i64, i64, p]
-                fn.restype = ctypes.c_int
-            L.mslkb_f8f8bf16_rowwise_grouped_offsets.argtypes = [p, p, p, p, p, p, i64, i64,
-                                                                 i64, i64, p]
-            L.mslkb_f8f8bf16_rowwise_grouped_offsets.restype = ctypes.c_int
-            L.mslkb_f8f8bf16_rowwise_grouped_batched.argtypes = [p, p, p, p, p, i64, i64, i64,
-                                                                 i64, p]
-            L.mslkb_f8f8bf16_rowwise_grouped_batched.restype = ctypes.c_int
-            L.mslkb_f8f8bf16_groupwise_grouped_dynamic.argtypes = [p, p, p, p, p, p, i64, i64,
-                                                                   i64, i64, p]
-            L.mslkb_f8f8bf16_groupwise_grouped_dynamic.restype = ctypes.c_int
-            L.mslkb_f8f8bf16_groupwise_grouped_batched.argtypes = [p, p, p, p, p, i64, i64, i64,
-                                                                   i64, p]
-            L.mslkb_f8f8bf16_groupwise_grouped_batched.restype = ctypes.c_int
-            for name in ("mslkb_f8f8bf16_rowwise_grouped_n_offsets",
-                         "mslkb_f8f8bf16_rowwise_grouped_k_offsets"):
-                fn = getattr(L, name)
-                fn.argtypes = [p, p, p, p, p, p, i64, i64, i64, i64, p]
-                fn.restype = ctypes.c_int
-            L.mslkb_status_string.argtypes = [ctypes.c_int]
-            L.mslkb_status_string.restype = ctypes.c_char_p
-            L.mslkb_last_cuda_error.argtypes = []
-            L.mslkb_last_cuda_error.restype = ctypes.c_int
-            L.mslkb_get_device_status.argtypes = [p, ctypes.POINTER(ctypes.c_uint32)]
-            L.mslkb_get_device_status.restype = ctypes.c_int
-            L.mslkb_plan.argtypes = [ctypes.c_int32, i64, i64, i64, i64, ctypes.c_int32, i64,
-                                     i64, ctypes.POINTER(PlanInfo)]
-            L.mslkb_plan.restype = ctypes.c_int
-            L.mslkb_num_variants.argtypes = []
-            L.mslkb_num_variants.restype = ctypes.c_int32
-            L.mslkb_variant_name.argtypes = [ctypes.c_int32]
-            L.mslkb_variant_name.restype = ctypes.c_char_p
-            L.mslkb_force_variant.argtypes = [ctypes.c_int32]
-            L.mslkb_force_variant.restype = ctypes.c_int
-            L.mslkb_variant_resources.argtypes = [ctypes.c_int32, ctypes.POINTER(ctypes.c_int32),
-                                                  ctypes.POINTER(ctypes.c_int32)]
-            L.mslkb_variant_resources.restype = ctypes.c_int
-            L.mslkb_set_split_k.argtypes = [ctypes.c_int32]
-            L.mslkb_set_split_k.restype = ctypes.c_int
-            L.mslkb_set_accumulation_chunk.argtypes = [ctypes.c_int32]
-            L.mslkb_set_accumulation_chunk.restype = ctypes.c_int
-            L.mslkb_accumulation_chunk.argtypes = []
-            L.mslkb_accumulation_chunk.restype = ctypes.c_int32
-            L.mslkb_set_weight_prefetch.argtypes = [ctypes.c_int32]
-            L.mslkb_set_weight_prefetch.restype = ctypes.c_int
-            L.mslkb_test_speculate_from_next_launch.argtypes = [ctypes.c_void_p]
-            L.mslkb_test_speculate_from_next_launch.restype = ctypes.c_int
-            L.mslkb_set_wait_timeout_us.argtypes = [i64]
-            L.mslkb_set_wait_timeout_us.restype = ctypes.c_int
-            L.mslkb_test_stall_next_launch.argtypes = []
-            L.mslkb_test_stall_next_launch.restype = ctypes.c_int
-            L.mslkb_release_workspace.argtypes = [p]
-            L.mslkb_release_workspace.restype = ctypes.c_int
-            L.mslkb_workspace_count.argtypes = []
-            L.mslkb_workspace_count.restype = ctypes.c_int32
-            L.mslkb_version.argtypes = []
-            L.mslkb_version.restype = ctypes.c_int32
-            _lib = L
+            _lib = declare(ctypes.CDLL(LIB_PATH))
     return _lib
 
 

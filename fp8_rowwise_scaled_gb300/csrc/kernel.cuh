@@ -53,6 +53,7 @@ constexpr int kBK = 128;  // bytes (= e4m3 elements) of K per pipeline stage
 constexpr uint32_t kStatusTimeout = 1u;
 constexpr uint32_t kStatusClamped = 2u;
 constexpr uint32_t kStatusBadSlice = 4u;  // ragged K: a slice bound not on 16 elements
+constexpr uint32_t kStatusBounds = 8u;    // checked builds: an index outside its buffer
 
 struct GemmParams {
   const uint8_t* A;        // [rows, K] e4m3
@@ -490,6 +491,134 @@ __device__ __forceinline__ bool wait_count(const uint32_t* cnt, uint32_t want,
   }
 }
 
+// Checked builds (compiled with MSLKB_CHECKED): every global access of the kernels is tested
+// against the extents of the buffers the call passed.  An index outside them sets
+// kStatusBounds in the device status word, together with one bit (16 + site) naming the kind
+// of access, and the access is not made as asked: a load reads element 0 of its buffer
+// instead, a store is dropped, a TMA copy takes coordinate 0 on the faulty axis (a TMA box
+// may lie partly or wholly past the tensor's extent -- zero fill -- but its innermost
+// coordinate must be 16-byte aligned and a store's start must not be negative).  Product
+// builds compile none of the tests: the helpers return their argument.
+enum CheckSite : uint32_t {
+  kCkMeta = 0,        // group metadata (m_sizes, offsets, zero_start_index_M)
+  kCkTmaX = 1,        // TMA load or prefetch: K coordinate out of range
+  kCkTmaY = 2,        // TMA load or prefetch: row / column / group coordinate out of range
+  kCkTmaAlign = 3,    // TMA load or prefetch: K coordinate not 16-byte aligned
+  kCkScale = 4,       // scale_a / scale_b
+  kCkStore = 5,       // direct output store
+  kCkTmaStore = 6,    // TMA output store
+  kCkSplit = 7,       // split-tile workspace and counters
+};
+__device__ __forceinline__ void ck_fail(const GemmParams& p, uint32_t site) {
+#ifdef MSLKB_CHECKED
+  atomicOr(p.status, kStatusBounds | (1u << (16 + site)));
+#else
+  (void)p;
+  (void)site;
+#endif
+}
+__device__ __forceinline__ int64_t ck_index(const GemmParams& p, int64_t i, int64_t n,
+                                            uint32_t site) {
+#ifdef MSLKB_CHECKED
+  if (i < 0 || i >= n) {
+    ck_fail(p, site);
+    return 0;
+  }
+#else
+  (void)p;
+  (void)n;
+  (void)site;
+#endif
+  return i;
+}
+__device__ __forceinline__ bool ck_range(const GemmParams& p, int64_t i, int64_t count,
+                                         int64_t n) {
+#ifdef MSLKB_CHECKED
+  if (i < 0 || count < 0 || i + count > n) {
+    ck_fail(p, kCkStore);
+    return false;
+  }
+#else
+  (void)p;
+  (void)i;
+  (void)count;
+  (void)n;
+#endif
+  return true;
+}
+// TMA load coordinate on an axis of `n` elements.  x (the K axis, one byte per element) must
+// start inside [lo, n) on a multiple of 16.  A box on the other axes may reach past the end,
+// or lie wholly past it (the second CTA of a pair on a group's last rows, the second half of
+// an N-tail weight tile): those elements read zero fill.  A start more than one box (256
+// rows) past the end is a coordinate gone wrong.
+__device__ __forceinline__ int32_t ck_tma(const GemmParams& p, int32_t v, int32_t lo, int64_t n,
+                                          bool inner) {
+#ifdef MSLKB_CHECKED
+  if (v < lo || v >= (inner ? n : n + 256)) {
+    ck_fail(p, inner ? kCkTmaX : kCkTmaY);
+    return 0;
+  }
+  if (inner && (v & 15) != 0) {
+    ck_fail(p, kCkTmaAlign);
+    return 0;
+  }
+#else
+  (void)p;
+  (void)lo;
+  (void)n;
+  (void)inner;
+#endif
+  return v;
+}
+
+// A pointer into [base, base + n) (a load through it reads *base instead otherwise).
+template <class T>
+__device__ __forceinline__ const T* ck_ptr(const GemmParams& p, const T* ptr, const T* base,
+                                           int64_t n) {
+  return base + ck_index(p, ptr - base, n, kCkScale);
+}
+// A TMA store of a 32 x 32 bf16 block at (x, y) into an [rows, cols] output: false (and the
+// status bits) if it would start before the output, off a 16-byte boundary, or reach past its
+// last row.  Columns at or past `cols` are clipped by the copy (a block of an N-tail tile may
+// lie wholly past N and write nothing).
+__device__ __forceinline__ bool ck_tma_store(const GemmParams& p, int32_t x, int32_t y,
+                                             int64_t rows, int64_t cols) {
+#ifdef MSLKB_CHECKED
+  if (x < 0 || x >= cols + 256 || (x & 7) != 0 || y < 0 || y + 32 > rows) {
+    ck_fail(p, kCkTmaStore);
+    return false;
+  }
+#else
+  (void)p;
+  (void)x;
+  (void)y;
+  (void)rows;
+  (void)cols;
+#endif
+  return true;
+}
+
+// Buffer extents of a call, in elements (for the checked build's tests).
+template <class Cfg>
+__device__ __forceinline__ int64_t ext_scale_a(const GemmParams& p) {
+  if constexpr (Cfg::kRagged) return static_cast<int64_t>(p.G) * p.E;
+  else if constexpr (Cfg::kBlockScale) return static_cast<int64_t>(p.rows) * p.num_kb;
+  else return p.rows;
+}
+template <class Cfg>
+__device__ __forceinline__ int64_t ext_scale_b(const GemmParams& p) {
+  if constexpr (Cfg::kRagN) return p.N;
+  else if constexpr (Cfg::kBlockScale)
+    return static_cast<int64_t>(p.G) * (p.N / Cfg::kScaleBlock) * p.num_kb;
+  else return static_cast<int64_t>(p.G) * p.N;
+}
+template <class Cfg>
+__device__ __forceinline__ int64_t ext_out_rows(const GemmParams& p) {
+  if constexpr (Cfg::kRagN) return p.E;
+  else if constexpr (Cfg::kRagK) return static_cast<int64_t>(p.G) * p.E;
+  else return p.rows;
+}
+
 // Two TMEM values into two fp32 register accumulators with one packed (f32x2) operation:
 // round-to-nearest adds, or (block scaling) fused multiply-adds by the K block's scale.
 // Each lane of the pair rounds exactly as the scalar operation would.
@@ -538,7 +667,8 @@ __device__ void build_sched(const GemmParams& p, int32_t* rowinfo, int32_t* tile
     for (int32_t g = g0; g < g1; ++g) {
       // full slabs (batched layout) read no metadata
       int64_t v = p.meta_kind == 2 ? p.E
-                  : (kSpec ? __ldcg(reinterpret_cast<const long long*>(meta) + g) : meta[g]);
+                  : (kSpec ? __ldcg(reinterpret_cast<const long long*>(meta) + ck_index(p, g, G, kCkMeta))
+                           : meta[ck_index(p, g, G, kCkMeta)]);
       v = v < 0 ? 0 : (v > p.E ? p.E : v);
       rowinfo[g] = static_cast<int32_t>(v);
     }
@@ -546,10 +676,13 @@ __device__ void build_sched(const GemmParams& p, int32_t* rowinfo, int32_t* tile
     // rows of group g: m_sizes[g], or the step between successive int32 inclusive
     // offsets (offsets[-1] = 0)
     const int32_t* offs = reinterpret_cast<const int32_t*>(meta);
-    auto ld32 = [&](int32_t g) -> int64_t { return kSpec ? __ldcg(offs + g) : offs[g]; };
+    auto ld32 = [&](int32_t g) -> int64_t {
+      return kSpec ? __ldcg(offs + ck_index(p, g, G, kCkMeta)) : offs[ck_index(p, g, G, kCkMeta)];
+    };
     auto count = [&](int32_t g) -> int64_t {
       if (p.meta_kind == 1) return ld32(g) - (g > 0 ? ld32(g - 1) : 0);
-      return kSpec ? __ldcg(reinterpret_cast<const long long*>(meta) + g) : meta[g];
+      return kSpec ? __ldcg(reinterpret_cast<const long long*>(meta) + ck_index(p, g, G, kCkMeta))
+                   : meta[ck_index(p, g, G, kCkMeta)];
     };
     // ragged layouts partition the columns (N) or the contraction (K) instead of the rows
     const int64_t total = Cfg::kRagN ? p.N : (Cfg::kRagK ? p.K : p.rows);
@@ -905,7 +1038,9 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
           const Item it = work_item(w, i, worker, workers);
           const TileCoord c = decode_tile<Cfg>(ss, it.tile, 0u);
           for (int32_t kb = it.kb0; kb < it.kb1 && budget > 0; ++kb, --budget)
-            ptx::tma_prefetch_3d(&tmB, kb * kBK, c.n0, c.g);
+            ptx::tma_prefetch_3d(&tmB, ck_tma(p, kb * kBK, 0, p.K, true),
+                                 ck_tma(p, c.n0, 0, p.N, false),
+                                 ck_tma(p, c.g, 0, p.G, false));
         }
       }
       __syncwarp();
@@ -1051,25 +1186,32 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                 // both CTAs' bytes complete on the leader's full barrier, which expects them all
                 const uint32_t fb = ptx::mapa_shared(full_bar(stage), 0u);
                 if (crank == 0) ptx::mbar_arrive_expect_tx(full_bar(stage), 2 * Cfg::kStageBytes);
-                ptx::tma_load_2d_pair(s_act + stage * Cfg::kActBytes, &tmA, fb, kb * kBK, c.m0);
-                ptx::tma_load_3d_pair(s_w + stage * Cfg::kWBytes, &tmB, fb, kb * kBK,
-                                      c.n0 + static_cast<int32_t>(crank) * Cfg::kWRows, c.g);
+                const int32_t x = ck_tma(p, kb * kBK, 0, p.K, true);
+                ptx::tma_load_2d_pair(s_act + stage * Cfg::kActBytes, &tmA, fb, x,
+                                      ck_tma(p, c.m0, 0, p.rows, false));
+                // (the second CTA's half of an N-tail tile may lie wholly past N: zero fill)
+                ptx::tma_load_3d_pair(
+                    s_w + stage * Cfg::kWBytes, &tmB, fb, x,
+                    ck_tma(p, c.n0 + static_cast<int32_t>(crank) * Cfg::kWRows, 0, p.N, false),
+                    ck_tma(p, c.g, 0, p.G, false));
               }
             } else if (withhold) {
               withhold = false;  // this stage's full barrier never completes
             } else {
               ptx::mbar_arrive_expect_tx(full_bar(stage), Cfg::kStageBytes);
               // k0: a ragged-K slice starts on a multiple of 16 elements (16 bytes)
+              const int32_t x = ck_tma(p, c.k0 + kb * kBK, 0, p.K, true);
+              const int32_t ya = ck_tma(p, c.m0, 0, p.rows, false);
+              const int32_t yb = ck_tma(p, c.n0, 0, p.N, false);
+              const int32_t zb = ck_tma(p, c.bz, 0, Cfg::kRagged ? 1 : p.G, false);
               if constexpr (Cfg::kSwap) {
-                ptx::tma_load_2d_hint(s_act + stage * Cfg::kActBytes, &tmA, full_bar(stage),
-                                      c.k0 + kb * kBK, c.m0, pol_act);
-                ptx::tma_load_3d_hint(s_w + stage * Cfg::kWBytes, &tmB, full_bar(stage),
-                                      c.k0 + kb * kBK, c.n0, c.bz, pol_w);
+                ptx::tma_load_2d_hint(s_act + stage * Cfg::kActBytes, &tmA, full_bar(stage), x,
+                                      ya, pol_act);
+                ptx::tma_load_3d_hint(s_w + stage * Cfg::kWBytes, &tmB, full_bar(stage), x, yb,
+                                      zb, pol_w);
               } else {
-                ptx::tma_load_2d(s_act + stage * Cfg::kActBytes, &tmA, full_bar(stage),
-                                 c.k0 + kb * kBK, c.m0);
-                ptx::tma_load_3d(s_w + stage * Cfg::kWBytes, &tmB, full_bar(stage),
-                                 c.k0 + kb * kBK, c.n0, c.bz);
+                ptx::tma_load_2d(s_act + stage * Cfg::kActBytes, &tmA, full_bar(stage), x, ya);
+                ptx::tma_load_3d(s_w + stage * Cfg::kWBytes, &tmB, full_bar(stage), x, yb, zb);
               }
             }
             if (++stage == Cfg::kStages) {
@@ -1337,7 +1479,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         for (int32_t r = z0 + gw; r < z1; r += nw) {
           uint16_t* orow = p.out + static_cast<size_t>(r) * p.N;
           for (int32_t col = lane * 8; col < p.N; col += 256)
-            *reinterpret_cast<uint4*>(orow + col) = make_uint4(0u, 0u, 0u, 0u);
+            if (ck_range(p, static_cast<int64_t>(r) * p.N + col, 8, ext_out_rows<Cfg>(p) * p.N))
+              *reinterpret_cast<uint4*>(orow + col) = make_uint4(0u, 0u, 0u, 0u);
         }
       }
     }
@@ -1398,24 +1541,30 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
       float sw_sa[(Cfg::kTileN + 31) / 32];
       if constexpr (Cfg::kSwap && !Cfg::kBlockScale) {
         const int32_t n = c.n0 + static_cast<int32_t>(32u * q + lane);
-        sw_sb = (n >= c.n_begin && n < c.n_end) ? __ldg(p.scale_b + c.sb_off + n) : 0.0f;
+        sw_sb = (n >= c.n_begin && n < c.n_end)
+                    ? __ldg(p.scale_b + ck_index(p, c.sb_off + n, ext_scale_b<Cfg>(p), kCkScale))
+                    : 0.0f;
 #pragma unroll
         for (int pc = 0; pc < (Cfg::kTileN + 31) / 32; ++pc) {
           constexpr int kCols = Cfg::kTileN < 32 ? Cfg::kTileN : 32;
           const int32_t Rl = c.m0 + pc * 32 + static_cast<int32_t>(lane);
           sw_sa[pc] = (lane < static_cast<uint32_t>(kCols) && Rl < c.valid_end)
-                          ? __ldg(p.scale_a + (Rl + c.srow_delta))
+                          ? __ldg(p.scale_a + ck_index(p, Rl + c.srow_delta,
+                                                       ext_scale_a<Cfg>(p), kCkScale))
                           : 0.0f;
         }
       }
       if constexpr (!Cfg::kSwap && !Cfg::kBlockScale) {
         const int32_t R = c.m0 + row_off + static_cast<int32_t>(lane);
-        if (active && R < c.valid_end) sa_pre = __ldg(p.scale_a + (R + c.srow_delta));
+        if (active && R < c.valid_end)
+          sa_pre = __ldg(p.scale_a + ck_index(p, R + c.srow_delta, ext_scale_a<Cfg>(p), kCkScale));
         const float* sb_g = p.scale_b + c.sb_off;
 #pragma unroll
         for (int pc = 0; pc < Cfg::kThreadCols / 32; ++pc) {
           const int32_t col = c.n0 + ocol + pc * 32 + static_cast<int32_t>(lane);
-          sb_pre[pc] = (active && col < c.n_end) ? __ldg(sb_g + col) : 0.0f;
+          sb_pre[pc] = (active && col < c.n_end)
+                           ? __ldg(ck_ptr(p, sb_g + col, p.scale_b, ext_scale_b<Cfg>(p)))
+                           : 0.0f;
         }
       }
       if constexpr (Cfg::kBlockScale && !Cfg::kSwap) {
@@ -1427,7 +1576,10 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         // (columns of a tile past N are never stored: clamp their block into range)
         const int32_t blk = min((c.n0 + ocol) / Cfg::kScaleBlock, nblk - 1);
         bs_b = p.scale_b + (static_cast<size_t>(c.g) * nblk + blk) * p.num_kb;
-        bs_next = (rv && it.kb0 < kb_end) ? __ldg(bs_a + it.kb0) * __ldg(bs_b + it.kb0) : 0.0f;
+        bs_next = (rv && it.kb0 < kb_end)
+                      ? __ldg(ck_ptr(p, bs_a + it.kb0, p.scale_a, ext_scale_a<Cfg>(p))) *
+                            __ldg(ck_ptr(p, bs_b + it.kb0, p.scale_b, ext_scale_b<Cfg>(p)))
+                      : 0.0f;
         sa_pre = 1.0f;
 #pragma unroll
         for (int pc = 0; pc < Cfg::kThreadCols / 32; ++pc) sb_pre[pc] = 1.0f;
@@ -1459,10 +1611,12 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
       }
       constexpr size_t kPerWarp = 32 * Cfg::kThreadCols;
       auto piece = [&](int32_t cta) -> float* {
-        return p.sk_ws + (static_cast<size_t>(cta * 2) * Cfg::kEpiWarps + ew) * kPerWarp;
+        return p.sk_ws + (static_cast<size_t>(ck_index(p, cta, gridDim.x, kCkSplit) * 2) * Cfg::kEpiWarps +
+                          ew) * kPerWarp;
       };
       uint32_t* const cnt =
-          it.sk_tile >= 0 ? p.sk_cnt + static_cast<size_t>(it.sk_tile) * Cfg::kEpiWarps + ew
+          it.sk_tile >= 0 ? p.sk_cnt + static_cast<size_t>(ck_index(p, it.sk_tile, 2 * gridDim.x, kCkSplit)) *
+                                           Cfg::kEpiWarps + ew
                           : nullptr;
       // The owner of a split tile whose other pieces are already counted in -- they are
       // their CTAs' first items and normally finished long before the owner's own piece --
@@ -1514,13 +1668,14 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
 #pragma unroll
             for (int j = 0; j < Cfg::kBSSub; ++j) {
               const int32_t kbj = min(kb0 + j, kb_end - 1);
-              sub_bs[j] = __ldg(bs_b + kbj);
-              sub_row[j] = __ldg(bs_a + kbj);
+              sub_bs[j] = __ldg(ck_ptr(p, bs_b + kbj, p.scale_b, ext_scale_b<Cfg>(p)));
+              sub_row[j] = __ldg(ck_ptr(p, bs_a + kbj, p.scale_a, ext_scale_a<Cfg>(p)));
             }
           } else if constexpr (Cfg::kBlockScale) {
             bs = bs_next;
             if (kb0 + 1 < kb_end && bs_a != nullptr)
-              bs_next = __ldg(bs_a + kb0 + 1) * __ldg(bs_b + kb0 + 1);
+              bs_next = __ldg(ck_ptr(p, bs_a + kb0 + 1, p.scale_a, ext_scale_a<Cfg>(p))) *
+                        __ldg(ck_ptr(p, bs_b + kb0 + 1, p.scale_b, ext_scale_b<Cfg>(p)));
           }
           // scale of accumulator column j (block scaling; swap-AB: row j's times column's)
           auto cs = [&](int j) -> float {
@@ -1727,7 +1882,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
             }
             ptx::fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) {
+            if (lane == 0 &&
+                ck_tma_store(p, col0, R_first + c.orow_delta, ext_out_rows<Cfg>(p), p.N)) {
               ptx::tma_store_2d(&tmC, stg, col0, R_first + c.orow_delta);
               ptx::bulk_commit();
             }
@@ -1750,20 +1906,25 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                 y[j] = (acc[pc * 32 + j8 * 8 + j] * sa) * sb;
               }
               const int32_t col = col0 + j8 * 8;  // a multiple of 8: 16-byte aligned
+              const int64_t o_idx = static_cast<int64_t>(R + c.orow_delta) * p.N + col;
               if (col + 7 < c.n_end && col >= c.n_begin) {
-                if (row_val) {
-                  *reinterpret_cast<uint4*>(orow + col) =
-                      make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]),
-                                 pack_bf16x2(y[4], y[5]), pack_bf16x2(y[6], y[7]));
-                } else if (row_zero) {
-                  *reinterpret_cast<uint4*>(orow + col) = make_uint4(0u, 0u, 0u, 0u);
+                if ((row_val || row_zero) &&
+                    ck_range(p, o_idx, 8, ext_out_rows<Cfg>(p) * p.N)) {
+                  if (row_val) {
+                    *reinterpret_cast<uint4*>(orow + col) =
+                        make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]),
+                                   pack_bf16x2(y[4], y[5]), pack_bf16x2(y[6], y[7]));
+                  } else {
+                    *reinterpret_cast<uint4*>(orow + col) = make_uint4(0u, 0u, 0u, 0u);
+                  }
                 }
               } else if (Cfg::kRagN && row_val && col < c.n_end && col + 7 >= c.n_begin) {
                 // a ragged-N group starting or ending inside these 8 columns: its own
                 // columns one by one
 #pragma unroll
                 for (int j = 0; j < 8; ++j)
-                  if (col + j >= c.n_begin && col + j < c.n_end)
+                  if (col + j >= c.n_begin && col + j < c.n_end &&
+                      ck_range(p, o_idx + j, 1, ext_out_rows<Cfg>(p) * p.N))
                     orow[col + j] = __bfloat16_as_ushort(__float2bfloat16_rn(y[j]));
               }
             }
@@ -1788,11 +1949,14 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
             const int32_t R = m_first + j;
             if (R < c.valid_end) {
               const float y = (acc[pc * 32 + j] * sa) * sb;
-              if (col_ok)
+              if (col_ok && ck_range(p, static_cast<int64_t>(R + c.orow_delta) * p.N + n, 1,
+                                     ext_out_rows<Cfg>(p) * p.N))
                 p.out[static_cast<size_t>(R + c.orow_delta) * p.N + n] =
                     __bfloat16_as_ushort(__float2bfloat16_rn(y));
             } else if (R < c.zero_end) {
-              if (col_ok) p.out[static_cast<size_t>(R + c.orow_delta) * p.N + n] = 0;
+              if (col_ok && ck_range(p, static_cast<int64_t>(R + c.orow_delta) * p.N + n, 1,
+                                     ext_out_rows<Cfg>(p) * p.N))
+                p.out[static_cast<size_t>(R + c.orow_delta) * p.N + n] = 0;
             }
           }
         }

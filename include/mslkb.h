@@ -73,6 +73,14 @@ typedef enum mslkb_status {
 #define MSLKB_DEV_TIMEOUT 0x1u        /* a pipeline wait in the kernel gave up (~1 s)  */
 #define MSLKB_DEV_MSIZES_CLAMPED 0x2u /* m_sizes had a negative entry or summed past total_M */
 #define MSLKB_DEV_BAD_SLICE 0x4u      /* ragged K: a slice bound not a multiple of 16 */
+#define MSLKB_DEV_BOUNDS 0x8u         /* checked build (libmslkb_checked.so) only: a kernel
+                                         index fell outside the buffers of the call; that
+                                         access was not made as asked.  Bits 16..23 then name
+                                         the kinds of access: 16 group metadata, 17 TMA load
+                                         K coordinate, 18 TMA load row / column / group
+                                         coordinate, 19 TMA K coordinate not 16-byte aligned,
+                                         20 scales, 21 direct output store, 22 TMA output
+                                         store, 23 split-tile workspace */
 
 /* Limits. */
 #define MSLKB_MAX_GROUPS 1024         /* G (kernel keeps per-group tables in shared memory) */
