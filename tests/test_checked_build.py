@@ -178,3 +178,23 @@ def test_full_size(orc, name):
     compare(got.ravel(), ref.ravel(), ab.ravel(), f"{name} (checked build)")
     del inp, prob, out
     torch.cuda.empty_cache()
+
+
+LIMITS = [("test_max_groups_stacked", (None, 256)), ("test_max_groups_stacked", (None, 200)),
+          ("test_max_groups_dynamic_and_batched", (None,)), ("test_max_groups_offsets", ()),
+          ("test_max_groups_ragged_n", (None,)), ("test_max_groups_ragged_k", (None,)),
+          ("test_max_groups_block_scaled_stacked", (None,)),
+          ("test_max_groups_block_scaled_dynamic", (None,)),
+          ("test_over_2_31_stacked", (8192,)), ("test_over_2_31_stacked", (8200,)),
+          ("test_over_2_31_dynamic", ()), ("test_over_2_31_weights_decode", ()),
+          ("test_over_2_31_ragged_k", ()), ("test_over_2_31_ragged_n", ())]
+
+
+@pytest.mark.parametrize("name,args", LIMITS, ids=[f"{n}{a}" for n, a in LIMITS])
+def test_limits(orc, name, args):
+    # 1024 groups on every layout, and operands past 2^31 elements, through the planner's
+    # kernels of the checked build (the cases assert a clean status word themselves)
+    import test_limits
+    fx.device_status()
+    getattr(test_limits, name)(orc, *args)
+    _clean(name)
