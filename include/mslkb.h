@@ -41,6 +41,13 @@
  * - Errors found on the device (a wait that timed out, m_sizes that overran total_M)
  *   cannot be returned by an asynchronous call; they are OR-ed into a per-device status
  *   word read by mslkb_get_device_status().
+ * - Host threads may call at the same time, on one stream or on several; the library's
+ *   tables (device set-up, stream workspaces) are guarded by a lock.
+ * - Every kernel launch is enqueued inside an NVTX push/pop range of the domain "mslkb"
+ *   whose message is the kernel variant's name (mslkb_variant_name) and whose int64
+ *   payload is the rows of A, so a profiler can select this library's launches (ncu:
+ *   --nvtx --nvtx-include "mslkb@<variant name>/").  With no tool attached the range
+ *   calls return at once; a launch captured in a CUDA graph replays without them.
  */
 #ifndef MSLKB_H_
 #define MSLKB_H_

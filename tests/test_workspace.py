@@ -80,3 +80,50 @@ def test_two_streams_at_once():
     for s in (s1, s2):
         fx.mslkb_release_workspace(s.cuda_stream)
     assert fx.device_status() == 0
+
+
+def test_host_threads_on_their_own_streams():
+    # five host threads call the library at once (ctypes drops the GIL for the call), each on
+    # a stream of its own: the first call on each stream creates its workspace under the
+    # library's lock while the others plan and launch; every result must match the oracle
+    import threading
+    cases = [_problem(8, 2048, 2048, [1, 0, 3, 2, 0, 1, 1, 2], 71),      # split swap-AB
+             _problem(8, 2048, 1024, [0, 2, 1, 1, 3, 0, 1, 4], 75),      # split swap-AB
+             _problem(2, 8192, 256, [1100, 1000], 72),                   # CTA pairs, claims
+             _problem(4, 520, 1000, [130, 0, 257, 64], 73),              # cp.async loader
+             _problem(5, 392, 688, [130, 1, 257, 64, 17], 74)]           # 128-row tiles
+    with_workspace = 3   # the split and pair plans; the others need none
+    orc = oracle.load(0)
+    refs = [p.oracle_full(orc) for p in cases]
+    base = fx.mslkb_workspace_count()
+    streams = [torch.cuda.Stream() for _ in cases]
+    outs = [[None] * 6 for _ in cases]
+    errors = []
+    start = threading.Barrier(len(cases))
+
+    def worker(i):
+        try:
+            torch.cuda.set_device(0)
+            start.wait()
+            with torch.cuda.stream(streams[i]):
+                for r in range(6):
+                    outs[i][r] = cases[i].run_gpu()
+            streams[i].synchronize()
+        except Exception as e:  # noqa: BLE001 - reported below
+            errors.append(f"thread {i}: {e!r}")
+
+    threads = [threading.Thread(target=worker, args=(i,)) for i in range(len(cases))]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join(timeout=120)
+    assert not any(t.is_alive() for t in threads), "a host thread did not finish"
+    assert not errors, errors
+    assert fx.mslkb_workspace_count() == base + with_workspace
+    for i, (ref, ab) in enumerate(refs):
+        for r in range(6):
+            compare(bits_of(outs[i][r]).ravel(), ref.ravel(), ab.ravel(), f"thread {i} call {r}")
+    for s in streams:
+        fx.mslkb_release_workspace(s.cuda_stream)
+    assert fx.mslkb_workspace_count() == base
+    assert fx.device_status() == 0
