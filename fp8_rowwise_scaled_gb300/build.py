@@ -8,7 +8,7 @@ report an index outside them in the device status word (MSLKB_DEV_BOUNDS) instea
 making the access.  A test build (the stand-in for a memory checker); slower.
 
 Each translation unit in csrc/ compiles in parallel to _build/*.o, then nvcc links them
-into fp8_rowwise_scaled_gb300/libmslkb.so (CUDA runtime linked statically; the driver's
+into fp8_rowwise_scaled_gb300/libmslkb.so (CUDA runtime linked statically; the CUDA driver's
 tensor-map encoder is fetched at run time, so the library loads on a machine without a
 GPU).  Rebuilds only when a source or header is newer than the library.
 """
