@@ -25,6 +25,9 @@ from parity_util import Problem, bits_of, compare
 pytestmark = pytest.mark.gpu
 
 
+_PRODUCT = []   # the product library, while the binding points at the checked one
+
+
 @pytest.fixture(scope="module", autouse=True)
 def checked_lib():
     if not torch.cuda.is_available():
@@ -33,6 +36,7 @@ def checked_lib():
     fx.lib()
     lib = fx.declare(ctypes.CDLL(fxbuild.build(checked=True)))
     saved = fx._lib
+    _PRODUCT.append(saved)
     fx._lib = lib
     try:
         fx.device_status()
@@ -198,3 +202,37 @@ def test_limits(orc, name, args):
     fx.device_status()
     getattr(test_limits, name)(orc, *args)
     _clean(name)
+
+
+@pytest.mark.parametrize("variant", _names("stacked", exclude=("blockscale",)) +
+                         _names("dynamic_blockscale_") + _names("blockscale_"))
+def test_same_bits_as_the_product_library(checked_lib, variant):
+    # the checks change no arithmetic: the same call through both libraries gives the same
+    # output bits
+    from test_parity import _rand_problem
+    outs = []
+    for lib in (_PRODUCT[0], checked_lib):
+        fx._lib = lib
+        try:
+            if "blockscale" in variant:
+                if variant.startswith("dynamic"):
+                    from test_blockscale_slabs import _case, _run
+                    zsi = [13, 0, 1, 24, 99, -3]
+                    A, B, sa, sb = _case(31, 6, 24, 384, 896, zsi)
+                    outs.append(_run(A, B, sa, sb, zsi, 24, variant))
+                else:
+                    from test_blockscale import _case, _run
+                    A, B, sa, sb, m, rows = _case(32, 5, [130, 0, 1, 257, 64], 384, 896, extra=5)
+                    outs.append(_run(A, B, sa, sb, m, rows, 384, variant))
+            else:
+                prob = _rand_problem("stacked", 7, 392, 688, [130, 0, 1, 257, 64, 0, 17], seed=33,
+                                     total_extra=9)
+                out = torch.full((prob.rows, prob.N), 0x5A5A, dtype=torch.int16,
+                                 device="cuda").view(torch.bfloat16)
+                prob.run_gpu(out=out, variant=variant)
+                torch.cuda.synchronize()
+                outs.append(bits_of(out))
+        finally:
+            fx._lib = checked_lib
+    assert np.array_equal(outs[0], outs[1]), f"{variant}: checked and product builds differ"
+    _clean(variant)
