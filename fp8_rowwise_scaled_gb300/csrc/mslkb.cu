@@ -32,7 +32,7 @@ constexpr int kVersion = 10000;  // 1.0.0
 constexpr int kMaxDevices = 64;
 constexpr uint64_t kWaitTimeoutNs = 1000000000ull;  // one pipeline wait gives up after ~1 s
 std::atomic<uint64_t> g_wait_timeout_ns{kWaitTimeoutNs};
-std::atomic<int> g_test_stall{0};  // one-shot: the next launch of run() withholds a stage
+std::atomic<int> g_test_stall{0};  // one-shot: the next launch withholds a stage
 // one-shot: the next launch's speculative schedule reads this metadata instead
 std::atomic<const void*> g_test_spec_meta{nullptr};
 
@@ -653,6 +653,7 @@ mslkb_status run_ragged(int layout, const void* A, const void* B, const float* s
     p.kb_per_chunk = (kpc <= 0 || kpc > p.num_kb) ? (p.num_kb > 0 ? p.num_kb : 1) : kpc;
   }
   p.timeout_ns = g_wait_timeout_ns.load();
+  p.test_stall = g_test_stall.exchange(0);
   p.split_k = 0;
   // A [a_rows, k_row]; B as a one-group [1, b_rows, k_row] map; out [out_rows, n_cols]
   if ((s = encode_maps(&la, v, A, B, a_rows, 1, b_rows, k_row)) != MSLKB_OK) return s;
@@ -734,6 +735,7 @@ mslkb_status run_stacked_with_scratch(const void* A, const void* B, const float*
     p.kb_per_chunk = (kpc <= 0 || kpc > p.num_kb) ? (p.num_kb > 0 ? p.num_kb : 1) : kpc;
   }
   p.timeout_ns = g_wait_timeout_ns.load();
+  p.test_stall = g_test_stall.exchange(0);
   p.prefetch_kb = prefetch_kb_for(v);
   p.spec_meta = p.meta;
   p.split_k = info.split_k;

@@ -78,12 +78,12 @@ MSLKB_API mslkb_status mslkb_set_weight_prefetch(int32_t kblocks);
 MSLKB_API mslkb_status mslkb_test_speculate_from_next_launch(const void* meta);
 
 /*
- * Test hook for failure detection: the next launch through the stacked, dynamic, offsets
- * or batched entry points has its first CTA (its first CTA pair's leader, on CTA-pair
- * kernels fed by TMA) withhold one pipeline stage, so that a wait of that CTA runs out
- * after the limit set by mslkb_set_wait_timeout_us and the kernel's abort path runs.  That
- * launch's output is incomplete and the status word reports MSLKB_DEV_TIMEOUT; a following
- * call computes normally.  Only kernels fed by TMA take part (others ignore it).
+ * Test hook for failure detection: the next launch, through any entry point, has its
+ * first CTA (both CTAs of its first pair, on CTA-pair kernels) withhold one pipeline stage,
+ * so that a wait of that CTA runs out after the limit set by mslkb_set_wait_timeout_us and
+ * the kernel's abort path runs.  That launch's output is incomplete and the status word
+ * reports MSLKB_DEV_TIMEOUT; a following call computes normally.  Only kernels fed by TMA
+ * take part: a launch of the cp.async kernels uses the hook up and computes normally.
  */
 MSLKB_API mslkb_status mslkb_test_stall_next_launch(void);
 

@@ -120,3 +120,71 @@ def test_cta_pair_wait_runs_out_and_the_next_calls_are_right(L, layout):
     assert fx.device_status() == 0
     compare(bits_of(outs[2]).ravel(), ref.ravel(), ab.ravel(),
             f"{layout} pairs, the second call after a timeout")
+
+
+def _stall_then_right(stalled_call, right_call, what):
+    """The next launch withholds a stage: it must return with MSLKB_DEV_TIMEOUT set; then
+    the same problem, called again, must match the oracle (right_call checks that)."""
+    fx.device_status()                        # start clean
+    fx.mslkb_set_wait_timeout_us(50_000)      # 50 ms
+    try:
+        fx.mslkb_test_stall_next_launch()
+        stalled_call()
+        torch.cuda.synchronize()              # the launch returns: no hang, no fault
+        assert fx.device_status() & fx.MSLKB_DEV_TIMEOUT, what
+    finally:
+        fx.mslkb_set_wait_timeout_us(0)
+    right_call()
+    torch.cuda.synchronize()
+    assert fx.device_status() == 0, what
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("family", ["blockscale_tile128x256_tma",
+                                    "dynamic_blockscale_swap_w128xa16_tma",
+                                    "ragn_tile128x256_tma", "ragk_tile128x256_tma"])
+def test_wait_runs_out_on_the_other_kernel_families(L, family):
+    """The same on the block-scaled kernels (whose stages the epilogue frees, and whose
+    128 x 256 tiles issue their K blocks from the unrolled runs: K = 2048 gives 16 blocks)
+    and on the ragged-N and ragged-K kernels."""
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    orc = oracle.load(0)
+    if family == "blockscale_tile128x256_tma":
+        from test_blockscale import _case, _check, _run
+        A, B, sa, sb, m, rows = _case(81, 4, [300, 0, 257, 411], 512, 2048)
+        _stall_then_right(lambda: _run(A, B, sa, sb, m, rows, 512, family),
+                          lambda: _check(orc, A, B, sa, sb, m, rows,
+                                         _run(A, B, sa, sb, m, rows, 512, family), family),
+                          family)
+    elif family == "dynamic_blockscale_swap_w128xa16_tma":
+        from test_blockscale_slabs import _case, _check, _run
+        zsi = [16, 3, 0, 9, 16, 1, 12, 7]
+        A, B, sa, sb = _case(82, 8, 16, 1024, 2048, zsi)
+        _stall_then_right(lambda: _run(A, B, sa, sb, zsi, 16, family),
+                          lambda: _check(orc, A, B, sa, sb, zsi, 16,
+                                         _run(A, B, sa, sb, zsi, 16, family), family),
+                          family)
+    elif family == "ragn_tile128x256_tma":
+        from test_ragged_layouts import _cuda, _data, _n_offsets_case, _run
+        G, M, total_N, K, cols = 4, 300, 2048, 1024, [500, 0, 777, 600]
+        A, B, sa, sb = _data(83, (G, M, K), (total_N, K), G * M, total_N)
+        tA, tB, tsa, tsb, toff = _cuda(A, B, sa, sb, np.cumsum(cols).astype(np.int32))
+        out = torch.empty((M, total_N), dtype=torch.bfloat16, device="cuda")
+        _stall_then_right(
+            lambda: _run(fx.f8f8bf16_rowwise_grouped_n_offsets, family, tA, tB, tsa, tsb, toff,
+                         out),
+            lambda: _n_offsets_case(orc, G, M, total_N, K, cols, seed=83, variant=family),
+            family)
+    else:
+        from test_ragged_layouts import _cuda, _data, _k_offsets_case, _run
+        G, M, N, ks = 4, 300, 512, [1024, 0, 2048, 512]
+        total_K = sum(ks)
+        A, B, sa, sb = _data(84, (M, total_K), (N, total_K), G * M, G * N)
+        tA, tB, tsa, tsb, toff = _cuda(A, B, sa, sb, np.cumsum(ks).astype(np.int32))
+        out = torch.empty((G, M, N), dtype=torch.bfloat16, device="cuda")
+        _stall_then_right(
+            lambda: _run(fx.f8f8bf16_rowwise_grouped_k_offsets, family, tA, tB, tsa, tsb, toff,
+                         out),
+            lambda: _k_offsets_case(orc, G, M, N, total_K, ks, seed=84, variant=family),
+            family)
