@@ -654,6 +654,7 @@ mslkb_status run_ragged(int layout, const void* A, const void* B, const float* s
   }
   p.timeout_ns = g_wait_timeout_ns.load();
   p.test_stall = g_test_stall.exchange(0);
+  g_test_spec_meta.store(nullptr);  // no weight prefetch here: the hook is used up
   p.split_k = 0;
   // A [a_rows, k_row]; B as a one-group [1, b_rows, k_row] map; out [out_rows, n_cols]
   if ((s = encode_maps(&la, v, A, B, a_rows, 1, b_rows, k_row)) != MSLKB_OK) return s;
@@ -737,7 +738,10 @@ mslkb_status run_stacked_with_scratch(const void* A, const void* B, const float*
   p.timeout_ns = g_wait_timeout_ns.load();
   p.test_stall = g_test_stall.exchange(0);
   p.prefetch_kb = prefetch_kb_for(v);
-  p.spec_meta = p.meta;
+  {
+    const void* spec = g_test_spec_meta.exchange(nullptr);
+    p.spec_meta = static_cast<const int64_t*>(spec != nullptr ? spec : p.meta);
+  }
   p.split_k = info.split_k;
   p.sk_ws = partials;
   p.sk_cnt = counters;

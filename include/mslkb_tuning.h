@@ -70,10 +70,11 @@ MSLKB_API int32_t mslkb_accumulation_chunk(void);
 MSLKB_API mslkb_status mslkb_set_weight_prefetch(int32_t kblocks);
 
 /*
- * Test hook for the weight prefetch: the next launch through the stacked, dynamic or
- * offsets entry points builds its speculative schedule from `meta` (a device buffer laid
- * out like that call's own metadata, G entries) instead of the call's metadata, so that
- * the prefetch goes to other tiles than the call computes.  The results must not change.
+ * Test hook for the weight prefetch: the next launch builds its speculative schedule from
+ * `meta` (a device buffer laid out like that call's own metadata, G entries) instead of
+ * the call's metadata, so that the prefetch goes to other tiles than the call computes.
+ * The results must not change.  A launch through the ragged entry points, which prefetch
+ * nothing, uses the hook up.
  */
 MSLKB_API mslkb_status mslkb_test_speculate_from_next_launch(const void* meta);
 

@@ -533,6 +533,21 @@ def test_weight_prefetch_is_only_a_hint(orc, layout):
         got = bits_of(prob.run_gpu(variant=v)).reshape(base.shape)
         torch.cuda.synchronize()
         assert np.array_equal(base, got), f"{layout}: speculation from {fake} leaked"
+        if layout == "stacked":   # the allocation-free entry point takes the hook too
+            out = torch.empty(base.shape, dtype=torch.bfloat16, device="cuda")
+            fx.mslkb_test_speculate_from_next_launch(f)
+            fx.mslkb_force_variant(fx.variant_index(v))
+            try:
+                s = fx.mslkb_f8f8bf16_rowwise_grouped_stacked_noalloc(
+                    prob.A.data_ptr(), prob.B.data_ptr(), prob.sa.data_ptr(), prob.sb.data_ptr(),
+                    prob.meta.data_ptr(), out.data_ptr(), prob.rows, prob.G, prob.N, prob.K,
+                    torch.cuda.current_stream().cuda_stream)
+            finally:
+                fx.mslkb_force_variant(-1)
+            assert s == fx.MSLKB_OK, fx.mslkb_status_string(s)
+            torch.cuda.synchronize()
+            got = bits_of(out).reshape(base.shape)
+            assert np.array_equal(base, got), f"allocation-free: speculation from {fake} leaked"
     assert fx.device_status() == 0
 
 
