@@ -1,7 +1,6 @@
 """C-ABI checks that need no GPU: the library builds, loads and exports every symbol
 include/*.h declare; argument errors are reported before any CUDA call; the host
 planner picks the intended kernel variant for each workload shape."""
-import ctypes
 import os
 import re
 
