@@ -535,8 +535,7 @@ mslkb_status run(int layout, const void* A, const void* B, const float* scale_a,
   const VariantInfo* v = variant(info.variant);
   if ((s = ensure_attr(st, info.variant)) != MSLKB_OK) return s;
 
-  LaunchArgs la;
-  std::memset(&la, 0, sizeof(la));
+  LaunchArgs la{};  // every parameter zero unless set below
   GemmParams& p = la.params;
   p.A = static_cast<const uint8_t*>(A);
   p.B = static_cast<const uint8_t*>(B);
@@ -630,8 +629,7 @@ mslkb_status run_ragged(int layout, const void* A, const void* B, const float* s
   const VariantInfo* v = variant(info.variant);
   if ((s = ensure_attr(st, info.variant)) != MSLKB_OK) return s;
 
-  LaunchArgs la;
-  std::memset(&la, 0, sizeof(la));
+  LaunchArgs la{};  // every parameter zero unless set below
   GemmParams& p = la.params;
   p.A = static_cast<const uint8_t*>(A);
   p.B = static_cast<const uint8_t*>(B);
@@ -714,8 +712,7 @@ mslkb_status run_stacked_with_scratch(const void* A, const void* B, const float*
     return MSLKB_ERR_TOO_LARGE;
   if ((s = ensure_attr(st, info.variant)) != MSLKB_OK) return s;
 
-  LaunchArgs la;
-  std::memset(&la, 0, sizeof(la));
+  LaunchArgs la{};  // every parameter zero unless set below
   GemmParams& p = la.params;
   p.A = static_cast<const uint8_t*>(A);
   p.B = static_cast<const uint8_t*>(B);
