@@ -440,6 +440,18 @@ def sweep_shape(fx, wl, pk, device):
     return {"wl": wl, "us": us, "window": (t0, t1), "variant": fx.variant_name(plan.variant)}
 
 
+def compact_row(name, us, tflops, bound, frac, frac_nominal, sm_mhz, variant):
+    """One PER_SHAPE_COLS row, short enough that all rows fit the last 1500 characters of
+    the output line: whole TFLOPS and MHz, 0.1 us, and the variant name without its
+    "stacked_" prefix and "_tma" suffix (the layout is the workload's; TMA unless "cpasync")."""
+    if variant.startswith("stacked_"):
+        variant = variant[len("stacked_"):]
+    if variant.endswith("_tma"):
+        variant = variant[:-len("_tma")]
+    return [name, round(us, 1), int(round(tflops)), bound, round(frac, 3),
+            round(frac_nominal, 3), None if sm_mhz is None else int(round(sm_mhz)), variant]
+
+
 def shape_row(res, pk, clk):
     """Compact per-shape row (PER_SHAPE_COLS) with the clocks of the shape's own window."""
     if "error" in res:
@@ -447,8 +459,8 @@ def shape_row(res, pk, clk):
     wl, us = res["wl"], res["us"]
     sm = clk.window(*res["window"])["sm_mhz"]
     r = roofline(wl, pk, us * 1e-6, sm)
-    return [wl.name, round(us, 2), round(wl.flops() / (us * 1e-6) / 1e12, 1), r["bound"],
-            round(r["frac"], 3), round(r["frac_nominal"], 3), sm, res["variant"]]
+    return compact_row(wl.name, us, wl.flops() / (us * 1e-6) / 1e12, r["bound"], r["frac"],
+                       r["frac_nominal"], sm, res["variant"])
 
 
 def link_bandwidth(device, nbytes=1 << 30, reps=3):
@@ -623,9 +635,9 @@ def gpu_arm(args):
         # compact rows, last on the line: each shape's roofline fraction against the peak
         # that matches the clocks of its own timed replays
         rows = [shape_row(r, pk, clk) for r in sweep]
-        rows.append([wl.name, round(ms_per_step * 1e3, 2), round(value / ws, 1), rf["bound"],
-                     round(rf["frac"], 3), round(rf["frac_nominal"], 3), clocks["sm_mhz"],
-                     fx.variant_name(plan.variant)])
+        rows.append(compact_row(wl.name, ms_per_step * 1e3, value / ws, rf["bound"], rf["frac"],
+                                rf["frac_nominal"], clocks["sm_mhz"],
+                                fx.variant_name(plan.variant)))
         result["per_shape_cols"] = PER_SHAPE_COLS
         result["per_shape"] = rows
     if rank == 0:

@@ -74,6 +74,24 @@ def test_compact_rows_name_every_column():
     wl = workloads()["c3_llama70b_m16"]
     row = bench.shape_row({"wl": wl, "us": 120.0, "window": (0, 1), "variant": "v"}, PK, Clk())
     assert len(row) == len(bench.PER_SHAPE_COLS)
-    assert row[0] == wl.name and row[3] == "hbm" and row[6] == 1500.0
+    assert row[0] == wl.name and row[3] == "hbm" and row[6] == 1500
     err = bench.shape_row({"workload": "x", "error": "boom"}, PK, Clk())
     assert len(err) == len(bench.PER_SHAPE_COLS) and err[0] == "x"
+
+
+def test_per_shape_rows_fit_the_tail_of_the_line():
+    # the rows come last on the output line; with the planner's variants and numbers as wide
+    # as the sweep's, they and their column names fit in its last 1500 characters
+    import json
+    import fp8_rowwise_scaled_gb300 as fx
+    from fp8_rowwise_scaled_gb300 import build as fxbuild
+    fxbuild.build()
+    wls = workloads()
+    rows = []
+    for n in list(bench.SWEEP) + [bench.HEADLINE]:
+        plan = bench.plan_for(fx, wls[n], 152)          # the planner's variant on 152 SMs
+        rows.append(bench.compact_row(n, 3074.14, 2861.32, "tensor", 0.8335, 0.6358, 2070.0,
+                                      fx.variant_name(plan.variant)))
+    tail = json.dumps({"per_shape_cols": bench.PER_SHAPE_COLS, "per_shape": rows},
+                      separators=(",", ":"))
+    assert len(tail) < 1500, len(tail)
