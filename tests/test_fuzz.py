@@ -5,6 +5,8 @@ cp.async loader), dynamic valid-row counts outside [0, E], scales over 16 binade
 layout does not own must keep their contents."""
 from __future__ import annotations
 
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -18,7 +20,10 @@ from parity_util import Problem, bits_of, compare
 pytestmark = pytest.mark.gpu
 
 LAYOUTS = ("stacked", "dynamic", "offsets", "batched")
-CASES_PER_LAYOUT = 16
+# cases per layout, and per ragged / block-scaled entry point; a longer run draws more seeds
+# (e.g. MSLKB_FUZZ_CASES=2500 MSLKB_FUZZ_SIDE_CASES=800)
+CASES_PER_LAYOUT = int(os.environ.get("MSLKB_FUZZ_CASES", "16"))
+SIDE_CASES = int(os.environ.get("MSLKB_FUZZ_SIDE_CASES", "10"))
 POISON = 0x5A5A
 
 
@@ -82,7 +87,7 @@ def test_fuzz(orc, layout, i):
 
 # -- the ragged and block-scaled entry points, through their own parity helpers ---------
 
-@pytest.mark.parametrize("i", range(10))
+@pytest.mark.parametrize("i", range(SIDE_CASES))
 def test_fuzz_ragged_n(orc, i):
     from test_ragged_layouts import _n_offsets_case
     rng = np.random.default_rng(5000 + i)
@@ -98,7 +103,7 @@ def test_fuzz_ragged_n(orc, i):
     assert fx.device_status() == 0
 
 
-@pytest.mark.parametrize("i", range(10))
+@pytest.mark.parametrize("i", range(SIDE_CASES))
 def test_fuzz_ragged_k(orc, i):
     from test_ragged_layouts import _k_offsets_case
     rng = np.random.default_rng(6000 + i)
@@ -114,7 +119,7 @@ def test_fuzz_ragged_k(orc, i):
     assert fx.device_status() == 0
 
 
-@pytest.mark.parametrize("i", range(10))
+@pytest.mark.parametrize("i", range(SIDE_CASES))
 def test_fuzz_groupwise(orc, i):
     from test_blockscale import _case, _check, _run
     rng = np.random.default_rng(7000 + i)
