@@ -135,3 +135,69 @@ def test_fuzz_groupwise(orc, i):
     got = _run(A, B, sa, sb, mm, rows, N)
     _check(orc, A, B, sa, sb, mm, rows, got, f"groupwise #{i}: G={G} N={N} K={K} m={m.tolist()}")
     assert fx.device_status() == 0
+
+
+# -- random problems sized to land on each of the planner's choices ----------------------
+
+PLAN_CASES = [
+    # (layout, expected variant, per-group rows, G range, N choices, K choices, empty groups:
+    # a fraction of G, or "one" -- exactly one, so that the mean the planner sees stays on
+    # the branch)
+    ("stacked", "stacked_swap_w128xa16_tma", (0, 16), (4, 32), (1024, 2048), (1024, 2048), 0.2),
+    ("stacked", "stacked_swap_w128xa32_tma", (18, 32), (4, 16), (1024, 2048), (512, 1024), 0.0),
+    ("stacked", "stacked_tile128x256_tma", (300, 600), (12, 16), (2048, 4096), (512, 1024), "one"),
+    ("stacked", "stacked_pair256x256_tma", (1200, 1500), (16, 20), (1024, 2048), (256, 512), "one"),
+    ("dynamic", "dynamic_pair256x256_tma", (512, 600), (16, 24), (2048,), (256, 512), 0.0),
+    ("stacked", "stacked_tile128x128_cpasync", (200, 600), (4, 8), (1024,),
+     (1000, 1001, 1004, 1036), 0.2),
+]
+
+
+PLAN_DRAWS = int(os.environ.get("MSLKB_FUZZ_PLAN_DRAWS", "2"))
+
+
+@pytest.mark.parametrize("case", range(len(PLAN_CASES) * PLAN_DRAWS))
+def test_fuzz_planner_choices(orc, case):
+    """Random groups around each branch of the planner (swap-AB 16 / 32, 128 x 256 tiles,
+    CTA pairs claiming their tiles on the stacked layout and in a fixed stride on slabs,
+    the cp.async loader), PLAN_DRAWS draws each: the planner must pick the expected kernel; the
+    sampled rows (first, last and random rows of every group) must match the oracle and no
+    owned element may keep the fill pattern."""
+    layout, want, (lo, hi), (g_lo, g_hi), n_choices, k_choices, empty = \
+        PLAN_CASES[case % len(PLAN_CASES)]
+    rng = np.random.default_rng(8000 + case)
+    G = int(rng.integers(g_lo, g_hi + 1))
+    N = int(rng.choice(n_choices))
+    K = int(rng.choice(k_choices))
+    g = torch.Generator().manual_seed(8100 + case)
+    if layout == "stacked":
+        counts = rng.integers(lo, hi + 1, size=G)
+        if empty == "one":
+            counts[int(rng.integers(G))] = 0
+        else:
+            counts[rng.random(G) < empty] = 0
+        rows, meta, E = int(counts.sum()), counts, 0
+    else:
+        E = int(rng.integers(lo, hi + 1))
+        rows, meta = G * E, rng.integers(-2, E + 3, size=G)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    plan = fx.mslkb_plan(0 if layout == "stacked" else 1, rows if layout == "stacked" else E,
+                         G, N, K, sms)
+    assert fx.variant_name(plan.variant) == want, (fx.variant_name(plan.variant), G, N, K, rows)
+    A = random_codes((rows, K), g).numpy()
+    B = random_codes((G, N, K), g).numpy()
+    sa = (np.exp2(rng.integers(-6, 6, size=rows)) * rng.uniform(0.5, 1.5, size=rows))
+    sb = (np.exp2(rng.integers(-6, 6, size=(G, N))) * rng.uniform(0.5, 1.5, size=(G, N)))
+    prob = Problem.from_numpy(layout, A, B, sa.astype(np.float32), sb.astype(np.float32), meta,
+                              expected_m=E)
+    out = torch.full((rows, N), 0x7E7E, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+    prob.run_gpu(out=out)
+    torch.cuda.synchronize()
+    assert fx.device_status() == 0
+    owned = torch.from_numpy(prob.owned_rows_mask()).cuda()
+    left = int((out.view(torch.int16)[owned] == 0x7E7E).sum().item())
+    assert left == 0, f"{want}: {left} owned elements still hold the fill pattern"
+    sample = prob.sample_rows(per_group_random=1, seed=case, cap=96)
+    got = bits_of(out[torch.from_numpy(sample).cuda()]).reshape(sample.size, N)
+    ref, ab = prob.oracle_rows(orc, sample)
+    compare(got.ravel(), ref.ravel(), ab.ravel(), f"{want} G={G} N={N} K={K} rows={rows}")
