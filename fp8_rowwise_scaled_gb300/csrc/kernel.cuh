@@ -1534,7 +1534,13 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
       // is loaded one chunk ahead, so its latency hides behind the chunk wait
       const float* bs_a = nullptr;
       const float* bs_b = nullptr;
-      float bs_next = 0.0f;
+      float bsa_next = 0.0f;  // the next K block's scale_a and scale_b, loaded a block ahead
+      float bsb_next = 0.0f;  // and multiplied only when the block is drained
+      // swap-AB: the next chunk's scales of each of its K blocks, loaded a chunk ahead
+      float sw_bs_next[Cfg::kBSSub];
+      float sw_row_next[Cfg::kBSSub];
+#pragma unroll
+      for (int j = 0; j < Cfg::kBSSub; ++j) sw_bs_next[j] = sw_row_next[j] = 0.0f;
       float sb_pre[Cfg::kSwap ? 1 : Cfg::kThreadCols / 32];
       // swap-AB: scale_b of this thread's weight row, and scale_a of row m0 + 32 pc + lane
       float sw_sb = 0.0f;
@@ -1576,10 +1582,10 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         // (columns of a tile past N are never stored: clamp their block into range)
         const int32_t blk = min((c.n0 + ocol) / Cfg::kScaleBlock, nblk - 1);
         bs_b = p.scale_b + (static_cast<size_t>(c.g) * nblk + blk) * p.num_kb;
-        bs_next = (rv && it.kb0 < kb_end)
-                      ? __ldg(ck_ptr(p, bs_a + it.kb0, p.scale_a, ext_scale_a<Cfg>(p))) *
-                            __ldg(ck_ptr(p, bs_b + it.kb0, p.scale_b, ext_scale_b<Cfg>(p)))
-                      : 0.0f;
+        if (rv && it.kb0 < kb_end) {
+          bsa_next = __ldg(ck_ptr(p, bs_a + it.kb0, p.scale_a, ext_scale_a<Cfg>(p)));
+          bsb_next = __ldg(ck_ptr(p, bs_b + it.kb0, p.scale_b, ext_scale_b<Cfg>(p)));
+        }
         sa_pre = 1.0f;
 #pragma unroll
         for (int pc = 0; pc < Cfg::kThreadCols / 32; ++pc) sb_pre[pc] = 1.0f;
@@ -1594,6 +1600,14 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         const int32_t Rl = c.m0 + static_cast<int32_t>(lane);
         const bool rv = lane < static_cast<uint32_t>(Cfg::kTileN) && Rl < c.valid_end;
         bs_a = p.scale_a + static_cast<size_t>(rv ? Rl : 0) * p.num_kb;
+        if (it.kb0 < kb_end) {
+#pragma unroll
+          for (int j = 0; j < Cfg::kBSSub; ++j) {
+            const int32_t kbj = min(it.kb0 + j, kb_end - 1);
+            sw_bs_next[j] = __ldg(ck_ptr(p, bs_b + kbj, p.scale_b, ext_scale_b<Cfg>(p)));
+            sw_row_next[j] = __ldg(ck_ptr(p, bs_a + kbj, p.scale_a, ext_scale_a<Cfg>(p)));
+          }
+        }
       }
       // fp32 accumulator of this thread (round-to-nearest adds of the TMEM chunks)
       float acc[Cfg::kThreadCols];
@@ -1658,24 +1672,35 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
           const int buf = static_cast<int>(chunk % Cfg::kNumAcc);
           const uint32_t use = chunk / Cfg::kNumAcc;
           const int32_t nsub = min(kpc, kb_end - kb0);  // K blocks in this chunk
-          // block scaling: the scale of K block kb0 (128-row tiles: loaded one chunk
-          // ahead), or of each of the chunk's blocks (swap-AB: loaded before the wait)
+          // block scaling: the scale of K block kb0 (128-row tiles), or of each of the
+          // chunk's blocks (swap-AB), loaded one chunk ahead
           float bs = 1.0f;      // this thread's scale of the block (swap-AB: its column's)
           float bs_row = 0.0f;  // swap-AB: lane j's activation-row scale
           float sub_bs[Cfg::kBSSub];
           float sub_row[Cfg::kBSSub];
           if constexpr (Cfg::kBlockScale && Cfg::kSwap) {
+            // this chunk's scales were loaded a chunk ago; the next chunk's go out now
 #pragma unroll
             for (int j = 0; j < Cfg::kBSSub; ++j) {
-              const int32_t kbj = min(kb0 + j, kb_end - 1);
-              sub_bs[j] = __ldg(ck_ptr(p, bs_b + kbj, p.scale_b, ext_scale_b<Cfg>(p)));
-              sub_row[j] = __ldg(ck_ptr(p, bs_a + kbj, p.scale_a, ext_scale_a<Cfg>(p)));
+              sub_bs[j] = sw_bs_next[j];
+              sub_row[j] = sw_row_next[j];
+            }
+            if (kb0 + kpc < kb_end) {
+#pragma unroll
+              for (int j = 0; j < Cfg::kBSSub; ++j) {
+                const int32_t kbj = min(kb0 + kpc + j, kb_end - 1);
+                sw_bs_next[j] = __ldg(ck_ptr(p, bs_b + kbj, p.scale_b, ext_scale_b<Cfg>(p)));
+                sw_row_next[j] = __ldg(ck_ptr(p, bs_a + kbj, p.scale_a, ext_scale_a<Cfg>(p)));
+              }
             }
           } else if constexpr (Cfg::kBlockScale) {
-            bs = bs_next;
-            if (kb0 + 1 < kb_end && bs_a != nullptr)
-              bs_next = __ldg(ck_ptr(p, bs_a + kb0 + 1, p.scale_a, ext_scale_a<Cfg>(p))) *
-                        __ldg(ck_ptr(p, bs_b + kb0 + 1, p.scale_b, ext_scale_b<Cfg>(p)));
+            // (the product is taken here, a block after its loads were issued, so that the
+            // loads' latency never holds up the wait and drain below)
+            bs = bsa_next * bsb_next;
+            if (kb0 + 1 < kb_end && bs_a != nullptr) {
+              bsa_next = __ldg(ck_ptr(p, bs_a + kb0 + 1, p.scale_a, ext_scale_a<Cfg>(p)));
+              bsb_next = __ldg(ck_ptr(p, bs_b + kb0 + 1, p.scale_b, ext_scale_b<Cfg>(p)));
+            }
           }
           // scale of accumulator column j (block scaling; swap-AB: row j's times column's)
           auto cs = [&](int j) -> float {
