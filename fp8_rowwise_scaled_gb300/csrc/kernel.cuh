@@ -730,6 +730,20 @@ __device__ void build_sched(const GemmParams& p, int32_t* rowinfo, int32_t* tile
   }
 }
 
+// The 16-byte chunk `chunk` of every row of one stage's activation and weight tiles set to
+// zero by the 32 lanes of a warp (rows strided over the lanes), made visible to the tensor
+// core's reads, and the lanes converged again.
+template <class Cfg>
+__device__ __forceinline__ void zero_stage_chunk(uint32_t sa_base, uint32_t sw_base,
+                                                 uint32_t chunk, uint32_t lane) {
+  for (int row = static_cast<int>(lane); row < Cfg::kActRows; row += 32)
+    ptx::st_shared_v4(sa_base + row * 128u + ((chunk ^ (row & 7u)) << 4), 0u, 0u, 0u, 0u);
+  for (int row = static_cast<int>(lane); row < Cfg::kWRows; row += 32)
+    ptx::st_shared_v4(sw_base + row * 128u + ((chunk ^ (row & 7u)) << 4), 0u, 0u, 0u, 0u);
+  ptx::fence_proxy_async_smem();
+  __syncwarp();
+}
+
 // Ragged K, the first K block of a slice that starts `lo` bytes into it and ends at `hi`
 // (<= 128): the block was loaded from the 128-byte boundary below the slice start, and
 // before lo and past hi lie other groups' K (or TMA zero fill).  Whole 32-byte steps
@@ -737,20 +751,16 @@ __device__ void build_sched(const GemmParams& p, int32_t* rowinfo, int32_t* tile
 // both operands are zeroed first (slices start and end on a 16-element boundary; both
 // operands, since 0 x NaN is NaN; 128-byte swizzle: chunk c of row r sits at c ^ (r & 7)).
 // The first issued step overwrites the accumulator.  Out of line: once per tile, off the
-// MMA thread's per-block path.
+// MMA warp's per-block path.  Called by every lane of the MMA warp: the zeroing is shared,
+// lane 0 issues the MMAs.
 template <class Cfg>
 __device__ __noinline__ void mma_ragk_first_block(uint32_t d_tmem, uint64_t a_desc,
                                                   uint64_t b_desc, uint32_t sa_base,
-                                                  uint32_t sw_base, int32_t lo, int32_t hi) {
-  auto zero_chunk = [&](uint32_t chunk) {
-    for (int row = 0; row < Cfg::kActRows; ++row)
-      ptx::st_shared_v4(sa_base + row * 128u + ((chunk ^ (row & 7u)) << 4), 0u, 0u, 0u, 0u);
-    for (int row = 0; row < Cfg::kWRows; ++row)
-      ptx::st_shared_v4(sw_base + row * 128u + ((chunk ^ (row & 7u)) << 4), 0u, 0u, 0u, 0u);
-  };
-  if (lo & 16) zero_chunk(static_cast<uint32_t>(lo >> 4) - 1u);
-  if (hi & 16) zero_chunk(static_cast<uint32_t>(hi >> 4));
-  if ((lo | hi) & 16) ptx::fence_proxy_async_smem();
+                                                  uint32_t sw_base, int32_t lo, int32_t hi,
+                                                  uint32_t lane) {
+  if (lo & 16) zero_stage_chunk<Cfg>(sa_base, sw_base, static_cast<uint32_t>(lo >> 4) - 1u, lane);
+  if (hi & 16) zero_stage_chunk<Cfg>(sa_base, sw_base, static_cast<uint32_t>(hi >> 4), lane);
+  if (lane != 0) return;
   const int k_first = lo / 32;
   const int k_end = (hi + 31) / 32;
   for (int k = k_first; k < k_end; ++k)
@@ -1304,7 +1314,17 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     // (two buffers, alternating); the epilogue adds every chunk into fp32 registers with
     // round-to-nearest, so the tensor core's own accumulation only ever spans a chunk.
     // A pair's MMAs are issued by its leader (rank 0) alone.
-    if (lane == 0 && has_k && crank == 0) {
+    // Ragged K: the whole warp walks the loop (every lane waits on the same barriers), so
+    // that the zeroing of a slice's half-used 32-byte steps is shared by 32 lanes; lane 0
+    // alone issues the MMAs and commits.  Other kernels: lane 0 alone.
+    const bool issuer = lane == 0;
+    // a wait's outcome, made the same for every lane walking the loop (so that a wait that
+    // runs out just as its barrier completes cannot send the lanes different ways)
+    auto warp_agrees = [&](bool ok_lane) -> bool {
+      if constexpr (Cfg::kRagK) return __all_sync(0xffffffffu, ok_lane);
+      else return ok_lane;
+    };
+    if ((issuer || Cfg::kRagK) && has_k && crank == 0) {
       int stage = 0;
       uint32_t phase = 0;
       uint32_t chunk = 0;  // chunks issued by this CTA: buffer = chunk % kNumAcc
@@ -1357,8 +1377,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
           }
           const int buf = static_cast<int>(chunk % Cfg::kNumAcc);
           const uint32_t use = chunk / Cfg::kNumAcc;  // how often this buffer was used before
-          if (!wait_bar<Cfg::kPair>(tempty_bar(buf), (use & 1u) ^ 1u, abort_flag, p.status,
-                                    p.timeout_ns)) {
+          if (!warp_agrees(wait_bar<Cfg::kPair>(tempty_bar(buf), (use & 1u) ^ 1u, abort_flag,
+                                                p.status, p.timeout_ns))) {
             ok = false;
             break;
           }
@@ -1381,7 +1401,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
             }
           }
           for (int32_t kb = kb0; kb < kb1; ++kb) {
-            if (!wait_bar(full_bar(stage), phase, abort_flag, p.status, p.timeout_ns)) {
+            if (!warp_agrees(wait_bar(full_bar(stage), phase, abort_flag, p.status,
+                                      p.timeout_ns))) {
               ok = false;
               break;
             }
@@ -1401,8 +1422,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
               // the out-of-line edge path
               mma_ragk_first_block<Cfg>(d_tmem, a_desc, b_desc, s_act + stage * Cfg::kActBytes,
                                         s_w + stage * Cfg::kWBytes, k_skip,
-                                        min(kBK, k_len));
-              ptx::mma_commit(empty_bar(stage));
+                                        min(kBK, k_len), lane);
+              if (issuer) ptx::mma_commit(empty_bar(stage));
               if (++stage == Cfg::kStages) {
                 stage = 0;
                 phase ^= 1u;
@@ -1417,23 +1438,15 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
               const int32_t r = k_len - kb * kBK;
               if (r < kBK) {
                 nmma = (r + 31) / 32;
-                if (r & 16) {
-                  const uint32_t chunk = static_cast<uint32_t>(r >> 4);
-                  const uint32_t sa_base = s_act + stage * Cfg::kActBytes;
-                  const uint32_t sw_base = s_w + stage * Cfg::kWBytes;
-                  for (int row = 0; row < Cfg::kActRows; ++row)
-                    ptx::st_shared_v4(sa_base + row * 128u + ((chunk ^ (row & 7u)) << 4), 0u,
-                                      0u, 0u, 0u);
-                  for (int row = 0; row < Cfg::kWRows; ++row)
-                    ptx::st_shared_v4(sw_base + row * 128u + ((chunk ^ (row & 7u)) << 4), 0u,
-                                      0u, 0u, 0u);
-                  ptx::fence_proxy_async_smem();
-                }
+                if (r & 16)
+                  zero_stage_chunk<Cfg>(s_act + stage * Cfg::kActBytes,
+                                        s_w + stage * Cfg::kWBytes,
+                                        static_cast<uint32_t>(r >> 4), lane);
               }
             }
 #pragma unroll
             for (int k = 0; k < kBK / 32; ++k) {
-              if (k >= nmma) break;
+              if (k >= nmma || !issuer) break;
               // advance 32 bytes of K inside the 128-byte swizzled row: +2 in 16-byte units
               if constexpr (Cfg::kPair)
                 ptx::mma_f8f6f4_pair(d_tmem, a_desc + 2u * k, b_desc + 2u * k, idesc,
@@ -1446,7 +1459,9 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
             // Block scaling (one K block = one stage per chunk) has one commit per block:
             // the epilogue frees the stage once it sees the chunk's accumulator commit.
             if constexpr (Cfg::kPair) ptx::mma_commit_pair(empty_bar(stage), 0x3);
-            else if constexpr (!Cfg::kBlockScale) ptx::mma_commit(empty_bar(stage));
+            else if constexpr (!Cfg::kBlockScale) {
+              if (issuer) ptx::mma_commit(empty_bar(stage));
+            }
             if (++stage == Cfg::kStages) {
               stage = 0;
               phase ^= 1u;
@@ -1454,7 +1469,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
           }
           if (!ok) break;
           if constexpr (Cfg::kPair) ptx::mma_commit_pair(tfull_bar(buf), 0x3);
-          else ptx::mma_commit(tfull_bar(buf));
+          else if (issuer) ptx::mma_commit(tfull_bar(buf));
           ++chunk;
         }
       }
