@@ -374,12 +374,13 @@ mslkb_status plan(int layout, int64_t rows, int64_t G, int64_t N, int64_t K, int
       if (wide >= 0 && tiles_bound(variant(wide), layout, rows, G, N) >= num_sms) tile_n = 256;
       // CTA pairs (256 x 256 tiles, a third fewer operand bytes per SM and K block, six
       // stages): measured on GB300 4-5 % ahead of 128 x 256 tiles on full slabs of >= 512
-      // rows, and 3.5 % ahead on stacked groups of ~1024 rows (16 x 1024 x 16384^2: 3103-3110
-      // against 3211-3235 us per call, 6.2 GB of DRAM traffic against 5.4); level with them
-      // on stacked groups of ~512 rows and 2.5 % behind on the Zipf-sized groups of the
-      // DS-V3 shapes, where a group's last, half-used pair tile weighs more.
+      // rows, 3.5 % ahead on stacked groups of ~1024 rows (16 x 1024 x 16384^2: 3103-3110
+      // against 3211-3235 us per call) and ~1.5 % ahead on stacked groups of ~512 rows
+      // (16 x 512 x 8192^2, tiles claimed in order: 455-459 against 462-467 us, five
+      // alternating rounds); 2.5 % behind on the Zipf-sized groups of the DS-V3 shapes
+      // (256 rows on average), where a group's last, half-used pair tile weighs more.
       const int pair = find_variant(dynamic, true, false, 256, 2);
-      if (tile_n == 256 && pair >= 0 && per_group >= (dynamic ? 512 : 1024) &&
+      if (tile_n == 256 && pair >= 0 && per_group >= 512 &&
           tiles_bound(variant(pair), layout, rows, G, N) >= 4 * (num_sms / 2))
         cluster = 2;
     }

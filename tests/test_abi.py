@@ -275,10 +275,10 @@ GB300_SMS = 152
     ("c3_llama70b_m16", "stacked_swap_w128xa16_tma"),
     ("c3_llama70b_m128", "stacked_swap_w128xa16_tma"),
     ("c3_llama70b_m1024", "stacked_tile128x256_tma"),
-    ("c3_llama70b_m8192", "stacked_tile128x256_tma"),
+    ("c3_llama70b_m8192", "stacked_pair256x256_tma"),
     ("c4_llama405b", "stacked_pair256x256_tma"),
     ("n1_batched_llama70b_m512", "dynamic_pair256x256_tma"),
-    ("n2_offsets_llama70b_m8192", "stacked_tile128x256_tma"),
+    ("n2_offsets_llama70b_m8192", "stacked_pair256x256_tma"),
 ])
 def test_plan_per_workload(L, name, expect):
     wl = workloads()[name]

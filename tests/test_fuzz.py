@@ -145,7 +145,7 @@ PLAN_CASES = [
     # the branch)
     ("stacked", "stacked_swap_w128xa16_tma", (0, 16), (4, 32), (1024, 2048), (1024, 2048), 0.2),
     ("stacked", "stacked_swap_w128xa32_tma", (18, 32), (4, 16), (1024, 2048), (512, 1024), 0.0),
-    ("stacked", "stacked_tile128x256_tma", (300, 600), (12, 16), (2048, 4096), (512, 1024), "one"),
+    ("stacked", "stacked_tile128x256_tma", (300, 480), (12, 16), (2048, 4096), (512, 1024), "one"),
     ("stacked", "stacked_pair256x256_tma", (1200, 1500), (16, 20), (1024, 2048), (256, 512), "one"),
     ("dynamic", "dynamic_pair256x256_tma", (512, 600), (16, 24), (2048,), (256, 512), 0.0),
     ("stacked", "stacked_tile128x128_cpasync", (200, 600), (4, 8), (1024,),
