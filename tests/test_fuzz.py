@@ -148,6 +148,9 @@ PLAN_CASES = [
     ("stacked", "stacked_tile128x256_tma", (300, 480), (12, 16), (2048, 4096), (512, 1024), "one"),
     ("stacked", "stacked_pair256x256_tma", (1200, 1500), (16, 20), (1024, 2048), (256, 512), "one"),
     ("dynamic", "dynamic_pair256x256_tma", (512, 600), (16, 24), (2048,), (256, 512), 0.0),
+    # skewed groups (a few large, many small: "zipf" draws rows ~ (rank + 1)^-1.1) with a
+    # mean of at least 512 rows: CTA pairs, many groups ending in half-used pair tiles
+    ("stacked", "stacked_pair256x256_tma", (600, 900), (16, 32), (2048,), (256, 512), "zipf"),
     ("stacked", "stacked_tile128x128_cpasync", (200, 600), (4, 8), (1024,),
      (1000, 1001, 1004, 1036), 0.2),
 ]
@@ -171,11 +174,17 @@ def test_fuzz_planner_choices(orc, case):
     K = int(rng.choice(k_choices))
     g = torch.Generator().manual_seed(8100 + case)
     if layout == "stacked":
-        counts = rng.integers(lo, hi + 1, size=G)
-        if empty == "one":
-            counts[int(rng.integers(G))] = 0
+        if empty == "zipf":   # G groups sharing G x mean rows, Zipf-sized, shuffled
+            mean = int(rng.integers(lo, hi + 1))
+            w = 1.0 / np.arange(1, G + 1) ** 1.1
+            counts = np.floor(w / w.sum() * G * mean).astype(np.int64)
+            rng.shuffle(counts)
         else:
-            counts[rng.random(G) < empty] = 0
+            counts = rng.integers(lo, hi + 1, size=G)
+            if empty == "one":
+                counts[int(rng.integers(G))] = 0
+            else:
+                counts[rng.random(G) < empty] = 0
         rows, meta, E = int(counts.sum()), counts, 0
     else:
         E = int(rng.integers(lo, hi + 1))
