@@ -82,6 +82,8 @@ struct GemmParams {
   int32_t test_stall;      // test hook: CTA 0 (CTA pairs: the first pair) withholds its
                            // first stage (TMA kernels), so the MMA wait runs out and the
                            // timeout path runs
+  int32_t w_pair;          // swap-AB: 1 when the weight map of two K blocks per box (the
+                           // kernel's tmB2) is valid, i.e. K is a multiple of 128
   int32_t prefetch_kb;     // swap-AB: K blocks of weights each CTA asks L2 to prefetch
                            // before the dependency wait (0: none)
   const int64_t* spec_meta;  // metadata the speculative schedule reads (= meta, unless a
@@ -939,7 +941,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ GemmParams p,
                         const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB,
-                        const __grid_constant__ CUtensorMap tmC) {
+                        const __grid_constant__ CUtensorMap tmC,
+                        const __grid_constant__ CUtensorMap tmB2) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -994,6 +997,9 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     if (warp == 0 && lane == 0 && p.num_kb > 0) {
       ptx::prefetch_tensormap(&tmA);
       ptx::prefetch_tensormap(&tmB);
+      if constexpr (Cfg::kSwap && !Cfg::kRagged && !Cfg::kBlockScale) {
+        if (p.w_pair != 0) ptx::prefetch_tensormap(&tmB2);
+      }
     }
   }
   if (warp == Cfg::kMmaWarp) {
@@ -1207,6 +1213,34 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
               }
             } else if (withhold) {
               withhold = false;  // this stage's full barrier never completes
+            } else if (Cfg::kSwap && !Cfg::kRagged && !Cfg::kBlockScale && p.w_pair != 0 &&
+                       stage + 1 < Cfg::kStages && kb + 1 < kb_end) {
+              // Swap-AB: the weights of K blocks kb and kb + 1 in one TMA operation (a box of
+              // two K blocks of a 4-D view of B, which lands as the two stages' weight tiles
+              // one after the other): an SM's weight stream is capped by its rate of TMA
+              // operations, 16 KB ones reaching about two thirds of what 32 KB ones do.  The
+              // next stage must be free as well; stage s's barrier takes both blocks' weight
+              // bytes (the MMA thread consumes s before s + 1), s + 1's its activations only.
+              if (!wait_bar(empty_bar(stage + 1), phase ^ 1u, abort_flag, p.status,
+                            p.timeout_ns)) {
+                ok = false;
+                break;
+              }
+              ptx::mbar_arrive_expect_tx(full_bar(stage), Cfg::kActBytes + 2 * Cfg::kWBytes);
+              ptx::mbar_arrive_expect_tx(full_bar(stage + 1), Cfg::kActBytes);
+              const int32_t x = ck_tma(p, kb * kBK, 0, p.K, true);
+              const int32_t x1 = ck_tma(p, (kb + 1) * kBK, 0, p.K, true);
+              const int32_t ya = ck_tma(p, c.m0, 0, p.rows, false);
+              const int32_t yb = ck_tma(p, c.n0, 0, p.N, false);
+              const int32_t zb = ck_tma(p, c.bz, 0, p.G, false);
+              ptx::tma_load_2d_hint(s_act + stage * Cfg::kActBytes, &tmA, full_bar(stage), x,
+                                    ya, pol_act);
+              ptx::tma_load_2d_hint(s_act + (stage + 1) * Cfg::kActBytes, &tmA,
+                                    full_bar(stage + 1), x1, ya, pol_act);
+              ptx::tma_load_4d_hint(s_w + stage * Cfg::kWBytes, &tmB2, full_bar(stage), 0, yb,
+                                    ck_tma(p, kb, 0, p.num_kb, false), zb, pol_w);
+              ++stage;  // the loop's own step below moves past stage + 1
+              ++kb;
             } else {
               ptx::mbar_arrive_expect_tx(full_bar(stage), Cfg::kStageBytes);
               // k0: a ragged-K slice starts on a multiple of 16 elements (16 bytes)

@@ -14,6 +14,7 @@ struct LaunchArgs {
   CUtensorMap tmA;   // activation tiles [rows, K], box (128 B, box_act)
   CUtensorMap tmB;   // weight tiles [G, N, K], box (128 B, box_w, 1)
   CUtensorMap tmC;   // output [rows, N] bf16, box (32, 32), 64-byte swizzle (128-row tiles)
+  CUtensorMap tmB2;  // swap-AB weights as (128 B, N, K / 128, G), box (128 B, box_w, 2, 1)
   dim3 grid;
   cudaStream_t stream;
 };
@@ -67,7 +68,8 @@ cudaError_t launch_variant(const LaunchArgs& a) {
     attr[1].val.clusterDim.z = 1;
     cfg.numAttrs = 2;
   }
-  return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<Cfg>, a.params, a.tmA, a.tmB, a.tmC);
+  return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<Cfg>, a.params, a.tmA, a.tmB, a.tmC,
+                            a.tmB2);
 }
 
 template <class Cfg>

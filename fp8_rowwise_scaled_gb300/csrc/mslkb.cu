@@ -461,6 +461,7 @@ mslkb_status encode_maps(LaunchArgs* la, const VariantInfo* v, const void* A, co
                          int64_t rows, int64_t G, int64_t N, int64_t K) {
   std::memset(&la->tmA, 0, sizeof(la->tmA));
   std::memset(&la->tmB, 0, sizeof(la->tmB));
+  std::memset(&la->tmB2, 0, sizeof(la->tmB2));
   if (!v->tma || K == 0) return MSLKB_OK;
   if (g_encode == nullptr) return cuda_fail(cudaErrorNotSupported);
   const cuuint32_t elem_strides[3] = {1, 1, 1};
@@ -493,7 +494,37 @@ mslkb_status encode_maps(LaunchArgs* la, const VariantInfo* v, const void* A, co
       return MSLKB_ERR_CUDA;
     }
   }
+  // swap-AB plans: the weights also as (128 bytes of a K block, N rows, K / 128 blocks, G),
+  // so that one box of two K blocks lands as two consecutive stages' [rows][128 B] tiles.
+  // Whole K blocks only: with K % 128 != 0 the last block's row would run into the next row.
+  la->params.w_pair = 0;
+  if (v->swap && v->ragged == 0 && K % 128 == 0) {
+    const cuuint64_t dims[4] = {128, static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(K / 128),
+                                static_cast<cuuint64_t>(G)};
+    const cuuint64_t strides[3] = {static_cast<cuuint64_t>(K), 128,
+                                   static_cast<cuuint64_t>(N * K)};
+    const cuuint32_t box[4] = {128, static_cast<cuuint32_t>(v->box_w), 2, 1};
+    const cuuint32_t es4[4] = {1, 1, 1, 1};
+    CUresult r = g_encode(&la->tmB2, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(B),
+                          dims, strides, box, es4, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r == CUDA_SUCCESS) la->params.w_pair = 1;  // else the kernel loads one block per box
+  }
   return MSLKB_OK;
+}
+
+// Two K blocks per weight box (tmB2) for the swap-AB plans that stream long K ranges per
+// CTA.  Measured on GB300 against one block per box (three alternating rounds): llama3-70b
+// decode with 16 rows 129.2 -> 126.7 us, 128 rows 159.7 -> 155.4; with one row (27 K blocks
+// per CTA, where a CTA's first MMA waits for both blocks of its first box) 15.8 -> 16.0, and
+// on the block-scaled swap-AB tiles (whose epilogue frees the stages) 130.5 -> 134.4 at 16
+// rows: those keep one block per box.
+void gate_weight_pairs(LaunchArgs* la, const VariantInfo* v, const mslkb_plan_info& info,
+                       int64_t K) {
+  const int64_t nkb = ceil_div(K, mslkb::kBK);
+  const int64_t per_cta = info.grid > 0 ? info.tiles_bound * nkb / info.grid : 0;
+  if (v->block_scale || per_cta < 64) la->params.w_pair = 0;
 }
 
 // ---------------------------------------------------------------------------------
@@ -588,6 +619,7 @@ mslkb_status run(int layout, const void* A, const void* B, const float* scale_a,
     if (ws.counters != nullptr) p.tile_ctr = ws.counters + pair_counter_offset(st);
   }
   if ((s = encode_maps(&la, v, A, B, rows, G, N, K)) != MSLKB_OK) return s;
+  gate_weight_pairs(&la, v, info, K);
   if ((s = encode_out_map(&la, v, out, rows, N)) != MSLKB_OK) return s;
   la.grid = dim3(launch_grid(st, info.variant, info.grid), 1, 1);
   la.stream = static_cast<cudaStream_t>(stream);
@@ -749,6 +781,7 @@ mslkb_status run_stacked_with_scratch(const void* A, const void* B, const float*
     if (e != cudaSuccess) return cuda_fail(e);
   }
   if ((s = encode_maps(&la, v, A, B, total_M, G, N, K)) != MSLKB_OK) return s;
+  gate_weight_pairs(&la, v, info, K);
   if ((s = encode_out_map(&la, v, out, total_M, N)) != MSLKB_OK) return s;
   la.grid = dim3(launch_grid(st, info.variant, info.grid), 1, 1);
   la.stream = cs;
