@@ -165,10 +165,12 @@ def test_split_tiles_and_the_allocation_free_call(orc, split):
     _clean(f"split {split}")
 
 
-@pytest.mark.parametrize("name", ["c4_llama405b", "c2a_dsv3_gate_up", "c3_llama70b_m1"])
+@pytest.mark.parametrize("name", ["c4_llama405b", "c2a_dsv3_gate_up", "c3_llama70b_m1",
+                                  "c3_llama70b_m16"])
 def test_full_size(orc, name):
     # the planner's kernels on benchmark workloads at full size: CTA pairs claiming their
-    # tiles (c4), Zipf-sized groups on 128 x 256 tiles (c2a), split decode tiles (M = 1)
+    # tiles (c4), Zipf-sized groups on 128 x 256 tiles (c2a), split decode tiles (M = 1),
+    # decode with two K blocks per weight box (M = 16)
     wl = workloads()[name]
     inp = make_inputs(wl, "cuda")
     prob = Problem.from_inputs(wl, inp)
