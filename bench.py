@@ -404,6 +404,9 @@ def sweep_shape(fx, wl, pk, device):
     outs = [torch.empty(out_shape(wl), dtype=torch.bfloat16, device=device) for _ in sets]
     stream = torch.cuda.Stream(device=device)
     sp = stream.cuda_stream
+    # the inputs were written by kernels on the current stream; the calls run on `stream`
+    stream.wait_stream(torch.cuda.current_stream(device))
+    fx.device_status(sp)  # start clean: the word is read and cleared
     with torch.cuda.stream(stream):
         t_end = time.perf_counter() + 0.5  # clock ramp
         while time.perf_counter() < t_end:
@@ -434,10 +437,12 @@ def sweep_shape(fx, wl, pk, device):
             times.append(e0.elapsed_time(e1) * 1e3 / reps)  # us per call
         t1 = time.time()
     us = statistics.median(times)
+    status = fx.device_status(sp)
     plan = plan_for(fx, wl, torch.cuda.get_device_properties(device).multi_processor_count)
     del graph, sets, outs, base
     torch.cuda.empty_cache()
-    return {"wl": wl, "us": us, "window": (t0, t1), "variant": fx.variant_name(plan.variant)}
+    return {"wl": wl, "us": us, "window": (t0, t1), "variant": fx.variant_name(plan.variant),
+            "status": status}
 
 
 def compact_row(name, us, tflops, bound, frac, frac_nominal, sm_mhz, variant):
@@ -523,6 +528,7 @@ def gpu_arm(args):
     out = torch.empty(out_shape(wl), dtype=torch.bfloat16, device=device)
     stream = torch.cuda.Stream(device=device)
     sp = stream.cuda_stream
+    stream.wait_stream(torch.cuda.current_stream(device))  # inputs written on the current stream
     sms = torch.cuda.get_device_properties(device).multi_processor_count
     plan = plan_for(fx, wl, sms)
     e0 = torch.cuda.Event(enable_timing=True)
@@ -638,6 +644,10 @@ def gpu_arm(args):
         rows.append(compact_row(wl.name, ms_per_step * 1e3, value / ws, rf["bound"], rf["frac"],
                                 rf["frac_nominal"], clocks["sm_mhz"],
                                 fx.variant_name(plan.variant)))
+        # the device status word after each shape's calls: 0 everywhere, else the
+        # shapes whose calls set a bit (MSLKB_DEV_*)
+        flagged = {r["wl"].name: r["status"] for r in sweep if r.get("status")}
+        result["sweep_device_status"] = flagged or 0
         result["per_shape_cols"] = PER_SHAPE_COLS
         result["per_shape"] = rows
     if rank == 0:
