@@ -170,8 +170,11 @@ struct KernelCfg {
                                                                  : 512;
   static constexpr int kCpLag = kStages - 2;  // cp.async groups kept in flight per thread
   static constexpr uint32_t kIdesc = ptx::idesc_e4m3_f32(kMmaM * kCtas, kTileN);
-  // CTA pairs, a group's last <= 128 rows: one M = 128 MMA over both CTAs (64 rows each)
-  static constexpr uint32_t kIdescHalf = ptx::idesc_e4m3_f32(kMmaM, kTileN);
+  // CTA pairs, a group's last <= 128 rows: the tile transposed, the weights as the M = 256
+  // operand (each CTA's 128 weight rows, as in a whole tile) and the tile's rows, rounded
+  // up to 16, as N (half of them in each CTA).  Each CTA's accumulator holds its 128 output
+  // columns (TMEM lanes) x the tile's rows (TMEM columns): the tensor core computes the
+  // remainder's rows only, not 128 (at the power cap the time follows the MACs computed).
 
   // 128-row tiles write the output through shared memory and TMA stores: each epilogue
   // warp stages 32 rows x 32 columns of bf16 (2 KB, 64-byte swizzle) at a time
@@ -203,7 +206,9 @@ struct KernelCfg {
   static_assert(kSmemBytes <= 232448, "shared memory per CTA");
   static_assert(kNumAcc * kBufCols <= 512, "the accumulators must fit TMEM");
   static_assert(kEpiWarps == 4 || (kEpiWarps == 8 && !kSwap), "epilogue warp split");
-  static_assert(!kPair || (kTma && !kSwap && kTileN == 256), "CTA pairs: 256 x 256 tiles, TMA");
+  static_assert(!kPair || (kTma && !kSwap && kTileN == 256 && kActBytes == kWBytes),
+                "CTA pairs: 256 x 256 tiles, TMA (operand tiles of one size: a transposed "
+                "tile swaps their descriptors)");
   static_assert(!kRagged || (kTma && !kPair && !kDynamic), "ragged layouts: TMA, single CTAs");
   static_assert(!kBlockScale || (kTma && !kPair && !kRagged && kBK == kScaleBlock &&
                                  (!kSwap || kTileN <= 32)),
@@ -221,7 +226,9 @@ struct TileCoord {
   int32_t n0;         // first weight row / output column
   int32_t valid_end;  // rows < valid_end get the product
   int32_t zero_end;   // rows in [valid_end, zero_end) get +0.0 (padding)
-  bool half;          // CTA pairs: a 128-row tile (64 rows per CTA, M = 128 MMA)
+  bool half;          // CTA pairs: a group's last <= 128 rows, run as a transposed tile
+                      // (m0 is then the tile's first row in both CTAs)
+  int32_t tr_n;       // ... its rows rounded up to 16: the MMA's N, half of them per CTA
   int32_t orow_delta; // output row = A row + orow_delta
   int32_t srow_delta; // scale_a index = A row + srow_delta
   int32_t n_begin;    // columns in [n_begin, n_end) belong to the tile's group
@@ -305,6 +312,7 @@ __device__ __forceinline__ TileCoord decode_tile(const Sched& s, int32_t t, uint
   TileCoord c;
   c.g = g;
   c.half = false;
+  c.tr_n = 0;
   if constexpr (Cfg::kRagged) {
     const int32_t mt = (s.E + Cfg::kTileAct - 1) / Cfg::kTileAct;
     const int32_t local = t - s.tile_pre[g];
@@ -367,9 +375,11 @@ __device__ __forceinline__ TileCoord decode_tile(const Sched& s, int32_t t, uint
   if constexpr (Cfg::kPair) {
     const int32_t rem = cnt - m_idx * Cfg::kTileAct;  // rows from this tile's first on
     c.half = rem <= Cfg::kTileAct / 2;
+    if (c.half) c.tr_n = (rem + 15) & ~15;
   }
-  const int32_t cta_rows = c.half ? Cfg::kActRows / 2 : Cfg::kActRows;
-  c.m0 = base + m_idx * Cfg::kTileAct + static_cast<int32_t>(crank) * cta_rows;
+  // (a transposed tile's m0 is its first row in both CTAs: each CTA's loader adds its own
+  // share, crank * tr_n / 2, for the rows it holds)
+  c.m0 = base + m_idx * Cfg::kTileAct + (c.half ? 0 : static_cast<int32_t>(crank) * Cfg::kActRows);
   c.n0 = n_idx * Cfg::kTileW;
   c.valid_end = base + cnt;
   c.zero_end = Cfg::kDynamic ? base + s.E : base + cnt;
@@ -1187,6 +1197,9 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
           const TileCoord c = decode_tile<Cfg>(sched, it.tile, crank);
           const int32_t kb_end = Cfg::kRagK ? c.nkb : it.kb1;  // a ragged-K tile's own K
           const int32_t kb_claim = max(it.kb0, kb_end - 4);    // pairs: next tile's claim
+          // pairs: this CTA's first activation row (a transposed tile: its share of the rows)
+          const int32_t a_row =
+              c.m0 + (Cfg::kPair && c.half ? static_cast<int32_t>(crank) * (c.tr_n / 2) : 0);
           for (int32_t kb = it.kb0; kb < kb_end; ++kb) {
             if (dyn && crank == 0 && kb == kb_claim) claim_early();
             if (!wait_bar(empty_bar(stage), phase ^ 1u, abort_flag, p.status, p.timeout_ns)) {
@@ -1204,7 +1217,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                 if (crank == 0) ptx::mbar_arrive_expect_tx(full_bar(stage), 2 * Cfg::kStageBytes);
                 const int32_t x = ck_tma(p, kb * kBK, 0, p.K, true);
                 ptx::tma_load_2d_pair(s_act + stage * Cfg::kActBytes, &tmA, fb, x,
-                                      ck_tma(p, c.m0, 0, p.rows, false));
+                                      ck_tma(p, a_row, 0, p.rows, false));
                 // (the second CTA's half of an N-tail tile may lie wholly past N: zero fill)
                 ptx::tma_load_3d_pair(
                     s_w + stage * Cfg::kWBytes, &tmB, fb, x,
@@ -1379,8 +1392,16 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
           it = work_item(work, i, worker, workers);
         }
         uint32_t idesc = Cfg::kIdesc;
+        uint32_t a_lo = a_lo0, b_lo = b_lo0;
+        bool tr = false;  // CTA pairs: a transposed tile (a group's last <= 128 rows)
         if constexpr (Cfg::kPair) {
-          if (decode_tile<Cfg>(sched, it.tile, 0u).half) idesc = Cfg::kIdescHalf;
+          const TileCoord tc = decode_tile<Cfg>(sched, it.tile, 0u);
+          if (tc.half) {
+            idesc = ptx::idesc_e4m3_f32(Cfg::kMmaM * Cfg::kCtas, tc.tr_n);
+            a_lo = b_lo0;
+            b_lo = a_lo0;
+            tr = true;
+          }
         }
         int32_t kb_end = it.kb1;
         int32_t k_len = 0;  // ragged K: the slice, counted from the first block's start
@@ -1422,8 +1443,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
           if constexpr (kUnrolledMma) {
             if (kb1 - kb0 == kUnrolledChunkKb) {
               // a whole default-length chunk: the compile-time unrolled path
-              if (!mma_chunk_at<Cfg>(stage, p, s_bar, tfull_bar(buf), d_buf, idesc, a_lo0,
-                                     b_lo0, phase, abort_flag)) {
+              if (!mma_chunk_at<Cfg>(stage, p, s_bar, tfull_bar(buf), d_buf, idesc, a_lo,
+                                     b_lo, phase, abort_flag)) {
                 ok = false;
                 break;
               }
@@ -1448,8 +1469,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
             ptx::tc_fence_after_sync();
             const uint64_t act_desc = ptx::sw128_kmajor_desc(s_act + stage * Cfg::kActBytes);
             const uint64_t w_desc = ptx::sw128_kmajor_desc(s_w + stage * Cfg::kWBytes);
-            const uint64_t a_desc = Cfg::kSwap ? w_desc : act_desc;
-            const uint64_t b_desc = Cfg::kSwap ? act_desc : w_desc;
+            const uint64_t a_desc = (Cfg::kSwap || tr) ? w_desc : act_desc;
+            const uint64_t b_desc = (Cfg::kSwap || tr) ? act_desc : w_desc;
             int nmma = kBK / 32;
             if (Cfg::kRagK && kb == 0 && k_skip != 0) {
               // a slice that starts inside its first block: that block's MMAs come from
@@ -1562,18 +1583,15 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
       const int32_t kb_end = Cfg::kRagK ? c.nkb : it.kb1;
       if (Cfg::kRagK && c.nkb == 0) c.valid_end = c.m0;
       // this warp's rows (row_off from c.m0) and output columns (ocol from c.n0).  A CTA
-      // pair's 128-row tile leaves each CTA 64 rows x 256 columns, folded into TMEM as
-      // lanes 0-63 = columns 0-127 and lanes 64-127 = columns 128-255 (TMEM columns
-      // 0-127): the four warps of column slice 0 hold it all, the others sit out.
+      // pair's transposed tile (a group's last <= 128 rows) leaves each CTA its 128 output
+      // columns as TMEM lanes and the tile's rows (from c.m0) as TMEM columns from 0: the
+      // four warps of column slice 0 (32 output columns each) hold it all, the others sit out
       int32_t row_off = static_cast<int32_t>(32u * q);
       int32_t ocol = col_base;
       bool active = true;
+      const bool tr = Cfg::kPair && c.half;
       if constexpr (Cfg::kPair) {
-        if (c.half) {
-          row_off = static_cast<int32_t>(32u * (q & 1u));
-          ocol = static_cast<int32_t>(q >> 1) * (Cfg::kTileN / 2);
-          active = col_base == 0;
-        }
+        if (tr) active = col_base == 0;
       }
       // scales this thread needs, loaded before the chunk waits so their latency hides
       // behind the MMA: scale_a of its row, and scale_b of column (col0 + lane) for each
@@ -1610,16 +1628,36 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         }
       }
       if constexpr (!Cfg::kSwap && !Cfg::kBlockScale) {
-        const int32_t R = c.m0 + row_off + static_cast<int32_t>(lane);
-        if (active && R < c.valid_end)
-          sa_pre = __ldg(p.scale_a + ck_index(p, R + c.srow_delta, ext_scale_a<Cfg>(p), kCkScale));
-        const float* sb_g = p.scale_b + c.sb_off;
+        if (Cfg::kPair && tr) {
+          // a transposed tile: sa_pre holds scale_b of this thread's output column and
+          // sb_pre[pc] scale_a of the tile's row 32 pc + lane (loaded here, ahead of the
+          // chunk waits, so that nothing more stays live across the drains)
+          const int32_t m_t = c.m0;
+          const int32_t v_end = c.valid_end;  // (K = 0 set it to m0: every row +0.0)
+          const int32_t n = c.n0 + static_cast<int32_t>(crank) * Cfg::kWRows +
+                            static_cast<int32_t>(32u * q + lane);
+          if (active && n < c.n_end)
+            sa_pre = __ldg(ck_ptr(p, p.scale_b + c.sb_off + n, p.scale_b, ext_scale_b<Cfg>(p)));
 #pragma unroll
-        for (int pc = 0; pc < Cfg::kThreadCols / 32; ++pc) {
-          const int32_t col = c.n0 + ocol + pc * 32 + static_cast<int32_t>(lane);
-          sb_pre[pc] = (active && col < c.n_end)
-                           ? __ldg(ck_ptr(p, sb_g + col, p.scale_b, ext_scale_b<Cfg>(p)))
-                           : 0.0f;
+          for (int pc = 0; pc < Cfg::kThreadCols / 32; ++pc) {
+            const int32_t Rl = m_t + pc * 32 + static_cast<int32_t>(lane);
+            sb_pre[pc] = (active && Rl < v_end)
+                             ? __ldg(p.scale_a + ck_index(p, Rl + c.srow_delta,
+                                                          ext_scale_a<Cfg>(p), kCkScale))
+                             : 0.0f;
+          }
+        } else {
+          const int32_t R = c.m0 + row_off + static_cast<int32_t>(lane);
+          if (active && R < c.valid_end)
+            sa_pre = __ldg(p.scale_a + ck_index(p, R + c.srow_delta, ext_scale_a<Cfg>(p), kCkScale));
+          const float* sb_g = p.scale_b + c.sb_off;
+#pragma unroll
+          for (int pc = 0; pc < Cfg::kThreadCols / 32; ++pc) {
+            const int32_t col = c.n0 + ocol + pc * 32 + static_cast<int32_t>(lane);
+            sb_pre[pc] = (active && col < c.n_end)
+                             ? __ldg(ck_ptr(p, sb_g + col, p.scale_b, ext_scale_b<Cfg>(p)))
+                             : 0.0f;
+          }
         }
       }
       if constexpr (Cfg::kBlockScale && !Cfg::kSwap) {
@@ -1712,7 +1750,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
       // TMEM data is needed only when this warp's lanes hold rows with computed values
       bool warp_any;
       if constexpr (!Cfg::kSwap) {
-        warp_any = active && c.m0 + row_off < c.valid_end;  // lane 0's row
+        warp_any = active && (tr || c.m0 + row_off < c.valid_end);  // lane 0's row
       } else {
         warp_any = c.n0 + static_cast<int32_t>(32u * q) < p.N && c.m0 < c.valid_end;
       }
@@ -1919,6 +1957,42 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
         if (lane == 0) *cnt = 0u;  // ready for the next call
       }
       if (!active) continue;
+      if constexpr (Cfg::kPair) {
+        if (tr) {
+          // thread = output column n (its TMEM lane), acc[j] = the tile's row m_t + j.  For
+          // each pair of rows, lanes 2i and 2i + 1 trade one value, so that each lane stores
+          // two adjacent columns of one row: even lanes row 2k, odd lanes row 2k + 1
+          // (scales: sa_pre = this column's scale_b, sb_pre[pc] = scale_a of row 32 pc + lane)
+          const int32_t m_t = c.m0;
+          const int32_t v_end = c.valid_end;  // (K = 0 set it to m0: every row +0.0)
+          const bool odd = (lane & 1u) != 0u;
+          // the first of the two columns this lane stores (N % 8 == 0: both in range)
+          const int32_t n_st = c.n0 + static_cast<int32_t>(crank) * Cfg::kWRows +
+                               static_cast<int32_t>(32u * q + (lane & ~1u));
+          const float sb = sa_pre;
+#pragma unroll
+          for (int pc = 0; pc < Cfg::kThreadCols / 32; ++pc) {
+            const int32_t r0 = m_t + pc * 32;
+            if (r0 >= c.zero_end) break;
+            const float sa_l = sb_pre[pc];
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+              const float y0 = (acc[pc * 32 + 2 * k] * __shfl_sync(0xffffffffu, sa_l, 2 * k)) * sb;
+              const float y1 =
+                  (acc[pc * 32 + 2 * k + 1] * __shfl_sync(0xffffffffu, sa_l, 2 * k + 1)) * sb;
+              const float other = __shfl_xor_sync(0xffffffffu, odd ? y0 : y1, 1);
+              const int32_t R = r0 + 2 * k + (odd ? 1 : 0);
+              if (R < c.zero_end && n_st < c.n_end) {
+                const int64_t o_idx = static_cast<int64_t>(R + c.orow_delta) * p.N + n_st;
+                if (ck_range(p, o_idx, 2, ext_out_rows<Cfg>(p) * p.N))
+                  *reinterpret_cast<uint32_t*>(p.out + o_idx) =
+                      R < v_end ? (odd ? pack_bf16x2(other, y1) : pack_bf16x2(y0, other)) : 0u;
+              }
+            }
+          }
+          continue;
+        }
+      }
       if constexpr (!Cfg::kSwap) {
         // thread = one activation row
         const int32_t R = c.m0 + row_off + static_cast<int32_t>(lane);

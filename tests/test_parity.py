@@ -154,6 +154,36 @@ def test_pair_tiles_many_waves(orc, layout):
     assert fx.device_status() == 0
 
 
+@pytest.mark.parametrize("K", [1024, 0])
+@pytest.mark.parametrize("layout", ["stacked", "dynamic"])
+def test_pair_transposed_remainders(orc, layout, K):
+    """A group's last <= 128 rows on CTA pairs run as a transposed tile: the weights as the
+    M = 256 operand, the rows, rounded up to 16, as N with half of them in each CTA.
+    Remainders of 1 to 128 rows (N = 16 ... 128; shares of 8 to 64 rows per CTA), 129 (a
+    whole tile), after zero or one whole tile of the group; N = 520, so that the last
+    column tile's second CTA lies wholly past N; one chunk per tile (K = 1024: eight K
+    blocks, the unrolled MMA path) and one per K block; K = 0 writes +0.0 to every owned
+    row."""
+    rems = [1, 15, 16, 17, 31, 48, 64, 65, 96, 112, 113, 127, 128, 129]
+    meta = [256 * (i % 2) + r for i, r in enumerate(rems)]
+    if layout == "stacked":
+        prob = _rand_problem("stacked", len(meta), 520, K, meta, seed=31 + K, total_extra=3)
+    else:
+        prob = _rand_problem("dynamic", len(meta), 520, K, meta, E=400, seed=32 + K)
+    v = f"{layout}_pair256x256_tma"
+    for kpc in (8, 1):
+        fx.mslkb_set_accumulation_chunk(kpc)
+        try:
+            gb, _ = _check_full(prob, orc, variant=v,
+                                poison_value=0x5A5A if layout == "stacked" else None,
+                                what=f"{v} K {K} chunk {kpc}")
+        finally:
+            fx.mslkb_set_accumulation_chunk(8)
+        if K == 0:
+            assert np.all(gb[prob.owned_rows_mask()] == 0)
+    assert fx.device_status() == 0
+
+
 @pytest.mark.parametrize("tile", ["tile128x128", "swap_w128xa16"])
 @pytest.mark.parametrize("layout", ["stacked", "dynamic"])
 def test_cpasync_bit_identical_to_tma(orc, tile, layout):
