@@ -144,6 +144,13 @@ struct KernelCfg {
   static constexpr bool kSpecWarp = kSwap && kTma && !kRagged;
   static constexpr int kIdleWarps = kRegSplit ? 2 : (kSpecWarp ? 1 : 0);
   static constexpr int kSpecWarpIdx = kLoaderWarps + 1;
+  // Ragged K: one of the register split's spare warps takes each loaded stage and zeroes
+  // the bytes of its tiles that lie outside the tile's K slice (the first block is loaded
+  // from the 128-byte boundary below the slice start, the last runs past its end), then
+  // hands the stage to the MMA thread through a barrier of its own, so that the MMA thread
+  // issues whole blocks only
+  static constexpr bool kEdgeWarp = kRagK && kRegSplit;
+  static constexpr int kEdgeWarpIdx = kLoaderWarps + 1;
   static constexpr int kEpiWarp0 = kLoaderWarps + 1 + kIdleWarps;
   static constexpr int kThreads = 32 * (kLoaderWarps + 1 + kIdleWarps + kEpiWarps);
   static constexpr int kLaunchRegs = kRegSplit ? 168 : 0;  // required at launch (0: any)
@@ -190,7 +197,7 @@ struct KernelCfg {
   // counter and hands to the pair's other roles (slots, then a full and an empty barrier
   // per slot)
   static constexpr int kTQ = kPair ? 4 : 0;
-  static constexpr int kNumBars = 2 * kStages + 2 * kNumAcc + 2 * kTQ;
+  static constexpr int kNumBars = 2 * kStages + 2 * kNumAcc + 2 * kTQ + (kEdgeWarp ? kStages : 0);
   static constexpr int kOffMisc = kOffBar + 8 * kNumBars;  // tmem address, abort flag
   static constexpr int kOffWork = kOffMisc + 16;           // the CTA's Work (below)
   static constexpr int kOffTQ = kOffWork + 64;             // the tile ring (pairs)
@@ -799,17 +806,18 @@ constexpr int kUnrolledChunkKb = 8;
 // empty barrier at s_bar + 8 (kStages + s).
 template <class Cfg, int kS0, int kJ = 0>
 __device__ __forceinline__ bool mma_chunk_unrolled(const GemmParams& p, uint32_t s_bar,
-                                                   uint32_t tfull, uint32_t d_buf,
-                                                   uint32_t idesc, uint32_t a_lo0,
-                                                   uint32_t b_lo0, uint32_t phase,
-                                                   volatile uint32_t* abort) {
+                                                   uint32_t s_wait, uint32_t tfull,
+                                                   uint32_t d_buf, uint32_t idesc,
+                                                   uint32_t a_lo0, uint32_t b_lo0,
+                                                   uint32_t phase, volatile uint32_t* abort) {
   if constexpr (kJ == kUnrolledChunkKb) {
     return true;
   } else {
     // block kJ of the chunk: its stage, and whether the ring wrapped since the chunk's start
+    // (s_wait: the barriers that say a stage is ready, one per stage from there)
     constexpr int kSt = (kS0 + kJ) % Cfg::kStages;
     constexpr uint32_t kFlip = static_cast<uint32_t>(((kS0 + kJ) / Cfg::kStages) & 1);
-    if (!wait_bar(s_bar + 8u * kSt, phase ^ kFlip, abort, p.status, p.timeout_ns)) return false;
+    if (!wait_bar(s_wait + 8u * kSt, phase ^ kFlip, abort, p.status, p.timeout_ns)) return false;
     ptx::tc_fence_after_sync();
     // the stage's operand tiles, then K steps of 32 bytes inside the 128-byte swizzled row
     // (+2 in 16-byte descriptor units each)
@@ -831,24 +839,24 @@ __device__ __forceinline__ bool mma_chunk_unrolled(const GemmParams& p, uint32_t
       if constexpr (kJ == kUnrolledChunkKb - 1) ptx::mma_commit(tfull);
       ptx::mma_commit(empty);
     }
-    return mma_chunk_unrolled<Cfg, kS0, kJ + 1>(p, s_bar, tfull, d_buf, idesc, a_lo0, b_lo0,
-                                                phase, abort);
+    return mma_chunk_unrolled<Cfg, kS0, kJ + 1>(p, s_bar, s_wait, tfull, d_buf, idesc, a_lo0,
+                                                b_lo0, phase, abort);
   }
 }
 
 // mma_chunk_unrolled for the runtime stage `stage` (one instance per ring position).
 template <class Cfg, int kS = 0>
 __device__ __forceinline__ bool mma_chunk_at(int stage, const GemmParams& p, uint32_t s_bar,
-                                             uint32_t tfull, uint32_t d_buf, uint32_t idesc,
-                                             uint32_t a_lo0, uint32_t b_lo0, uint32_t phase,
-                                             volatile uint32_t* abort) {
+                                             uint32_t s_wait, uint32_t tfull, uint32_t d_buf,
+                                             uint32_t idesc, uint32_t a_lo0, uint32_t b_lo0,
+                                             uint32_t phase, volatile uint32_t* abort) {
   if constexpr (kS + 1 < Cfg::kStages) {
     if (stage != kS)
-      return mma_chunk_at<Cfg, kS + 1>(stage, p, s_bar, tfull, d_buf, idesc, a_lo0, b_lo0,
-                                       phase, abort);
+      return mma_chunk_at<Cfg, kS + 1>(stage, p, s_bar, s_wait, tfull, d_buf, idesc, a_lo0,
+                                       b_lo0, phase, abort);
   }
-  return mma_chunk_unrolled<Cfg, kS>(p, s_bar, tfull, d_buf, idesc, a_lo0, b_lo0, phase,
-                                     abort);
+  return mma_chunk_unrolled<Cfg, kS>(p, s_bar, s_wait, tfull, d_buf, idesc, a_lo0, b_lo0,
+                                     phase, abort);
 }
 
 // Block scaling on 128-row tiles: every K block sums into an accumulator of its own (a TMEM
@@ -970,6 +978,10 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
   auto tq_empty_bar = [&](int i) {
     return s_bar + 8u * (2 * Cfg::kStages + 2 * Cfg::kNumAcc + Cfg::kTQ + i);
   };
+  // ragged K: stage s loaded and trimmed to the tile's K slice (the MMA thread waits on
+  // these instead of the full barriers)
+  const uint32_t s_ready = s_bar + 8u * (2 * Cfg::kStages + 2 * Cfg::kNumAcc + 2 * Cfg::kTQ);
+  auto ready_bar = [&](int s) { return s_ready + 8u * s; };
   volatile int32_t* tq = reinterpret_cast<volatile int32_t*>(smem + Cfg::kOffTQ);
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + Cfg::kOffMisc);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + Cfg::kOffMisc + 4);
@@ -993,6 +1005,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
       // pairs: the leader's MMA waits for the epilogue warps of both CTAs
       ptx::mbar_init(tempty_bar(b), static_cast<uint32_t>(Cfg::kEpiWarps * Cfg::kCtas));
     }
+    if constexpr (Cfg::kEdgeWarp)
+      for (int st = 0; st < Cfg::kStages; ++st) ptx::mbar_init(ready_bar(st), 1u);
     for (int i = 0; i < Cfg::kTQ; ++i) {
       ptx::mbar_init(tq_full_bar(i), 1u);
       // on the leader: its MMA thread and epilogue warps, the peer's loader and epilogue
@@ -1361,25 +1375,30 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
     // (two buffers, alternating); the epilogue adds every chunk into fp32 registers with
     // round-to-nearest, so the tensor core's own accumulation only ever spans a chunk.
     // A pair's MMAs are issued by its leader (rank 0) alone.
-    // Ragged K: the whole warp walks the loop (every lane waits on the same barriers), so
-    // that the zeroing of a slice's half-used 32-byte steps is shared by 32 lanes; lane 0
-    // alone issues the MMAs and commits.  Other kernels: lane 0 alone.
+    // Ragged K without the edge warp: the whole warp walks the loop (every lane waits on the
+    // same barriers), so that the zeroing of a slice's half-used 32-byte steps is shared by
+    // 32 lanes; lane 0 alone issues the MMAs and commits.  Other kernels (and ragged K with
+    // the edge warp, which trims the stages and passes them on through the ready barriers):
+    // lane 0 alone.
+    constexpr bool kWarpWalks = Cfg::kRagK && !Cfg::kEdgeWarp;
     const bool issuer = lane == 0;
     // a wait's outcome, made the same for every lane walking the loop (so that a wait that
     // runs out just as its barrier completes cannot send the lanes different ways)
     auto warp_agrees = [&](bool ok_lane) -> bool {
-      if constexpr (Cfg::kRagK) return __all_sync(0xffffffffu, ok_lane);
+      if constexpr (kWarpWalks) return __all_sync(0xffffffffu, ok_lane);
       else return ok_lane;
     };
-    if ((issuer || Cfg::kRagK) && has_k && crank == 0) {
+    // the barriers that say a stage is ready for the MMAs
+    const uint32_t s_wait = Cfg::kEdgeWarp ? s_ready : s_bar;
+    if ((issuer || kWarpWalks) && has_k && crank == 0) {
       int stage = 0;
       uint32_t phase = 0;
       uint32_t chunk = 0;  // chunks issued by this CTA: buffer = chunk % kNumAcc
       bool ok = true;
       const int32_t kpc = Cfg::kBlockScale ? Cfg::kBSSub : p.kb_per_chunk;
-      // the unrolled chunk path (128-row and pair tiles; ragged K, block scaling and the
-      // swap-AB tiles keep the general loop)
-      constexpr bool kUnrolledMma = !Cfg::kSwap && !Cfg::kRagK && !Cfg::kBlockScale;
+      // the unrolled chunk path (128-row and pair tiles, ragged K with the edge warp; the
+      // other ragged-K tiles, block scaling and the swap-AB tiles keep the general loop)
+      constexpr bool kUnrolledMma = !Cfg::kSwap && !kWarpWalks && !Cfg::kBlockScale;
       const uint32_t a_lo0 = ptx::sw128_kmajor_desc_lo(Cfg::kSwap ? s_w : s_act);
       const uint32_t b_lo0 = ptx::sw128_kmajor_desc_lo(Cfg::kSwap ? s_act : s_w);
       for (int32_t i = 0; ok && (dyn || i < work.n_items); ++i) {
@@ -1443,8 +1462,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
           if constexpr (kUnrolledMma) {
             if (kb1 - kb0 == kUnrolledChunkKb) {
               // a whole default-length chunk: the compile-time unrolled path
-              if (!mma_chunk_at<Cfg>(stage, p, s_bar, tfull_bar(buf), d_buf, idesc, a_lo,
-                                     b_lo, phase, abort_flag)) {
+              if (!mma_chunk_at<Cfg>(stage, p, s_bar, s_wait, tfull_bar(buf), d_buf, idesc,
+                                     a_lo, b_lo, phase, abort_flag)) {
                 ok = false;
                 break;
               }
@@ -1456,8 +1475,8 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
             }
           }
           for (int32_t kb = kb0; kb < kb1; ++kb) {
-            if (!warp_agrees(wait_bar(full_bar(stage), phase, abort_flag, p.status,
-                                      p.timeout_ns))) {
+            if (!warp_agrees(wait_bar(s_wait + 8u * static_cast<uint32_t>(stage), phase,
+                                      abort_flag, p.status, p.timeout_ns))) {
               ok = false;
               break;
             }
@@ -1472,7 +1491,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
             const uint64_t a_desc = (Cfg::kSwap || tr) ? w_desc : act_desc;
             const uint64_t b_desc = (Cfg::kSwap || tr) ? act_desc : w_desc;
             int nmma = kBK / 32;
-            if (Cfg::kRagK && kb == 0 && k_skip != 0) {
+            if (kWarpWalks && kb == 0 && k_skip != 0) {
               // a slice that starts inside its first block: that block's MMAs come from
               // the out-of-line edge path
               mma_ragk_first_block<Cfg>(d_tmem, a_desc, b_desc, s_act + stage * Cfg::kActBytes,
@@ -1485,7 +1504,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
               }
               continue;
             }
-            if constexpr (Cfg::kRagK) {
+            if constexpr (kWarpWalks) {
               // the last block of a K slice: the bytes past the slice belong to the next
               // group (or are TMA zero fill past total_K).  Whole 32-byte steps past it are
               // not issued; in a half-used step the unused 16 bytes of every row of both
@@ -1526,6 +1545,55 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
           if constexpr (Cfg::kPair) ptx::mma_commit_pair(tfull_bar(buf), 0x3);
           else if (issuer) ptx::mma_commit(tfull_bar(buf));
           ++chunk;
+        }
+      }
+    }
+    __syncwarp();
+  } else if (Cfg::kEdgeWarp && warp == static_cast<uint32_t>(Cfg::kEdgeWarpIdx)) {
+    // ------------------------------------------------------------------ ragged-K edges
+    // Every stage in the MMA thread's order: wait (lane 0, bounded) until it is loaded,
+    // zero the 16-byte chunks of every row of both operand tiles that lie outside the
+    // tile's K slice (before the slice start in its first block, past its end in its last;
+    // both operands, since 0 x NaN is NaN; 128-byte swizzle: chunk c of row r sits at
+    // c ^ (r & 7)), make that visible to the tensor core and pass the stage on.
+    if (has_k) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int32_t i = 0; ok && i < work.n_items; ++i) {
+        const Item it = work_item(work, i, worker, workers);
+        const TileCoord c = decode_tile<Cfg>(sched, it.tile, 0u);
+        const int32_t k_end = c.k_skip + c.k_len;  // slice end, from the first block's start
+        for (int32_t kb = it.kb0; kb < c.nkb; ++kb) {
+          uint32_t got = 1u;
+          if (lane == 0)
+            got = wait_bar(full_bar(stage), phase, abort_flag, p.status, p.timeout_ns) ? 1u : 0u;
+          if (__shfl_sync(0xffffffffu, got, 0) == 0u) {
+            ok = false;
+            break;
+          }
+          const uint32_t c_lo = kb == 0 ? static_cast<uint32_t>(c.k_skip) >> 4 : 0u;
+          const int32_t hi = k_end - kb * kBK;
+          const uint32_t c_hi = hi < kBK ? static_cast<uint32_t>(hi) >> 4 : 8u;
+          if (c_lo > 0u || c_hi < 8u) {
+            const uint32_t sa = s_act + static_cast<uint32_t>(stage * Cfg::kActBytes);
+            const uint32_t sw = s_w + static_cast<uint32_t>(stage * Cfg::kWBytes);
+            for (int row = static_cast<int>(lane); row < Cfg::kActRows + Cfg::kWRows; row += 32) {
+              const uint32_t base = row < Cfg::kActRows ? sa + static_cast<uint32_t>(row) * 128u
+                                                        : sw + static_cast<uint32_t>(row - Cfg::kActRows) * 128u;
+              const uint32_t sw_row = static_cast<uint32_t>(row) & 7u;  // kActRows % 8 == 0
+              for (uint32_t ch = 0; ch < 8u; ++ch)
+                if (ch < c_lo || ch >= c_hi)
+                  ptx::st_shared_v4(base + ((ch ^ sw_row) << 4), 0u, 0u, 0u, 0u);
+            }
+            ptx::fence_proxy_async_smem();
+          }
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(ready_bar(stage));
+          if (++stage == Cfg::kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
         }
       }
     }
