@@ -1411,6 +1411,14 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
           it = work_item(work, i, worker, workers);
         }
         uint32_t idesc = Cfg::kIdesc;
+        if constexpr (Cfg::kRagN && !Cfg::kSwap) {
+          // a group's last column tile: the MMA's N cut to the group's columns in it,
+          // rounded up to 16 (the accumulator's other columns are never stored; swap-AB
+          // tiles hold the columns on the MMA's M side)
+          const TileCoord tc = decode_tile<Cfg>(sched, it.tile, 0u);
+          const int32_t cols = tc.n_end - tc.n0;
+          if (cols < Cfg::kTileN) idesc = ptx::idesc_e4m3_f32(Cfg::kMmaM, (cols + 15) & ~15);
+        }
         uint32_t a_lo = a_lo0, b_lo = b_lo0;
         bool tr = false;  // CTA pairs: a transposed tile (a group's last <= 128 rows)
         if constexpr (Cfg::kPair) {
@@ -1526,7 +1534,7 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
                 ptx::mma_f8f6f4_pair(d_tmem, a_desc + 2u * k, b_desc + 2u * k, idesc,
                                      (!first_of_acc || k > 0) ? 1u : 0u);
               else
-                ptx::mma_f8f6f4(d_tmem, a_desc + 2u * k, b_desc + 2u * k, Cfg::kIdesc,
+                ptx::mma_f8f6f4(d_tmem, a_desc + 2u * k, b_desc + 2u * k, idesc,
                                 (!first_of_acc || k > 0) ? 1u : 0u);
             }
             // pairs: the stage is free in both CTAs once the MMAs reading it complete.
