@@ -802,8 +802,9 @@ constexpr int kUnrolledChunkKb = 8;
 // tile's MMA stream takes ~669 cycles per K block of four MMAs in the general loop below
 // and ~565 in this form, a CTA pair's ~696 and ~562 (512 at the nominal rate).  The
 // chunk's commit to its TMEM buffer's barrier goes before the last stage's commit.  The
-// barrier addresses follow the kernel's layout: stage s's full barrier at s_bar + 8 s, its
-// empty barrier at s_bar + 8 (kStages + s).
+// barrier addresses follow the kernel's layout: the barrier that says stage s is ready at
+// s_wait + 8 s (its full barrier, s_bar + 8 s; on ragged-K tiles with the edge warp its
+// ready barrier), its empty barrier at s_bar + 8 (kStages + s).
 template <class Cfg, int kS0, int kJ = 0>
 __device__ __forceinline__ bool mma_chunk_unrolled(const GemmParams& p, uint32_t s_bar,
                                                    uint32_t s_wait, uint32_t tfull,
