@@ -2088,22 +2088,23 @@ __global__ void __launch_bounds__(Cfg::kThreads, 1)
           for (int pc = 0; pc < Cfg::kThreadCols / 32; ++pc) {
             const int32_t col0 = c.n0 + ocol + pc * 32;
             const float sb_l = sb_pre[pc];
+            // the block's 32 columns scaled and packed first, while the previous block's TMA
+            // store may still be reading the staging buffer
+            uint32_t w[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const float sb0 = __shfl_sync(0xffffffffu, sb_l, 2 * j);
+              const float sb1 = __shfl_sync(0xffffffffu, sb_l, 2 * j + 1);
+              w[j] = row_val ? pack_bf16x2((acc[pc * 32 + 2 * j] * sa_pre) * sb0,
+                                           (acc[pc * 32 + 2 * j + 1] * sa_pre) * sb1)
+                             : 0u;
+            }
             if (lane == 0) ptx::bulk_wait_read_all();  // staging buffer free again
             __syncwarp();
 #pragma unroll
             for (int ch = 0; ch < 4; ++ch) {  // 8 columns = one 16-byte chunk at a time
-              uint32_t w[4];
-#pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                const int cc = ch * 8 + 2 * j;
-                const float sb0 = __shfl_sync(0xffffffffu, sb_l, cc);
-                const float sb1 = __shfl_sync(0xffffffffu, sb_l, cc + 1);
-                w[j] = row_val ? pack_bf16x2((acc[pc * 32 + cc] * sa_pre) * sb0,
-                                             (acc[pc * 32 + cc + 1] * sa_pre) * sb1)
-                               : 0u;
-              }
               const uint32_t a = stg + lane * 64u + ((static_cast<uint32_t>(ch) ^ ((lane >> 1) & 3u)) << 4);
-              ptx::st_shared_v4(a, w[0], w[1], w[2], w[3]);
+              ptx::st_shared_v4(a, w[4 * ch], w[4 * ch + 1], w[4 * ch + 2], w[4 * ch + 3]);
             }
             ptx::fence_proxy_async_smem();
             __syncwarp();
